@@ -1,0 +1,266 @@
+"""Thin Python binding of libdflash (ctypes): argument marshalling only.
+
+Every function takes torch CUDA tensors, checks their dtype, shape and
+contiguity, and passes raw device pointers plus the current CUDA stream to the
+C ABI declared in ``include/dflash.h``. All arithmetic runs in the library's
+kernels; there is no fallback path. Workspaces are zero-initialised device
+buffers cached per device and stream-ordered like every other tensor.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdflash.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4
+F32, BF16 = 0, 1
+FLAG_ACCEPT_BOUNDARY, FLAG_CDF_BOUNDARY, FLAG_DEGENERATE, FLAG_INVALID = 1, 2, 4, 8
+FLAG_GATE_BOUNDARY = 1
+WS_COUNTER_BYTES = 16384
+
+
+class DflashError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"dflash error {code}: {msg}")
+        self.code = code
+
+
+c_i32 = ctypes.c_int32
+c_p = ctypes.c_void_p
+
+
+class CtxKvDims(ctypes.Structure):
+    _fields_ = [(n, c_i32) for n in ("B", "rows_max", "m", "d", "L", "Hkv", "D", "page_size",
+                                     "max_pages", "num_pages", "dtype")]
+
+
+class AttnDims(ctypes.Structure):
+    _fields_ = [(n, c_i32) for n in ("B", "n_q", "n_kv_blk", "Hq", "Hkv", "D", "page_size",
+                                     "max_pages", "num_pages", "max_ctx", "dtype")]
+
+
+class VerifyDims(ctypes.Structure):
+    _fields_ = [(n, c_i32) for n in ("B", "n_max", "V", "dtype")]
+
+
+class GateDims(ctypes.Structure):
+    _fields_ = [(n, c_i32) for n in ("B", "k", "V", "dtype")]
+
+
+_SIGS = {
+    "dflash_last_error": (ctypes.c_char_p, []),
+    "dflash_last_launch_count": (ctypes.c_int, []),
+    "dflash_verify_greedy_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
+    "dflash_verify_greedy": (ctypes.c_int, [ctypes.POINTER(VerifyDims), c_p, c_p, c_p, c_p, c_p, c_p,
+                                            c_p, c_p, c_p, ctypes.c_size_t, c_p]),
+    "dflash_verify_sample_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
+    "dflash_verify_sample": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float, c_p, c_p, c_p,
+                                            c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p,
+                                            ctypes.c_size_t, c_p]),
+    "dflash_gate_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GateDims)]),
+    "dflash_gate": (ctypes.c_int, [ctypes.POINTER(GateDims), ctypes.c_float, ctypes.c_float, c_p, c_p,
+                                   c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_size_t, c_p]),
+    "dflash_block_attn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnDims)]),
+    "dflash_block_attn": (ctypes.c_int, [ctypes.POINTER(AttnDims), c_p, c_p, c_p, c_p, c_p, c_p, c_p,
+                                         ctypes.c_float, c_p, c_p, ctypes.c_size_t, c_p]),
+    "dflash_materialize_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(CtxKvDims)]),
+    "dflash_materialize_ctx_kv": (ctypes.c_int, [ctypes.POINTER(CtxKvDims), c_p, c_p, c_p, c_p, c_p,
+                                                 c_p, c_p, ctypes.c_float, ctypes.c_float, c_p, c_p,
+                                                 c_p, c_p, c_p, ctypes.c_size_t, c_p]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdflash.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "block_diffusion_speculative_fusion_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name, None)
+            if fn is None:
+                continue
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().dflash_last_error().decode()
+
+
+def last_launch_count() -> int:
+    return int(lib().dflash_last_launch_count())
+
+
+def _check(rc: int):
+    if rc != OK:
+        raise DflashError(rc, last_error())
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    return _DT[t.dtype]
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def _opt(t: Optional[torch.Tensor], name: str, dtype=None, shape=None):
+    return None if t is None else _dev(t, name, dtype, shape)
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+_WS: Dict[Tuple[int, int], torch.Tensor] = {}
+
+
+def workspace(device: torch.device, nbytes: int, slot: int = 0) -> torch.Tensor:
+    """A zero-initialised device workspace of at least ``nbytes`` (cached per
+    device and slot; calls on one stream may share a slot)."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    key = (idx, slot)
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, WS_COUNTER_BYTES), dtype=torch.uint8, device=f"cuda:{idx}")
+        _WS[key] = ws
+    return ws
+
+
+def reset_workspaces():
+    _WS.clear()
+
+
+# ---------------------------------------------------------------------------
+# (c) verify
+# ---------------------------------------------------------------------------
+def verify_greedy(target_logits: torch.Tensor, cand: torch.Tensor, n_draft: Optional[torch.Tensor] = None,
+                  want_target_pred: bool = False, out: Optional[dict] = None, ws: Optional[torch.Tensor] = None):
+    """Greedy accept rule (``dflash_verify_greedy``). Returns a dict of device
+    tensors: accept_len, bonus, commit_len, out_tokens[, target_pred]."""
+    _dev(target_logits, "target_logits")
+    B, R, V = target_logits.shape
+    n_max = R - 1
+    dev = target_logits.device
+    dims = VerifyDims(B, n_max, V, _dtype_code(target_logits))
+    o = out if out is not None else {}
+    o.setdefault("accept_len", torch.empty(B, dtype=torch.int32, device=dev))
+    o.setdefault("bonus", torch.empty(B, dtype=torch.int64, device=dev))
+    o.setdefault("commit_len", torch.empty(B, dtype=torch.int32, device=dev))
+    o.setdefault("out_tokens", torch.empty((B, R), dtype=torch.int64, device=dev))
+    if want_target_pred:
+        o.setdefault("target_pred", torch.empty((B, R), dtype=torch.int64, device=dev))
+    need = lib().dflash_verify_greedy_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(dev, need)
+    rc = lib().dflash_verify_greedy(
+        ctypes.byref(dims), _dev(target_logits, "target_logits"), _dev(cand, "cand", torch.int64, (B, R)),
+        _opt(n_draft, "n_draft", torch.int32, (B,)),
+        _dev(o["accept_len"], "accept_len", torch.int32), _dev(o["bonus"], "bonus", torch.int64),
+        _dev(o["commit_len"], "commit_len", torch.int32), _opt(o.get("out_tokens"), "out_tokens", torch.int64),
+        _opt(o.get("target_pred"), "target_pred", torch.int64), w.data_ptr(), w.numel(), _stream(dev))
+    _check(rc)
+    return o
+
+
+def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor, cand: torch.Tensor,
+                  u_accept: torch.Tensor, u_final: torch.Tensor, temperature: float = 1.0,
+                  n_draft: Optional[torch.Tensor] = None, want_probs: bool = False,
+                  out: Optional[dict] = None, ws: Optional[torch.Tensor] = None):
+    """Sampled accept rule with residual resample (``dflash_verify_sample``).
+    Returns accept_len, bonus, commit_len, out_tokens, flags[, probs]."""
+    _dev(target_logits, "target_logits")
+    B, R, V = target_logits.shape
+    n_max = R - 1
+    dev = target_logits.device
+    dt = _dtype_code(target_logits)
+    if draft_logits.dtype != target_logits.dtype:
+        raise TypeError("draft_logits and target_logits must share a dtype")
+    dims = VerifyDims(B, n_max, V, dt)
+    o = out if out is not None else {}
+    o.setdefault("accept_len", torch.empty(B, dtype=torch.int32, device=dev))
+    o.setdefault("bonus", torch.empty(B, dtype=torch.int64, device=dev))
+    o.setdefault("commit_len", torch.empty(B, dtype=torch.int32, device=dev))
+    o.setdefault("out_tokens", torch.empty((B, R), dtype=torch.int64, device=dev))
+    o.setdefault("flags", torch.empty(B, dtype=torch.uint8, device=dev))
+    if want_probs:
+        o.setdefault("probs", torch.empty((B, 2 * n_max + 1), dtype=torch.float32, device=dev))
+    need = lib().dflash_verify_sample_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(dev, need)
+    rc = lib().dflash_verify_sample(
+        ctypes.byref(dims), ctypes.c_float(temperature), _dev(target_logits, "target_logits"),
+        _dev(draft_logits, "draft_logits", None, (B, n_max, V)), _dev(cand, "cand", torch.int64, (B, R)),
+        _opt(n_draft, "n_draft", torch.int32, (B,)), _dev(u_accept, "u_accept", torch.float32, (B, n_max)),
+        _dev(u_final, "u_final", torch.float32, (B,)),
+        _dev(o["accept_len"], "accept_len", torch.int32), _dev(o["bonus"], "bonus", torch.int64),
+        _dev(o["commit_len"], "commit_len", torch.int32), _opt(o.get("out_tokens"), "out_tokens", torch.int64),
+        _opt(o.get("flags"), "flags", torch.uint8), _opt(o.get("probs"), "probs", torch.float32),
+        w.data_ptr(), w.numel(), _stream(dev))
+    _check(rc)
+    return o
+
+
+# ---------------------------------------------------------------------------
+# DLoop gate
+# ---------------------------------------------------------------------------
+def gate(draft_logits: torch.Tensor, tokens: torch.Tensor, temperature: float = 1.0, g: float = -0.5,
+         active: Optional[torch.Tensor] = None, want_row_lse: bool = False,
+         out: Optional[dict] = None, ws: Optional[torch.Tensor] = None):
+    """DLoop block gate (``dflash_gate``). Returns c, cont, flags[, row_lse]."""
+    _dev(draft_logits, "draft_logits")
+    B, k, V = draft_logits.shape
+    dev = draft_logits.device
+    dims = GateDims(B, k, V, _dtype_code(draft_logits))
+    o = out if out is not None else {}
+    o.setdefault("c", torch.empty(B, dtype=torch.float32, device=dev))
+    o.setdefault("cont", torch.empty(B, dtype=torch.uint8, device=dev))
+    o.setdefault("flags", torch.empty(B, dtype=torch.uint8, device=dev))
+    if want_row_lse:
+        o.setdefault("row_lse", torch.empty((B, k), dtype=torch.float32, device=dev))
+    need = lib().dflash_gate_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(dev, need)
+    rc = lib().dflash_gate(
+        ctypes.byref(dims), ctypes.c_float(temperature), ctypes.c_float(g), _dev(draft_logits, "draft_logits"),
+        _dev(tokens, "tokens", torch.int64, (B, k)), _opt(active, "active", torch.uint8, (B,)),
+        _dev(o["c"], "c", torch.float32), _dev(o["cont"], "cont", torch.uint8),
+        _opt(o.get("row_lse"), "row_lse", torch.float32), _opt(o.get("flags"), "flags", torch.uint8),
+        w.data_ptr(), w.numel(), _stream(dev))
+    _check(rc)
+    return o

@@ -1,0 +1,183 @@
+// C ABI of libdflash: host-side validation, workspace layout and dispatch.
+// Nothing here allocates device memory; every call is asynchronous on the
+// caller's stream.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/dflash.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+thread_local int g_launches = 0;
+
+// Kernel plans are sized for the 152-SM GB300 so that workspace sizes depend on
+// the dims alone (no device query, callable without a GPU).
+constexpr int kPlanSms = 152;
+constexpr int kMaxCounters = DFLASH_WS_COUNTER_BYTES / 4;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int ok(int launches) {
+  g_err.clear();
+  g_launches = launches;
+  return DFLASH_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool bad_dtype(int dt) { return dt != DFLASH_F32 && dt != DFLASH_BF16; }
+
+int check_ws(void* ws, size_t have, size_t need) {
+  if (need > 0 && ws == nullptr) return fail(DFLASH_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", need);
+  if (have < need) return fail(DFLASH_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", have, need);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(DFLASH_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  return DFLASH_OK;
+}
+
+int check_verify_dims(const dflash_verify_dims* d, bool sampled) {
+  if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->n_max < 0 || d->V < 1) return fail(DFLASH_ERR_INVALID_ARG, "bad dims B=%d n_max=%d V=%d", d->B, d->n_max, d->V);
+  if (bad_dtype(d->dtype)) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
+  if (d->n_max + 1 > 256) return fail(DFLASH_ERR_UNSUPPORTED, "n_max=%d > 255", d->n_max);
+  if ((sampled ? 2 : 1) * d->B > kMaxCounters) return fail(DFLASH_ERR_UNSUPPORTED, "B=%d too large", d->B);
+  if ((long)d->B * (2L * d->n_max + 1) > 65535L) return fail(DFLASH_ERR_UNSUPPORTED, "B*(2*n_max+1) > 65535");
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_last_error(void) { return g_err.c_str(); }
+int dflash_last_launch_count(void) { return g_launches; }
+
+// ------------------------------------------------------------------ verify ---
+size_t dflash_verify_greedy_workspace_size(const dflash_verify_dims* d) {
+  if (check_verify_dims(d, false) != DFLASH_OK) return 0;
+  return DFLASH_WS_COUNTER_BYTES + dflash::verify_greedy_ws_bytes(d->B, d->n_max, d->V, d->dtype, kPlanSms);
+}
+
+int dflash_verify_greedy(const dflash_verify_dims* d, const void* target_logits, const int64_t* cand,
+                         const int32_t* n_draft, int32_t* accept_len, int64_t* bonus,
+                         int32_t* commit_len, int64_t* out_tokens, int64_t* target_pred,
+                         void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_verify_dims(d, false);
+  if (rc) return rc;
+  if (!target_logits || !cand || !accept_len || !bonus || !commit_len)
+    return fail(DFLASH_ERR_INVALID_ARG, "verify_greedy: a required pointer is NULL");
+  rc = check_ws(workspace, ws_bytes, dflash_verify_greedy_workspace_size(d));
+  if (rc) return rc;
+  dflash::VerifyArgs a{};
+  a.B = d->B; a.n_max = d->n_max; a.V = d->V; a.dtype = d->dtype; a.temperature = 1.f;
+  a.target_logits = target_logits; a.cand = cand; a.n_draft = n_draft;
+  a.accept_len = accept_len; a.bonus = bonus; a.commit_len = commit_len;
+  a.out_tokens = out_tokens; a.target_pred = target_pred;
+  a.counters = (int32_t*)workspace;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = dflash::launch_verify_greedy(a, kPlanSms);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_greedy launch");
+  return ok(1);
+}
+
+size_t dflash_verify_sample_workspace_size(const dflash_verify_dims* d) {
+  if (check_verify_dims(d, true) != DFLASH_OK) return 0;
+  return DFLASH_WS_COUNTER_BYTES + dflash::verify_sample_ws_bytes(d->B, d->n_max, d->V, d->dtype, kPlanSms);
+}
+
+int dflash_verify_sample(const dflash_verify_dims* d, float temperature, const void* target_logits,
+                         const void* draft_logits, const int64_t* cand, const int32_t* n_draft,
+                         const float* u_accept, const float* u_final, int32_t* accept_len,
+                         int64_t* bonus, int32_t* commit_len, int64_t* out_tokens, uint8_t* flags,
+                         float* probs, void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_verify_dims(d, true);
+  if (rc) return rc;
+  if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
+  if (!target_logits || !cand || !u_final || !accept_len || !bonus || !commit_len ||
+      (d->n_max > 0 && (!draft_logits || !u_accept)))
+    return fail(DFLASH_ERR_INVALID_ARG, "verify_sample: a required pointer is NULL");
+  rc = check_ws(workspace, ws_bytes, dflash_verify_sample_workspace_size(d));
+  if (rc) return rc;
+  dflash::VerifyArgs a{};
+  a.B = d->B; a.n_max = d->n_max; a.V = d->V; a.dtype = d->dtype; a.temperature = temperature;
+  a.target_logits = target_logits; a.draft_logits = draft_logits; a.cand = cand;
+  a.n_draft = n_draft; a.u_accept = u_accept; a.u_final = u_final;
+  a.accept_len = accept_len; a.bonus = bonus; a.commit_len = commit_len;
+  a.out_tokens = out_tokens; a.flags = flags; a.probs = probs;
+  a.counters = (int32_t*)workspace;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = dflash::launch_verify_sample(a, kPlanSms);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_sample launch");
+  return ok(2);
+}
+
+// -------------------------------------------------------------------- gate ---
+static int check_gate_dims(const dflash_gate_dims* d) {
+  if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->k < 1 || d->V < 1) return fail(DFLASH_ERR_INVALID_ARG, "bad dims B=%d k=%d V=%d", d->B, d->k, d->V);
+  if (bad_dtype(d->dtype)) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
+  if (d->k > 256) return fail(DFLASH_ERR_UNSUPPORTED, "k=%d > 256", d->k);
+  if (d->B > kMaxCounters) return fail(DFLASH_ERR_UNSUPPORTED, "B=%d too large", d->B);
+  if ((long)d->B * d->k > 65535L) return fail(DFLASH_ERR_UNSUPPORTED, "B*k > 65535");
+  return DFLASH_OK;
+}
+
+size_t dflash_gate_workspace_size(const dflash_gate_dims* d) {
+  if (check_gate_dims(d) != DFLASH_OK) return 0;
+  return DFLASH_WS_COUNTER_BYTES + dflash::gate_ws_bytes(d->B, d->k, d->V, d->dtype, kPlanSms);
+}
+
+int dflash_gate(const dflash_gate_dims* d, float temperature, float g, const void* draft_logits,
+                const int64_t* tokens, const uint8_t* active, float* c_s, uint8_t* cont,
+                float* row_lse, uint8_t* flags, void* workspace, size_t ws_bytes,
+                dflash_stream_t stream) {
+  int rc = check_gate_dims(d);
+  if (rc) return rc;
+  if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
+  if (!draft_logits || !tokens || !c_s || !cont) return fail(DFLASH_ERR_INVALID_ARG, "gate: a required pointer is NULL");
+  rc = check_ws(workspace, ws_bytes, dflash_gate_workspace_size(d));
+  if (rc) return rc;
+  dflash::GateArgs a{};
+  a.B = d->B; a.k = d->k; a.V = d->V; a.dtype = d->dtype; a.temperature = temperature; a.g = g;
+  a.draft_logits = draft_logits; a.tokens = tokens; a.active = active;
+  a.c_s = c_s; a.cont = cont; a.row_lse = row_lse; a.flags = flags;
+  a.counters = (int32_t*)workspace;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = dflash::launch_gate(a, kPlanSms);
+  if (e != cudaSuccess) return cuda_fail(e, "gate launch");
+  return ok(1);
+}
+
+}  // extern "C"
+
+// Placeholders replaced as the attention and materialisation kernels land.
+extern "C" {
+size_t dflash_block_attn_workspace_size(const dflash_attn_dims*) { return 0; }
+int dflash_block_attn(const dflash_attn_dims*, const void*, const void*, const void*, const void*,
+                      const void*, const int32_t*, const int32_t*, float, void*, void*, size_t,
+                      dflash_stream_t) {
+  return fail(DFLASH_ERR_UNSUPPORTED, "block_attn not available in this build");
+}
+size_t dflash_materialize_workspace_size(const dflash_ctx_kv_dims*) { return 0; }
+int dflash_materialize_ctx_kv(const dflash_ctx_kv_dims*, const void*, const int32_t*, const int32_t*,
+                              const void*, const void*, const void*, const void*, float, float,
+                              void* const*, void* const*, const int32_t*, int32_t*, void*, size_t,
+                              dflash_stream_t) {
+  return fail(DFLASH_ERR_UNSUPPORTED, "materialize not available in this build");
+}
+}

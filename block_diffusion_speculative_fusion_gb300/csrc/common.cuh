@@ -1,0 +1,117 @@
+// Shared device helpers of the DFlash kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+namespace dflash {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of logits, unpacked to fp32
+// ---------------------------------------------------------------------------
+template <typename T> struct VecTraits;
+template <> struct VecTraits<float> { static constexpr int N = 4; };
+template <> struct VecTraits<bf16> { static constexpr int N = 8; };
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Streaming 16-byte load that does not allocate in L1 (every logit is read once).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& u, float* f);
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<bf16>(const uint4& u, float* f) {
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+
+__device__ __forceinline__ float ld_scalar(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ld_scalar(const bf16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------------------
+// Completion tickets: the last CTA of a group does the group's epilogue.
+// Every thread has already written its part of the CTA's partial results; each
+// publishes its writes with a device-scope fence, then thread 0 takes a ticket.
+// Readers in the last CTA must load partials through L2 (__ldcg). No CTA waits.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool take_ticket_is_last(int32_t* counter, int group_size) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = atomicAdd(counter, 1);
+    s_last = (t == group_size - 1);
+  }
+  __syncthreads();
+  const bool last = s_last != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+__device__ __forceinline__ void reset_ticket(int32_t* counter) {
+  if (threadIdx.x == 0) atomicExch(counter, 0);
+}
+
+// ---------------------------------------------------------------------------
+// Online max / scaled-sum pairs: s = sum exp2((z - m) * k)
+// ---------------------------------------------------------------------------
+struct MS { float m; float s; };
+
+__device__ __forceinline__ MS ms_merge(MS a, MS b, float k2) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -CUDART_INF_F) return MS{M, 0.f};
+  const float sa = (a.m == -CUDART_INF_F) ? 0.f : a.s * exp2f((a.m - M) * k2);
+  const float sb = (b.m == -CUDART_INF_F) ? 0.f : b.s * exp2f((b.m - M) * k2);
+  return MS{M, sa + sb};
+}
+
+__device__ __forceinline__ MS warp_ms(MS v, float k2) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
+    v = ms_merge(v, w, k2);
+  }
+  return v;
+}
+
+// (value, index) maximum with the lowest index among equal values.
+struct VI { float v; int32_t i; };
+
+__device__ __forceinline__ bool vi_better(float v, int32_t i, const VI& b) {
+  return v > b.v || (v == b.v && i < b.i);
+}
+
+__device__ __forceinline__ VI warp_vi(VI a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    VI w{__shfl_xor_sync(0xffffffffu, a.v, o), __shfl_xor_sync(0xffffffffu, a.i, o)};
+    if (vi_better(w.v, w.i, a)) a = w;
+  }
+  return a;
+}
+
+}  // namespace dflash

@@ -1,0 +1,66 @@
+// Internal interface between the C ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dflash {
+
+inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
+
+struct ChunkPlan {
+  int chunk;   // elements per chunk (multiple of one 16-byte vector per thread)
+  int nch;     // chunks per row
+};
+
+ChunkPlan plan_chunks(int rows, int V, int dtype, int num_sms);
+int resample_chunks(int V, int dtype);
+
+// ---------------------------------------------------------------- verify ---
+struct VerifyArgs {
+  int B, n_max, V, dtype;
+  float temperature;
+  const void* target_logits;
+  const void* draft_logits;
+  const int64_t* cand;
+  const int32_t* n_draft;
+  const float* u_accept;
+  const float* u_final;
+  int32_t* accept_len;
+  int64_t* bonus;
+  int32_t* commit_len;
+  int64_t* out_tokens;
+  int64_t* target_pred;
+  uint8_t* flags;
+  float* probs;
+  int32_t* counters;   // zeroed region at the workspace start
+  void* scratch;       // workspace after the counter region
+  cudaStream_t stream;
+};
+
+size_t verify_greedy_ws_bytes(int B, int n_max, int V, int dtype, int num_sms);
+size_t verify_sample_ws_bytes(int B, int n_max, int V, int dtype, int num_sms);
+cudaError_t launch_verify_greedy(const VerifyArgs& a, int num_sms);
+cudaError_t launch_verify_sample(const VerifyArgs& a, int num_sms);
+
+// ------------------------------------------------------------------ gate ---
+struct GateArgs {
+  int B, k, V, dtype;
+  float temperature, g;
+  const void* draft_logits;
+  const int64_t* tokens;
+  const uint8_t* active;
+  float* c_s;
+  uint8_t* cont;
+  float* row_lse;
+  uint8_t* flags;
+  int32_t* counters;
+  void* scratch;
+  cudaStream_t stream;
+};
+
+size_t gate_ws_bytes(int B, int k, int V, int dtype, int num_sms);
+cudaError_t launch_gate(const GateArgs& a, int num_sms);
+
+}  // namespace dflash

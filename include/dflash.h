@@ -1,0 +1,264 @@
+/*
+ * dflash.h -- C ABI of the GB300 (sm_103a) DFlash hot path.
+ *
+ * Five operations of one block-diffusion speculative-decoding step, each a
+ * hand-written CUDA kernel sequence:
+ *   dflash_materialize_ctx_kv  target-context K/V materialisation into the paged
+ *                              draft KV cache of every draft layer
+ *   dflash_block_attn          the draft block's bidirectional (unmasked) GQA
+ *                              attention over [context K/V ; block K/V]
+ *   dflash_verify_greedy       the greedy accept rule over the vocabulary
+ *   dflash_verify_sample       the min(1, p/q) accept rule with residual resample
+ *   dflash_gate                the DLoop block gate c_s >= g
+ *
+ * Conventions shared by every call:
+ *   - Tensor arguments are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them. Shapes are row-major with the last
+ *     dimension contiguous, as stated per argument.
+ *   - Scratch memory is a caller-owned device workspace of at least
+ *     dflash_*_workspace_size(dims) bytes, 256-byte aligned. Its first
+ *     DFLASH_WS_COUNTER_BYTES bytes hold completion counters: they must be zero
+ *     before a workspace is first used (e.g. allocate it zeroed) and every call
+ *     that completes leaves them zero again. One workspace may serve any number
+ *     of calls issued in order on one stream; calls that overlap on the GPU
+ *     must use different workspaces.
+ *   - Every call is asynchronous on the given stream and performs no host
+ *     synchronisation. Outputs are valid once the stream reaches that point.
+ *   - Return value: DFLASH_OK, or an error code with a message available from
+ *     dflash_last_error() (thread-local). Argument errors are detected on the
+ *     host before anything is launched; DFLASH_ERR_CUDA reports a launch error.
+ *   - dtype selects the element type of every floating-point tensor of the
+ *     call: DFLASH_F32 (float) or DFLASH_BF16 (bfloat16). Accumulation is fp32.
+ *
+ * Citations name the source page and its section:
+ *   [DFlash]  "DFlash 块扩散解码：以并行扩散替代自回归草稿" -- sections 块扩散,
+ *             KV 注入, 验证流程.
+ *   [SGLang]  "详解SGlang 最新DFlash投机解码算法的工程实现" -- section 3 (decode,
+ *             greedy rule), 4.1 (KV materialisation), 5.1 (KV headroom).
+ *   [SpecDec] "让大模型快 8 倍：从投机解码到 DDTree" -- sections 3 and 4.
+ *   [DLoop]   "DLoop 完全拆解" -- 机制一 (confidence gate) and the looped verify.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* dflash_stream_t;
+
+enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shape */
+  DFLASH_ERR_UNSUPPORTED = 2,   /* valid but outside the compiled kernels */
+  DFLASH_ERR_WORKSPACE = 3,     /* workspace too small or misaligned */
+  DFLASH_ERR_CUDA = 4           /* a CUDA launch or API call failed */
+};
+
+enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
+
+/* Bits of the per-sequence flags of dflash_verify_sample. A flagged sequence's
+ * integer outputs are valid draws but may differ from an exact-arithmetic
+ * evaluation, because a uniform sat within 1e-6 of a decision boundary. */
+enum {
+  DFLASH_FLAG_ACCEPT_BOUNDARY = 1,  /* |u - p(x)/q(x)| < 1e-6 at an evaluated test */
+  DFLASH_FLAG_CDF_BOUNDARY = 2,     /* u_final within 1e-6 of a CDF step */
+  DFLASH_FLAG_DEGENERATE = 4,       /* zero residual mass; bonus drawn from p */
+  DFLASH_FLAG_INVALID = 8           /* q(x) == 0: candidate was not drawn from q */
+};
+
+/* Bit of the per-sequence flags of dflash_gate: |c_s - g| < 1e-4. */
+enum { DFLASH_FLAG_GATE_BOUNDARY = 1 };
+
+#define DFLASH_WS_COUNTER_BYTES 16384
+
+/* ------------------------------------------------------------------------- */
+/* (a) Target-context KV materialisation                                      */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t B;          /* sequences */
+  int32_t rows_max;   /* rows per sequence in `hidden` (>= every commit_len) */
+  int32_t m;          /* captured target layers */
+  int32_t d;          /* d_model */
+  int32_t L;          /* draft layers (1..16) */
+  int32_t Hkv;        /* kv heads of a draft layer */
+  int32_t D;          /* head dim (even) */
+  int32_t page_size;  /* rows per KV page */
+  int32_t max_pages;  /* row stride of page_table */
+  int32_t num_pages;  /* pages in every pool; table entries must be < num_pages */
+  int32_t dtype;      /* DFLASH_F32 | DFLASH_BF16 */
+} dflash_ctx_kv_dims;
+
+/*
+ * Writes, for every sequence b and every row j < commit_len[b], the context K/V
+ * of all L draft layers into the paged pools; no other pool row is touched.
+ *
+ *   h_ctx = W_f [h_l1; ...; h_lm] + b_f              [DFlash] KV 注入, step 2
+ *   K^(l) = W_K^(l) h_ctx,  V^(l) = W_V^(l) h_ctx    [DFlash] KV 注入, step 3
+ *   K^(l) <- k_norm, then RoPE at position start_pos[b] + j, then a
+ *   prefix-valid write of the first commit_len[b] rows  [SGLang] 4.1
+ *   slot of position p: page_table[b][p / page_size] * page_size + p % page_size
+ *                                                     [SGLang] 5.1
+ *
+ * hidden     [B, rows_max, m*d]  captured target hidden of each candidate row
+ * commit_len [B] int32  rows to write, 0 <= commit_len[b] <= rows_max
+ * start_pos  [B] int32  absolute position of row 0 (the committed prefix length)
+ * W_f [d, m*d], b_f [d] (nullable: no bias); stored [out, in]
+ * W_kv       [L, 2, Hkv*D, d]  K then V projection of each draft layer, [out, in]
+ * k_norm_w   [L, D] or NULL. Non-null: K <- K / sqrt(mean(K^2) + rms_eps) * w over D
+ * rope_theta  > 0: rotate-half RoPE, pair (i, i + D/2) turned by
+ *             pos * rope_theta^(-2i/D); 0 disables RoPE
+ * k_pools, v_pools  HOST arrays of L device pointers, each [num_pages, page_size, Hkv, D]
+ * page_table [B, max_pages] int32
+ * new_len    [B] int32 or NULL: start_pos[b] + commit_len[b]; must not alias start_pos
+ *
+ * bf16 calls round h_ctx to bf16 before the K/V projection. Positions whose
+ * page index is >= max_pages or whose page is outside [0, num_pages) are
+ * skipped, not written.
+ */
+size_t dflash_materialize_workspace_size(const dflash_ctx_kv_dims* dims);
+int dflash_materialize_ctx_kv(const dflash_ctx_kv_dims* dims,
+                              const void* hidden, const int32_t* commit_len,
+                              const int32_t* start_pos,
+                              const void* W_f, const void* b_f, const void* W_kv,
+                              const void* k_norm_w, float rms_eps, float rope_theta,
+                              void* const* k_pools, void* const* v_pools,
+                              const int32_t* page_table, int32_t* new_len,
+                              void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* (b) Draft block attention                                                  */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t B;          /* sequences */
+  int32_t n_q;        /* query rows of the block (k) */
+  int32_t n_kv_blk;   /* the block's own K/V rows (k, plus rows a looped stage appends) */
+  int32_t Hq, Hkv, D; /* Hq % Hkv == 0 */
+  int32_t page_size;
+  int32_t max_pages;  /* row stride of page_table */
+  int32_t num_pages;
+  int32_t max_ctx;    /* upper bound on every ctx_len[b] (sizes the launch) */
+  int32_t dtype;
+} dflash_attn_dims;
+
+/*
+ * out = softmax(scale * Q K^T) V with no mask, where for sequence b the keys and
+ * values are the ctx_len[b] context rows of the paged pools followed by the
+ * n_kv_blk rows of the block; q-head h reads kv-head h / (Hq / Hkv).
+ *   [DFlash] 块扩散: the draft attends bidirectionally inside the block;
+ *   [DFlash] KV 注入, step 3: Attention(Q_draft, [K_draft; K_ctx], [V_draft; V_ctx]).
+ *
+ * q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv_blk, Hkv, D]
+ * k_pool, v_pool  one draft layer's pools [num_pages, page_size, Hkv, D]
+ * page_table [B, max_pages] int32; ctx_len [B] int32, 0 <= ctx_len[b] <= max_ctx
+ * scale: softmax scale (1/sqrt(D) for the standard form)
+ * out [B, n_q, Hq, D]
+ */
+size_t dflash_block_attn_workspace_size(const dflash_attn_dims* dims);
+int dflash_block_attn(const dflash_attn_dims* dims,
+                      const void* q, const void* k_blk, const void* v_blk,
+                      const void* k_pool, const void* v_pool,
+                      const int32_t* page_table, const int32_t* ctx_len, float scale,
+                      void* out, void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* (c) Verify                                                                 */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t B;      /* sequences */
+  int32_t n_max;  /* maximum drafts per sequence (row stride of cand is n_max+1) */
+  int32_t V;      /* vocabulary */
+  int32_t dtype;  /* type of the logits */
+} dflash_verify_dims;
+
+/*
+ * Greedy rule, [SGLang] 3 and [DFlash] 验证流程:
+ *   target_pred[i] = argmax_v target_logits[b, i, v]   (lowest index among ties)
+ *   accept_len = number of leading i < n_b with cand[b, i+1] == target_pred[i]
+ *   bonus = target_pred[accept_len];  commit_len = accept_len + 1
+ *   out_tokens = cand[b, 1..accept_len] followed by bonus, then -1 padding.
+ *
+ * target_logits [B, n_max+1, V]; cand [B, n_max+1] int64, cand[:, 0] the anchor
+ * n_draft [B] int32 in [0, n_max], or NULL for n_max everywhere
+ * accept_len, commit_len [B] int32; bonus [B] int64
+ * out_tokens [B, n_max+1] int64 or NULL; target_pred [B, n_max+1] int64 or NULL
+ *   (argmax of rows 0..n_b, -1 beyond)
+ */
+size_t dflash_verify_greedy_workspace_size(const dflash_verify_dims* dims);
+int dflash_verify_greedy(const dflash_verify_dims* dims,
+                         const void* target_logits, const int64_t* cand,
+                         const int32_t* n_draft,
+                         int32_t* accept_len, int64_t* bonus, int32_t* commit_len,
+                         int64_t* out_tokens, int64_t* target_pred,
+                         void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/*
+ * Sampled rule, [SpecDec] 3 and 4, [DLoop] looped verify:
+ *   p_r = softmax(target_logits[b, r] / T), q_r = softmax(draft_logits[b, r] / T)
+ *   for i = 1..n_b: x = cand[b, i]; accept iff u_accept[b, i-1] < p_{i-1}(x) / q_{i-1}(x);
+ *   stop at the first rejection (later drafts are discarded).
+ *   On a rejection at draft i: bonus ~ max(0, p_{i-1} - q_{i-1}) / Z with
+ *   Z = sum_y max(0, p_{i-1}(y) - q_{i-1}(y)) (= 1 - beta); if all n_b are
+ *   accepted: bonus ~ p_{n_b}. The draw is the inverse CDF in ascending token
+ *   order: the smallest y with C(y) > u_final[b] * Z. If Z == 0 the draw uses p.
+ *
+ * target_logits [B, n_max+1, V]; draft_logits [B, n_max, V] (row i-1 is the law
+ *   cand[b, i] was drawn from); cand [B, n_max+1] int64; n_draft [B] or NULL
+ * u_accept [B, n_max] float, u_final [B] float: uniforms on [0, 1)
+ * temperature > 0
+ * accept_len, commit_len [B] int32; bonus [B] int64; out_tokens [B, n_max+1] int64
+ *   or NULL; flags [B] uint8 or NULL (DFLASH_FLAG_* bits)
+ * probs [B, 2*n_max + 1] float or NULL: p(x_i) for i = 1..n_max, then q(x_i),
+ *   then the mass Z of the distribution the bonus was drawn from (1 for p).
+ *   Entries of draft positions that were not evaluated are 0.
+ */
+size_t dflash_verify_sample_workspace_size(const dflash_verify_dims* dims);
+int dflash_verify_sample(const dflash_verify_dims* dims, float temperature,
+                         const void* target_logits, const void* draft_logits,
+                         const int64_t* cand, const int32_t* n_draft,
+                         const float* u_accept, const float* u_final,
+                         int32_t* accept_len, int64_t* bonus, int32_t* commit_len,
+                         int64_t* out_tokens, uint8_t* flags, float* probs,
+                         void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* DLoop block gate                                                           */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t B;      /* sequences */
+  int32_t k;      /* drafted tokens of the stage's block */
+  int32_t V;
+  int32_t dtype;  /* type of the logits */
+} dflash_gate_dims;
+
+/*
+ * [DLoop] 机制一: c_s = sum_{i<k} log softmax(draft_logits[b, i] / T)[tokens[b, i]];
+ * cont = (c_s >= g). Inactive sequences (active[b] == 0) get c = 0, cont = 0.
+ *
+ * draft_logits [B, k, V]; tokens [B, k] int64; active [B] uint8 or NULL (all active)
+ * c_s [B] float; cont [B] uint8; row_lse [B, k] float or NULL (LSE of row / T);
+ * flags [B] uint8 or NULL (DFLASH_FLAG_GATE_BOUNDARY)
+ */
+size_t dflash_gate_workspace_size(const dflash_gate_dims* dims);
+int dflash_gate(const dflash_gate_dims* dims, float temperature, float g,
+                const void* draft_logits, const int64_t* tokens, const uint8_t* active,
+                float* c_s, uint8_t* cont, float* row_lse, uint8_t* flags,
+                void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Diagnostics                                                                */
+/* ------------------------------------------------------------------------- */
+/* Message of the last error on this thread ("" if none). */
+const char* dflash_last_error(void);
+/* Number of kernel launches (memsets included) the last successful call on this
+ * thread enqueued. */
+int dflash_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

@@ -1,0 +1,93 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+symbol the header declares, sizes workspaces from dims alone, and rejects bad
+arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_diffusion_speculative_fusion_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return api.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(dflash_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_functions()
+    assert len(names) >= 12
+    for n in sorted(names):
+        assert hasattr(L, n), n
+    # the binding binds every declared symbol with a signature
+    assert names <= set(api._SIGS), names - set(api._SIGS)
+
+
+def test_workspace_sizes_need_no_gpu(L):
+    d = api.VerifyDims(64, 15, 128256, api.BF16)
+    g = L.dflash_verify_greedy_workspace_size(ctypes.byref(d))
+    s = L.dflash_verify_sample_workspace_size(ctypes.byref(d))
+    assert g > api.WS_COUNTER_BYTES and s > g
+    gd = api.GateDims(32, 7, 151936, api.BF16)
+    assert L.dflash_gate_workspace_size(ctypes.byref(gd)) > api.WS_COUNTER_BYTES
+    bad = api.VerifyDims(0, 15, 100, api.BF16)
+    assert L.dflash_verify_greedy_workspace_size(ctypes.byref(bad)) == 0
+    assert "bad dims" in api.last_error()
+
+
+def _p(x):
+    return ctypes.c_void_p(x)
+
+
+def test_verify_rejects_bad_arguments_before_launch(L):
+    d = api.VerifyDims(2, 3, 100, api.BF16)
+    ws_need = L.dflash_verify_greedy_workspace_size(ctypes.byref(d))
+    fake = 0x10000   # never dereferenced: every call below fails validation first
+    args = [_p(fake)] * 5 + [None, None]
+    rc = L.dflash_verify_greedy(ctypes.byref(d), None, *args, _p(fake), ws_need, None)
+    assert rc == api.ERR_INVALID_ARG and "NULL" in api.last_error()
+    rc = L.dflash_verify_greedy(ctypes.byref(d), _p(fake), *args, None, ws_need, None)
+    assert rc == api.ERR_WORKSPACE
+    rc = L.dflash_verify_greedy(ctypes.byref(d), _p(fake), *args, _p(fake), ws_need - 1, None)
+    assert rc == api.ERR_WORKSPACE and "required" in api.last_error()
+    rc = L.dflash_verify_greedy(ctypes.byref(d), _p(fake), *args, _p(fake + 8), ws_need, None)
+    assert rc == api.ERR_WORKSPACE and "aligned" in api.last_error()
+    d2 = api.VerifyDims(2, 300, 100, api.BF16)
+    rc = L.dflash_verify_greedy(ctypes.byref(d2), _p(fake), *args, _p(fake), 1 << 30, None)
+    assert rc == api.ERR_UNSUPPORTED
+    d3 = api.VerifyDims(2, 3, 100, 7)
+    rc = L.dflash_verify_greedy(ctypes.byref(d3), _p(fake), *args, _p(fake), 1 << 30, None)
+    assert rc == api.ERR_INVALID_ARG and "dtype" in api.last_error()
+
+
+def test_sample_and_gate_reject_bad_temperature(L):
+    d = api.VerifyDims(2, 3, 100, api.F32)
+    fake = _p(0x10000)
+    rc = L.dflash_verify_sample(ctypes.byref(d), ctypes.c_float(0.0), *([fake] * 13), 1 << 30, None)
+    assert rc == api.ERR_INVALID_ARG and "temperature" in api.last_error()
+    gd = api.GateDims(2, 3, 100, api.F32)
+    rc = L.dflash_gate(ctypes.byref(gd), ctypes.c_float(-1.0), ctypes.c_float(-0.5), *([fake] * 8),
+                       1 << 30, None)
+    assert rc == api.ERR_INVALID_ARG
+
+
+def test_binding_requires_cuda_tensors(L):
+    import torch
+    with pytest.raises((ValueError, TypeError)):
+        api.verify_greedy(torch.zeros(1, 2, 8), torch.zeros(1, 2, dtype=torch.int64))
