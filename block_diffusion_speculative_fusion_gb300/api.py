@@ -264,3 +264,50 @@ def gate(draft_logits: torch.Tensor, tokens: torch.Tensor, temperature: float = 
         w.data_ptr(), w.numel(), _stream(dev))
     _check(rc)
     return o
+
+
+# ---------------------------------------------------------------------------
+# (b) block attention
+# ---------------------------------------------------------------------------
+def block_attn(q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor, k_pool: torch.Tensor,
+               v_pool: torch.Tensor, page_table: torch.Tensor, ctx_len: torch.Tensor,
+               max_ctx: Optional[int] = None, scale: Optional[float] = None,
+               out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Unmasked GQA attention of the draft block over [paged context ; block]
+    (``dflash_block_attn``). q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv, Hkv, D];
+    pools [num_pages, page, Hkv, D]; page_table [B, max_pages] int32; ctx_len [B]
+    int32. ``max_ctx`` bounds every ctx_len (defaults to the page table's
+    capacity)."""
+    _dev(q, "q")
+    B, n_q, Hq, D = q.shape
+    n_kv, Hkv = k_blk.shape[1], k_blk.shape[2]
+    num_pages, page = k_pool.shape[0], k_pool.shape[1]
+    max_pages = page_table.shape[1]
+    if max_ctx is None:
+        max_ctx = max_pages * page
+    dt = _dtype_code(q)
+    for name, t in (("k_blk", k_blk), ("v_blk", v_blk), ("k_pool", k_pool), ("v_pool", v_pool)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have the dtype of q")
+    dims = AttnDims(B, n_q, n_kv, Hq, Hkv, D, page, max_pages, num_pages, int(max_ctx), dt)
+    if out is None:
+        out = torch.empty_like(q)
+    need = lib().dflash_block_attn_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(q.device, need, slot=1)
+    rc = lib().dflash_block_attn(
+        ctypes.byref(dims), _dev(q, "q"), _dev(k_blk, "k_blk", None, (B, n_kv, Hkv, D)),
+        _dev(v_blk, "v_blk", None, (B, n_kv, Hkv, D)), _dev(k_pool, "k_pool", None, (num_pages, page, Hkv, D)),
+        _dev(v_pool, "v_pool", None, (num_pages, page, Hkv, D)),
+        _dev(page_table, "page_table", torch.int32, (B, max_pages)), _dev(ctx_len, "ctx_len", torch.int32, (B,)),
+        ctypes.c_float(scale if scale is not None else D ** -0.5), _dev(out, "out", q.dtype, q.shape),
+        w.data_ptr(), w.numel(), _stream(q.device))
+    _check(rc)
+    return out
+
+
+def device_error_word(ws: torch.Tensor) -> int:
+    """The sticky device-side error word of a workspace (0: no kernel gave up
+    waiting for a copy)."""
+    return int(ws[WS_COUNTER_BYTES - 4:WS_COUNTER_BYTES].view(torch.int32).item())

@@ -16,7 +16,8 @@ thread_local int g_launches = 0;
 // Kernel plans are sized for the 152-SM GB300 so that workspace sizes depend on
 // the dims alone (no device query, callable without a GPU).
 constexpr int kPlanSms = 152;
-constexpr int kMaxCounters = DFLASH_WS_COUNTER_BYTES / 4;
+// The last int of the counter region is a sticky device-side error word.
+constexpr int kMaxCounters = DFLASH_WS_COUNTER_BYTES / 4 - 1;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -163,16 +164,57 @@ int dflash_gate(const dflash_gate_dims* d, float temperature, float g, const voi
   return ok(1);
 }
 
+// --------------------------------------------------------------- attention ---
+static int check_attn_dims(const dflash_attn_dims* d) {
+  if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->n_q < 1 || d->n_kv_blk < 0 || d->Hq < 1 || d->Hkv < 1 || d->D < 2 ||
+      d->page_size < 1 || d->max_pages < 1 || d->num_pages < 1 || d->max_ctx < 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad attention dims");
+  if (d->Hq % d->Hkv) return fail(DFLASH_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", d->Hq, d->Hkv);
+  if (bad_dtype(d->dtype)) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
+  if ((long)d->max_ctx > (long)d->max_pages * d->page_size)
+    return fail(DFLASH_ERR_INVALID_ARG, "max_ctx=%d exceeds max_pages*page_size", d->max_ctx);
+  if (d->D > 256) return fail(DFLASH_ERR_UNSUPPORTED, "D=%d > 256", d->D);
+  if ((long)d->B * d->Hkv > kMaxCounters) return fail(DFLASH_ERR_UNSUPPORTED, "B*Hkv too large");
+  if (d->n_q > 65535 || d->Hq > 65535 || d->B > 65535) return fail(DFLASH_ERR_UNSUPPORTED, "grid too large");
+  return DFLASH_OK;
+}
+
+size_t dflash_block_attn_workspace_size(const dflash_attn_dims* d) {
+  if (check_attn_dims(d) != DFLASH_OK) return 0;
+  return DFLASH_WS_COUNTER_BYTES +
+         dflash::attn_ws_bytes(d->B, d->n_q, d->n_kv_blk, d->Hq, d->Hkv, d->D, d->max_ctx, d->dtype);
+}
+
+int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_blk, const void* v_blk,
+                      const void* k_pool, const void* v_pool, const int32_t* page_table,
+                      const int32_t* ctx_len, float scale, void* out, void* workspace, size_t ws_bytes,
+                      dflash_stream_t stream) {
+  int rc = check_attn_dims(d);
+  if (rc) return rc;
+  if (!q || !k_pool || !v_pool || !page_table || !ctx_len || !out || (d->n_kv_blk > 0 && (!k_blk || !v_blk)))
+    return fail(DFLASH_ERR_INVALID_ARG, "block_attn: a required pointer is NULL");
+  rc = check_ws(workspace, ws_bytes, dflash_block_attn_workspace_size(d));
+  if (rc) return rc;
+  dflash::AttnArgs a{};
+  a.B = d->B; a.n_q = d->n_q; a.n_kv = d->n_kv_blk; a.Hq = d->Hq; a.Hkv = d->Hkv; a.D = d->D;
+  a.page_size = d->page_size; a.max_pages = d->max_pages; a.num_pages = d->num_pages;
+  a.max_ctx = d->max_ctx; a.dtype = d->dtype;
+  a.q = q; a.k_blk = k_blk; a.v_blk = v_blk; a.k_pool = k_pool; a.v_pool = v_pool;
+  a.page_table = page_table; a.ctx_len = ctx_len; a.scale = scale; a.out = out;
+  a.counters = (int32_t*)workspace;
+  a.err = (int*)workspace + kMaxCounters;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = dflash::launch_block_attn(a);
+  if (e != cudaSuccess) return cuda_fail(e, "block_attn launch");
+  return ok(1);
+}
+
 }  // extern "C"
 
-// Placeholders replaced as the attention and materialisation kernels land.
+// Placeholder replaced when the materialisation kernels land.
 extern "C" {
-size_t dflash_block_attn_workspace_size(const dflash_attn_dims*) { return 0; }
-int dflash_block_attn(const dflash_attn_dims*, const void*, const void*, const void*, const void*,
-                      const void*, const int32_t*, const int32_t*, float, void*, void*, size_t,
-                      dflash_stream_t) {
-  return fail(DFLASH_ERR_UNSUPPORTED, "block_attn not available in this build");
-}
 size_t dflash_materialize_workspace_size(const dflash_ctx_kv_dims*) { return 0; }
 int dflash_materialize_ctx_kv(const dflash_ctx_kv_dims*, const void*, const int32_t*, const int32_t*,
                               const void*, const void*, const void*, const void*, float, float,

@@ -63,4 +63,25 @@ struct GateArgs {
 size_t gate_ws_bytes(int B, int k, int V, int dtype, int num_sms);
 cudaError_t launch_gate(const GateArgs& a, int num_sms);
 
+// ------------------------------------------------------------- attention ---
+struct AttnArgs {
+  int B, n_q, n_kv, Hq, Hkv, D, page_size, max_pages, num_pages, max_ctx, dtype;
+  const void* q;
+  const void* k_blk;
+  const void* v_blk;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* page_table;
+  const int32_t* ctx_len;
+  float scale;
+  void* out;
+  int32_t* counters;
+  int* err;
+  void* scratch;
+  cudaStream_t stream;
+};
+
+size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int dtype);
+cudaError_t launch_block_attn(const AttnArgs& a);
+
 }  // namespace dflash

@@ -1,0 +1,133 @@
+"""GPU parity of the draft block attention against the CPU oracle (max-abs
+2e-2 for bf16 I/O with fp32 accumulation; 1e-4 for the fp32 path)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_diffusion_speculative_fusion_gb300 import api, synth
+from block_diffusion_speculative_fusion_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_diffusion_speculative_fusion_gb300 import build
+    build.build()
+    api.lib()
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _case(wl, ctx, seed=0, n_q=None, n_kv=None, page=None, headroom=16, nan_tail=False):
+    import dataclasses
+    kw = {}
+    if n_q is not None:
+        kw["k"] = n_q
+    if page is not None:
+        kw["page_size"] = page
+    w = dataclasses.replace(wl, B=len(ctx), **kw)
+    ctx_len = torch.tensor(ctx, dtype=torch.int32)
+    cache = synth.paged_cache(w, headroom=headroom, seed=seed, layers=1, ctx_len=ctx_len)
+    blk = synth.block_qkv(w, 0, seed=seed, n_kv_blk=n_kv)
+    if nan_tail:
+        # rows past each context hold NaN: the kernel must mask them completely
+        P = w.page_size
+        for b, c in enumerate(ctx):
+            for pos in range(c, cache.max_pages * P):
+                pg = int(cache.page_table[b, pos // P])
+                if pg >= 0:
+                    cache.k_pools[0][pg, pos % P] = float("nan")
+                    cache.v_pools[0][pg, pos % P] = float("nan")
+    return w, cache, blk
+
+
+def _run(w, cache, blk, atol, seqs=None):
+    out = api.block_attn(blk["q"].to(DEV), blk["k_blk"].to(DEV), blk["v_blk"].to(DEV),
+                         cache.k_pools[0].to(DEV), cache.v_pools[0].to(DEV), cache.page_table.to(DEV),
+                         cache.ctx_len.to(DEV))
+    torch.cuda.synchronize()
+    got = f64(out)
+    assert np.all(np.isfinite(got))
+    seqs = range(w.B) if seqs is None else seqs
+    pt = cache.page_table.numpy()
+    for b in seqs:
+        ref = O.block_attn(f64(blk["q"][b:b + 1]), f64(blk["k_blk"][b:b + 1]), f64(blk["v_blk"][b:b + 1]),
+                           f64(cache.k_pools[0]), f64(cache.v_pools[0]), pt[b:b + 1],
+                           cache.ctx_len.numpy()[b:b + 1], w.page_size)
+        err = np.abs(got[b] - ref[0]).max()
+        assert err < atol, (b, err)
+    return got
+
+
+def test_attn_tiny_f32_generic_path():
+    wl = W.TINY_F32
+    w, cache, blk = _case(wl, [32])
+    _run(w, cache, blk, 1e-4)
+
+
+def test_attn_tiny_f32_ragged():
+    w, cache, blk = _case(W.TINY_F32, [0, 5, 31, 77], seed=3)
+    _run(w, cache, blk, 1e-4)
+
+
+@pytest.mark.parametrize("ctx", [[0, 1, 63, 64, 65], [37, 1024, 1100, 2100, 3000]])
+def test_attn_bf16_tiles_splits_and_tails(ctx):
+    w, cache, blk = _case(W.LLAMA8B_B64, ctx, seed=1)
+    _run(w, cache, blk, 2e-2)
+
+
+def test_attn_bf16_block_of_ten_m40():
+    w, cache, blk = _case(W.LLAMA8B_B1, [2048, 700], seed=2)
+    _run(w, cache, blk, 2e-2)
+
+
+@pytest.mark.parametrize("stage", [1, 3])
+def test_attn_bf16_dloop_stage_extra_rows(stage):
+    wl = W.DLOOP_QWEN3_4B
+    w, cache, blk = _case(wl, [1024, 1031, 500], seed=4, n_kv=wl.k + stage - 1)
+    _run(w, cache, blk, 2e-2)
+
+
+@pytest.mark.parametrize("page", [8, 32, 64])
+def test_attn_bf16_page_sizes(page):
+    w, cache, blk = _case(W.QWEN3_4B_B8, [1024, 333, 2049], seed=5, page=page)
+    _run(w, cache, blk, 2e-2)
+
+
+def test_attn_bf16_masks_garbage_past_context():
+    w, cache, blk = _case(W.LLAMA8B_B64, [17, 1030, 64], seed=6, headroom=80, nan_tail=True)
+    _run(w, cache, blk, 2e-2)
+
+
+def test_attn_bf16_generic_fallback_shape():
+    # D = 64 is outside the tensor-core kernel: the generic kernel serves it
+    import dataclasses
+    wl = dataclasses.replace(W.QWEN3_4B_B8, D=64)
+    w, cache, blk = _case(wl, [100, 300], seed=7)
+    _run(w, cache, blk, 2e-2)
+
+
+def test_attn_full_size_batched_llama8b_b64_sampled_sequences():
+    wl = W.LLAMA8B_B64
+    ctx_len = synth.ctx_lengths(wl, 0)
+    cache = synth.paged_cache(wl, headroom=16, seed=0, layers=1, ctx_len=ctx_len)
+    blk = synth.block_qkv(wl, 0, seed=0)
+    order = np.argsort(ctx_len.numpy())
+    seqs = [int(order[0]), int(order[len(order) // 2]), int(order[-1]), 5]
+    _run(wl, cache, blk, 2e-2, seqs=seqs)
+
+
+def test_attn_deterministic_and_error_word_clear():
+    w, cache, blk = _case(W.LLAMA8B_B64, [1500, 4000], seed=8)
+    args = [blk["q"].to(DEV), blk["k_blk"].to(DEV), blk["v_blk"].to(DEV), cache.k_pools[0].to(DEV),
+            cache.v_pools[0].to(DEV), cache.page_table.to(DEV), cache.ctx_len.to(DEV)]
+    ws = api.workspace(torch.device(DEV), 1 << 26, slot=7)
+    a = api.block_attn(*args, ws=ws).clone()
+    b = api.block_attn(*args, ws=ws)
+    assert torch.equal(a, b)
+    assert api.device_error_word(ws) == 0

