@@ -476,7 +476,7 @@ cudaError_t launch_block_attn(const AttnArgs& a) {
                          strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_pool), dims,
                          strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+    return cudaErrorNotSupported;   // tensor-map encoding refused the pool layout
   AttnParams p;
   p.q = (const bf16*)a.q;
   p.k_blk = (const bf16*)a.k_blk;
@@ -499,10 +499,11 @@ cudaError_t launch_block_attn(const AttnArgs& a) {
   p.err = a.err;
   const int nwarps = (M + 15) / 16;
   const size_t smem = 1024 + kStages * 2 * kTileBytes + kStages * 8;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    attr_set = true;
+  static size_t smem_set = 0;   // largest dynamic shared memory opted into so far
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
   }
   dim3 grid(p.max_splits, a.Hkv, a.B);
   attn_bf16_kernel<<<grid, nwarps * 32, smem, a.stream>>>(kmap, vmap, p);

@@ -241,7 +241,7 @@ def test_sample_identity_monte_carlo_on_gpu(V):
     lq = rng.normal(0, 1.5, V).astype(np.float32)
     p = np.exp(lp.astype(np.float64) - lp.max()); p /= p.sum()
     q = np.exp(lq.astype(np.float64) - lq.max()); q /= q.sum()
-    B, calls = 2048, 500
+    B, calls = 2000, 512
     zt = torch.from_numpy(np.broadcast_to(lp, (B, 2, V)).copy()).to(DEV)
     zd = torch.from_numpy(np.broadcast_to(lq, (B, 1, V)).copy()).to(DEV)
     counts = np.zeros(V)
