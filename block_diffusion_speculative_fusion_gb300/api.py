@@ -311,3 +311,50 @@ def device_error_word(ws: torch.Tensor) -> int:
     """The sticky device-side error word of a workspace (0: no kernel gave up
     waiting for a copy)."""
     return int(ws[WS_COUNTER_BYTES - 4:WS_COUNTER_BYTES].view(torch.int32).item())
+
+
+# ---------------------------------------------------------------------------
+# (a) context-KV materialisation
+# ---------------------------------------------------------------------------
+def materialize_ctx_kv(hidden: torch.Tensor, commit_len: torch.Tensor, start_pos: torch.Tensor,
+                       W_f: torch.Tensor, b_f: Optional[torch.Tensor], W_kv: torch.Tensor,
+                       k_norm_w: Optional[torch.Tensor], rms_eps: float, rope_theta: float,
+                       k_pools: Sequence[torch.Tensor], v_pools: Sequence[torch.Tensor],
+                       page_table: torch.Tensor, new_len: Optional[torch.Tensor] = None,
+                       ws: Optional[torch.Tensor] = None) -> None:
+    """Write the committed rows' context K/V of every draft layer into the paged
+    pools (``dflash_materialize_ctx_kv``). hidden [B, rows_max, m*d];
+    W_f [d, m*d]; b_f [d] or None; W_kv [L, 2, Hkv*D, d]; k_norm_w [L, D] or
+    None; pools: L tensors [num_pages, page, Hkv, D]; page_table [B, max_pages]."""
+    _dev(hidden, "hidden")
+    B, rows_max, md = hidden.shape
+    d = W_f.shape[0]
+    m = md // d
+    L, two, HD, d2 = W_kv.shape
+    if two != 2 or d2 != d or m * d != md:
+        raise ValueError("inconsistent hidden / W_f / W_kv shapes")
+    if len(k_pools) != L or len(v_pools) != L:
+        raise ValueError("need one K and one V pool per draft layer")
+    num_pages, page, Hkv, D = k_pools[0].shape
+    if Hkv * D != HD:
+        raise ValueError("pool head layout does not match W_kv")
+    dt = _dtype_code(hidden)
+    for name, t in (("W_f", W_f), ("W_kv", W_kv)):
+        if t.dtype != hidden.dtype:
+            raise TypeError(f"{name} must have the dtype of hidden")
+    max_pages = page_table.shape[1]
+    dims = CtxKvDims(B, rows_max, m, d, L, Hkv, D, page, max_pages, num_pages, dt)
+    need = lib().dflash_materialize_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(hidden.device, need, slot=2)
+    kp = (c_p * L)(*[_dev(t, f"k_pools[{i}]", hidden.dtype, (num_pages, page, Hkv, D)) for i, t in enumerate(k_pools)])
+    vp = (c_p * L)(*[_dev(t, f"v_pools[{i}]", hidden.dtype, (num_pages, page, Hkv, D)) for i, t in enumerate(v_pools)])
+    rc = lib().dflash_materialize_ctx_kv(
+        ctypes.byref(dims), _dev(hidden, "hidden"), _dev(commit_len, "commit_len", torch.int32, (B,)),
+        _dev(start_pos, "start_pos", torch.int32, (B,)), _dev(W_f, "W_f", None, (d, md)),
+        _opt(b_f, "b_f", hidden.dtype, (d,)), _dev(W_kv, "W_kv"), _opt(k_norm_w, "k_norm_w", hidden.dtype, (L, D)),
+        ctypes.c_float(rms_eps), ctypes.c_float(rope_theta), ctypes.cast(kp, c_p), ctypes.cast(vp, c_p),
+        _dev(page_table, "page_table", torch.int32, (B, max_pages)), _opt(new_len, "new_len", torch.int32, (B,)),
+        w.data_ptr(), w.numel(), _stream(hidden.device))
+    _check(rc)

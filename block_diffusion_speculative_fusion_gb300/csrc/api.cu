@@ -211,15 +211,61 @@ int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_bl
   return ok(1);
 }
 
-}  // extern "C"
+// ------------------------------------------------------------- materialise ---
+static int check_mat_dims(const dflash_ctx_kv_dims* d) {
+  if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->rows_max < 1 || d->m < 1 || d->d < 1 || d->L < 1 || d->Hkv < 1 || d->D < 2 ||
+      d->page_size < 1 || d->max_pages < 1 || d->num_pages < 1)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad materialise dims");
+  if (d->D % 2) return fail(DFLASH_ERR_INVALID_ARG, "D=%d must be even (RoPE pairs)", d->D);
+  if (bad_dtype(d->dtype)) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
+  if (d->L > dflash::kMaxLayers) return fail(DFLASH_ERR_UNSUPPORTED, "L=%d > %d", d->L, dflash::kMaxLayers);
+  if (d->D > 256) return fail(DFLASH_ERR_UNSUPPORTED, "D=%d > 256", d->D);
+  if ((long)d->B * d->rows_max > 65535L) return fail(DFLASH_ERR_UNSUPPORTED, "B*rows_max > 65535");
+  const long el = d->dtype == DFLASH_BF16 ? 2 : 4;
+  if (((long)d->m * d->d * el) % 16 || ((long)d->d * el) % 16)
+    return fail(DFLASH_ERR_UNSUPPORTED, "rows of hidden and W_kv must be multiples of 16 bytes");
+  return DFLASH_OK;
+}
 
-// Placeholder replaced when the materialisation kernels land.
-extern "C" {
-size_t dflash_materialize_workspace_size(const dflash_ctx_kv_dims*) { return 0; }
-int dflash_materialize_ctx_kv(const dflash_ctx_kv_dims*, const void*, const int32_t*, const int32_t*,
-                              const void*, const void*, const void*, const void*, float, float,
-                              void* const*, void* const*, const int32_t*, int32_t*, void*, size_t,
-                              dflash_stream_t) {
-  return fail(DFLASH_ERR_UNSUPPORTED, "materialize not available in this build");
+size_t dflash_materialize_workspace_size(const dflash_ctx_kv_dims* d) {
+  if (check_mat_dims(d) != DFLASH_OK) return 0;
+  const dflash::MatPlan p = dflash::mat_plan(d->B, d->rows_max, d->m, d->d, d->L, d->Hkv, d->D, d->dtype);
+  return DFLASH_WS_COUNTER_BYTES + dflash::mat_ws_bytes(p, d->dtype);
 }
+
+int dflash_materialize_ctx_kv(const dflash_ctx_kv_dims* d, const void* hidden, const int32_t* commit_len,
+                              const int32_t* start_pos, const void* W_f, const void* b_f, const void* W_kv,
+                              const void* k_norm_w, float rms_eps, float rope_theta, void* const* k_pools,
+                              void* const* v_pools, const int32_t* page_table, int32_t* new_len,
+                              void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_mat_dims(d);
+  if (rc) return rc;
+  if (!hidden || !commit_len || !start_pos || !W_f || !W_kv || !k_pools || !v_pools || !page_table)
+    return fail(DFLASH_ERR_INVALID_ARG, "materialize: a required pointer is NULL");
+  if (new_len && new_len == start_pos) return fail(DFLASH_ERR_INVALID_ARG, "new_len must not alias start_pos");
+  if (rope_theta < 0.f || !(rms_eps >= 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "bad rope_theta or rms_eps");
+  rc = check_ws(workspace, ws_bytes, dflash_materialize_workspace_size(d));
+  if (rc) return rc;
+  dflash::MatArgs a{};
+  a.B = d->B; a.rows_max = d->rows_max; a.m = d->m; a.d = d->d; a.L = d->L; a.Hkv = d->Hkv; a.D = d->D;
+  a.page_size = d->page_size; a.max_pages = d->max_pages; a.num_pages = d->num_pages; a.dtype = d->dtype;
+  a.hidden = hidden; a.commit_len = commit_len; a.start_pos = start_pos; a.W_f = W_f; a.b_f = b_f;
+  a.W_kv = W_kv; a.k_norm_w = k_norm_w; a.rms_eps = rms_eps; a.rope_theta = rope_theta;
+  for (int l = 0; l < d->L; ++l) {
+    if (!k_pools[l] || !v_pools[l]) return fail(DFLASH_ERR_INVALID_ARG, "pool pointer of layer %d is NULL", l);
+    a.pools.k[l] = k_pools[l];
+    a.pools.v[l] = v_pools[l];
+  }
+  a.page_table = page_table; a.new_len = new_len;
+  a.counters = (int32_t*)workspace;
+  a.err = (int*)workspace + kMaxCounters;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  int launches = 0;
+  cudaError_t e = dflash::launch_materialize(a, &launches);
+  if (e != cudaSuccess) return cuda_fail(e, "materialize launch");
+  return ok(launches);
 }
+
+}  // extern "C"

@@ -84,4 +84,45 @@ struct AttnArgs {
 size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int dtype);
 cudaError_t launch_block_attn(const AttnArgs& a);
 
+// ----------------------------------------------------------- materialise ---
+constexpr int kMaxLayers = 16;
+struct MatPools {
+  void* k[kMaxLayers];
+  void* v[kMaxLayers];
+};
+
+struct MatArgs {
+  int B, rows_max, m, d, L, Hkv, D, page_size, max_pages, num_pages, dtype;
+  const void* hidden;
+  const int32_t* commit_len;
+  const int32_t* start_pos;
+  const void* W_f;
+  const void* b_f;
+  const void* W_kv;
+  const void* k_norm_w;
+  float rms_eps, rope_theta;
+  MatPools pools;
+  const int32_t* page_table;
+  int32_t* new_len;
+  int32_t* counters;
+  int* err;
+  void* scratch;
+  cudaStream_t stream;
+};
+
+struct MatPlan {
+  int T_max, K1, N1, K2, N2, S1, S2;
+  bool tc;   // GEMMs on tcgen05 tensor cores
+};
+
+MatPlan mat_plan(int B, int rows_max, int m, int d, int L, int Hkv, int D, int dtype);
+size_t mat_ws_bytes(const MatPlan& p, int dtype);
+cudaError_t launch_materialize(const MatArgs& a, int* launches);
+
+// tcgen05 GEMM: part[s][t][n] = sum_{k in split s} X[t][k] W[n][k], bf16 in, fp32 out
+bool gemm_tc_supported(int K, int N);
+int gemm_tc_splits(int T_max, int N, int K);
+cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int32_t* meta, int T_max, int N,
+                           int K, int S, int* err, cudaStream_t st);
+
 }  // namespace dflash

@@ -1,0 +1,305 @@
+// Target-context KV materialisation.
+//   DFlash page, KV 注入 step 2: h_ctx = W_f [h_l1; ...; h_lm] + b_f
+//   DFlash page, KV 注入 step 3: K^(l) = h_ctx W_K^(l), V^(l) = h_ctx W_V^(l)
+//   SGLang page, 4.1: kv_proj, k_norm, k_rope(positions), then a prefix-valid
+//     write of the first commit_len rows of each sequence; 5.1: position ->
+//     KV slot through the request's page table.
+//
+// Pipeline (one stream, no host synchronisation; the number of committed rows
+// is known only on the device):
+//   plan      1 CTA: prefix sum of commit_len -> compact row list, new_len
+//   gather    committed hidden rows -> a dense [T, m*d] operand
+//   GEMM 1    partial sums of H W_f^T (split over K)
+//   bias      h_ctx = sum of partials + b_f, rounded to the I/O type
+//   GEMM 2    partial sums of h_ctx W_kv^T for all L layers at once
+//   epilogue  per token: sum partials, k_norm, RoPE, cast, paged write
+// GEMMs run on tcgen05 tensor cores for bf16 (gemm_tc.cu) and on CUDA cores
+// for fp32 or shapes the tensor-core kernel does not take.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dflash {
+
+// ---------------------------------------------------------------------------
+// plan: compact row list of the committed rows
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restrict__ start_pos, int B,
+                int rows_max, int32_t* __restrict__ meta, int32_t* __restrict__ row_b,
+                int32_t* __restrict__ row_j, int32_t* __restrict__ new_len) {
+  __shared__ int32_t scan[256];
+  const int tid = threadIdx.x;
+  const int per = (B + blockDim.x - 1) / blockDim.x;
+  const int b0 = tid * per, b1 = min(B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += max(0, min(commit_len[b], rows_max));
+  scan[tid] = local;
+  __syncthreads();
+  for (int off = 1; off < (int)blockDim.x; off <<= 1) {
+    const int v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  int row = scan[tid] - local;
+  for (int b = b0; b < b1; ++b) {
+    const int n = max(0, min(commit_len[b], rows_max));
+    for (int j = 0; j < n; ++j, ++row) {
+      row_b[row] = b;
+      row_j[row] = j;
+    }
+    if (new_len) new_len[b] = start_pos[b] + n;
+  }
+  if (tid == blockDim.x - 1) meta[0] = scan[tid];
+}
+
+// ---------------------------------------------------------------------------
+// gather: hidden[b, j, :] -> X[t, :]
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+mat_gather_kernel(const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, const int32_t* __restrict__ meta,
+                  const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j, int rows_max,
+                  size_t row_bytes) {
+  const int t = blockIdx.y;
+  if (t >= meta[0]) return;
+  const uint8_t* src = hidden + ((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes;
+  uint8_t* dst = X + (size_t)t * row_bytes;
+  const size_t nvec = row_bytes / 16;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < nvec; v += (size_t)gridDim.x * blockDim.x)
+    reinterpret_cast<uint4*>(dst)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+  if (blockIdx.x == 0)
+    for (size_t e = nvec * 16 + threadIdx.x; e < row_bytes; e += blockDim.x) dst[e] = src[e];
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core GEMM: part[s][t][n] = sum_{k in split s} X[t][k] W[n][k]
+// 64 x 64 output tile per CTA, 4 x 4 per thread, K steps of 16.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(const T* __restrict__ X, const T* __restrict__ W, float* __restrict__ part,
+                 const int32_t* __restrict__ meta, int T_max, int N, int K, int k_per_split) {
+  __shared__ float As[16][68];
+  __shared__ float Bs[16][68];
+  const int n0 = blockIdx.x * 64, t0 = blockIdx.y * 64, s = blockIdx.z;
+  const int Tv = min(meta[0], T_max);
+  if (t0 >= Tv) return;
+  const int k_begin = s * k_per_split, k_end = min(K, k_begin + k_per_split);
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float acc[4][4] = {};
+  const int lr = tid >> 2, lk = (tid & 3) * 4;
+  for (int k0 = k_begin; k0 < k_end; k0 += 16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = k0 + lk + q;
+      const int tr = t0 + lr, nr = n0 + lr;
+      As[lk + q][lr] = (tr < Tv && k < k_end) ? to_f32(X[(size_t)tr * K + k]) : 0.f;
+      Bs[lk + q][lr] = (nr < N && k < k_end) ? to_f32(W[(size_t)nr * K + k]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float a[4], bb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = As[k][ty * 4 + i]; bb[i] = Bs[k][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= Tv) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n < N) part[((size_t)s * T_max + t) * N + n] = acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// h_ctx = sum of split partials + b_f, rounded to the I/O type
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256)
+mat_bias_kernel(const float* __restrict__ part, int splits, const T* __restrict__ b_f, T* __restrict__ h,
+                const int32_t* __restrict__ meta, int T_max, int d) {
+  const int t = blockIdx.y;
+  if (t >= meta[0]) return;
+  for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < d; f += gridDim.x * blockDim.x) {
+    float v = b_f ? to_f32(b_f[f]) : 0.f;
+    for (int s = 0; s < splits; ++s) v += part[((size_t)s * T_max + t) * d + f];
+    h[(size_t)t * d + f] = from_f32<T>(v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// epilogue: one CTA per committed token; one warp per (layer, K|V, kv head)
+// vector of D values. K: RMSNorm over D, then rotate-half RoPE at the token's
+// absolute position; then the cast and the paged write.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256)
+mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* __restrict__ meta,
+                    const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j,
+                    const int32_t* __restrict__ start_pos, const int32_t* __restrict__ page_table,
+                    const T* __restrict__ k_norm_w, float rms_eps, float rope_theta, MatPools pools,
+                    int T_max, int L, int Hkv, int D, int page_size, int max_pages, int num_pages) {
+  extern __shared__ float esm[];             // [D/2] cos, [D/2] sin, [warps][D] staging
+  float* cs = esm;
+  float* sn = esm + D / 2;
+  const int t = blockIdx.x;
+  if (t >= meta[0]) return;
+  const int b = row_b[t], j = row_j[t];
+  const int pos = start_pos[b] + j;
+  const int lp = pos / page_size;
+  if (pos < 0 || lp >= max_pages) return;
+  const int phys = page_table[(size_t)b * max_pages + lp];
+  if (phys < 0 || phys >= num_pages) return;
+  const size_t slot = (size_t)phys * page_size + pos % page_size;
+  const int half = D / 2;
+  if (rope_theta > 0.f) {
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+      // angle in double: positions reach ~1e4 radians at the lowest frequency
+      const double inv_freq = exp(-(2.0 * i / D) * log((double)rope_theta));
+      double sd, cd;
+      sincos((double)pos * inv_freq, &sd, &cd);
+      cs[i] = (float)cd;
+      sn[i] = (float)sd;
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  float* xs = esm + D + warp * D;
+  const int N = L * 2 * Hkv * D;
+  for (int v = warp; v < L * 2 * Hkv; v += nwarps) {
+    const int h = v % Hkv, kv = (v / Hkv) & 1, l = v / (2 * Hkv);
+    const size_t n0 = (size_t)v * D;   // column of (l, kv, h) in [L, 2, Hkv*D]
+    float ss = 0.f;
+    for (int d = lane; d < D; d += 32) {
+      float x = 0.f;
+      for (int s = 0; s < splits; ++s) x += part[((size_t)s * T_max + t) * N + n0 + d];
+      xs[d] = x;
+      ss += x * x;
+    }
+    __syncwarp();
+    T* dst = (kv == 0 ? (T*)pools.k[l] : (T*)pools.v[l]) + (slot * Hkv + h) * D;
+    if (kv == 1) {
+      for (int d = lane; d < D; d += 32) dst[d] = from_f32<T>(xs[d]);
+      __syncwarp();
+      continue;
+    }
+    float scale = 1.f;
+    if (k_norm_w) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      scale = 1.f / sqrtf(ss / D + rms_eps);
+    }
+    for (int d = lane; d < D; d += 32) {
+      float x = xs[d] * scale;
+      if (k_norm_w) x *= to_f32(k_norm_w[(size_t)l * D + d]);
+      if (rope_theta > 0.f) {
+        const int i = d < half ? d : d - half;
+        float y = xs[d < half ? d + half : d - half] * scale;
+        if (k_norm_w) y *= to_f32(k_norm_w[(size_t)l * D + (d < half ? d + half : d - half)]);
+        x = d < half ? x * cs[i] - y * sn[i] : x * cs[i] + y * sn[i];
+      }
+      dst[d] = from_f32<T>(x);
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+MatPlan mat_plan(int B, int rows_max, int m, int d, int L, int Hkv, int D, int dtype) {
+  MatPlan p;
+  p.T_max = B * rows_max;
+  p.K1 = m * d;
+  p.N1 = d;
+  p.K2 = d;
+  p.N2 = L * 2 * Hkv * D;
+  p.tc = dtype == 1 && gemm_tc_supported(p.K1, p.N1) && gemm_tc_supported(p.K2, p.N2);
+  if (p.tc) {
+    p.S1 = gemm_tc_splits(p.T_max, p.N1, p.K1);
+    p.S2 = gemm_tc_splits(p.T_max, p.N2, p.K2);
+  } else {
+    p.S1 = std::max(1, std::min(8, (p.K1 + 4095) / 4096));
+    p.S2 = std::max(1, std::min(8, (p.K2 + 4095) / 4096));
+  }
+  return p;
+}
+
+size_t mat_ws_bytes(const MatPlan& p, int dtype) {
+  const size_t el = dtype == 1 ? 2 : 4;
+  const size_t Nmax = std::max(p.N1, p.N2);
+  size_t s = align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max));
+  s += align_up((size_t)p.T_max * p.K1 * el);     // gathered operand X
+  s += align_up((size_t)p.T_max * p.N1 * el);     // h_ctx
+  s += align_up((size_t)std::max(p.S1, p.S2) * p.T_max * Nmax * sizeof(float));
+  return s;
+}
+
+template <typename T>
+static cudaError_t run_gemm(const MatPlan& p, bool tc, const void* X, const void* W, float* part,
+                            const int32_t* meta, int N, int K, int S, int* err, cudaStream_t st) {
+  if (tc) return launch_gemm_tc(X, W, part, meta, p.T_max, N, K, S, err, st);
+  const int kps = ((K + S - 1) / S + 15) / 16 * 16;
+  dim3 grid((N + 63) / 64, (p.T_max + 63) / 64, S);
+  gemm_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)X, (const T*)W, part, meta, p.T_max, N, K, kps);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
+  const MatPlan p = mat_plan(a.B, a.rows_max, a.m, a.d, a.L, a.Hkv, a.D, a.dtype);
+  const size_t el = sizeof(T);
+  char* ws = (char*)a.scratch;
+  int32_t* meta = (int32_t*)ws;
+  int32_t* row_b = meta + 64;
+  int32_t* row_j = row_b + p.T_max;
+  ws += align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max));
+  T* X = (T*)ws;
+  ws += align_up((size_t)p.T_max * p.K1 * el);
+  T* h = (T*)ws;
+  ws += align_up((size_t)p.T_max * p.N1 * el);
+  float* part = (float*)ws;
+  cudaStream_t st = a.stream;
+  int n = 0;
+  mat_plan_kernel<<<1, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, meta, row_b, row_j, a.new_len);
+  ++n;
+  const size_t row_bytes = (size_t)p.K1 * el;
+  dim3 gg((unsigned)std::min<size_t>(8, (row_bytes / 16 + 255) / 256 + 1), p.T_max);
+  mat_gather_kernel<<<gg, 256, 0, st>>>((const uint8_t*)a.hidden, (uint8_t*)X, meta, row_b, row_j, a.rows_max,
+                                        row_bytes);
+  ++n;
+  cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, a.err, st);
+  if (e != cudaSuccess) return e;
+  ++n;
+  dim3 gb((p.N1 + 255) / 256, p.T_max);
+  mat_bias_kernel<T><<<gb, 256, 0, st>>>(part, p.S1, (const T*)a.b_f, h, meta, p.T_max, p.N1);
+  ++n;
+  e = run_gemm<T>(p, p.tc, h, a.W_kv, part, meta, p.N2, p.K2, p.S2, a.err, st);
+  if (e != cudaSuccess) return e;
+  ++n;
+  const size_t esmem = sizeof(float) * (a.D + 8 * (size_t)a.D);
+  mat_epilogue_kernel<T><<<p.T_max, 256, esmem, st>>>(
+      part, p.S2, meta, row_b, row_j, a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, a.rope_theta,
+      a.pools, p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages);
+  ++n;
+  *launches = n;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_materialize(const MatArgs& a, int* launches) {
+  return a.dtype == 0 ? launch_mat_t<float>(a, launches) : launch_mat_t<bf16>(a, launches);
+}
+
+}  // namespace dflash
