@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Throughput of the DFlash hot path on GB300.
+
+One step = block attention in each of the 5 draft layers, greedy verify of
+sequences 0-31 and sampled verify of sequences 32-63, and the context-KV
+materialisation of every sequence's committed rows -- the batched serving
+workload at the Llama-3.1-8B shape (B = 64, block 16, ragged contexts of
+512-8192 tokens in 16-token pages, vocabulary 128256), synthetic inputs.
+
+Prints one JSON line. ``--impl reference`` times the CPU oracle instead (the
+reference arm of this build), on a bounded sample of the same workload.
+Multi-GPU runs (torchrun) are independent replicas: each rank runs its own
+batch; the barrier and the max over ranks bracket the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft+verify steps/s & verified tokens/s at 8B shape (B=64,k=16); % HBM roofline"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        sm_sorted = sorted(sm)
+        med = sm_sorted[len(sm_sorted) // 2] if sm_sorted else None
+        return {"sm_mhz": med, "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step_estimate(wl, ctx_all, commit_rows, n_attn=2, n_verify=2, n_rows=4, seed=0):
+    """Time the oracle on a bounded sample of one step and scale each part to
+    the full step by its work units. Returns (seconds per full step, sample
+    description)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    from block_diffusion_speculative_fusion_gb300 import synth
+
+    def f64(t):
+        return t.float().numpy().astype(np.float64)
+
+    # attention: n_attn sequences of one layer, scaled by keys and by L layers
+    ctx = ctx_all[:n_attn].clone()
+    w_a = dataclasses.replace(wl, B=n_attn)
+    cache = synth.paged_cache(w_a, headroom=16, seed=seed, layers=1, ctx_len=ctx)
+    blk = synth.block_qkv(w_a, 0, seed)
+    args = [f64(blk["q"]), f64(blk["k_blk"]), f64(blk["v_blk"]), f64(cache.k_pools[0]), f64(cache.v_pools[0]),
+            cache.page_table.numpy(), ctx.numpy(), wl.page_size]
+    t0 = time.perf_counter()
+    O.block_attn(*args)
+    t_attn = time.perf_counter() - t0
+    keys_sample = float((ctx + wl.k).sum())
+    keys_all = float((ctx_all + wl.k).sum())
+    attn_full = t_attn * keys_all / keys_sample * wl.L
+
+    # verify: n_verify greedy and n_verify sampled sequences
+    vb = synth.verify_batch(wl, seed, n_max=wl.n_draft, B=2 * n_verify, greedy_rows=n_verify)
+    zt, zd = f64(vb["target_logits"]), f64(vb["draft_logits"])
+    t0 = time.perf_counter()
+    O.verify_greedy(zt[:n_verify], vb["cand"].numpy()[:n_verify], vb["n_draft"].numpy()[:n_verify])
+    t_g = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    O.verify_sample(zt[n_verify:], zd[n_verify:], vb["cand"].numpy()[n_verify:], vb["n_draft"].numpy()[n_verify:],
+                    vb["u_acc"].numpy()[n_verify:], vb["u_final"].numpy()[n_verify:], wl.temperature)
+    t_s = time.perf_counter() - t0
+    verify_full = t_g * wl.n_greedy / n_verify + t_s * (wl.B - wl.n_greedy) / n_verify
+
+    # materialise: n_rows committed rows of one sequence, scaled by committed rows
+    w = synth.ctx_weights(wl, seed)
+    hid = synth.captured_hidden(wl, n_rows, seed, B=1)
+    pages = (n_rows + wl.page_size - 1) // wl.page_size + 1
+    pt = np.arange(pages, dtype=np.int32)[None, :]
+    pool = [np.zeros((pages, wl.page_size, wl.Hkv, wl.D)) for _ in range(wl.L)]
+    t0 = time.perf_counter()
+    O.materialize_ctx_kv(f64(hid), [n_rows], [0], f64(w["W_f"]), f64(w["b_f"]), f64(w["W_kv"]),
+                         None if w["k_norm_w"] is None else f64(w["k_norm_w"]), wl.rms_eps, wl.rope_theta,
+                         pool, [p.copy() for p in pool], pt, wl.page_size)
+    t_m = time.perf_counter() - t0
+    mat_full = t_m * commit_rows / n_rows
+    total = attn_full + verify_full + mat_full
+    sample = (f"attention: {n_attn} sequences x 1 layer (scaled by keys and x{wl.L} layers); verify: "
+              f"{n_verify} greedy + {n_verify} sampled sequences (scaled to {wl.n_greedy}+{wl.B - wl.n_greedy}); "
+              f"materialise: {n_rows} rows (scaled to {commit_rows} committed rows)")
+    return total, sample, {"attn_s": attn_full, "verify_s": verify_full, "materialize_s": mat_full,
+                           "sample_cpu_s": t_attn + t_g + t_s + t_m}
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, wl):
+    """Reference arm: the CPU oracle as it stands, one bounded sample per step."""
+    import torch
+    from block_diffusion_speculative_fusion_gb300 import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    ctx_all = synth.ctx_lengths(wl, 0)
+    commit_rows = wl.B * 4          # expected committed rows per step (mean accept length ~3)
+    for _ in range(args.warmup):
+        oracle_step_estimate(wl, ctx_all, commit_rows, n_attn=1, n_verify=1, n_rows=2)
+    est = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s, sample, parts = oracle_step_estimate(wl, ctx_all, commit_rows, n_attn=1, n_verify=1, n_rows=2)
+        est.append(s)
+    wall = time.perf_counter() - t0
+    per_step = sum(est) / len(est)
+    value = 1.0 / per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "k": wl.k, "V": wl.V, "ctx": f"U[{wl.ctx_lo},{wl.ctx_hi}]",
+                   "page": wl.page_size},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall, "parts_s": parts,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def attn_bytes(ctx_mean_sum, wl):
+    """Algorithmic HBM bytes of one block-attention launch (one draft layer):
+    every context and block K/V row once, Q read once, O written once."""
+    el = 2
+    kv = (ctx_mean_sum + wl.B * wl.k) * wl.Hkv * wl.D * 2 * el
+    qo = 2 * wl.B * wl.k * wl.Hq * wl.D * el
+    return kv + qo
+
+
+def traffic_from_profile(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel."""
+    path = os.path.join(ROOT, "profiles", "attn_bf16_kernel_llama8b_b64.md")
+    src = os.path.join(ROOT, "block_diffusion_speculative_fusion_gb300", "csrc", kernel_file)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_diffusion_speculative_fusion_gb300 import api
+    from block_diffusion_speculative_fusion_gb300.step import DflashStep
+
+    st = DflashStep(wl, seed=rank, device=dev, headroom_steps=2 * (args.warmup + args.steps) + 4,
+                    pinned_inputs=True)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    ctx_start = st.ctx_len().clone()
+    # ---------------- device-resident timed region ----------------
+    ev = {"attn": [], "verify": [], "mat": []}
+    pending = {}
+
+    def timer(tag):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        kind, edge = tag.rsplit("_", 1)
+        if edge == "start":
+            pending[kind] = e
+        else:
+            ev[kind].append((pending.pop(kind), e))
+
+    clocks = Clocks(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        st.step(timer=timer)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_max = ms_total
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    ctx_end = st.ctx_len().clone()
+    commit_sum = float((ctx_end - ctx_start).sum().item()) / args.steps   # committed rows per step
+    per_kernel = {k: (sum(a.elapsed_time(b) for a, b in v) / len(v)) * 1e3 for k, v in ev.items() if v}
+    ms_per_step = ms_max / args.steps
+    value = world * args.steps / (ms_max / 1e3)
+    tokens_per_s = value * commit_sum
+
+    # ---------------- roofline of the dominant kernel (block attention) ----------------
+    hbm, tf, tf_sus, peak_kind = _peaks()
+    ctx_mean_sum = float((ctx_start.double() + ctx_end.double()).sum().item()) / 2.0
+    ab = attn_bytes(ctx_mean_sum, wl)
+    attn_us = per_kernel["attn"]
+    achieved = ab / (attn_us * 1e-6) / 1e9
+    roof = {"kernel": "attn_bf16_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind ==
+            "measured" else "fallback 6.8 TB/s", "traffic": traffic_from_profile("attn.cu"),
+            "algorithmic_bytes_per_launch": ab, "us_per_launch": attn_us}
+
+    # ---------------- end to end through the public API with host buffers ----------------
+    st.reset()
+    h2d = st.input_bytes()
+    outs = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in st.out.items()}
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    for _ in range(2):
+        st.copy_inputs_from_host()
+        st.step()
+        for k, v in outs.items():
+            v.copy_(st.out[k], non_blocking=True)
+        stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        st.copy_inputs_from_host()
+        st.step()
+        for k, v in outs.items():
+            v.copy_(st.out[k], non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * args.steps / (e2e_ms / 1e3)
+
+    # ---------------- CPU baseline: the oracle on a bounded sample ----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        est, sample, parts = oracle_step_estimate(wl, st.ctx0, int(round(commit_sum)), n_attn=4, n_verify=4,
+                                                  n_rows=8)
+        cpu = {"value": 1.0 / est, "unit": "steps/s", "cores": host_cores(), "kind": "oracle", "sample": sample,
+               "parts_s": parts}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "k": wl.k, "L": wl.L, "V": wl.V, "d": wl.d,
+                       "Hq/Hkv/D": f"{wl.Hq}/{wl.Hkv}/{wl.D}", "ctx": f"U[{wl.ctx_lo},{wl.ctx_hi}]",
+                       "page": wl.page_size, "verify": f"greedy {wl.n_greedy} + sampled {wl.B - wl.n_greedy}",
+                       "l2": "inputs larger than L2: ~5.7 GB of context K/V read per step",
+                       "parallelism": f"replicas x{world}"},
+            "verified_tokens_per_s": tokens_per_s, "committed_rows_per_step": commit_sum,
+            "kernels_us_per_step": {"attn_per_layer": per_kernel.get("attn"),
+                                    "attn_total": per_kernel.get("attn", 0) * wl.L,
+                                    "verify": per_kernel.get("verify"), "materialize": per_kernel.get("mat")},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": st.launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from block_diffusion_speculative_fusion_gb300 import workloads as W
+    wl = W.LLAMA8B_B64
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()
