@@ -1,11 +1,327 @@
-// tcgen05 GEMM (placeholder until the tensor-core kernel lands).
+// tcgen05 tensor-core GEMM for the context-KV projections (sm_103a):
+//   part[seg][t][n] = sum over one K segment of W[n][k] * X[t][k]
+// with W [N, K] (weights, K contiguous) and X [T, K] (committed rows, K
+// contiguous), bf16 in, fp32 out.
+//
+// Weights are the A operand (M = 128 output features per tile) and the rows
+// are the B operand (N = up to 256 rows per tile), so a decode-sized T reads
+// each weight byte once while the MMA's N shrinks to the rows present.
+//
+// Persistent CTAs (one per SM) split the (tile, 64-wide k-block) space into
+// equal contiguous ranges (stream-K style); a range that covers part of a tile
+// writes that tile's partial sum to its own segment slot, and the consumers sum
+// a tile's segments in a fixed order, so results are deterministic.
+//
+// Per CTA: warp 0 = TMA producer (4-stage ring of 128B-swizzled tiles), warp 1
+// = TMEM allocator and single-thread MMA issuer, warps 2-5 = epilogue (TMEM ->
+// registers -> global). Two 256-column TMEM accumulators let the epilogue of
+// one range piece overlap the MMAs of the next. Every mbarrier wait is bounded:
+// a wait that gives up records an error code, the CTA drains its own copies and
+// MMAs (again bounded), frees TMEM and returns.
+#include <algorithm>
+
+#include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace dflash {
-bool gemm_tc_supported(int, int) { return false; }
-int gemm_tc_splits(int, int, int) { return 1; }
-cudaError_t launch_gemm_tc(const void*, const void*, float*, const int32_t*, int, int, int, int, int*,
-                           cudaStream_t) {
-  return cudaErrorNotSupported;
+
+namespace tc {
+using namespace tcplan;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BYTES = BN * BK * 2;    // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;          // two 256-column fp32 accumulators
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
+// tcgen05 PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
 }
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// Arrive on the mbarrier once every tcgen05 op issued so far by this thread completes.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand in 128-byte swizzle atoms of
+// 8 rows x 128 bytes, atoms of consecutive row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;              // descriptor version
+  d |= (uint64_t)2 << 61;              // layout: 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Bounded wait that also gives up when another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                              int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > 2000000000ull) {
+      *abort_flag = 1;
+      if (err) atomicCAS(err, 0, code);
+      return false;
+    }
+  }
+}
+
+struct TcWork {
+  int T, per, G, total, MT, KB;
+};
+
+__device__ __forceinline__ TcWork tc_work(const int32_t* meta, int per_idx, int MT, int KB, int T_max) {
+  TcWork w;
+  w.T = min(meta[0], T_max);
+  w.per = meta[per_idx];
+  w.MT = MT;
+  w.KB = KB;
+  w.G = (w.T + tc::BN - 1) / tc::BN;
+  w.total = MT * w.G * KB;
+  return w;
+}
+
+__global__ void __launch_bounds__(tc::THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+               float* __restrict__ part, const int32_t* __restrict__ meta, int per_idx, int T_max, int N, int MT,
+               int KB, int b_rows, int* err) {
+  using namespace tc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;       // [2]
+  uint64_t* tempty = tfull + 2;           // [2]
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sm + 1);
+  int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
+
+  const TcWork w = tc_work(meta, per_idx, MT, KB, T_max);
+  const int lo = blockIdx.x * w.per;
+  const int hi = min(w.total, lo + w.per);
+  if (w.per <= 0 || lo >= hi) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int producer_issued = 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    *consumed_sm = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_base_sm, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_sm;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int pos = lo; pos < hi && ok;) {
+        const int tile = pos / w.KB, kb0 = pos - tile * w.KB;
+        const int kb1 = min(w.KB, kb0 + (hi - pos));
+        const int m_tile = tile % w.MT, group = tile / w.MT;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_or_abort(&empty[stage], phase ^ 1u, abort_flag, err, 2)) { ok = false; break; }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(A_BYTES + b_rows * BK * 2));
+          tma_load_2d(sa, &wmap, &full[stage], kb * BK, m_tile * BM);
+          tma_load_2d(sa + A_BYTES, &xmap, &full[stage], kb * BK, group * BN);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        pos += kb1 - kb0;
+      }
+      producer_issued = issued;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int consumed = 0;
+      bool ok = true;
+      for (int pos = lo; pos < hi && ok;) {
+        const int tile = pos / w.KB, kb0 = pos - tile * w.KB;
+        const int kb1 = min(w.KB, kb0 + (hi - pos));
+        const int group = tile / w.MT;
+        const int rows = min(BN, w.T - group * BN);
+        const int n_mma = (rows + 15) / 16 * 16;
+        const uint32_t idesc = idesc_bf16(BM, n_mma);
+        if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 4)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_or_abort(&full[stage], phase, abort_flag, err, 5)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t adesc = sdesc_sw128(sa);
+          const uint64_t bdesc = sdesc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j)   // 16 bf16 = 32 bytes of K per instruction
+            tc_mma_bf16(d_tmem, adesc + (uint64_t)(j * 2), bdesc + (uint64_t)(j * 2), idesc,
+                        (kb > kb0 || j > 0) ? 1u : 0u);
+          tc_commit(&empty[stage]);       // stage is free once these MMAs have read it
+          ++consumed;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);           // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        pos += kb1 - kb0;
+      }
+      *consumed_sm = consumed;
+      // every MMA issued by this thread has completed before TMEM is released
+      tc_commit(mma_done);
+      mbar_wait_bounded(mma_done, 0, err, 6);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue (warps 2..5) ------------------------------
+    const int quarter = warp & 3;         // TMEM lanes [32 q, 32 q + 32) belong to warp q mod 4
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int pos = lo; pos < hi;) {
+      const int tile = pos / w.KB, kb0 = pos - tile * w.KB;
+      const int kb1 = min(w.KB, kb0 + (hi - pos));
+      const int m_tile = tile % w.MT, group = tile / w.MT;
+      const int seg = blockIdx.x - (tile * w.KB) / w.per;
+      const int rows = min(BN, w.T - group * BN);
+      if (!wait_or_abort(&tfull[acc], acc_phase, abort_flag, err, 7)) break;
+      tc_fence_after();
+      const int f = m_tile * BM + quarter * 32 + lane;
+      float* dst = part + ((size_t)seg * T_max + (size_t)group * BN) * N + f;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      for (int c0 = 0; c0 < rows; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tbase + (uint32_t)c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c0 + c < rows) dst[(size_t)(c0 + c) * N] = __uint_as_float(r[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      pos += kb1 - kb0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // After an abort, copies issued but never consumed may still be in flight:
+  // wait for them (bounded) so that none lands after this CTA has exited.
+  if (warp == 0 && lane == 0 && *abort_flag)
+    for (int i = *consumed_sm; i < producer_issued; ++i)
+      mbar_wait_bounded(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), err, 3);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+bool gemm_tc_supported(int K, int N) { return K % tc::BK == 0 && N % tc::BM == 0 && K >= tc::BK; }
+
+// Upper bound of the segment count of any tile: a CTA range covers at least
+// ceil(MT * KB / GRID) k-blocks, so a tile of KB k-blocks meets at most
+// ceil(GRID / MT) + 1 ranges.
+int gemm_tc_splits(int /*T_max*/, int N, int /*K*/) {
+  const int MT = N / tc::BM;
+  return (tc::GRID + MT - 1) / MT + 1;
+}
+
+cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int32_t* meta, int T_max, int N, int K,
+                           int per_idx, int* err, cudaStream_t st) {
+  using namespace tc;
+  CUtensorMap wmap, xmap;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tensor_map(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorNotSupported;
+  }
+  // rows per B box: a full tile, or all of a small T_max (16-row granularity)
+  const int b_rows = std::min(BN, (T_max + 15) / 16 * 16);
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)T_max};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {BK, (uint32_t)b_rows};
+    if (!encode_tensor_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorNotSupported;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  gemm_tc_kernel<<<GRID, THREADS, SMEM_BYTES, st>>>(wmap, xmap, part, meta, per_idx, T_max, N, N / BM, K / BK,
+                                                    b_rows, err);
+  return cudaGetLastError();
+}
+
 }  // namespace dflash

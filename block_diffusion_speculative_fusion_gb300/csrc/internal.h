@@ -119,10 +119,39 @@ MatPlan mat_plan(int B, int rows_max, int m, int d, int L, int Hkv, int D, int d
 size_t mat_ws_bytes(const MatPlan& p, int dtype);
 cudaError_t launch_materialize(const MatArgs& a, int* launches);
 
-// tcgen05 GEMM: part[s][t][n] = sum_{k in split s} X[t][k] W[n][k], bf16 in, fp32 out
+// tcgen05 GEMM: part[seg][t][n] = sum over one K segment of X[t][k] W[n][k], bf16 in, fp32 out.
+namespace tcplan {
+constexpr int BM = 128;      // output features per tile (MMA M)
+constexpr int BN = 256;      // rows per tile (MMA N upper bound)
+constexpr int BK = 64;       // K per k-block: one 128-byte swizzle atom of bf16
+constexpr int GRID = 152;    // persistent CTAs: one per SM of a GB300
+constexpr int MIN_PER = 8;   // smallest k-block range per CTA
+}  // namespace tcplan
+
+// k-block range per CTA when T rows are valid (tiles = N/BM x ceil(T/BN)).
+inline __host__ __device__ int gemm_tc_per(int T, int N, int K) {
+  const int MT = N / tcplan::BM, KB = K / tcplan::BK;
+  const int G = (T + tcplan::BN - 1) / tcplan::BN;
+  const long total = (long)MT * G * KB;
+  long per = (total + tcplan::GRID - 1) / tcplan::GRID;
+  if (per < tcplan::MIN_PER) per = tcplan::MIN_PER;
+  return (int)per;
+}
+// Number of K segments (CTA ranges) that tile `tile` spans.
+inline __host__ __device__ int gemm_tc_tile_segs(int tile, int KB, int per) {
+  return ((tile + 1) * KB - 1) / per - (tile * KB) / per + 1;
+}
+// Partial-sum slots of a GEMM with segment rule `per` (0: fixed S splits) for
+// the output element (t, n).
+inline __host__ __device__ int part_segs(int t, int n, int N, int K, int per, int S) {
+  if (per <= 0) return S;
+  const int tile = (t / tcplan::BN) * (N / tcplan::BM) + n / tcplan::BM;
+  return gemm_tc_tile_segs(tile, K / tcplan::BK, per);
+}
+
 bool gemm_tc_supported(int K, int N);
 int gemm_tc_splits(int T_max, int N, int K);
 cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int32_t* meta, int T_max, int N,
-                           int K, int S, int* err, cudaStream_t st);
+                           int K, int per_idx, int* err, cudaStream_t st);
 
 }  // namespace dflash

@@ -28,7 +28,8 @@ namespace dflash {
 __global__ void __launch_bounds__(256)
 mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restrict__ start_pos, int B,
                 int rows_max, int32_t* __restrict__ meta, int32_t* __restrict__ row_b,
-                int32_t* __restrict__ row_j, int32_t* __restrict__ new_len) {
+                int32_t* __restrict__ row_j, int32_t* __restrict__ new_len, int tc, int N1, int K1, int N2,
+                int K2) {
   __shared__ int32_t scan[256];
   const int tid = threadIdx.x;
   const int per = (B + blockDim.x - 1) / blockDim.x;
@@ -52,7 +53,13 @@ mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restric
     }
     if (new_len) new_len[b] = start_pos[b] + n;
   }
-  if (tid == blockDim.x - 1) meta[0] = scan[tid];
+  if (tid == blockDim.x - 1) {
+    const int T = scan[tid];
+    meta[0] = T;
+    // tensor-core GEMMs: k-block range per persistent CTA for T rows (0: fixed splits)
+    meta[1] = tc ? gemm_tc_per(T, N1, K1) : 0;
+    meta[2] = tc ? gemm_tc_per(T, N2, K2) : 0;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -129,12 +136,14 @@ gemm_simt_kernel(const T* __restrict__ X, const T* __restrict__ W, float* __rest
 template <typename T>
 __global__ void __launch_bounds__(256)
 mat_bias_kernel(const float* __restrict__ part, int splits, const T* __restrict__ b_f, T* __restrict__ h,
-                const int32_t* __restrict__ meta, int T_max, int d) {
+                const int32_t* __restrict__ meta, int T_max, int d, int K1) {
   const int t = blockIdx.y;
   if (t >= meta[0]) return;
+  const int per = meta[1];
   for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < d; f += gridDim.x * blockDim.x) {
     float v = b_f ? to_f32(b_f[f]) : 0.f;
-    for (int s = 0; s < splits; ++s) v += part[((size_t)s * T_max + t) * d + f];
+    const int segs = part_segs(t, f, d, K1, per, splits);
+    for (int s = 0; s < segs; ++s) v += part[((size_t)s * T_max + t) * d + f];
     h[(size_t)t * d + f] = from_f32<T>(v);
   }
 }
@@ -150,7 +159,7 @@ mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* _
                     const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j,
                     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ page_table,
                     const T* __restrict__ k_norm_w, float rms_eps, float rope_theta, MatPools pools,
-                    int T_max, int L, int Hkv, int D, int page_size, int max_pages, int num_pages) {
+                    int T_max, int L, int Hkv, int D, int page_size, int max_pages, int num_pages, int K2) {
   extern __shared__ float esm[];             // [D/2] cos, [D/2] sin, [warps][D] staging
   float* cs = esm;
   float* sn = esm + D / 2;
@@ -178,13 +187,15 @@ mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* _
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   float* xs = esm + D + warp * D;
   const int N = L * 2 * Hkv * D;
+  const int per = meta[2];
   for (int v = warp; v < L * 2 * Hkv; v += nwarps) {
     const int h = v % Hkv, kv = (v / Hkv) & 1, l = v / (2 * Hkv);
     const size_t n0 = (size_t)v * D;   // column of (l, kv, h) in [L, 2, Hkv*D]
     float ss = 0.f;
     for (int d = lane; d < D; d += 32) {
       float x = 0.f;
-      for (int s = 0; s < splits; ++s) x += part[((size_t)s * T_max + t) * N + n0 + d];
+      const int segs = part_segs(t, (int)n0 + d, N, K2, per, splits);
+      for (int s = 0; s < segs; ++s) x += part[((size_t)s * T_max + t) * N + n0 + d];
       xs[d] = x;
       ss += x * x;
     }
@@ -249,8 +260,8 @@ size_t mat_ws_bytes(const MatPlan& p, int dtype) {
 
 template <typename T>
 static cudaError_t run_gemm(const MatPlan& p, bool tc, const void* X, const void* W, float* part,
-                            const int32_t* meta, int N, int K, int S, int* err, cudaStream_t st) {
-  if (tc) return launch_gemm_tc(X, W, part, meta, p.T_max, N, K, S, err, st);
+                            const int32_t* meta, int N, int K, int S, int per_idx, int* err, cudaStream_t st) {
+  if (tc) return launch_gemm_tc(X, W, part, meta, p.T_max, N, K, per_idx, err, st);
   const int kps = ((K + S - 1) / S + 15) / 16 * 16;
   dim3 grid((N + 63) / 64, (p.T_max + 63) / 64, S);
   gemm_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)X, (const T*)W, part, meta, p.T_max, N, K, kps);
@@ -273,26 +284,27 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   float* part = (float*)ws;
   cudaStream_t st = a.stream;
   int n = 0;
-  mat_plan_kernel<<<1, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, meta, row_b, row_j, a.new_len);
+  mat_plan_kernel<<<1, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, meta, row_b, row_j, a.new_len,
+                                     p.tc ? 1 : 0, p.N1, p.K1, p.N2, p.K2);
   ++n;
   const size_t row_bytes = (size_t)p.K1 * el;
   dim3 gg((unsigned)std::min<size_t>(8, (row_bytes / 16 + 255) / 256 + 1), p.T_max);
   mat_gather_kernel<<<gg, 256, 0, st>>>((const uint8_t*)a.hidden, (uint8_t*)X, meta, row_b, row_j, a.rows_max,
                                         row_bytes);
   ++n;
-  cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, a.err, st);
+  cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, 1, a.err, st);
   if (e != cudaSuccess) return e;
   ++n;
   dim3 gb((p.N1 + 255) / 256, p.T_max);
-  mat_bias_kernel<T><<<gb, 256, 0, st>>>(part, p.S1, (const T*)a.b_f, h, meta, p.T_max, p.N1);
+  mat_bias_kernel<T><<<gb, 256, 0, st>>>(part, p.S1, (const T*)a.b_f, h, meta, p.T_max, p.N1, p.K1);
   ++n;
-  e = run_gemm<T>(p, p.tc, h, a.W_kv, part, meta, p.N2, p.K2, p.S2, a.err, st);
+  e = run_gemm<T>(p, p.tc, h, a.W_kv, part, meta, p.N2, p.K2, p.S2, 2, a.err, st);
   if (e != cudaSuccess) return e;
   ++n;
   const size_t esmem = sizeof(float) * (a.D + 8 * (size_t)a.D);
   mat_epilogue_kernel<T><<<p.T_max, 256, esmem, st>>>(
       part, p.S2, meta, row_b, row_j, a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, a.rope_theta,
-      a.pools, p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages);
+      a.pools, p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages, p.K2);
   ++n;
   *launches = n;
   return cudaGetLastError();
