@@ -359,6 +359,53 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_kernel(args, wl):
+    """One call of the step timed alone on the step's workload (attention: draft
+    layer 0 only, so that one pool pair is resident)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_diffusion_speculative_fusion_gb300 import api, synth
+    from block_diffusion_speculative_fusion_gb300.step import DflashStep
+    if args.batch:
+        wl = dataclasses.replace(wl, B=args.batch, n_greedy=min(wl.n_greedy, args.batch // 2))
+    one = dataclasses.replace(wl, L=1) if args.kernel == "attn" else wl
+    st = DflashStep(one, seed=0, device="cuda:0", headroom_steps=4)
+    inp = st.inp
+    ng = wl.n_greedy
+
+    def call():
+        if args.kernel == "attn":
+            api.block_attn(inp["q0"], inp["k_blk0"], inp["v_blk0"], st.k_pools[0], st.v_pools[0], st.page_table,
+                           st.ctx[0], max_ctx=st.max_ctx, out=st.attn_out[0])
+        elif args.kernel == "verify":
+            api.verify_greedy(inp["target_logits"][:ng], inp["cand"][:ng], inp["n_draft"][:ng], out=st.out_g)
+            api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"][ng:], inp["cand"][ng:],
+                              inp["u_acc"][ng:], inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:],
+                              out=st.out_s)
+        else:
+            st.out["commit_len"].fill_(5)
+            api.materialize_ctx_kv(inp["hidden"], st.out["commit_len"], st.ctx[0], st.W_f, st.b_f, st.W_kv,
+                                   st.k_norm_w, wl.rms_eps, wl.rope_theta, st.k_pools, st.v_pools, st.page_table,
+                                   new_len=st.ctx[1])
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    out = {"kernel": args.kernel, "workload": one.name, "B": one.B, "us_per_call": us}
+    if args.kernel == "attn":
+        ab = attn_bytes(float(st.ctx0.sum()), one)
+        hbm = _peaks()[0]
+        out.update({"bytes": ab, "GBps": ab / us / 1e3, "frac_hbm": ab / us / 1e3 / hbm})
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -366,11 +413,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["attn", "verify", "materialize"], default=None,
+                    help="time one call of the step in isolation (profiling aid)")
+    ap.add_argument("--batch", type=int, default=None, help="override B (with --kernel)")
     args = ap.parse_args()
     from block_diffusion_speculative_fusion_gb300 import workloads as W
     wl = W.LLAMA8B_B64
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.kernel:
+        run_kernel(args, wl)
     else:
         run_ours(args, wl)
 

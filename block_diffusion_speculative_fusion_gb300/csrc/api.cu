@@ -175,7 +175,7 @@ static int check_attn_dims(const dflash_attn_dims* d) {
   if ((long)d->max_ctx > (long)d->max_pages * d->page_size)
     return fail(DFLASH_ERR_INVALID_ARG, "max_ctx=%d exceeds max_pages*page_size", d->max_ctx);
   if (d->D > 256) return fail(DFLASH_ERR_UNSUPPORTED, "D=%d > 256", d->D);
-  if ((long)d->B * d->Hkv > kMaxCounters) return fail(DFLASH_ERR_UNSUPPORTED, "B*Hkv too large");
+  if ((long)d->B * d->Hkv > kMaxCounters - 2) return fail(DFLASH_ERR_UNSUPPORTED, "B*Hkv too large");
   if (d->n_q > 65535 || d->Hq > 65535 || d->B > 65535) return fail(DFLASH_ERR_UNSUPPORTED, "grid too large");
   return DFLASH_OK;
 }
@@ -203,12 +203,14 @@ int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_bl
   a.q = q; a.k_blk = k_blk; a.v_blk = v_blk; a.k_pool = k_pool; a.v_pool = v_pool;
   a.page_table = page_table; a.ctx_len = ctx_len; a.scale = scale; a.out = out;
   a.counters = (int32_t*)workspace;
+  a.sched = (int32_t*)workspace + kMaxCounters - 2;
   a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
   a.stream = (cudaStream_t)stream;
-  cudaError_t e = dflash::launch_block_attn(a);
+  int launches = 0;
+  cudaError_t e = dflash::launch_block_attn(a, &launches);
   if (e != cudaSuccess) return cuda_fail(e, "block_attn launch");
-  return ok(1);
+  return ok(launches);
 }
 
 // ------------------------------------------------------------- materialise ---

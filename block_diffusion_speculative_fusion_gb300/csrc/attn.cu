@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 #include "tma.cuh"
 
 namespace dflash {
@@ -349,6 +350,604 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 }
 
 // ===========================================================================
+// tcgen05 path: persistent, warp-specialised, TMEM accumulators.
+//   softmax     warps 0..W-1 (W = ceil(M / 32)): thread r owns packed query
+//               row r (TMEM lane r)
+//   producer    warp 2 (W <= 2) or 4: claims work items, loads Q, streams
+//               context K/V pages by TMA into a ring of 64-key stages
+//   MMA         the next warp: TMEM allocator and single-thread MMA issuer
+// A work item is (key split, kv head, sequence). Per 64-key tile t:
+// S_t = Q K_t^T (M = 128, N = 64) into TMEM buffer t % 2; the softmax threads
+// read their S row, write P_t (bf16) to shared memory, and the MMA thread
+// accumulates O += P_t V_t (M = 128, N = 128, V read MN-major) into the item's
+// TMEM O buffer. The running max is only raised (O rescaled in TMEM) when a
+// tile's max exceeds it by more than 2^8, so rescaling is rare. Q and O are
+// double-buffered per item so that one item's output overlaps the next
+// item's MMAs; the K/V ring runs across item boundaries.
+// ===========================================================================
+namespace attn_tc {
+constexpr int kTileK = 64;
+constexpr int kMaxStages = 5;
+constexpr int kTileBytes = 2 * 64 * 128;   // K (or V) of one tile: two d-halves x 64 keys x 128 B
+constexpr int kMaxThreads = 448;
+constexpr int kTmemCols = 512;              // S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384)
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kGrid = 152;                  // persistent CTAs: one per SM
+constexpr int kMaxSeqs = 1024;              // sequences per call on this path
+constexpr int kPtMax = 128;                 // page-table entries of one item (page size >= 8)
+constexpr int kBarBytes = 41 * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + 2 * kPtMax * 4 + (2 * 2 * 128 + 2 * 3 * 128) * 4 + 64;
+}  // namespace attn_tc
+
+struct AttnItem {
+  int b, g, split, nsplit, C, n_tiles_ctx, n_tiles;
+};
+
+__device__ __forceinline__ int item_splits(const AttnParams& p, int b) {
+  const int C = max(0, min(p.ctx_len[b], p.max_ctx));
+  const int n_ctx_tiles = (C + attn_tc::kTileK - 1) / attn_tc::kTileK;
+  return max(1, (n_ctx_tiles + attn::kTilesPerSplit - 1) / attn::kTilesPerSplit);
+}
+
+// Work item k (0 <= k < cum[B]) in sequence-major, then kv-head, then split
+// order; cum[b] = number of items of sequences before b.
+__device__ __forceinline__ void decode_item(const AttnParams& p, const int* cum, int k, AttnItem& it) {
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {          // last b with cum[b] <= k
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= k) lo = mid; else hi = mid - 1;
+  }
+  it.b = lo;
+  it.C = max(0, min(p.ctx_len[it.b], p.max_ctx));
+  const int n_ctx_tiles = (it.C + attn_tc::kTileK - 1) / attn_tc::kTileK;
+  it.nsplit = max(1, (n_ctx_tiles + attn::kTilesPerSplit - 1) / attn::kTilesPerSplit);
+  const int rem = k - cum[it.b];
+  it.g = rem / it.nsplit;
+  it.split = rem - it.g * it.nsplit;
+  const int t0 = it.split * attn::kTilesPerSplit;
+  it.n_tiles_ctx = max(0, min(n_ctx_tiles, t0 + attn::kTilesPerSplit) - t0);
+  it.n_tiles = it.n_tiles_ctx + ((it.split == it.nsplit - 1 && p.n_kv > 0) ? 1 : 0);
+}
+
+// 2^x on the special-function unit (flush-to-zero; P is rounded to bf16 anyway).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int kThreadsT>
+__global__ void __launch_bounds__(kThreadsT, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kbmap,
+               const __grid_constant__ CUtensorMap vbmap, const AttnParams p, int Ms, int S, int32_t* sched) {
+  using namespace attn_tc;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Roles, with W = ceil(M / 32) TMEM lane quarters holding real rows:
+  //   softmax   warps q and q + 4 for q < W (key columns 0-31 / 32-63 of a tile)
+  //   epilogue  warps 8 + q for q < W (O read-out of finished items)
+  //   producer  warp 2 (W <= 2) or 12; MMA issuer the warp after it
+  const int W = (p.M + 31) / 32;
+  const int n_sm = 2 * W;                    // softmax warps
+  const int prod_warp = W <= 2 ? 2 : 12, mma_warp = prod_warp + 1;
+  const int quarter = warp & 3, chalf = (warp >> 2) & 1;
+  const bool is_softmax = warp < 8 && quarter < W && warp != prod_warp && warp != mma_warp;
+  const bool is_epi = warp >= 8 && warp < 12 && quarter < W;
+
+  // shared memory: [Q0][Q1: 2 atoms x Ms rows each][P0][P1: Ms rows each][S stages: K | V][barriers, tables]
+  // A 128-row MMA reads past the Ms stored rows into the next buffer; those
+  // padding rows only produce padding rows of S, P and O, which are never used.
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int atom = Ms * 128;                 // one 64-wide column block of Ms rows
+  uint8_t* q_s = smem;                       // Q buffer i at + 2 i atom: d 0-63, then d 64-127
+  uint8_t* p_s = smem + 4 * atom;            // P buffer i at + i atom
+  uint8_t* kv_s = smem + 6 * atom;           // stage s: K at s*2*T, V at s*2*T + T
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + S * 2 * kTileBytes);
+  uint64_t* kv_full = bars;          // [5]
+  uint64_t* kv_empty = bars + 5;     // [5]
+  uint64_t* s_full = bars + 10;      // [2]
+  uint64_t* s_empty = bars + 12;     // [2]
+  uint64_t* p_full = bars + 14;      // [2]
+  uint64_t* pv_done = bars + 16;     // [2]
+  uint64_t* q_full = bars + 18;      // [2]
+  uint64_t* q_empty = bars + 20;     // [2]
+  uint64_t* it_full = bars + 22;     // [2]
+  uint64_t* it_empty = bars + 24;    // [2]
+  uint64_t* o_full = bars + 26;      // [2]  MMA -> epilogue: last P V of the item done
+  uint64_t* o_empty = bars + 28;     // [2]  epilogue -> MMA: O buffer read out
+  uint64_t* mma_done = bars + 30;
+  uint64_t* xbar = bars + 31;        // [4 quarters][2]: the two softmax warps of a quarter
+  uint64_t* l_full = bars + 39;      // [2]  softmax -> epilogue: row max and sums of the item
+  int* ring = reinterpret_cast<int*>(bars + 41);               // [2] item ids
+  int* cum = ring + 2;                                         // [B + 1] item prefix per sequence
+  int* pt_s = cum + (kMaxSeqs + 1);                            // [2][kPtMax] page rows of two items
+  float* xch = reinterpret_cast<float*>(pt_s + 2 * kPtMax);    // [2 tiles][2 halves][128] tile maxima
+  float* ml_s = xch + 2 * 2 * 128;                             // [2 slots][3][128]: m, l half 0, l half 1
+  uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(ml_s + 2 * 3 * 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sm + 1);
+  int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
+
+  if (tid == 0) {
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], n_sm);
+      mbar_init(&p_full[i], n_sm);
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&it_full[i], 1);
+      mbar_init(&it_empty[i], 1 + n_sm + W);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], W);
+      mbar_init(&l_full[i], n_sm);
+    }
+    mbar_init(mma_done, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 2);
+    *abort_flag = 0;
+    *consumed_sm = 0;
+    fence_barrier_init();
+  }
+  if (warp == mma_warp) tmem_alloc(tmem_base_sm, kTmemCols);
+  if (warp == 0) {
+    // cum[b] = sum over b' < b of Hkv * splits(b'): lane-contiguous runs, then a warp scan
+    const int per = (p.B + 31) / 32;
+    const int b0 = lane * per, b1 = min(p.B, b0 + per);
+    int tot = 0;
+    for (int bb = b0; bb < b1; ++bb) tot += p.Hkv * item_splits(p, bb);
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - tot;
+    for (int bb = b0; bb < b1; ++bb) {
+      cum[bb] = run;
+      run += p.Hkv * item_splits(p, bb);
+    }
+    if (lane == 31) cum[p.B] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_sm;
+  const int n_items = cum[p.B];
+  int producer_issued = 0;
+
+  if (warp == prod_warp) {
+    // ------------------------------ producer ------------------------------
+    // Items are claimed two ahead, and the page rows and Q of the next item are
+    // fetched while the current item's tiles stream, so that item boundaries
+    // leave no gap in the K/V stream.
+    const int ps = p.page_size;
+    int item_seq = 0, tile_seq = 0;
+    bool ok = true;
+    // page rows of item `item` into table `tb` (whole warp)
+    auto load_pages = [&](int item, int tb) {
+      AttnItem it;
+      decode_item(p, cum, item, it);
+      const int lp0 = it.split * attn::kTilesPerSplit * kTileK / ps;
+      const int n_lp = it.n_tiles_ctx * kTileK / ps;
+      for (int i = lane; i < n_lp; i += 32) {
+        const int lp = lp0 + i;
+        int row = 0;   // pages past the context (or bad entries) read page 0; masked later
+        if (lp * ps < it.C && lp < p.max_pages) {
+          const int phys = p.page_table[(size_t)it.b * p.max_pages + lp];
+          if (phys >= 0 && phys < p.num_pages) row = phys * ps;
+        }
+        pt_s[tb * kPtMax + i] = row;
+      }
+      __syncwarp();
+    };
+    // Q of item `item` into Q buffer `slot` (lane 0); false on abort
+    auto load_q = [&](int item, int seq) -> bool {
+      const int slot = seq & 1;
+      bool w = true;
+      if (lane == 0) {
+        w = wait_or_abort(&q_empty[slot], (uint32_t)(((seq >> 1) & 1) ^ 1), abort_flag, p.err, 22);
+        if (w) {
+          AttnItem it;
+          decode_item(p, cum, item, it);
+          uint8_t* qb = q_s + slot * 2 * atom;
+          // one TMA box [n_q][G][64] per d-half lands in the packed row order r = i * G + hh
+          mbar_arrive_expect_tx(&q_full[slot], (uint32_t)(2 * p.M * 128));
+          tma_load_3d(qb, &qmap, &q_full[slot], 0, it.g * p.G, it.b * p.n_q);
+          tma_load_3d(qb + atom, &qmap, &q_full[slot], 64, it.g * p.G, it.b * p.n_q);
+        }
+      }
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    };
+    int cur = 0, nxt = 0;
+    if (lane == 0) {
+      cur = atomicAdd(&sched[0], 1);
+      nxt = atomicAdd(&sched[0], 1);
+    }
+    cur = __shfl_sync(0xffffffffu, cur, 0);
+    nxt = __shfl_sync(0xffffffffu, nxt, 0);
+    if (cur < n_items) {
+      load_pages(cur, 0);
+      ok = load_q(cur, 0);
+    }
+    while (ok) {
+      const bool last = cur >= n_items;
+      const int slot = item_seq & 1;
+      bool w = true;
+      if (lane == 0) w = wait_or_abort(&it_empty[slot], (uint32_t)(((item_seq >> 1) & 1) ^ 1), abort_flag, p.err, 21);
+      if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) break;
+      if (lane == 0) {
+        ring[slot] = last ? -1 : cur;
+        mbar_arrive(&it_full[slot]);    // release semantics publish the ring entry
+      }
+      if (last) break;
+      int claimed = 0;                  // item after next; needed one item from now
+      if (lane == 0 && nxt < n_items) claimed = atomicAdd(&sched[0], 1);
+      AttnItem it;
+      decode_item(p, cum, cur, it);
+      const int* pt = pt_s + slot * kPtMax;
+      for (int j = 0; j < it.n_tiles && ok; ++j, ++tile_seq) {
+        if (lane == 0) {
+          const int st = tile_seq % S;
+          uint8_t* ks = kv_s + st * 2 * kTileBytes;
+          uint8_t* vs = ks + kTileBytes;
+          if (!wait_or_abort(&kv_empty[st], (uint32_t)(((tile_seq / S) & 1) ^ 1), abort_flag, p.err, 23)) {
+            ok = false;
+          } else if (j < it.n_tiles_ctx) {
+            mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
+            for (int pg = 0; pg < kTileK / ps; ++pg) {
+              const int row = pt[j * (kTileK / ps) + pg];
+              for (int h = 0; h < 2; ++h) {
+                tma_load_3d(ks + h * (kTileBytes / 2) + pg * ps * 128, &kmap, &kv_full[st], h * 64, it.g, row);
+                tma_load_3d(vs + h * (kTileBytes / 2) + pg * ps * 128, &vmap, &kv_full[st], h * 64, it.g, row);
+              }
+            }
+            ++producer_issued;
+          } else {
+            // the block's own n_kv K/V rows; rows past n_kv are masked (K) and
+            // zeroed (V) by the softmax warps
+            mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(4 * p.n_kv * 128));
+            for (int h = 0; h < 2; ++h) {
+              tma_load_3d(ks + h * (kTileBytes / 2), &kbmap, &kv_full[st], h * 64, it.g, it.b * p.n_kv);
+              tma_load_3d(vs + h * (kTileBytes / 2), &vbmap, &kv_full[st], h * 64, it.g, it.b * p.n_kv);
+            }
+            ++producer_issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        // a few tiles into this item, fetch the next item's page rows and Q
+        if (ok && j == min(2, it.n_tiles - 1) && nxt < n_items) {
+          load_pages(nxt, slot ^ 1);
+          ok = load_q(nxt, item_seq + 1);
+        }
+      }
+      cur = nxt;
+      nxt = __shfl_sync(0xffffffffu, nxt < n_items ? claimed : nxt, 0);
+      ++item_seq;
+    }
+    // the last CTA to finish resets the work counter for the next launch
+    if (lane == 0) {
+      __threadfence();
+      if (atomicAdd(&sched[1], 1) == (int)gridDim.x - 1) {
+        sched[0] = 0;
+        sched[1] = 0;
+        __threadfence();
+      }
+    }
+    __syncwarp();
+  } else if (warp == mma_warp) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_ab(128, kTileK, 0);
+      const uint32_t id_pv = idesc_bf16_ab(128, attn::kD, 1);
+      int consumed = 0, item_seq = 0, tile_seq = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = item_seq & 1;
+        const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
+        if (!wait_or_abort(&it_full[slot], par, abort_flag, p.err, 24)) break;
+        const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
+        mbar_arrive(&it_empty[slot]);
+        if (item < 0) break;
+        AttnItem it;
+        decode_item(p, cum, item, it);
+        if (!wait_or_abort(&q_full[slot], par, abort_flag, p.err, 25)) break;
+        if (!wait_or_abort(&o_empty[slot], par ^ 1u, abort_flag, p.err, 26)) break;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(q_s + slot * 2 * atom);
+        const uint32_t o_tmem = tmem_base + 128 + (uint32_t)(slot * attn::kD);
+        auto issue_pv = [&](int t, int j) -> bool {
+          if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
+          tc_fence_after();
+          const uint32_t pa = smem_u32(p_s + (t & 1) * atom);
+          const uint32_t va = smem_u32(kv_s + (t % S) * 2 * kTileBytes + kTileBytes);
+#pragma unroll
+          for (int i = 0; i < kTileK / 16; ++i)
+            tc_mma_bf16(o_tmem, sdesc_sw128(pa + i * 32), sdesc_sw128_mn(va + i * 2048, kTileBytes / 2), id_pv,
+                        (j > 0 || i > 0) ? 1u : 0u);
+          tc_commit(&pv_done[t & 1]);
+          tc_commit(&kv_empty[t % S]);
+          ++consumed;
+          return true;
+        };
+        for (int j = 0; j < it.n_tiles && ok; ++j) {
+          const int t = tile_seq + j;
+          const int st = t % S;
+          if (!wait_or_abort(&kv_full[st], (uint32_t)((t / S) & 1), abort_flag, p.err, 28)) { ok = false; break; }
+          if (!wait_or_abort(&s_empty[t & 1], (uint32_t)(((t >> 1) & 1) ^ 1), abort_flag, p.err, 29)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ka = smem_u32(kv_s + st * 2 * kTileBytes);
+#pragma unroll
+          for (int i = 0; i < attn::kD / 16; ++i) {
+            const uint32_t off = (uint32_t)((i >> 2) * (kTileBytes / 2) + (i & 3) * 32);
+            const uint32_t qoff = (uint32_t)((i >> 2) * atom + (i & 3) * 32);
+            tc_mma_bf16(tmem_base + (uint32_t)((t & 1) * kTileK), sdesc_sw128(qa + qoff), sdesc_sw128(ka + off),
+                        id_s, i > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[t & 1]);
+          if (j == it.n_tiles - 1) tc_commit(&q_empty[slot]);   // Q is no longer read
+          if (j >= 1) ok = issue_pv(t - 1, j - 1);
+        }
+        if (!ok) break;
+        if (!issue_pv(tile_seq + it.n_tiles - 1, it.n_tiles - 1)) break;
+        tc_commit(&o_full[slot]);
+        tile_seq += it.n_tiles;
+        ++item_seq;
+      }
+      *consumed_sm = consumed;
+      tc_commit(mma_done);
+      mbar_wait_bounded(mma_done, 0, p.err, 30);
+    }
+    __syncwarp();
+  } else if (is_softmax) {
+    // ------------------------------ softmax ------------------------------
+    const int r = quarter * 32 + lane;              // packed query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int c0 = chalf * 32;                      // this warp's 32 key columns of a tile
+    const uint32_t oc0 = (uint32_t)(chalf * 64);    // and 64 of the 128 O columns for rescaling
+    int item_seq = 0, tile_seq = 0;
+    bool ok = true;
+    int xs = 0;   // exchanges with the partner warp so far (both warps make the same sequence)
+    // publish this warp's shared-memory values to its partner and wait for the partner's
+    auto pair_exchange = [&]() -> bool {
+      uint64_t* bar = &xbar[quarter * 2 + (xs & 1)];
+      const uint32_t par = (uint32_t)((xs >> 1) & 1);
+      ++xs;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+      return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err, 37));
+    };
+    while (ok) {
+      const int slot = item_seq & 1;
+      const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
+      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[slot], par, abort_flag, p.err, 31))) break;
+      const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[slot]);
+      if (item < 0) break;
+      AttnItem it;
+      decode_item(p, cum, item, it);
+      const int t0 = it.split * attn::kTilesPerSplit;
+      const uint32_t o_col = 128 + (uint32_t)(slot * attn::kD) + oc0;
+      float m_run = -CUDART_INF_F, l_part = 0.f;
+      for (int j = 0; j < it.n_tiles; ++j) {
+        const int t = tile_seq + j;
+        const int sb = t & 1;
+        if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[sb], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 32))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[32];
+        {
+          uint32_t raw[32];
+          tmem_ld32(tmem_base + lane_off + (uint32_t)(sb * kTileK + c0), raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(raw[c]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[sb]);
+        const int valid = (j < it.n_tiles_ctx) ? min(kTileK, it.C - (t0 + j) * kTileK) : p.n_kv;
+        float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = (c0 + c) < valid ? sv[c] * p.scale_log2 : -CUDART_INF_F;
+          mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+        }
+        // tile max of the row over both column halves
+        float* xb = xch + (t & 1) * 256;
+        xb[chalf * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        if (!pair_exchange()) {
+          ok = false;
+          break;
+        }
+        const float mt = fmaxf(xb[r], xb[128 + r]);
+        const bool raise = mt > m_run + kRescaleLog2 || (m_run == -CUDART_INF_F && mt != -CUDART_INF_F);
+        const float m_new = raise ? mt : m_run;
+        const float alpha = raise ? (m_run == -CUDART_INF_F ? 0.f : exp2f(m_run - m_new)) : 1.f;
+        if (j >= 1 && __any_sync(0xffffffffu, raise)) {
+          // O must hold every earlier tile of the item before it is rescaled
+          if (!__all_sync(0xffffffffu, wait_or_abort(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1),
+                                                     abort_flag, p.err, 33))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem_base + lane_off + o_col + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+            tmem_st32(tmem_base + lane_off + o_col + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+        m_run = m_new;
+        const float base = (m_run == -CUDART_INF_F) ? 0.f : m_run;
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = ex2_ftz(sv[c] - base);
+          rs[c & 3] += sv[c];
+        }
+        l_part = l_part * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        // P buffer t & 1 was last read by the P V of tile t - 2
+        if (t >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&pv_done[sb], (uint32_t)(((t - 2) >> 1) & 1),
+                                                           abort_flag, p.err, 34))) {
+          ok = false;
+          break;
+        }
+        uint8_t* prow = p_s + sb * atom;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint4 v;
+          v.x = pack_bf16(sv[ch * 8 + 0], sv[ch * 8 + 1]);
+          v.y = pack_bf16(sv[ch * 8 + 2], sv[ch * 8 + 3]);
+          v.z = pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
+          v.w = pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
+          *reinterpret_cast<uint4*>(prow + swz(r, chalf * 4 + ch)) = v;
+        }
+        if (valid < kTileK) {
+          // V rows past the valid keys may hold anything (P is 0 there, but 0 * NaN is NaN)
+          uint8_t* vs = kv_s + (t % S) * 2 * kTileBytes + kTileBytes;
+          const int me = (chalf * W + quarter) * 32 + lane;
+          for (int vr = valid + me; vr < kTileK; vr += n_sm * 32)
+            for (int ch = 0; ch < 16; ++ch)
+              *reinterpret_cast<uint4*>((ch < 8 ? vs : vs + kTileBytes / 2) + swz(vr, ch & 7)) =
+                  make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+      }
+      if (!ok) break;
+      // hand the row max and this half's row sums to the epilogue warps; the
+      // slot is free again once the epilogue of item_seq - 2 released O (the
+      // MMA only started this item after that)
+      float* mls = ml_s + slot * 384;
+      if (chalf == 0) mls[r] = m_run;
+      mls[128 * (1 + chalf) + r] = l_part;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&l_full[slot]);
+      tile_seq += it.n_tiles;
+      ++item_seq;
+    }
+  } else if (is_epi) {
+    // ------------------------------ epilogue ------------------------------
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    int item_seq = 0;
+    while (true) {
+      const int slot = item_seq & 1;
+      const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
+      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[slot], par, abort_flag, p.err, 38))) break;
+      const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[slot]);
+      if (item < 0) break;
+      AttnItem it;
+      decode_item(p, cum, item, it);
+      if (!__all_sync(0xffffffffu, wait_or_abort(&l_full[slot], par, abort_flag, p.err, 39))) break;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&o_full[slot], par, abort_flag, p.err, 35))) break;
+      tc_fence_after();
+      const float* mls = ml_s + slot * 384;
+      const float m_run = mls[r];
+      const float l_run = mls[128 + r] + mls[256 + r];
+      const bool single = (it.nsplit == 1);
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const size_t cta = ((size_t)it.b * p.Hkv + it.g) * p.max_splits + it.split;
+      const uint32_t o_col = 128 + (uint32_t)(slot * attn::kD);
+      for (int c = 0; c < attn::kD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem_base + lane_off + o_col + c * 32, o);
+        tmem_ld_wait();
+        if (r < p.M) {
+          if (single) {
+            const int i = r / p.G, hh = r - i * p.G;
+            bf16* dst = p.out + ((size_t)(it.b * p.n_q + i) * p.Hq + it.g * p.G + hh) * attn::kD + c * 32;
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(o[q + 0]) * inv, __uint_as_float(o[q + 1]) * inv);
+              v.y = pack_bf16(__uint_as_float(o[q + 2]) * inv, __uint_as_float(o[q + 3]) * inv);
+              v.z = pack_bf16(__uint_as_float(o[q + 4]) * inv, __uint_as_float(o[q + 5]) * inv);
+              v.w = pack_bf16(__uint_as_float(o[q + 6]) * inv, __uint_as_float(o[q + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + q) = v;
+            }
+          } else {
+            float* dst = p.part_o + (cta * p.M + r) * attn::kD + c * 32;
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+              *reinterpret_cast<float4*>(dst + q) = make_float4(__uint_as_float(o[q]), __uint_as_float(o[q + 1]),
+                                                                __uint_as_float(o[q + 2]), __uint_as_float(o[q + 3]));
+          }
+        }
+      }
+      if (!single && r < p.M) p.part_ml[cta * p.M + r] = make_float2(m_run, l_run);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[slot]);
+      ++item_seq;
+    }
+  }
+
+  // ------------------------------ teardown ------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == prod_warp && lane == 0 && *abort_flag)
+    for (int i = *consumed_sm; i < producer_issued; ++i)
+      mbar_wait_bounded(&kv_full[i % S], (uint32_t)((i / S) & 1), p.err, 36);
+  __syncthreads();
+  if (warp == mma_warp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Merge the split partials of every (sequence, kv head) that was split.
+__global__ void __launch_bounds__(256)
+attn_merge_kernel(const AttnParams p) {
+  const int g = blockIdx.x, b = blockIdx.y;
+  const int C = max(0, min(p.ctx_len[b], p.max_ctx));
+  const int n_ctx_tiles = (C + attn_tc::kTileK - 1) / attn_tc::kTileK;
+  const int nsplit = max(1, (n_ctx_tiles + attn::kTilesPerSplit - 1) / attn::kTilesPerSplit);
+  if (nsplit == 1) return;
+  const size_t group = (size_t)b * p.Hkv + g;
+  for (int idx = threadIdx.x; idx < p.M * (attn::kD / 4); idx += blockDim.x) {
+    const int row = idx / (attn::kD / 4), d4 = idx - row * (attn::kD / 4);
+    float M = -CUDART_INF_F;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, p.part_ml[(group * p.max_splits + sp) * p.M + row].x);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -CUDART_INF_F) {
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const size_t c2 = group * p.max_splits + sp;
+        const float2 ml = p.part_ml[c2 * p.M + row];
+        const float w = (ml.x == -CUDART_INF_F) ? 0.f : exp2f(ml.x - M);
+        L += ml.y * w;
+        const float4 v = reinterpret_cast<const float4*>(p.part_o + (c2 * p.M + row) * attn::kD)[d4];
+        acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int i = row / p.G, hh = row - i * p.G;
+    bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.G + hh) * attn::kD + d4 * 4;
+    reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  }
+}
+
+// ===========================================================================
 // Generic path: one CTA per (query position, q head, sequence), fp32 math.
 // ===========================================================================
 template <typename T>
@@ -432,7 +1031,8 @@ attn_generic_kernel(const T* __restrict__ q, const T* __restrict__ k_blk, const 
 // ===========================================================================
 static bool bf16_fast_ok(const AttnArgs& a) {
   const int M = a.n_q * (a.Hq / a.Hkv);
-  return a.dtype == 1 && a.D == 128 && M <= 16 * attn::kMaxWarps && a.n_kv <= attn::kTileK &&
+  return a.dtype == 1 && a.D == 128 && M <= 16 * attn::kMaxWarps && a.n_kv >= 1 && a.n_kv <= attn::kTileK &&
+         a.B <= attn_tc::kMaxSeqs &&
          (a.page_size == 8 || a.page_size == 16 || a.page_size == 32 || a.page_size == 64) &&
          a.num_pages * (long)a.page_size < (1L << 31) &&
          (reinterpret_cast<uintptr_t>(a.k_pool) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.v_pool) & 15) == 0 &&
@@ -452,7 +1052,8 @@ size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_c
   return align_up(ctas * M * 128 * sizeof(float)) + align_up(ctas * M * sizeof(float2));
 }
 
-cudaError_t launch_block_attn(const AttnArgs& a) {
+cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
+  *launches = 1;
   if (!bf16_fast_ok(a)) {
     dim3 grid(a.n_q, a.Hq, a.B);
     if (a.dtype == 0)
@@ -497,16 +1098,46 @@ cudaError_t launch_block_attn(const AttnArgs& a) {
   p.part_ml = (float2*)(ws + align_up(ctas * M * 128 * sizeof(float)));
   p.counters = a.counters;
   p.err = a.err;
-  const int nwarps = (M + 15) / 16;
-  const size_t smem = 1024 + kStages * 2 * kTileBytes + kStages * 8;
-  static size_t smem_set = 0;   // largest dynamic shared memory opted into so far
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set = smem;
+  CUtensorMap qmap, kbmap, vbmap;
+  {
+    const uint64_t qd[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)a.B * a.n_q};
+    const uint64_t qs[2] = {(uint64_t)kD * 2, (uint64_t)a.Hq * kD * 2};
+    const uint32_t qb[3] = {64, (uint32_t)(a.Hq / a.Hkv), (uint32_t)a.n_q};
+    const uint64_t bd[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.B * a.n_kv};
+    const uint64_t bs[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};
+    const uint32_t bb[3] = {64, 1, (uint32_t)a.n_kv};
+    if (!encode_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qd, qs, qb,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&kbmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_blk), bd, bs, bb,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&vbmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_blk), bd, bs, bb,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorNotSupported;
   }
-  dim3 grid(p.max_splits, a.Hkv, a.B);
-  attn_bf16_kernel<<<grid, nwarps * 32, smem, a.stream>>>(kmap, vmap, p);
+  const int Ms = M <= 64 ? 64 : 128;     // stored query rows per operand atom
+  const int S = Ms == 64 ? 5 : 3;        // K/V stages that fit beside Q and P
+  const size_t smem = 1024 + 6 * (size_t)Ms * 128 + (size_t)S * 2 * attn_tc::kTileBytes + attn_tc::kBarBytes;
+  // warps 0-9 (two softmax quarters, producer, MMA, epilogue 8-9) or 0-13
+  const bool wide = (M + 31) / 32 > 2;
+  static size_t smem_set[2] = {0, 0};   // largest dynamic shared memory opted into so far
+  if (smem > smem_set[wide]) {
+    cudaError_t e = wide ? cudaFuncSetAttribute(attn_tc_kernel<448>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)smem)
+                         : cudaFuncSetAttribute(attn_tc_kernel<320>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set[wide] = smem;
+  }
+  if (wide)
+    attn_tc_kernel<448><<<attn_tc::kGrid, 448, smem, a.stream>>>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, a.sched);
+  else
+    attn_tc_kernel<320><<<attn_tc::kGrid, 320, smem, a.stream>>>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, a.sched);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.max_splits > 1) {
+    attn_merge_kernel<<<dim3(a.Hkv, a.B), 256, 0, a.stream>>>(p);
+    *launches = 2;
+  }
   return cudaGetLastError();
 }
 

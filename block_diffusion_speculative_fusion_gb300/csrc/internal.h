@@ -76,13 +76,14 @@ struct AttnArgs {
   float scale;
   void* out;
   int32_t* counters;
+  int32_t* sched;   // two zeroed ints: persistent-kernel work counter and exit counter
   int* err;
   void* scratch;
   cudaStream_t stream;
 };
 
 size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int dtype);
-cudaError_t launch_block_attn(const AttnArgs& a);
+cudaError_t launch_block_attn(const AttnArgs& a, int* launches);
 
 // ----------------------------------------------------------- materialise ---
 constexpr int kMaxLayers = 16;
