@@ -369,7 +369,7 @@ def run_kernel(args, wl):
     from block_diffusion_speculative_fusion_gb300.step import DflashStep
     if args.batch:
         wl = dataclasses.replace(wl, B=args.batch, n_greedy=min(wl.n_greedy, args.batch // 2))
-    one = dataclasses.replace(wl, L=1) if args.kernel == "attn" else wl
+    one = dataclasses.replace(wl, L=1) if args.kernel in ("attn", "verify") else wl
     st = DflashStep(one, seed=0, device="cuda:0", headroom_steps=4)
     inp = st.inp
     ng = wl.n_greedy

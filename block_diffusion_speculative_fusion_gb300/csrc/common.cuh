@@ -76,6 +76,20 @@ __device__ __forceinline__ void reset_ticket(int32_t* counter) {
   if (threadIdx.x == 0) atomicExch(counter, 0);
 }
 
+// Variant for results written by thread 0 alone: only thread 0 fences.
+__device__ __forceinline__ bool take_ticket_is_last_t0(int32_t* counter, int group_size) {
+  __shared__ int s_last0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int t = atomicAdd(counter, 1);
+    s_last0 = (t == group_size - 1);
+    if (s_last0) __threadfence();
+  }
+  __syncthreads();
+  return s_last0 != 0;
+}
+
 // ---------------------------------------------------------------------------
 // Online max / scaled-sum pairs: s = sum exp2((z - m) * k)
 // ---------------------------------------------------------------------------

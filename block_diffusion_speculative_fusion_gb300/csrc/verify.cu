@@ -82,6 +82,14 @@ __device__ __forceinline__ MS block_ms(MS x, float k2) {
   return x;  // valid in thread 0
 }
 
+// 2^x on the special-function unit, flushing denormal results to zero (terms
+// below 2^-126 of a row maximum do not change a sum that contains 1).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Streaming (max, sum exp2((z - max) * k2)) of elements [e0, e1) of one row.
 // The same code serves target and draft rows, so identical rows give
 // bit-identical statistics.
@@ -100,7 +108,7 @@ __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2)
     if (acc.m == -CUDART_INF_F) return;
     float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < N; ++j) s += exp2f((f[j] - acc.m) * k2);
+    for (int j = 0; j < N; ++j) s += ex2_ftz((f[j] - acc.m) * k2);
     acc.s += s;
   };
   auto add_one = [&](float v, int) {
@@ -108,7 +116,7 @@ __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2)
       acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f((acc.m - v) * k2);
       acc.m = v;
     }
-    if (acc.m != -CUDART_INF_F) acc.s += exp2f((v - acc.m) * k2);
+    if (acc.m != -CUDART_INF_F) acc.s += ex2_ftz((v - acc.m) * k2);
   };
   for_range<T, 4>(z, e0, e1, add_vec, add_one);
   return block_ms(acc, k2);
@@ -146,7 +154,7 @@ greedy_kernel(const T* __restrict__ logits, const int64_t* __restrict__ cand,
     best = block_vi(best);
   }
   if (threadIdx.x == 0) parts[(size_t)row * nch + c] = best;
-  if (!take_ticket_is_last(&counters[b], R * nch)) return;
+  if (!take_ticket_is_last_t0(&counters[b], R * nch)) return;
 
   // ---- last CTA of sequence b: argmax per row, then the accept rule ----
   __shared__ int32_t tp[kMaxRows];
@@ -223,7 +231,7 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
     }
   }
   if (threadIdx.x == 0) parts[((size_t)b * RR + r) * nch + c] = ms;
-  if (!take_ticket_is_last(&counters[b], RR * nch)) return;
+  if (!take_ticket_is_last_t0(&counters[b], RR * nch)) return;
 
   // ---- last CTA of sequence b ----
   __shared__ MS rs[2 * kMaxRows];
@@ -388,7 +396,7 @@ sample_resample_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
     for (int q = 0; q < (int)(blockDim.x >> 5); ++q) { tr += shr[q]; tp += shp[q]; }
     parts[(size_t)b * nch + c] = make_float2(tr, tp);
   }
-  if (!take_ticket_is_last(&counters[b], nch)) return;
+  if (!take_ticket_is_last_t0(&counters[b], nch)) return;
 
   // ---- last CTA of sequence b: locate the chunk, then the token ----
   // Column x of the partials holds the drawn weights (residual, or p after a
@@ -532,7 +540,7 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
     }
   }
   if (threadIdx.x == 0) parts[(size_t)row * nch + c] = ms;
-  if (!take_ticket_is_last(&counters[b], k * nch)) return;
+  if (!take_ticket_is_last_t0(&counters[b], k * nch)) return;
 
   __shared__ MS rs[kMaxRows];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -573,17 +581,18 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
 // ===========================================================================
 static int vec_elems(int dtype) { return dtype == 0 ? 4 : 8; }
 
-// Chunks per row: enough CTAs to cover every SM several times over, each
-// thread handling at least one 16-byte vector per chunk.
+// Chunks per row: the grid (rows x chunks) is sized to one wave of resident
+// CTAs (8 per SM) so that no partial wave trails the kernel; each thread
+// handles at least one 16-byte vector per chunk.
 ChunkPlan plan_chunks(int rows, int V, int dtype, int num_sms) {
   const int per_thread_vec = kThreads * vec_elems(dtype);
-  const int units = (V + per_thread_vec - 1) / per_thread_vec;   // vectors per thread for a whole row
-  const long target = 8L * num_sms;
-  long u = (long)rows * units / target;
-  if (u < 1) u = 1;
-  if (u > units) u = units;
+  const int units = (V + per_thread_vec - 1) / per_thread_vec;   // vector rounds for a whole row
+  const long wave = 8L * num_sms;
+  long nch = wave / (rows > 0 ? rows : 1);
+  if (nch < 1) nch = 1;
+  if (nch > units) nch = units;
   ChunkPlan p;
-  p.chunk = (int)u * per_thread_vec;
+  p.chunk = (int)((units + nch - 1) / nch) * per_thread_vec;
   p.nch = (V + p.chunk - 1) / p.chunk;
   return p;
 }
