@@ -53,7 +53,9 @@ int check_verify_dims(const dflash_verify_dims* d, bool sampled) {
   if (d->B < 1 || d->n_max < 0 || d->V < 1) return fail(DFLASH_ERR_INVALID_ARG, "bad dims B=%d n_max=%d V=%d", d->B, d->n_max, d->V);
   if (bad_dtype(d->dtype)) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
   if (d->n_max + 1 > 256) return fail(DFLASH_ERR_UNSUPPORTED, "n_max=%d > 255", d->n_max);
-  if ((sampled ? 2 : 1) * d->B > kMaxCounters) return fail(DFLASH_ERR_UNSUPPORTED, "B=%d too large", d->B);
+  if (sampled && (long)d->V > 1024L * 16384L) return fail(DFLASH_ERR_UNSUPPORTED, "V=%d too large", d->V);
+  if (d->B > kMaxCounters) return fail(DFLASH_ERR_UNSUPPORTED, "B=%d too large", d->B);
+  (void)sampled;
   if ((long)d->B * (2L * d->n_max + 1) > 65535L) return fail(DFLASH_ERR_UNSUPPORTED, "B*(2*n_max+1) > 65535");
   return DFLASH_OK;
 }

@@ -91,25 +91,42 @@ __device__ __forceinline__ bool take_ticket_is_last_t0(int32_t* counter, int gro
 }
 
 // ---------------------------------------------------------------------------
-// Online max / scaled-sum pairs: s = sum exp2((z - m) * k)
+// Online max / scaled-sum pairs in log2 units: a row's statistics are
+// m = max(z) * k2 (rounded once) and s = sum 2^(z * k2 - m) with every exponent
+// formed by one fused multiply-add, so that the same expression evaluated later
+// for one element of the row is consistent with the sum.
 // ---------------------------------------------------------------------------
 struct MS { float m; float s; };
 
-__device__ __forceinline__ MS ms_merge(MS a, MS b, float k2) {
+__device__ __forceinline__ MS ms_merge(MS a, MS b) {
   const float M = fmaxf(a.m, b.m);
   if (M == -CUDART_INF_F) return MS{M, 0.f};
-  const float sa = (a.m == -CUDART_INF_F) ? 0.f : a.s * exp2f((a.m - M) * k2);
-  const float sb = (b.m == -CUDART_INF_F) ? 0.f : b.s * exp2f((b.m - M) * k2);
+  const float sa = (a.m == -CUDART_INF_F) ? 0.f : a.s * exp2f(a.m - M);
+  const float sb = (b.m == -CUDART_INF_F) ? 0.f : b.s * exp2f(b.m - M);
   return MS{M, sa + sb};
 }
 
-__device__ __forceinline__ MS warp_ms(MS v, float k2) {
+__device__ __forceinline__ MS warp_ms(MS v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
-    v = ms_merge(v, w, k2);
+    v = ms_merge(v, w);
   }
   return v;
+}
+
+// Largest of the 8 (bf16) or 4 (fp32) values of a 16-byte vector.
+template <typename T> __device__ __forceinline__ float vec_max(const uint4& u);
+template <> __device__ __forceinline__ float vec_max<bf16>(const uint4& u) {
+  const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.x),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u.z),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&u.w));
+  const __nv_bfloat162 c = __hmax2(a, b);
+  return fmaxf(__low2float(c), __high2float(c));
+}
+template <> __device__ __forceinline__ float vec_max<float>(const uint4& u) {
+  return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)), fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
 }
 
 // (value, index) maximum with the lowest index among equal values.

@@ -15,7 +15,6 @@ struct ChunkPlan {
 };
 
 ChunkPlan plan_chunks(int rows, int V, int dtype, int num_sms);
-int resample_chunks(int V, int dtype);
 
 // ---------------------------------------------------------------- verify ---
 struct VerifyArgs {

@@ -17,9 +17,11 @@ namespace dflash {
 
 constexpr int kThreads = 256;
 constexpr int kMaxRows = 256;    // n_max + 1 limit (drafts per verify <= 255)
+constexpr int kMaxDrawChunks = 1024;   // vocabulary <= 1024 x 16384
 
 // Visit elements [e0, e1) of row z: 16-byte vectors in the aligned middle,
-// scalars at both ends. fv(f, first_index) gets N unpacked values, fs(v, i) one.
+// scalars at both ends. fv(u, first_index) gets one raw 16-byte vector, fs(v, i)
+// one value. A thread visits its vectors in ascending index order.
 template <typename T, int UNROLL, typename FV, typename FS>
 __device__ __forceinline__ void for_range(const T* z, int e0, int e1, FV&& fv, FS&& fs) {
   constexpr int N = VecTraits<T>::N;
@@ -38,17 +40,9 @@ __device__ __forceinline__ void for_range(const T* z, int e0, int e1, FV&& fv, F
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) r[u] = ld_stream16(vp + v + u * blockDim.x);
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      float f[N];
-      unpack16<T>(r[u], f);
-      fv(f, a + (v + u * (int)blockDim.x) * N);
-    }
+    for (int u = 0; u < UNROLL; ++u) fv(r[u], a + (v + u * (int)blockDim.x) * N);
   }
-  for (; v < nvec; v += blockDim.x) {
-    float f[N];
-    unpack16<T>(ld_stream16(vp + v), f);
-    fv(f, a + v * N);
-  }
+  for (; v < nvec; v += blockDim.x) fv(ld_stream16(vp + v), a + v * N);
 }
 
 // ---------------------------------------------------------------------------
@@ -68,16 +62,16 @@ __device__ __forceinline__ VI block_vi(VI x) {
   return x;  // valid in thread 0
 }
 
-__device__ __forceinline__ MS block_ms(MS x, float k2) {
+__device__ __forceinline__ MS block_ms(MS x) {
   __shared__ MS sh[kThreads / 32];
-  x = warp_ms(x, k2);
+  x = warp_ms(x);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
   if (l == 0) sh[w] = x;
   __syncthreads();
   if (w == 0) {
     x = (l < (int)(blockDim.x >> 5)) ? sh[l] : MS{-CUDART_INF_F, 0.f};
-    x = warp_ms(x, k2);
+    x = warp_ms(x);
   }
   return x;  // valid in thread 0
 }
@@ -90,36 +84,37 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   return y;
 }
 
-// Streaming (max, sum exp2((z - max) * k2)) of elements [e0, e1) of one row.
-// The same code serves target and draft rows, so identical rows give
-// bit-identical statistics.
+// Streaming statistics of elements [e0, e1) of one row in log2 units:
+// m = max(z) * k2, s = sum 2^(fma(z, k2, -m)). The same code serves target and
+// draft rows, so identical rows give bit-identical statistics.
 template <typename T>
 __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2) {
   constexpr int N = VecTraits<T>::N;
+  float zmax = -CUDART_INF_F;   // running max in logit units (exact comparisons)
   MS acc{-CUDART_INF_F, 0.f};
-  auto add_vec = [&](const float* f, int) {
-    float vm = f[0];
-#pragma unroll
-    for (int j = 1; j < N; ++j) vm = fmaxf(vm, f[j]);
-    if (vm > acc.m) {
-      acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f((acc.m - vm) * k2);
-      acc.m = vm;
-    }
-    if (acc.m == -CUDART_INF_F) return;
+  auto raise_to = [&](float v) {
+    const float m2 = v * k2;
+    acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f(acc.m - m2);
+    acc.m = m2;
+    zmax = v;
+  };
+  auto add_vec = [&](const uint4& u, int) {
+    const float vm = vec_max<T>(u);
+    if (vm > zmax) raise_to(vm);
+    if (zmax == -CUDART_INF_F) return;
+    float f[N];
+    unpack16<T>(u, f);
     float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < N; ++j) s += ex2_ftz((f[j] - acc.m) * k2);
+    for (int j = 0; j < N; ++j) s += ex2_ftz(fmaf(f[j], k2, -acc.m));
     acc.s += s;
   };
   auto add_one = [&](float v, int) {
-    if (v > acc.m) {
-      acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f((acc.m - v) * k2);
-      acc.m = v;
-    }
-    if (acc.m != -CUDART_INF_F) acc.s += ex2_ftz((v - acc.m) * k2);
+    if (v > zmax) raise_to(v);
+    if (zmax != -CUDART_INF_F) acc.s += ex2_ftz(fmaf(v, k2, -acc.m));
   };
-  for_range<T, 4>(z, e0, e1, add_vec, add_one);
-  return block_ms(acc, k2);
+  for_range<T, 8>(z, e0, e1, add_vec, add_one);
+  return block_ms(acc);
 }
 
 // ===========================================================================
@@ -142,15 +137,20 @@ greedy_kernel(const T* __restrict__ logits, const int64_t* __restrict__ cand,
     const T* z = logits + (size_t)row * V;
     const int e0 = c * chunk, e1 = min(V, e0 + chunk);
     constexpr int N = VecTraits<T>::N;
-    auto on_vec = [&](const float* f, int i0) {
+    auto on_vec = [&](const uint4& u, int i0) {
+      const float vm = vec_max<T>(u);          // packed max; the index search is rare
+      if (vm > best.v || (vm == best.v && i0 < best.i)) {
+        float f[N];
+        unpack16<T>(u, f);
 #pragma unroll
-      for (int j = 0; j < N; ++j)
-        if (vi_better(f[j], i0 + j, best)) best = VI{f[j], i0 + j};
+        for (int j = N - 1; j >= 0; --j)
+          if (f[j] == vm) best = VI{vm, i0 + j};   // ends on the lowest index
+      }
     };
     auto on_one = [&](float v, int e) {
       if (vi_better(v, e, best)) best = VI{v, e};
     };
-    for_range<T, 4>(z, e0, e1, on_vec, on_one);
+    for_range<T, 8>(z, e0, e1, on_vec, on_one);
     best = block_vi(best);
   }
   if (threadIdx.x == 0) parts[(size_t)row * nch + c] = best;
@@ -191,9 +191,6 @@ greedy_kernel(const T* __restrict__ logits, const int64_t* __restrict__ cand,
   reset_ticket(&counters[b]);
 }
 
-// ===========================================================================
-// Sampled rule, pass 1: row statistics, then the sequential accept test
-// ===========================================================================
 struct SampleJob {
   int32_t row;     // target row the bonus is drawn from (= accept_len)
   int32_t mode;    // 0: residual max(0, p - q) at that row, 1: p at that row
@@ -202,6 +199,244 @@ struct SampleJob {
   int32_t acc;
   int32_t flags;
 };
+
+// ===========================================================================
+// Sampled rule, pass 2: inverse-CDF draw of the bonus from the residual
+// max(0, p - q) (or from p after a full accept) in ascending token order:
+// chunk sums, then segment sums of the chosen chunk (fp64 prefix), then a warp
+// scan over the chosen 64-token segment.
+// ===========================================================================
+// Weights of the 16-byte vectors (t, d) at token e: residual, or p (use_p),
+// and the p values themselves. Tokens past V weigh 0.
+template <typename T>
+__device__ __forceinline__ void pair_weights(const uint4& vt, const uint4& vd, const SampleJob& j, float k2,
+                                             bool use_p, float* w, float* pv) {
+  constexpr int N = VecTraits<T>::N;
+  float ft[N], fd[N];
+  unpack16<T>(vt, ft);
+  if (!use_p) unpack16<T>(vd, fd);
+  const float inv_st = 1.f / j.st, inv_sd = 1.f / j.sd;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    pv[q] = exp2f(fmaf(ft[q], k2, -j.mt)) * inv_st;
+    w[q] = use_p ? pv[q] : fmaxf(0.f, pv[q] - exp2f(fmaf(fd[q], k2, -j.md)) * inv_sd);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 load_vec_or_pad(const T* row, int e, int V) {
+  constexpr int N = VecTraits<T>::N;
+  if (e + N <= V && (reinterpret_cast<uintptr_t>(row + e) & 15u) == 0)
+    return __ldg(reinterpret_cast<const uint4*>(row + e));
+  T tmp[N];
+#pragma unroll
+  for (int q = 0; q < N; ++q) tmp[q] = (e + q < V) ? row[e + q] : from_f32<T>(-CUDART_INF_F);
+  return *reinterpret_cast<const uint4*>(tmp);
+}
+
+// Pass 2 grid: CTA (c, b) owns tokens [c * kDrawChunk, (c + 1) * kDrawChunk) of
+// sequence b's drawn row; thread t owns the contiguous segment of kDrawSeg
+// tokens at c * kDrawChunk + t * kDrawSeg. The CDF order is chunk, thread, token.
+constexpr int kDrawSeg = 64;                      // tokens per thread
+constexpr int kDrawChunk = kThreads * kDrawSeg;   // tokens per CTA
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+sample_draw_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const float* __restrict__ u_final,
+                   int n_max, int V, int nch, float k2, const SampleJob* __restrict__ jobs,
+                   float2* __restrict__ parts, float2* __restrict__ segs, int32_t* __restrict__ counters,
+                   int64_t* __restrict__ bonus, int64_t* __restrict__ out_tokens, uint8_t* __restrict__ flags_out,
+                   float* __restrict__ probs) {
+  constexpr int N = VecTraits<T>::N;
+  constexpr int NV = kDrawSeg / N;
+  const int c = blockIdx.x, b = blockIdx.y;
+  const int R = n_max + 1;
+  const SampleJob j = jobs[b];
+  const bool usep_r = (j.mode == 1);
+  const T* zt_row = zt + ((size_t)b * R + j.row) * V;
+  const T* zd_row = zd + ((size_t)b * n_max + min(j.row, max(n_max - 1, 0))) * V;
+  const int e0 = c * kDrawChunk + (int)threadIdx.x * kDrawSeg;
+  // ---- pass 1: segment sums of the drawn weights (residual, or p) and of p ----
+  float sr = 0.f, sp = 0.f;
+  {
+    uint4 vt[NV], vd[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      vt[i] = load_vec_or_pad<T>(zt_row, e0 + i * N, V);
+      if (!usep_r) vd[i] = load_vec_or_pad<T>(zd_row, e0 + i * N, V);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      float w[N], pv[N];
+      pair_weights<T>(vt[i], vd[i], j, k2, usep_r, w, pv);
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        sr += w[q];
+        sp += pv[q];
+      }
+    }
+  }
+  segs[((size_t)b * nch + c) * kThreads + threadIdx.x] = make_float2(sr, sp);
+  __shared__ float shr[kThreads / 32], shp[kThreads / 32];
+  float xr = sr, xp = sp;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    xr += __shfl_xor_sync(0xffffffffu, xr, o);
+    xp += __shfl_xor_sync(0xffffffffu, xp, o);
+  }
+  const int wid = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) { shr[wid] = xr; shp[wid] = xp; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tr = 0.f, tp = 0.f;
+    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) { tr += shr[q]; tp += shp[q]; }
+    parts[(size_t)b * nch + c] = make_float2(tr, tp);
+  }
+  if (!take_ticket_is_last(&counters[b], nch)) return;
+
+  // ---- last CTA of sequence b: chunk, then segment, then token ----
+  __shared__ float2 csum[kMaxDrawChunks];
+  __shared__ double s_target, s_Z, s_before;
+  __shared__ int s_chunk, s_degenerate, s_seg, s_y;
+  __shared__ double s_clo, s_chi;
+  for (int cc = threadIdx.x; cc < nch; cc += blockDim.x) csum[cc] = __ldcg(parts + (size_t)b * nch + cc);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double Zr = 0.0, Zp = 0.0;
+    for (int cc = 0; cc < nch; ++cc) {
+      Zr += csum[cc].x;
+      Zp += csum[cc].y;
+    }
+    const int degenerate = (j.mode == 0 && Zr == 0.0) ? 1 : 0;
+    const double Z = degenerate ? Zp : Zr;
+    const double target = (double)u_final[b] * Z;
+    double cum = 0.0, before = 0.0;
+    int cstar = -1, last_nz = 0;
+    for (int cc = 0; cc < nch; ++cc) {
+      const double sc = degenerate ? csum[cc].y : csum[cc].x;
+      if (sc > 0.0) last_nz = cc;
+      if (cstar < 0 && cum + sc > target) { cstar = cc; before = cum; }
+      cum += sc;
+    }
+    if (cstar < 0) {   // rounding put the target past the last step
+      cstar = last_nz;
+      before = 0.0;
+      for (int cc = 0; cc < last_nz; ++cc) before += degenerate ? csum[cc].y : csum[cc].x;
+    }
+    s_target = target;
+    s_Z = Z;
+    s_before = before;
+    s_chunk = cstar;
+    s_degenerate = degenerate;
+    s_seg = -1;
+    s_y = INT32_MAX;
+  }
+  __syncthreads();
+  const bool degenerate = s_degenerate != 0;
+  // segment sums of the chosen chunk (written by its CTA) and their fp64 prefix
+  const float2 sv = __ldcg(segs + ((size_t)b * nch + s_chunk) * kThreads + threadIdx.x);
+  const float ts = degenerate ? sv.y : sv.x;
+  double incl = ts;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (l >= o) incl += x;
+  }
+  __shared__ double wsum[kThreads / 32];
+  if (l == 31) wsum[wid] = incl;
+  __syncthreads();
+  double base = s_before;
+  for (int q = 0; q < wid; ++q) base += wsum[q];
+  const double excl = base + incl - (double)ts;
+  if (ts > 0.f && excl <= s_target && excl + (double)ts > s_target) {
+    s_seg = threadIdx.x;        // unique: the segment ranges are disjoint
+    s_clo = excl;
+  }
+  __syncthreads();
+  // warp 0 walks the chosen segment: lane k holds tokens [2k, 2k + 2) of it
+  if (wid == 0) {
+    int seg = s_seg;
+    double sbase = s_clo;
+    if (seg < 0) {              // rounding: take the last segment with weight
+      seg = kThreads - 1;
+      sbase = s_target;
+    }
+    const int es = s_chunk * kDrawChunk + seg * kDrawSeg;
+    float w2[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int e = es + 2 * l + q;
+      float wt = 0.f;
+      if (e < V) {
+        const float pt = exp2f(fmaf(to_f32(zt_row[e]), k2, -j.mt)) / j.st;
+        if (usep_r || degenerate) {
+          wt = pt;
+        } else {
+          const float qd = exp2f(fmaf(to_f32(zd_row[e]), k2, -j.md)) / j.sd;
+          wt = fmaxf(0.f, pt - qd);
+        }
+      }
+      w2[q] = wt;
+    }
+    const float pair = w2[0] + w2[1];
+    float inc = pair;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float x = __shfl_up_sync(0xffffffffu, inc, o);
+      if (l >= o) inc += x;
+    }
+    const float rel = (float)(s_target - sbase);
+    const float ex = inc - pair;
+    int yl = INT32_MAX;
+    double clo = 0.0, chi = 0.0;
+    if (s_seg >= 0 && ex <= rel && inc > rel) {
+      const bool first = ex + w2[0] > rel;
+      yl = es + 2 * l + (first ? 0 : 1);
+      clo = sbase + (double)(first ? ex : ex + w2[0]);
+      chi = sbase + (double)(first ? ex + w2[0] : inc);
+    }
+    // lowest lane that holds the crossing (ties from rounding resolve low)
+    const unsigned hit = __ballot_sync(0xffffffffu, yl != INT32_MAX);
+    int lastw = -1;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (w2[q] > 0.f) lastw = es + 2 * l + q;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lastw = max(lastw, __shfl_xor_sync(0xffffffffu, lastw, o));
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      if (l == src) {
+        s_y = yl;
+        s_clo = clo;
+        s_chi = chi;
+      }
+    } else if (l == 0) {
+      s_y = lastw >= 0 ? lastw : es;
+      s_clo = s_target;
+      s_chi = s_target;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int y = s_y;
+    const double Z = s_Z, u = u_final[b];
+    int flags = j.flags;
+    if (Z > 0.0 && (fabs(s_clo / Z - u) < 1e-6 || fabs(s_chi / Z - u) < 1e-6)) flags |= 2;  // CDF_BOUNDARY
+    if (degenerate) flags |= 4;                                                           // DEGENERATE
+    bonus[b] = y;
+    if (flags_out) flags_out[b] = (uint8_t)flags;
+    if (probs) probs[(size_t)b * (2 * n_max + 1) + 2 * n_max] = (float)Z;
+    if (out_tokens) {
+      out_tokens[(size_t)b * R + j.acc] = y;
+      for (int rr = j.acc + 1; rr < R; ++rr) out_tokens[(size_t)b * R + rr] = -1;
+    }
+  }
+  reset_ticket(&counters[b]);
+}
+
+// ===========================================================================
+// Sampled rule, pass 1: row statistics, then the sequential accept test
+// ===========================================================================
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
@@ -244,10 +479,10 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
     const MS* pr = parts + ((size_t)b * RR + rr) * nch;
     for (int cc = l; cc < nch; cc += 32) {
       const float2 raw = __ldcg(reinterpret_cast<const float2*>(pr + cc));
-      x = ms_merge(x, MS{raw.x, raw.y}, k2);
+      x = ms_merge(x, MS{raw.x, raw.y});
     }
     // fixed-order combine across lanes
-    x = warp_ms(x, k2);
+    x = warp_ms(x);
     if (l == 0) rs[rr] = x;
   }
   __syncthreads();
@@ -259,7 +494,9 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
       const MS pt = rs[i - 1], pd = rs[R + i - 1];
       const float zxt = __ldcg(zx + (size_t)b * RR + (i - 1));
       const float zxd = __ldcg(zx + (size_t)b * RR + R + (i - 1));
-      const float et = exp2f((zxt - pt.m) * k2), ed = exp2f((zxd - pd.m) * k2);
+      // exponents formed exactly as in the row sums
+      const float at = fmaf(zxt, k2, -pt.m), ad = fmaf(zxd, k2, -pd.m);
+      const float et = exp2f(at), ed = exp2f(ad);
       const float px = et / pt.s, qx = ed / pd.s;
       if (probs) {
         probs[(size_t)b * (2 * n_max + 1) + (i - 1)] = px;
@@ -270,8 +507,8 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
         flags |= 8;                      // DFLASH_FLAG_INVALID
         ratio = CUDART_INF_F;
       } else {
-        // p/q = exp2((zt_x - mt) - (zd_x - md)) * sd / st, differences taken first
-        ratio = exp2f(((zxt - pt.m) - (zxd - pd.m)) * k2) * (pd.s / pt.s);
+        // p/q = 2^(at - ad) * sd / st
+        ratio = exp2f(at - ad) * (pd.s / pt.s);
       }
       const float u = u_acc[(size_t)b * n_max + (i - 1)];
       if (ratio < 1.f && fabsf(u - ratio) < 1e-6f) flags |= 1;   // ACCEPT_BOUNDARY
@@ -303,213 +540,10 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
   }
   __syncthreads();
   if (out_tokens) {
-    // accepted drafts now; the bonus slot and padding are written by pass 2
+    // accepted drafts now; the bonus slot and padding are written by the draw
     const int a = s_a;
     for (int rr = threadIdx.x; rr < a; rr += blockDim.x)
       out_tokens[(size_t)b * R + rr] = cand[(size_t)b * R + rr + 1];
-  }
-  reset_ticket(&counters[b]);
-}
-
-// ===========================================================================
-// Sampled rule, pass 2: inverse-CDF draw of the bonus from the residual
-// max(0, p - q) (or from p after a full accept), in ascending token order.
-// Each thread owns one 16-byte vector of the chunk, so the CDF order is the
-// token order and every thread's partial sum is recomputed identically.
-// ===========================================================================
-template <typename T>
-__device__ __forceinline__ void resample_weights(const T* zt_row, const T* zd_row, int e0, int V,
-                                                 const SampleJob& j, float k2, bool use_p,
-                                                 float* wgt) {
-  constexpr int N = VecTraits<T>::N;
-  const float inv_st = 1.f / j.st;
-  const float inv_sd = 1.f / j.sd;
-#pragma unroll
-  for (int q = 0; q < N; ++q) wgt[q] = 0.f;
-  const int base = e0 + (int)threadIdx.x * N;
-  if (base >= V) return;
-  float ft[N], fd[N];
-  if (base + N <= V && ((reinterpret_cast<uintptr_t>(zt_row + base) & 15u) == 0) &&
-      (use_p || (reinterpret_cast<uintptr_t>(zd_row + base) & 15u) == 0)) {
-    unpack16<T>(*reinterpret_cast<const uint4*>(zt_row + base), ft);
-    if (!use_p) unpack16<T>(*reinterpret_cast<const uint4*>(zd_row + base), fd);
-  } else {
-#pragma unroll
-    for (int q = 0; q < N; ++q) {
-      ft[q] = base + q < V ? ld_scalar(zt_row + base + q) : -CUDART_INF_F;
-      fd[q] = (!use_p && base + q < V) ? ld_scalar(zd_row + base + q) : -CUDART_INF_F;
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < N; ++q) {
-    const float p = exp2f((ft[q] - j.mt) * k2) * inv_st;
-    if (use_p) {
-      wgt[q] = p;
-    } else {
-      const float qq = exp2f((fd[q] - j.md) * k2) * inv_sd;
-      wgt[q] = fmaxf(0.f, p - qq);
-    }
-  }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-sample_resample_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
-                       const int64_t* __restrict__ cand, const float* __restrict__ u_final,
-                       int n_max, int V, int nch, float k2, const SampleJob* __restrict__ jobs,
-                       float2* __restrict__ parts, int32_t* __restrict__ counters,
-                       int64_t* __restrict__ bonus, int64_t* __restrict__ out_tokens,
-                       uint8_t* __restrict__ flags_out, float* __restrict__ probs) {
-  constexpr int N = VecTraits<T>::N;
-  const int chunk = kThreads * N;
-  const int c = blockIdx.x, b = blockIdx.y;
-  const int R = n_max + 1;
-  const SampleJob j = jobs[b];
-  const T* zt_row = zt + ((size_t)b * R + j.row) * V;
-  const T* zd_row = zd + ((size_t)b * n_max + min(j.row, max(n_max - 1, 0))) * V;
-  const int e0 = c * chunk;
-  float wr[N], wp[N];
-  resample_weights<T>(zt_row, zd_row, e0, V, j, k2, j.mode == 1, wr);
-  float sr = 0.f;
-#pragma unroll
-  for (int q = 0; q < N; ++q) sr += wr[q];
-  float sp = sr;
-  if (j.mode == 0) {
-    resample_weights<T>(zt_row, zd_row, e0, V, j, k2, true, wp);
-    sp = 0.f;
-#pragma unroll
-    for (int q = 0; q < N; ++q) sp += wp[q];
-  }
-  // block sums of the residual and of p (p is the fallback when Z == 0)
-  __shared__ float shr[kThreads / 32], shp[kThreads / 32];
-  float xr = sr, xp = sp;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    xr += __shfl_xor_sync(0xffffffffu, xr, o);
-    xp += __shfl_xor_sync(0xffffffffu, xp, o);
-  }
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) { shr[w] = xr; shp[w] = xp; }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tr = 0.f, tp = 0.f;
-    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) { tr += shr[q]; tp += shp[q]; }
-    parts[(size_t)b * nch + c] = make_float2(tr, tp);
-  }
-  if (!take_ticket_is_last_t0(&counters[b], nch)) return;
-
-  // ---- last CTA of sequence b: locate the chunk, then the token ----
-  // Column x of the partials holds the drawn weights (residual, or p after a
-  // full accept); column y holds p, used when the residual mass is zero.
-  __shared__ double s_target, s_before, s_Z;
-  __shared__ int s_chunk, s_degenerate;
-  if (threadIdx.x == 0) {
-    double Zr = 0.0, Zp = 0.0;
-    for (int cc = 0; cc < nch; ++cc) {
-      const float2 v = __ldcg(parts + (size_t)b * nch + cc);
-      Zr += v.x;
-      Zp += v.y;
-    }
-    const int degenerate = (j.mode == 0 && Zr == 0.0) ? 1 : 0;
-    const double Z = degenerate ? Zp : Zr;
-    const double target = (double)u_final[b] * Z;
-    double cum = 0.0, before = 0.0;
-    int cstar = -1, last_nz = 0;
-    for (int cc = 0; cc < nch; ++cc) {
-      const float2 v = __ldcg(parts + (size_t)b * nch + cc);
-      const double sc = degenerate ? v.y : v.x;
-      if (sc > 0.0) last_nz = cc;
-      if (cstar < 0 && cum + sc > target) { cstar = cc; before = cum; }
-      cum += sc;
-    }
-    if (cstar < 0) {   // rounding put the target past the last step
-      cstar = last_nz;
-      before = 0.0;
-      for (int cc = 0; cc < last_nz; ++cc) {
-        const float2 v = __ldcg(parts + (size_t)b * nch + cc);
-        before += degenerate ? v.y : v.x;
-      }
-    }
-    s_target = target;
-    s_before = before;
-    s_Z = Z;
-    s_chunk = cstar;
-    s_degenerate = degenerate;
-  }
-  __syncthreads();
-  const bool usep = (j.mode == 1) || s_degenerate;
-  const int e0s = s_chunk * chunk;
-  float wv[N];
-  resample_weights<T>(zt_row, zd_row, e0s, V, j, k2, usep, wv);
-  double ts = 0.0;
-  {
-    float f = 0.f;
-#pragma unroll
-    for (int q = 0; q < N; ++q) f += wv[q];
-    ts = f;
-  }
-  // exclusive scan of per-thread sums over the block, in fp64
-  __shared__ double scan_sh[kThreads];
-  scan_sh[threadIdx.x] = ts;
-  __syncthreads();
-  for (int off = 1; off < (int)blockDim.x; off <<= 1) {
-    const double v = (threadIdx.x >= (unsigned)off) ? scan_sh[threadIdx.x - off] : 0.0;
-    __syncthreads();
-    scan_sh[threadIdx.x] += v;
-    __syncthreads();
-  }
-  const double incl = scan_sh[threadIdx.x];
-  const double excl = incl - ts;
-  __shared__ int s_y, s_lastpos;
-  __shared__ double s_clo, s_chi;
-  if (threadIdx.x == 0) { s_y = INT32_MAX; s_lastpos = -1; }
-  __syncthreads();
-  const double target = s_target;
-  double cum = s_before + excl;
-  const int base = e0s + (int)threadIdx.x * N;
-  for (int q = 0; q < N; ++q) {
-    if (wv[q] > 0.f) atomicMax(&s_lastpos, base + q);
-  }
-  if (ts > 0.0 && cum <= target && cum + ts > target) {
-    for (int q = 0; q < N; ++q) {
-      const double nxt = cum + (double)wv[q];
-      if (nxt > target) {
-        s_y = base + q;        // unique: the thread ranges are disjoint
-        s_clo = cum;
-        s_chi = nxt;
-        break;
-      }
-      cum = nxt;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int y = s_y;
-    double clo, chi;
-    int flags = j.flags;
-    if (y == INT32_MAX) {       // rounding: fall back to the last positive weight
-      y = s_lastpos >= 0 ? s_lastpos : 0;
-      clo = s_target;
-      chi = s_target;
-    } else {
-      clo = s_clo;
-      chi = s_chi;
-    }
-    const double Z = s_Z;
-    const double u = u_final[b];
-    if (Z > 0.0 && (fabs(clo / Z - u) < 1e-6 || fabs(chi / Z - u) < 1e-6)) flags |= 2;  // CDF_BOUNDARY
-    if (s_degenerate) flags |= 4;                                                         // DEGENERATE
-    bonus[b] = y;
-    if (flags_out) flags_out[b] = (uint8_t)flags;
-    if (probs) probs[(size_t)b * (2 * n_max + 1) + 2 * n_max] = (float)Z;
-  }
-  __shared__ int64_t s_yb;
-  if (threadIdx.x == 0) s_yb = bonus[b];
-  if (out_tokens) {
-    __syncthreads();
-    const int64_t yb = s_yb;
-    for (int rr = j.acc + (int)threadIdx.x; rr < R; rr += blockDim.x)
-      out_tokens[(size_t)b * R + rr] = (rr == j.acc) ? yb : -1;
   }
   reset_ticket(&counters[b]);
 }
@@ -550,9 +584,9 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
       const MS* pr = parts + ((size_t)b * k + ii) * nch;
       for (int cc = l; cc < nch; cc += 32) {
         const float2 raw = __ldcg(reinterpret_cast<const float2*>(pr + cc));
-        x = ms_merge(x, MS{raw.x, raw.y}, k2);
+        x = ms_merge(x, MS{raw.x, raw.y});
       }
-      x = warp_ms(x, k2);
+      x = warp_ms(x);
       if (l == 0) rs[ii] = x;
     }
   }
@@ -561,11 +595,12 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
     double csum = 0.0;
     for (int ii = 0; ii < k; ++ii) {
       const MS r = rs[ii];
-      if (need && row_lse) row_lse[(size_t)b * k + ii] = r.m * inv_t + logf(r.s);
+      // natural-log values from log2-unit statistics: ln v = ln 2 * log2 v
+      if (need && row_lse) row_lse[(size_t)b * k + ii] = (r.m + log2f(r.s)) * 0.6931471805599453f;
       if (on) {
         const float zxv = __ldcg(zx + (size_t)b * k + ii);
-        // log q(x) = (z_x - max) / T - ln(sum exp((z - max) / T))
-        csum += (double)((zxv - r.m) * inv_t) - (double)logf(r.s);
+        // log2 q(x) = (z_x k2 - m) - log2(sum)
+        csum += ((double)fmaf(zxv, k2, -r.m) - (double)log2f(r.s)) * 0.6931471805599453;
       }
     }
     const float cval = on ? (float)csum : 0.f;
@@ -597,10 +632,6 @@ ChunkPlan plan_chunks(int rows, int V, int dtype, int num_sms) {
   return p;
 }
 
-int resample_chunks(int V, int dtype) {
-  const int chunk = kThreads * vec_elems(dtype);
-  return (V + chunk - 1) / chunk;
-}
 
 size_t verify_greedy_ws_bytes(int B, int n_max, int V, int dtype, int num_sms) {
   const int R = n_max + 1;
@@ -615,7 +646,9 @@ size_t verify_sample_ws_bytes(int B, int n_max, int V, int dtype, int num_sms) {
   s += align_up((size_t)B * RR * p.nch * sizeof(MS));             // stats partials
   s += align_up((size_t)B * RR * sizeof(float));                  // z at candidates
   s += align_up((size_t)B * sizeof(SampleJob));                   // per-sequence job
-  s += align_up((size_t)B * resample_chunks(V, dtype) * sizeof(float2));
+  const int nch2 = (V + kDrawChunk - 1) / kDrawChunk;
+  s += align_up((size_t)B * nch2 * sizeof(float2));                // chunk sums
+  s += align_up((size_t)B * nch2 * kThreads * sizeof(float2));     // segment sums
   return s;
 }
 
@@ -651,20 +684,21 @@ static cudaError_t launch_sample_t(const VerifyArgs& a, int num_sms) {
   ws += align_up((size_t)a.B * RR * sizeof(float));
   SampleJob* jobs = (SampleJob*)ws;
   ws += align_up((size_t)a.B * sizeof(SampleJob));
-  float2* rparts = (float2*)ws;
+  const int nch2 = (a.V + kDrawChunk - 1) / kDrawChunk;
+  float2* dparts = (float2*)ws;
+  ws += align_up((size_t)a.B * nch2 * sizeof(float2));
+  float2* dsegs = (float2*)ws;
   const float k2 = kLog2e / a.temperature;
   dim3 g1(p.nch, a.B * RR);
   sample_stats_kernel<T><<<g1, kThreads, 0, a.stream>>>(
       (const T*)a.target_logits, (const T*)a.draft_logits, a.cand, a.n_draft, a.u_accept,
-      a.n_max, a.V, p.nch, p.chunk, k2, parts, zx, a.counters, jobs, a.accept_len,
-      a.commit_len, a.out_tokens, a.probs);
+      a.n_max, a.V, p.nch, p.chunk, k2, parts, zx, a.counters, jobs, a.accept_len, a.commit_len,
+      a.out_tokens, a.probs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int nch2 = resample_chunks(a.V, a.dtype);
-  dim3 g2(nch2, a.B);
-  sample_resample_kernel<T><<<g2, kThreads, 0, a.stream>>>(
-      (const T*)a.target_logits, (const T*)a.draft_logits, a.cand, a.u_final, a.n_max, a.V,
-      nch2, k2, jobs, rparts, a.counters + a.B, a.bonus, a.out_tokens, a.flags, a.probs);
+  sample_draw_kernel<T><<<dim3(nch2, a.B), kThreads, 0, a.stream>>>(
+      (const T*)a.target_logits, (const T*)a.draft_logits, a.u_final, a.n_max, a.V, nch2, k2, jobs, dparts, dsegs,
+      a.counters, a.bonus, a.out_tokens, a.flags, a.probs);
   (void)R;
   return cudaGetLastError();
 }
