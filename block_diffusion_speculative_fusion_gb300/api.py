@@ -58,6 +58,8 @@ _SIGS = {
     "dflash_verify_greedy_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
     "dflash_verify_greedy": (ctypes.c_int, [ctypes.POINTER(VerifyDims), c_p, c_p, c_p, c_p, c_p, c_p,
                                             c_p, c_p, c_p, ctypes.c_size_t, c_p]),
+    "dflash_verify_greedy_noalloc": (ctypes.c_int, [ctypes.POINTER(VerifyDims), c_p, c_p, c_p, c_p, c_p,
+                                                    c_p, c_p, c_p, c_p]),
     "dflash_verify_sample_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
     "dflash_verify_sample": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float, c_p, c_p, c_p,
                                             c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p,
@@ -192,6 +194,32 @@ def verify_greedy(target_logits: torch.Tensor, cand: torch.Tensor, n_draft: Opti
         _dev(o["accept_len"], "accept_len", torch.int32), _dev(o["bonus"], "bonus", torch.int64),
         _dev(o["commit_len"], "commit_len", torch.int32), _opt(o.get("out_tokens"), "out_tokens", torch.int64),
         _opt(o.get("target_pred"), "target_pred", torch.int64), w.data_ptr(), w.numel(), _stream(dev))
+    _check(rc)
+    return o
+
+
+def verify_greedy_noalloc(target_logits: torch.Tensor, cand: torch.Tensor, n_draft: Optional[torch.Tensor] = None,
+                          want_target_pred: bool = False, out: Optional[dict] = None):
+    """Greedy accept rule on the library's fixed scratch
+    (``dflash_verify_greedy_noalloc``). Outputs are caller tensors (``out``),
+    created here only when not given; the C call itself allocates nothing."""
+    _dev(target_logits, "target_logits")
+    B, R, V = target_logits.shape
+    dev = target_logits.device
+    dims = VerifyDims(B, R - 1, V, _dtype_code(target_logits))
+    o = out if out is not None else {}
+    o.setdefault("accept_len", torch.empty(B, dtype=torch.int32, device=dev))
+    o.setdefault("bonus", torch.empty(B, dtype=torch.int64, device=dev))
+    o.setdefault("commit_len", torch.empty(B, dtype=torch.int32, device=dev))
+    o.setdefault("out_tokens", torch.empty((B, R), dtype=torch.int64, device=dev))
+    if want_target_pred:
+        o.setdefault("target_pred", torch.empty((B, R), dtype=torch.int64, device=dev))
+    rc = lib().dflash_verify_greedy_noalloc(
+        ctypes.byref(dims), _dev(target_logits, "target_logits"), _dev(cand, "cand", torch.int64, (B, R)),
+        _opt(n_draft, "n_draft", torch.int32, (B,)),
+        _dev(o["accept_len"], "accept_len", torch.int32), _dev(o["bonus"], "bonus", torch.int64),
+        _dev(o["commit_len"], "commit_len", torch.int32), _opt(o.get("out_tokens"), "out_tokens", torch.int64),
+        _opt(o.get("target_pred"), "target_pred", torch.int64), _stream(dev))
     _check(rc)
     return o
 

@@ -3,6 +3,7 @@
 // caller's stream.
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/dflash.h"
@@ -94,6 +95,68 @@ int dflash_verify_greedy(const dflash_verify_dims* d, const void* target_logits,
   cudaError_t e = dflash::launch_verify_greedy(a, kPlanSms);
   if (e != cudaSuccess) return cuda_fail(e, "verify_greedy launch");
   return ok(1);
+}
+
+}  // extern "C"
+
+// ------------------------------------------- verify, greedy, no allocation ---
+// Scratch for dflash_verify_greedy_noalloc: a fixed device array in this
+// module, one instance per device. It is laid out like a caller workspace
+// (counters first, then the chunk partials). Static device storage is zero
+// when the module loads, which is the state the completion counters need; a
+// call that completes leaves them zero again.
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[DFLASH_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the current device's scratch array. The first call on a
+// device resolves it (cudaGetSymbolAddress, which may load the module on that
+// device); later calls read the cached pointer.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_greedy_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DFLASH_ERR_UNSUPPORTED, "device %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "verify_greedy_noalloc: cudaGetSymbolAddress");
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 255u) != 0)
+      return fail(DFLASH_ERR_CUDA, "verify_greedy_noalloc: scratch address %p not 256-byte aligned", p);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dflash_verify_greedy_noalloc(const dflash_verify_dims* d, const void* target_logits, const int64_t* cand,
+                                 const int32_t* n_draft, int32_t* accept_len, int64_t* bonus,
+                                 int32_t* commit_len, int64_t* out_tokens, int64_t* target_pred,
+                                 dflash_stream_t stream) {
+  int rc = check_verify_dims(d, false);
+  if (rc) return rc;
+  if (!target_logits || !cand || !accept_len || !bonus || !commit_len)
+    return fail(DFLASH_ERR_INVALID_ARG, "verify_greedy_noalloc: a required pointer is NULL");
+  const size_t need = dflash_verify_greedy_workspace_size(d);
+  if (need > DFLASH_NOALLOC_SCRATCH_BYTES)
+    return fail(DFLASH_ERR_UNSUPPORTED,
+                "verify_greedy_noalloc: B=%d n_max=%d V=%d needs %zu bytes of scratch > the fixed %d; "
+                "use dflash_verify_greedy with a caller workspace",
+                d->B, d->n_max, d->V, need, (int)DFLASH_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  return dflash_verify_greedy(d, target_logits, cand, n_draft, accept_len, bonus, commit_len, out_tokens,
+                              target_pred, scratch, DFLASH_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 size_t dflash_verify_sample_workspace_size(const dflash_verify_dims* d) {

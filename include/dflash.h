@@ -197,6 +197,39 @@ int dflash_verify_greedy(const dflash_verify_dims* dims,
                          void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
 /*
+ * dflash_verify_greedy without a caller workspace. The pages have no
+ * counterpart: this is a deployment variant of dflash_verify_greedy (same
+ * arguments minus the workspace, same kernels, same results).
+ *
+ * It serves callers that cannot allocate device memory at the call site: a
+ * plain C host that holds no device allocator, or a serving loop that reserves
+ * all device memory up front (weights, paged KV pools) and permits no
+ * allocation per decode round. Scratch is a fixed array of
+ * DFLASH_NOALLOC_SCRATCH_BYTES in device memory of the library's module, one
+ * per device; the call allocates nothing.
+ *   - Limit: dims whose dflash_verify_greedy_workspace_size exceeds
+ *     DFLASH_NOALLOC_SCRATCH_BYTES are rejected with DFLASH_ERR_UNSUPPORTED
+ *     before anything is launched (B*(n_max+1) up to about 30000 rows fit).
+ *   - Set-up: the first call on a device (the device current on the calling
+ *     thread) resolves the array's address with cudaGetSymbolAddress, which may
+ *     load the module on that device; make that first call before any stream
+ *     capture begins. Later calls only read the cached address.
+ *   - Zero state: the array's counter region must be zero when a call starts.
+ *     Module load zeroes it and every completed call leaves it zero; nothing
+ *     else writes it.
+ *   - Races: all calls on one device share the array. Calls must be ordered on
+ *     the GPU (one stream, or streams ordered by events); calls that overlap
+ *     in time, from any thread or stream, corrupt each other's results.
+ */
+#define DFLASH_NOALLOC_SCRATCH_BYTES (256 * 1024)
+int dflash_verify_greedy_noalloc(const dflash_verify_dims* dims,
+                                 const void* target_logits, const int64_t* cand,
+                                 const int32_t* n_draft,
+                                 int32_t* accept_len, int64_t* bonus, int32_t* commit_len,
+                                 int64_t* out_tokens, int64_t* target_pred,
+                                 dflash_stream_t stream);
+
+/*
  * Sampled rule, [SpecDec] 3 and 4, [DLoop] looped verify:
  *   p_r = softmax(target_logits[b, r] / T), q_r = softmax(draft_logits[b, r] / T)
  *   for i = 1..n_b: x = cand[b, i]; accept iff u_accept[b, i-1] < p_{i-1}(x) / q_{i-1}(x);
