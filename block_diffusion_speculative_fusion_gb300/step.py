@@ -27,8 +27,13 @@ from .workloads import Workload
 
 class DflashStep:
     def __init__(self, wl: Workload, seed: int = 0, device: str = "cuda:0", headroom_steps: int = 64,
-                 pools_on_device: bool = True, pinned_inputs: bool = False):
+                 pools_on_device: bool = True, pinned_inputs: bool = False, stationary: bool = False):
+        """``stationary``: every step starts from the initial context lengths
+        (the committed rows of one step are rewritten by the next), so that the
+        workload does not drift as steps repeat; otherwise each step starts
+        where the previous one left the cache."""
         self.wl = wl
+        self.stationary = stationary
         self.dev = torch.device(device)
         dev = self.dev
         dt = synth.io_dtype(wl)
@@ -42,6 +47,7 @@ class DflashStep:
         self.page_table = cache.page_table.to(dev)
         self.max_ctx = cache.max_pages * wl.page_size
         self.ctx = [ctx_len.to(dev), torch.empty_like(ctx_len, device=dev)]
+        self.ctx_start = ctx_len.to(dev)
         self.cur = 0
         # ---- per-step inputs from the upstream models (host copies kept for e2e) ----
         host: Dict[str, torch.Tensor] = {}
@@ -102,7 +108,10 @@ class DflashStep:
         to record per-kernel events."""
         wl = self.wl
         inp = self.inp
-        cur, nxt = self.ctx[self.cur], self.ctx[1 - self.cur]
+        if self.stationary:
+            cur, nxt = self.ctx_start, self.ctx[1]
+        else:
+            cur, nxt = self.ctx[self.cur], self.ctx[1 - self.cur]
         launches = 0
         for layer in range(wl.L):
             if timer:
@@ -133,5 +142,6 @@ class DflashStep:
         launches += api.last_launch_count()
         if timer:
             timer("mat_end")
-        self.cur = 1 - self.cur
+        if not self.stationary:
+            self.cur = 1 - self.cur
         self.launches_per_step = launches
