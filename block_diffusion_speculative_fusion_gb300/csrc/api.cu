@@ -248,7 +248,7 @@ static int check_attn_dims(const dflash_attn_dims* d) {
 size_t dflash_block_attn_workspace_size(const dflash_attn_dims* d) {
   if (check_attn_dims(d) != DFLASH_OK) return 0;
   return DFLASH_WS_COUNTER_BYTES +
-         dflash::attn_ws_bytes(d->B, d->n_q, d->n_kv_blk, d->Hq, d->Hkv, d->D, d->max_ctx, d->dtype);
+         dflash::attn_ws_bytes(d->B, d->n_q, d->n_kv_blk, d->Hq, d->Hkv, d->D, d->max_ctx, d->page_size, d->dtype);
 }
 
 int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_blk, const void* v_blk,

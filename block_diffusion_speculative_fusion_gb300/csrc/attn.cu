@@ -4,13 +4,11 @@
 //   DFlash page, section 块扩散 (bidirectional attention inside the block) and
 //   KV 注入 step 3 (Attention(Q_draft, [K_draft; K_ctx], [V_draft; V_ctx])).
 //
-// bf16 / D = 128 path (the serving shapes): one CTA per (key split, kv head,
-// sequence). The n_q * (Hq/Hkv) query rows that share a kv head are packed into
-// the M dimension (GQA packing), so each K/V byte is read from HBM once per
-// kv head. Context pages arrive by TMA (one 128B-swizzled box per page half)
-// into a 3-stage ring; scores and P V run on mma.sync bf16 tensor cores with an
-// online softmax in fp32. Splits of one (sequence, kv head) are merged by the
-// last CTA to finish (completion ticket, no waiting).
+// bf16 / D = 128 path (the serving shapes): a persistent, warp-specialised
+// tcgen05 kernel (below). The n_q * (Hq/Hkv) query rows that share a kv head
+// are packed into the MMA's M dimension (GQA packing), so each K/V byte is read
+// from HBM once per kv head. Context pages arrive by TMA into a ring of 64-key
+// stages; S and O live in TMEM; the online softmax runs in fp32.
 //
 // Generic path (fp32, or shapes outside the bf16 kernel): one CTA per query
 // row with fp32 CUDA-core arithmetic; used for the tiny fp32 configuration.
@@ -26,10 +24,7 @@ namespace dflash {
 namespace attn {
 constexpr int kD = 128;
 constexpr int kTileK = 64;                   // keys per tile
-constexpr int kStages = 3;
-constexpr int kHalfBytes = kTileK * 128;     // [64 keys][64 d] bf16 = 8 KB
-constexpr int kTileBytes = 2 * kHalfBytes;   // K (or V) of one tile = 16 KB
-constexpr int kTilesPerSplit = 16;           // 1024 keys per CTA
+constexpr int kMinSplitTiles = 16;           // smallest key split: 1024 keys
 constexpr int kMaxWarps = 8;                 // M <= 128 packed query rows
 }  // namespace attn
 
@@ -40,29 +35,18 @@ struct AttnParams {
   const int32_t* page_table;
   const int32_t* ctx_len;
   bf16* out;
-  float* part_o;     // [B * Hkv * max_splits][M][128]
+  float* part_o;     // [B * Hkv * max_splits][M][128]  (max_splits for the smallest split)
   float2* part_ml;   // [B * Hkv * max_splits][M]  (max in log2 units, sum)
   int32_t* counters; // [B * Hkv]
   int* err;
   int B, n_q, n_kv, Hq, Hkv, G, M, page_size, max_pages, num_pages, max_splits, max_ctx;
+  // work items: hpi kv heads (1 or 2) per item, Gi = hpi * G query heads and
+  // Mi = n_q * Gi packed rows per item, n_groups = Hkv / hpi items per split of
+  // a sequence, TK = 64 / hpi keys per tile, br = K/V rows per TMA box
+  int hpi, Gi, Mi, n_groups, TK, br;
   float scale_log2;  // softmax scale * log2(e)
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -72,339 +56,104 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // tile with the 128-byte TMA swizzle (chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-// Copy one 128-element bf16 row into two swizzled half tiles (or zero it).
-__device__ __forceinline__ void put_row(uint8_t* half0, uint8_t* half1, int r, const bf16* src, int chunk) {
-  uint4 v = src ? *reinterpret_cast<const uint4*>(src + chunk * 8) : make_uint4(0, 0, 0, 0);
-  uint8_t* h = chunk < 8 ? half0 : half1;
-  *reinterpret_cast<uint4*>(h + swz(r, chunk & 7)) = v;
-}
-
-__global__ void __launch_bounds__(256, 1)
-attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                 const AttnParams p) {
-  using namespace attn;
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  // a length outside [0, max_ctx] would overrun the split workspace: clamp it
-  const int C = max(0, min(p.ctx_len[b], p.max_ctx));
-  const int n_ctx_tiles = (C + kTileK - 1) / kTileK;
-  const int nsplit = max(1, (n_ctx_tiles + kTilesPerSplit - 1) / kTilesPerSplit);
-  if (split >= nsplit) return;
-  const int t0 = split * kTilesPerSplit;
-  const int n_tiles_ctx = max(0, min(n_ctx_tiles, t0 + kTilesPerSplit) - t0);
-  const bool has_blk = (split == nsplit - 1) && p.n_kv > 0;
-  const int n_tiles = n_tiles_ctx + (has_blk ? 1 : 0);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nwarps = blockDim.x >> 5;
-  const int Mpad = nwarps * 16;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* kv = smem;                                        // stage s: K at s*2*T, V at s*2*T + T
-  // Q halves [Mpad][64] x 2 live in the last stage until they are in registers
-  uint8_t* qs = smem + (kStages - 1) * 2 * kTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-    fence_barrier_init();
-  }
-  // Q rows of this kv head: packed row r = i * G + hh  (position i, head g*G + hh)
-  for (int idx = tid; idx < Mpad * 16; idx += blockDim.x) {
-    const int r = idx >> 4, ch = idx & 15;
-    const bf16* src = nullptr;
-    if (r < p.M) {
-      const int i = r / p.G, hh = r - i * p.G;
-      src = p.q + ((size_t)(b * p.n_q + i) * p.Hq + g * p.G + hh) * kD;
-    }
-    put_row(qs, qs + Mpad * 128, r, src, ch);
-  }
-  __syncthreads();
-
-  const int ps = p.page_size;
-  auto issue = [&](int tile, int stage) {
-    uint64_t* bar = &bars[stage];
-    mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-    const int key0 = (t0 + tile) * kTileK;
-    uint8_t* kdst = kv + stage * 2 * kTileBytes;
-    uint8_t* vdst = kdst + kTileBytes;
-    for (int pg = 0; pg < kTileK / ps; ++pg) {
-      const int lp = key0 / ps + pg;
-      int row = 0;   // pages past the context (or bad table entries) read page 0; masked below
-      if (lp * ps < C && lp < p.max_pages) {
-        const int phys = p.page_table[(size_t)b * p.max_pages + lp];
-        if (phys >= 0 && phys < p.num_pages) row = phys * ps;
-      }
-      for (int h = 0; h < 2; ++h) {
-        tma_load_3d(kdst + h * kHalfBytes + pg * ps * 128, &kmap, bar, h * 64, g, row);
-        tma_load_3d(vdst + h * kHalfBytes + pg * ps * 128, &vmap, bar, h * 64, g, row);
-      }
-    }
-  };
-  if (tid == 0)
-    for (int s = 0; s < kStages - 1 && s < n_tiles_ctx; ++s) issue(s, s);
-
-  // Q fragments of this warp's 16 rows, all 8 k-slices of D = 128
-  uint32_t qa[8][4];
-  {
-    const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int ch = (kk & 3) * 2 + (lane >> 4);
-      const uint32_t addr = smem_u32(qs + (kk >> 2) * Mpad * 128) + swz(r, ch);
-      ldsm_x4(addr, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-    }
-  }
-  __syncthreads();   // the last stage is free for TMA once every warp holds its Q fragments
-
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
-  float l_run[2] = {0.f, 0.f};
-  const int qd = lane & 3;    // thread's column pair within an n-tile
-  bool failed = false;
-  int fail_t = 0;
-
-  for (int t = 0; t < n_tiles; ++t) {
-    const int stage = t % kStages;
-    const bool is_blk = (t == n_tiles_ctx);
-    if (tid == 0 && t + kStages - 1 < n_tiles_ctx) issue(t + kStages - 1, (t + kStages - 1) % kStages);
-    uint8_t* ks = kv + stage * 2 * kTileBytes;
-    uint8_t* vs = ks + kTileBytes;
-    int valid;
-    if (!is_blk) {
-      const bool ok = mbar_wait_bounded(&bars[stage], (uint32_t)((t / kStages) & 1), p.err, 1);
-      if (__syncthreads_or(!ok)) { failed = true; fail_t = t; break; }
-      valid = min(kTileK, C - (t0 + t) * kTileK);
-    } else {
-      for (int idx = tid; idx < kTileK * 16; idx += blockDim.x) {
-        const int r = idx >> 4, ch = idx & 15;
-        const size_t off = ((size_t)(b * p.n_kv + r) * p.Hkv + g) * kD;
-        put_row(ks, ks + kHalfBytes, r, r < p.n_kv ? p.k_blk + off : nullptr, ch);
-        put_row(vs, vs + kHalfBytes, r, r < p.n_kv ? p.v_blk + off : nullptr, ch);
-      }
-      __syncthreads();
-      valid = p.n_kv;
-    }
-
-    // ---- S = Q K^T for this warp's 16 rows x 64 keys ----
-    float s[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t kbase = smem_u32(ks + (kk >> 2) * kHalfBytes);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int r = np * 16 + (lane & 7) + (lane >> 4) * 8;
-        const int ch = (kk & 3) * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + swz(r, ch), b0, b1, b2, b3);
-        mma_bf16_16816(s[2 * np], qa[kk], b0, b1);
-        mma_bf16_16816(s[2 * np + 1], qa[kk], b2, b3);
-      }
-    }
-    // ---- online softmax (base 2) ----
-    float mx[2] = {m_run[0], m_run[1]};
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int key = n * 8 + qd * 2 + (j & 1);
-        const float v = key < valid ? s[n][j] * p.scale_log2 : -CUDART_INF_F;
-        s[n][j] = v;
-        mx[j >> 1] = fmaxf(mx[j >> 1], v);
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-    }
-    float alpha[2], base[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      base[r] = (mx[r] == -CUDART_INF_F) ? 0.f : mx[r];
-      alpha[r] = (m_run[r] == -CUDART_INF_F) ? 0.f : exp2f(m_run[r] - base[r]);
-      m_run[r] = mx[r];
-    }
-    float rs[2] = {0.f, 0.f};
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float e = exp2f(s[n][j] - base[j >> 1]);
-        s[n][j] = e;
-        rs[j >> 1] += e;
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + rs[r];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
-      o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
-    }
-    // ---- O += P V ----
-#pragma unroll
-    for (int kv4 = 0; kv4 < 4; ++kv4) {
-      uint32_t a[4];
-      a[0] = pack_bf16(s[2 * kv4][0], s[2 * kv4][1]);
-      a[1] = pack_bf16(s[2 * kv4][2], s[2 * kv4][3]);
-      a[2] = pack_bf16(s[2 * kv4 + 1][0], s[2 * kv4 + 1][1]);
-      a[3] = pack_bf16(s[2 * kv4 + 1][2], s[2 * kv4 + 1][3]);
-      const int r = kv4 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-      // keys of this thread's B fragments: kv4*16 + qd*2 + {0,1} (+8 for b1/b3)
-      const int kb = kv4 * 16 + qd * 2;
-      const bool partial = valid < kTileK;
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        const int ch = (dp & 3) * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(vs + (dp >> 2) * kHalfBytes) + swz(r, ch), b0, b1, b2, b3);
-        if (partial) {   // rows past the valid keys may hold anything: zero them
-          const uint32_t m0 = (kb < valid ? 0xffffu : 0u) | (kb + 1 < valid ? 0xffff0000u : 0u);
-          const uint32_t m1 = (kb + 8 < valid ? 0xffffu : 0u) | (kb + 9 < valid ? 0xffff0000u : 0u);
-          b0 &= m0; b2 &= m0; b1 &= m1; b3 &= m1;
-        }
-        mma_bf16_16816(o[2 * dp], a, b0, b1);
-        mma_bf16_16816(o[2 * dp + 1], a, b2, b3);
-      }
-    }
-    __syncthreads();   // every warp is done with this stage before it is refilled
-  }
-
-  if (failed) {
-    // A TMA did not land in time (error recorded): wait, again bounded, for the
-    // copies this CTA still has in flight, so none lands after the CTA exits.
-    if (tid == 0)
-      for (int tt = fail_t; tt < min(n_tiles_ctx, fail_t + kStages); ++tt)
-        mbar_wait_bounded(&bars[tt % kStages], (uint32_t)((tt / kStages) & 1), p.err, 1);
-    __syncthreads();
-    return;
-  }
-
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-  }
-  const int g8 = lane >> 2;
-  const int rows[2] = {warp * 16 + g8, warp * 16 + g8 + 8};
-
-  if (nsplit == 1) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = rows[r];
-      if (row >= p.M) continue;
-      const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
-      const int i = row / p.G, hh = row - i * p.G;
-      bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.G + hh) * kD;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int d = n * 8 + qd * 2;
-        *reinterpret_cast<__nv_bfloat162*>(dst + d) =
-            __floats2bfloat162_rn(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
-      }
-    }
-    return;
-  }
-
-  // ---- split partials, then the last split of this (sequence, kv head) merges ----
-  const size_t group = (size_t)b * p.Hkv + g;
-  const size_t cta = group * p.max_splits + split;
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = rows[r];
-    if (row >= p.M) continue;
-    float* dst = p.part_o + (cta * p.M + row) * kD;
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<float2*>(dst + n * 8 + qd * 2) = make_float2(o[n][2 * r], o[n][2 * r + 1]);
-    if (qd == 0) p.part_ml[cta * p.M + row] = make_float2(m_run[r], l_run[r]);
-  }
-  if (!take_ticket_is_last(&p.counters[group], nsplit)) return;
-
-  for (int idx = tid; idx < p.M * (kD / 4); idx += blockDim.x) {
-    const int row = idx / (kD / 4), d4 = idx - row * (kD / 4);
-    float M = -CUDART_INF_F;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(&p.part_ml[(group * p.max_splits + sp) * p.M + row]).x);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -CUDART_INF_F) {
-      for (int sp = 0; sp < nsplit; ++sp) {
-        const size_t c2 = group * p.max_splits + sp;
-        const float2 ml = __ldcg(&p.part_ml[c2 * p.M + row]);
-        const float w = (ml.x == -CUDART_INF_F) ? 0.f : exp2f(ml.x - M);
-        L += ml.y * w;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (c2 * p.M + row) * kD) + d4);
-        acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
-      }
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int i = row / p.G, hh = row - i * p.G;
-    bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.G + hh) * kD + d4 * 4;
-    reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  }
-  reset_ticket(&p.counters[group]);
-}
-
 // ===========================================================================
 // tcgen05 path: persistent, warp-specialised, TMEM accumulators.
-//   softmax     warps 0..W-1 (W = ceil(M / 32)): thread r owns packed query
-//               row r (TMEM lane r)
-//   producer    warp 2 (W <= 2) or 4: claims work items, loads Q, streams
-//               context K/V pages by TMA into a ring of 64-key stages
-//   MMA         the next warp: TMEM allocator and single-thread MMA issuer
-// A work item is (key split, kv head, sequence). Per 64-key tile t:
-// S_t = Q K_t^T (M = 128, N = 64) into TMEM buffer t % 2; the softmax threads
-// read their S row, write P_t (bf16) to shared memory, and the MMA thread
-// accumulates O += P_t V_t (M = 128, N = 128, V read MN-major) into the item's
-// TMEM O buffer. The running max is only raised (O rescaled in TMEM) when a
-// tile's max exceeds it by more than 2^8, so rescaling is rare. Q and O are
-// double-buffered per item so that one item's output overlaps the next
-// item's MMAs; the K/V ring runs across item boundaries.
+//   softmax     warps q and q + 4 for q < W = ceil(M / 32): TMEM lane quarter q
+//               (packed query row 32 q + lane), key columns 0-31 / 32-63
+//   producer    warp 2 (W <= 2) or 12: claims work items, loads Q and the
+//               page rows, streams context K/V pages by TMA into a ring of
+//               64-key stages
+//   MMA         the warp after the producer: TMEM allocator, one issuing thread
+//   epilogue    warps 8 + q: read O out of TMEM, normalise, store
+// A work item is (sequence, kv head, key split); items are handed out longest
+// first from a global counter. Per 64-key tile t: S_t = Q K_t^T (M = 128,
+// N = 64) into TMEM buffer t % 2; the softmax threads read their S row, write
+// P_t (bf16) to shared memory, and the MMA thread accumulates O += P_t V_t
+// (M = 128, N = 128, V read MN-major) into the item's TMEM O buffer. The
+// running max is only raised (O rescaled in TMEM) when a tile's max exceeds it
+// by more than 2^8, so rescaling is rare. Q and O are double-buffered per item
+// so that one item's output overlaps the next item's MMAs; the K/V ring runs
+// across item boundaries.
 // ===========================================================================
 namespace attn_tc {
 constexpr int kTileK = 64;
 constexpr int kMaxStages = 5;
 constexpr int kTileBytes = 2 * 64 * 128;   // K (or V) of one tile: two d-halves x 64 keys x 128 B
-constexpr int kMaxThreads = 448;
-constexpr int kTmemCols = 512;              // S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384)
+constexpr int kTmemCols = 512;   // S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384), P0/P1 [384,448)
+constexpr uint32_t kPCol = 384;      // P_t (bf16 pairs) at kPCol + 32 (t % 2)
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kGrid = 152;                  // persistent CTAs: one per SM
 constexpr int kMaxSeqs = 1024;              // sequences per call on this path
-constexpr int kPtMax = 128;                 // page-table entries of one item (page size >= 8)
-constexpr int kBarBytes = 41 * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + 2 * kPtMax * 4 + (2 * 2 * 128 + 2 * 3 * 128) * 4 + 64;
+constexpr int kPtMax = 256;                 // page-table entries of one item
+constexpr int kClaimAhead = 3;              // tiles before an item's end at which the next is claimed
+constexpr int kBarBytes = 41 * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
+                          (2 * 2 * 128 + 2 * 3 * 128) * 4 + 64;
 }  // namespace attn_tc
 
+// Work items are (sequence, kv-head group, key split). A split covers tiles
+// [t0, t0 + n_tiles_ctx) of the context; the last split of a sequence also
+// takes the block's own rows as one more tile.
 struct AttnItem {
-  int b, g, split, nsplit, C, n_tiles_ctx, n_tiles;
+  int b, g, split, nsplit, t0, C, n_tiles_ctx, n_tiles;
 };
 
-__device__ __forceinline__ int item_splits(const AttnParams& p, int b) {
-  const int C = max(0, min(p.ctx_len[b], p.max_ctx));
-  const int n_ctx_tiles = (C + attn_tc::kTileK - 1) / attn_tc::kTileK;
-  return max(1, (n_ctx_tiles + attn::kTilesPerSplit - 1) / attn::kTilesPerSplit);
+// Largest split, in 64-key tiles, of one launch: the mean work per CTA when
+// that is more than 16 tiles (a context no longer than that is processed whole,
+// with no partial results to merge), capped by what one item's page table
+// holds. Items are then handed out longest first, which balances the CTAs
+// without cutting long contexts into short pieces.
+__device__ __forceinline__ int split_cap(const AttnParams& p, long long total_tiles) {
+  const long long share = (total_tiles + attn_tc::kGrid - 1) / attn_tc::kGrid;
+  // one page more than the split spans, for splits that start inside a page
+  const long long table = (long long)(attn_tc::kPtMax - 1) * p.page_size / p.TK;
+  return (int)max((long long)attn::kMinSplitTiles, min(share, table));
 }
 
-// Work item k (0 <= k < cum[B]) in sequence-major, then kv-head, then split
-// order; cum[b] = number of items of sequences before b.
-__device__ __forceinline__ void decode_item(const AttnParams& p, const int* cum, int k, AttnItem& it) {
+__device__ __forceinline__ int ctx_tiles(const AttnParams& p, int b) {
+  const int C = max(0, min(p.ctx_len[b], p.max_ctx));
+  return (C + p.TK - 1) / p.TK;
+}
+
+// Total tiles of the launch (every kv head of every sequence).
+__device__ __forceinline__ long long launch_tiles_warp(const AttnParams& p, int lane) {
+  long long tot = 0;
+  for (int b = lane; b < p.B; b += 32) tot += (long long)p.n_groups * (ctx_tiles(p, b) + (p.n_kv > 0 ? 1 : 0));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  return tot;
+}
+
+// Near-equal split of a context of nt tiles into ceil(nt / cap) parts.
+struct SeqSplit {
+  int nt, nsplit, per;
+};
+__device__ __forceinline__ SeqSplit seq_split(const AttnParams& p, int b, int cap) {
+  SeqSplit q;
+  q.nt = ctx_tiles(p, b);
+  q.nsplit = max(1, (q.nt + cap - 1) / cap);
+  q.per = (q.nt + q.nsplit - 1) / q.nsplit;
+  return q;
+}
+
+// Work item k (0 <= k < cum[B]): sequences in the order `order` (longest items
+// first), then kv head, then split; cum[r] = items of the sequences ranked
+// before r.
+__device__ __forceinline__ void decode_item(const AttnParams& p, const int* cum, const uint16_t* order, int cap,
+                                            int k, AttnItem& it) {
   int lo = 0, hi = p.B - 1;
-  while (lo < hi) {          // last b with cum[b] <= k
+  while (lo < hi) {          // last rank r with cum[r] <= k
     const int mid = (lo + hi + 1) >> 1;
     if (cum[mid] <= k) lo = mid; else hi = mid - 1;
   }
-  it.b = lo;
+  it.b = order[lo];
   it.C = max(0, min(p.ctx_len[it.b], p.max_ctx));
-  const int n_ctx_tiles = (it.C + attn_tc::kTileK - 1) / attn_tc::kTileK;
-  it.nsplit = max(1, (n_ctx_tiles + attn::kTilesPerSplit - 1) / attn::kTilesPerSplit);
-  const int rem = k - cum[it.b];
-  it.g = rem / it.nsplit;
-  it.split = rem - it.g * it.nsplit;
-  const int t0 = it.split * attn::kTilesPerSplit;
-  it.n_tiles_ctx = max(0, min(n_ctx_tiles, t0 + attn::kTilesPerSplit) - t0);
+  const SeqSplit q = seq_split(p, it.b, cap);
+  it.nsplit = q.nsplit;
+  const int rem = k - cum[lo];
+  it.g = rem / q.nsplit;
+  it.split = rem - it.g * q.nsplit;
+  it.t0 = it.split * q.per;
+  it.n_tiles_ctx = max(0, min(q.nt, it.t0 + q.per) - it.t0);
   it.n_tiles = it.n_tiles_ctx + ((it.split == it.nsplit - 1 && p.n_kv > 0) ? 1 : 0);
 }
 
@@ -415,33 +164,40 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   return y;
 }
 
-template <int kThreadsT>
+template <int kThreadsT, int HPI>
 __global__ void __launch_bounds__(kThreadsT, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kbmap,
                const __grid_constant__ CUtensorMap vbmap, const AttnParams p, int Ms, int S, int32_t* sched) {
   using namespace attn_tc;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Roles, with W = ceil(M / 32) TMEM lane quarters holding real rows:
-  //   softmax   warps q and q + 4 for q < W (key columns 0-31 / 32-63 of a tile)
+  // Roles, with W = ceil(Mi / 32) TMEM lane quarters holding real rows.
+  // One head per item (SPL = 2 softmax warps per quarter):
+  //   softmax   warps q and q + 4 for q < W (keys 0-31 / 32-63 of a tile)
   //   epilogue  warps 8 + q for q < W (O read-out of finished items)
   //   producer  warp 2 (W <= 2) or 12; MMA issuer the warp after it
-  const int W = (p.M + 31) / 32;
-  const int n_sm = 2 * W;                    // softmax warps
-  const int prod_warp = W <= 2 ? 2 : 12, mma_warp = prod_warp + 1;
-  const int quarter = warp & 3, chalf = (warp >> 2) & 1;
-  const bool is_softmax = warp < 8 && quarter < W && warp != prod_warp && warp != mma_warp;
-  const bool is_epi = warp >= 8 && warp < 12 && quarter < W;
+  // Two heads per item (SPL = 1: a thread owns its whole row):
+  //   softmax   warps q < W;  epilogue warps 4 + q;  producer 8;  MMA 9
+  constexpr int TK = kTileK / HPI;          // keys per tile (of each of the HPI heads)
+  constexpr int SPL = HPI == 1 ? 2 : 1;     // softmax warps per TMEM lane quarter
+  constexpr int NK = TK / SPL;              // keys of a tile per softmax thread
+  constexpr int NCOL = NK * HPI;            // S columns per softmax thread (both heads)
+  const int W = (p.Mi + 31) / 32;
+  const int n_sm = SPL * W;                 // softmax warps
+  const int prod_warp = SPL == 1 ? 8 : (W <= 2 ? 2 : 12), mma_warp = prod_warp + 1;
+  const int quarter = warp & 3, chalf = SPL == 1 ? 0 : (warp >> 2) & 1;
+  const bool is_softmax = SPL == 1 ? warp < 4 && quarter < W
+                                   : warp < 8 && quarter < W && warp != prod_warp && warp != mma_warp;
+  const bool is_epi = SPL == 1 ? warp >= 4 && warp < 8 && quarter < W : warp >= 8 && warp < 12 && quarter < W;
 
-  // shared memory: [Q0][Q1: 2 atoms x Ms rows each][P0][P1: Ms rows each][S stages: K | V][barriers, tables]
+  // shared memory: [Q0][Q1: 2 atoms x Ms rows each][S stages: K | V][barriers, tables]
   // A 128-row MMA reads past the Ms stored rows into the next buffer; those
   // padding rows only produce padding rows of S, P and O, which are never used.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int atom = Ms * 128;                 // one 64-wide column block of Ms rows
   uint8_t* q_s = smem;                       // Q buffer i at + 2 i atom: d 0-63, then d 64-127
-  uint8_t* p_s = smem + 4 * atom;            // P buffer i at + i atom
-  uint8_t* kv_s = smem + 6 * atom;           // stage s: K at s*2*T, V at s*2*T + T
+  uint8_t* kv_s = smem + 4 * atom;           // stage s: K at s*2*T, V at s*2*T + T
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + S * 2 * kTileBytes);
   uint64_t* kv_full = bars;          // [5]
   uint64_t* kv_empty = bars + 5;     // [5]
@@ -459,13 +215,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint64_t* xbar = bars + 31;        // [4 quarters][2]: the two softmax warps of a quarter
   uint64_t* l_full = bars + 39;      // [2]  softmax -> epilogue: row max and sums of the item
   int* ring = reinterpret_cast<int*>(bars + 41);               // [2] item ids
-  int* cum = ring + 2;                                         // [B + 1] item prefix per sequence
-  int* pt_s = cum + (kMaxSeqs + 1);                            // [2][kPtMax] page rows of two items
+  int* cum = ring + 2;                                         // [B + 1] item prefix per rank
+  uint16_t* order = reinterpret_cast<uint16_t*>(cum + (kMaxSeqs + 1));   // [B] sequence of each rank
+  int* pt_s = reinterpret_cast<int*>(order + kMaxSeqs);        // [2][kPtMax] page rows of two items
   float* xch = reinterpret_cast<float*>(pt_s + 2 * kPtMax);    // [2 tiles][2 halves][128] tile maxima
   float* ml_s = xch + 2 * 2 * 128;                             // [2 slots][3][128]: m, l half 0, l half 1
   uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(ml_s + 2 * 3 * 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sm + 1);
   int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
+  int* cap_sm = reinterpret_cast<int*>(tmem_base_sm + 3);
 
   if (tid == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
@@ -492,12 +250,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     fence_barrier_init();
   }
   if (warp == mma_warp) tmem_alloc(tmem_base_sm, kTmemCols);
+  // ---- work list: the split size, then sequences ranked by item size ----
   if (warp == 0) {
-    // cum[b] = sum over b' < b of Hkv * splits(b'): lane-contiguous runs, then a warp scan
+    const long long tot = launch_tiles_warp(p, lane);
+    if (lane == 0) *cap_sm = split_cap(p, tot);
+  }
+  __syncthreads();
+  const int cap = *cap_sm;
+  for (int bb = tid; bb < p.B; bb += blockDim.x) cum[bb] = seq_split(p, bb, cap).per;
+  __syncthreads();
+  for (int bb = tid; bb < p.B; bb += blockDim.x) {
+    const int key = cum[bb];
+    int rank = 0;   // larger items first; equal items in sequence order
+    for (int o = 0; o < p.B; ++o) {
+      const int ko = cum[o];
+      rank += (ko > key || (ko == key && o < bb)) ? 1 : 0;
+    }
+    order[rank] = (uint16_t)bb;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // cum[r] = sum over ranks r' < r of Hkv * splits: lane-contiguous runs, then a warp scan
     const int per = (p.B + 31) / 32;
-    const int b0 = lane * per, b1 = min(p.B, b0 + per);
+    const int r0 = lane * per, r1 = min(p.B, r0 + per);
     int tot = 0;
-    for (int bb = b0; bb < b1; ++bb) tot += p.Hkv * item_splits(p, bb);
+    for (int rr = r0; rr < r1; ++rr) tot += p.n_groups * seq_split(p, order[rr], cap).nsplit;
     int incl = tot;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -505,9 +282,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (lane >= o) incl += v;
     }
     int run = incl - tot;
-    for (int bb = b0; bb < b1; ++bb) {
-      cum[bb] = run;
-      run += p.Hkv * item_splits(p, bb);
+    for (int rr = r0; rr < r1; ++rr) {
+      cum[rr] = run;
+      run += p.n_groups * seq_split(p, order[rr], cap).nsplit;
     }
     if (lane == 31) cum[p.B] = incl;
   }
@@ -520,26 +297,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 
   if (warp == prod_warp) {
     // ------------------------------ producer ------------------------------
-    // Items are claimed two ahead, and the page rows and Q of the next item are
-    // fetched while the current item's tiles stream, so that item boundaries
-    // leave no gap in the K/V stream.
+    // The next item's page rows and Q are fetched while the current item's last
+    // tiles stream, so that item boundaries leave no gap in the K/V stream.
     const int ps = p.page_size;
     int item_seq = 0, tile_seq = 0;
     bool ok = true;
-    // page rows of item `item` into table `tb` (whole warp)
+    // page rows of item `item` into table `tb` (whole warp). Every lane issues
+    // its loads together before storing any, so the fetch costs one memory
+    // latency instead of one per round.
     auto load_pages = [&](int item, int tb) {
       AttnItem it;
-      decode_item(p, cum, item, it);
-      const int lp0 = it.split * attn::kTilesPerSplit * kTileK / ps;
-      const int n_lp = it.n_tiles_ctx * kTileK / ps;
-      for (int i = lane; i < n_lp; i += 32) {
-        const int lp = lp0 + i;
-        int row = 0;   // pages past the context (or bad entries) read page 0; masked later
-        if (lp * ps < it.C && lp < p.max_pages) {
-          const int phys = p.page_table[(size_t)it.b * p.max_pages + lp];
-          if (phys >= 0 && phys < p.num_pages) row = phys * ps;
-        }
-        pt_s[tb * kPtMax + i] = row;
+      decode_item(p, cum, order, cap, item, it);
+      const int lp0 = it.t0 * TK / ps;
+      const int n_lp = ((it.t0 + it.n_tiles_ctx) * TK + ps - 1) / ps - lp0;
+      const int32_t* ptb = p.page_table + (size_t)it.b * p.max_pages;
+      constexpr int kPer = kPtMax / 32;
+      int phys[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int lp = lp0 + u * 32 + lane;
+        // pages past the context (or bad entries) read page 0; masked later
+        const bool use = u * 32 + lane < n_lp && lp * ps < it.C && lp < p.max_pages;
+        phys[u] = use ? __ldg(ptb + lp) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int ph = (phys[u] >= 0 && phys[u] < p.num_pages) ? phys[u] : 0;
+        if (u * 32 + lane < n_lp) pt_s[tb * kPtMax + u * 32 + lane] = ph * ps;
       }
       __syncwarp();
     };
@@ -551,23 +335,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         w = wait_or_abort(&q_empty[slot], (uint32_t)(((seq >> 1) & 1) ^ 1), abort_flag, p.err, 22);
         if (w) {
           AttnItem it;
-          decode_item(p, cum, item, it);
+          decode_item(p, cum, order, cap, item, it);
           uint8_t* qb = q_s + slot * 2 * atom;
-          // one TMA box [n_q][G][64] per d-half lands in the packed row order r = i * G + hh
-          mbar_arrive_expect_tx(&q_full[slot], (uint32_t)(2 * p.M * 128));
-          tma_load_3d(qb, &qmap, &q_full[slot], 0, it.g * p.G, it.b * p.n_q);
-          tma_load_3d(qb + atom, &qmap, &q_full[slot], 64, it.g * p.G, it.b * p.n_q);
+          // one TMA box [n_q][Gi][64] per d-half lands in the packed row order r = i * Gi + hh
+          mbar_arrive_expect_tx(&q_full[slot], (uint32_t)(2 * p.Mi * 128));
+          tma_load_3d(qb, &qmap, &q_full[slot], 0, it.g * p.Gi, it.b * p.n_q);
+          tma_load_3d(qb + atom, &qmap, &q_full[slot], 64, it.g * p.Gi, it.b * p.n_q);
         }
       }
       return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
     };
-    int cur = 0, nxt = 0;
-    if (lane == 0) {
-      cur = atomicAdd(&sched[0], 1);
-      nxt = atomicAdd(&sched[0], 1);
-    }
+    int cur = 0;
+    if (lane == 0) cur = atomicAdd(&sched[0], 1);
     cur = __shfl_sync(0xffffffffu, cur, 0);
-    nxt = __shfl_sync(0xffffffffu, nxt, 0);
     if (cur < n_items) {
       load_pages(cur, 0);
       ok = load_q(cur, 0);
@@ -583,11 +363,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         mbar_arrive(&it_full[slot]);    // release semantics publish the ring entry
       }
       if (last) break;
-      int claimed = 0;                  // item after next; needed one item from now
-      if (lane == 0 && nxt < n_items) claimed = atomicAdd(&sched[0], 1);
       AttnItem it;
-      decode_item(p, cum, cur, it);
+      decode_item(p, cum, order, cap, cur, it);
       const int* pt = pt_s + slot * kPtMax;
+      // the next item is claimed a few tiles before this one ends (late enough
+      // that the items still go to whichever CTA frees up first, early enough
+      // to fetch its page rows and Q before its first tile)
+      int nxt = n_items;
+      const int j_claim = max(0, it.n_tiles - kClaimAhead);
       for (int j = 0; j < it.n_tiles && ok; ++j, ++tile_seq) {
         if (lane == 0) {
           const int st = tile_seq % S;
@@ -597,34 +380,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             ok = false;
           } else if (j < it.n_tiles_ctx) {
             mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
-            for (int pg = 0; pg < kTileK / ps; ++pg) {
-              const int row = pt[j * (kTileK / ps) + pg];
+            // box jb: br keys of each of the HPI heads, landing [key][head][64 d] per
+            // d-half, so that tile row n holds key n / HPI of head n % HPI
+            const int br = p.br;
+            const int lp0 = it.t0 * TK / ps;
+            for (int jb = 0; jb < TK / br; ++jb) {
+              const int key0 = (it.t0 + j) * TK + jb * br;
+              const int row = pt[key0 / ps - lp0] + key0 % ps;
+              const int off = jb * HPI * br * 128;
               for (int h = 0; h < 2; ++h) {
-                tma_load_3d(ks + h * (kTileBytes / 2) + pg * ps * 128, &kmap, &kv_full[st], h * 64, it.g, row);
-                tma_load_3d(vs + h * (kTileBytes / 2) + pg * ps * 128, &vmap, &kv_full[st], h * 64, it.g, row);
+                tma_load_3d(ks + h * (kTileBytes / 2) + off, &kmap, &kv_full[st], h * 64, it.g * HPI, row);
+                tma_load_3d(vs + h * (kTileBytes / 2) + off, &vmap, &kv_full[st], h * 64, it.g * HPI, row);
               }
             }
             ++producer_issued;
           } else {
-            // the block's own n_kv K/V rows; rows past n_kv are masked (K) and
-            // zeroed (V) by the softmax warps
-            mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(4 * p.n_kv * 128));
+            // the block's own n_kv K/V rows of the HPI heads; rows past n_kv are
+            // masked (K) and zeroed (V) by the softmax warps
+            mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(4 * HPI * p.n_kv * 128));
             for (int h = 0; h < 2; ++h) {
-              tma_load_3d(ks + h * (kTileBytes / 2), &kbmap, &kv_full[st], h * 64, it.g, it.b * p.n_kv);
-              tma_load_3d(vs + h * (kTileBytes / 2), &vbmap, &kv_full[st], h * 64, it.g, it.b * p.n_kv);
+              tma_load_3d(ks + h * (kTileBytes / 2), &kbmap, &kv_full[st], h * 64, it.g * HPI, it.b * p.n_kv);
+              tma_load_3d(vs + h * (kTileBytes / 2), &vbmap, &kv_full[st], h * 64, it.g * HPI, it.b * p.n_kv);
             }
             ++producer_issued;
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        // a few tiles into this item, fetch the next item's page rows and Q
-        if (ok && j == min(2, it.n_tiles - 1) && nxt < n_items) {
-          load_pages(nxt, slot ^ 1);
-          ok = load_q(nxt, item_seq + 1);
+        if (ok && j == j_claim) {
+          if (lane == 0) nxt = atomicAdd(&sched[0], 1);
+          nxt = __shfl_sync(0xffffffffu, nxt, 0);
+          if (nxt < n_items) {
+            load_pages(nxt, slot ^ 1);
+            ok = load_q(nxt, item_seq + 1);
+          }
         }
       }
       cur = nxt;
-      nxt = __shfl_sync(0xffffffffu, nxt < n_items ? claimed : nxt, 0);
       ++item_seq;
     }
     // the last CTA to finish resets the work counter for the next launch
@@ -652,7 +443,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         mbar_arrive(&it_empty[slot]);
         if (item < 0) break;
         AttnItem it;
-        decode_item(p, cum, item, it);
+        decode_item(p, cum, order, cap, item, it);
         if (!wait_or_abort(&q_full[slot], par, abort_flag, p.err, 25)) break;
         if (!wait_or_abort(&o_empty[slot], par ^ 1u, abort_flag, p.err, 26)) break;
         tc_fence_after();
@@ -661,12 +452,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         auto issue_pv = [&](int t, int j) -> bool {
           if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
           tc_fence_after();
-          const uint32_t pa = smem_u32(p_s + (t & 1) * atom);
+          // P_t from TMEM (8 packed columns per 16-row K step), V_t MN-major from smem
+          const uint32_t pa = tmem_base + kPCol + (uint32_t)((t & 1) * 32);
           const uint32_t va = smem_u32(kv_s + (t % S) * 2 * kTileBytes + kTileBytes);
 #pragma unroll
           for (int i = 0; i < kTileK / 16; ++i)
-            tc_mma_bf16(o_tmem, sdesc_sw128(pa + i * 32), sdesc_sw128_mn(va + i * 2048, kTileBytes / 2), id_pv,
-                        (j > 0 || i > 0) ? 1u : 0u);
+            tc_mma_bf16_ta(o_tmem, pa + (uint32_t)(i * 8), sdesc_sw128_mn(va + i * 2048, kTileBytes / 2), id_pv,
+                           (j > 0 || i > 0) ? 1u : 0u);
           tc_commit(&pv_done[t & 1]);
           tc_commit(&kv_empty[t % S]);
           ++consumed;
@@ -708,8 +500,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // ------------------------------ softmax ------------------------------
     const int r = quarter * 32 + lane;              // packed query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int c0 = chalf * 32;                      // this warp's 32 key columns of a tile
-    const uint32_t oc0 = (uint32_t)(chalf * 64);    // and 64 of the 128 O columns for rescaling
+    // this warp's NK keys of a tile: keys kk0 .. kk0 + NK - 1 of the row's own
+    // kv head hr; key kk of head h sits in S column (and V row) kk * HPI + h, so
+    // the warp's columns are c0 .. c0 + 31 for both heads together
+    const int hr = HPI == 1 ? 0 : (r % p.Gi) / p.G;
+    const int kk0 = chalf * NK;
+    const int c0 = chalf * NCOL;
+    constexpr int OCOLS = attn::kD / SPL;           // O columns this thread rescales
+    const uint32_t oc0 = (uint32_t)(chalf * OCOLS);
     int item_seq = 0, tile_seq = 0;
     bool ok = true;
     int xs = 0;   // exchanges with the partner warp so far (both warps make the same sequence)
@@ -731,8 +529,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (lane == 0) mbar_arrive(&it_empty[slot]);
       if (item < 0) break;
       AttnItem it;
-      decode_item(p, cum, item, it);
-      const int t0 = it.split * attn::kTilesPerSplit;
+      decode_item(p, cum, order, cap, item, it);
+      const int t0 = it.t0;
       const uint32_t o_col = 128 + (uint32_t)(slot * attn::kD) + oc0;
       float m_run = -CUDART_INF_F, l_part = 0.f;
       for (int j = 0; j < it.n_tiles; ++j) {
@@ -743,32 +541,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           break;
         }
         tc_fence_after();
-        float sv[32];
+        float sv[NK];
         {
-          uint32_t raw[32];
-          tmem_ld32(tmem_base + lane_off + (uint32_t)(sb * kTileK + c0), raw);
+          // a TMEM load takes one column address for the whole warp, whose lanes
+          // may hold rows of both heads: load both heads' columns and select
+          uint32_t raw[NCOL];
+#pragma unroll
+          for (int c = 0; c < NCOL; c += 32) tmem_ld32(tmem_base + lane_off + (uint32_t)(sb * kTileK + c0 + c), raw + c);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(raw[c]);
+          for (int c = 0; c < NK; ++c)
+            sv[c] = __uint_as_float(HPI == 1 ? raw[c] : (hr ? raw[HPI * c + 1] : raw[HPI * c]));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[sb]);
-        const int valid = (j < it.n_tiles_ctx) ? min(kTileK, it.C - (t0 + j) * kTileK) : p.n_kv;
+        // keys 0 .. valid - 1 of the tile are real (per head); scores stay
+        // unscaled here (the scale is > 0, so the max commutes with it)
+        const int valid = (j < it.n_tiles_ctx) ? min(TK, it.C - (t0 + j) * TK) : p.n_kv;
         float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+        if (valid < TK) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          sv[c] = (c0 + c) < valid ? sv[c] * p.scale_log2 : -CUDART_INF_F;
-          mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+          for (int c = 0; c < NK; ++c)
+            if (kk0 + c >= valid) sv[c] = -CUDART_INF_F;
         }
-        // tile max of the row over both column halves
-        float* xb = xch + (t & 1) * 256;
-        xb[chalf * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        if (!pair_exchange()) {
-          ok = false;
-          break;
+#pragma unroll
+        for (int c = 0; c < NK; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+        float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+        if constexpr (SPL == 2) {
+          // tile max of the row over both column halves
+          float* xb = xch + (t & 1) * 256;
+          xb[chalf * 128 + r] = mt;
+          if (!pair_exchange()) {
+            ok = false;
+            break;
+          }
+          mt = fmaxf(xb[r], xb[128 + r]);
         }
-        const float mt = fmaxf(xb[r], xb[128 + r]);
         const bool raise = mt > m_run + kRescaleLog2 || (m_run == -CUDART_INF_F && mt != -CUDART_INF_F);
         const float m_new = raise ? mt : m_run;
         const float alpha = raise ? (m_run == -CUDART_INF_F ? 0.f : exp2f(m_run - m_new)) : 1.f;
@@ -781,7 +590,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < OCOLS / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tmem_base + lane_off + o_col + c * 32, o);
             tmem_ld_wait();
@@ -795,8 +604,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         const float base = (m_run == -CUDART_INF_F) ? 0.f : m_run;
         float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          sv[c] = ex2_ftz(sv[c] - base);
+        for (int c = 0; c < NK; ++c) {
+          sv[c] = ex2_ftz(fmaf(sv[c], p.scale_log2, -base));
           rs[c & 3] += sv[c];
         }
         l_part = l_part * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
@@ -806,26 +615,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           ok = false;
           break;
         }
-        uint8_t* prow = p_s + sb * atom;
+        // P_t (bf16) into its TMEM buffer: K entry n of the row (the S column /
+        // V row n) in packed column n / 2; this thread's NCOL entries start at
+        // c0, with 0 in the entries of the other head
+        {
+          const uint32_t pcol = tmem_base + lane_off + kPCol + (uint32_t)(sb * 32 + c0 / 2);
+          if constexpr (HPI == 1) {
+            uint32_t pk[NCOL / 2];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint4 v;
-          v.x = pack_bf16(sv[ch * 8 + 0], sv[ch * 8 + 1]);
-          v.y = pack_bf16(sv[ch * 8 + 2], sv[ch * 8 + 3]);
-          v.z = pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
-          v.w = pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
-          *reinterpret_cast<uint4*>(prow + swz(r, chalf * 4 + ch)) = v;
+            for (int i = 0; i < NCOL / 2; ++i) pk[i] = pack_bf16(sv[2 * i], sv[2 * i + 1]);
+            tmem_st16(pcol, pk);
+          } else {
+            uint32_t pk[NCOL / 2];
+#pragma unroll
+            for (int i = 0; i < NCOL / 2; ++i) pk[i] = hr ? pack_bf16(0.f, sv[i]) : pack_bf16(sv[i], 0.f);
+            tmem_st32(pcol, pk);
+          }
+          tmem_st_wait();
         }
-        if (valid < kTileK) {
-          // V rows past the valid keys may hold anything (P is 0 there, but 0 * NaN is NaN)
+        if (valid < TK) {
+          // V rows of keys past the valid ones may hold anything (P is 0 there,
+          // but 0 * NaN is NaN): zero them. V row n holds key n / HPI.
           uint8_t* vs = kv_s + (t % S) * 2 * kTileBytes + kTileBytes;
           const int me = (chalf * W + quarter) * 32 + lane;
-          for (int vr = valid + me; vr < kTileK; vr += n_sm * 32)
+          for (int n = me; n < kTileK; n += n_sm * 32) {
+            if (n / HPI < valid) continue;
             for (int ch = 0; ch < 16; ++ch)
-              *reinterpret_cast<uint4*>((ch < 8 ? vs : vs + kTileBytes / 2) + swz(vr, ch & 7)) =
+              *reinterpret_cast<uint4*>((ch < 8 ? vs : vs + kTileBytes / 2) + swz(n, ch & 7)) =
                   make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[sb]);
@@ -837,6 +657,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       float* mls = ml_s + slot * 384;
       if (chalf == 0) mls[r] = m_run;
       mls[128 * (1 + chalf) + r] = l_part;
+      if (SPL == 1) mls[256 + r] = 0.f;
       __syncwarp();
       if (lane == 0) mbar_arrive(&l_full[slot]);
       tile_seq += it.n_tiles;
@@ -856,7 +677,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (lane == 0) mbar_arrive(&it_empty[slot]);
       if (item < 0) break;
       AttnItem it;
-      decode_item(p, cum, item, it);
+      decode_item(p, cum, order, cap, item, it);
       if (!__all_sync(0xffffffffu, wait_or_abort(&l_full[slot], par, abort_flag, p.err, 39))) break;
       if (!__all_sync(0xffffffffu, wait_or_abort(&o_full[slot], par, abort_flag, p.err, 35))) break;
       tc_fence_after();
@@ -865,16 +686,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const float l_run = mls[128 + r] + mls[256 + r];
       const bool single = (it.nsplit == 1);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const size_t cta = ((size_t)it.b * p.Hkv + it.g) * p.max_splits + it.split;
+      const size_t cta = ((size_t)it.b * p.n_groups + it.g) * p.max_splits + it.split;
       const uint32_t o_col = 128 + (uint32_t)(slot * attn::kD);
       for (int c = 0; c < attn::kD / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tmem_base + lane_off + o_col + c * 32, o);
         tmem_ld_wait();
-        if (r < p.M) {
+        if (r < p.Mi) {
           if (single) {
-            const int i = r / p.G, hh = r - i * p.G;
-            bf16* dst = p.out + ((size_t)(it.b * p.n_q + i) * p.Hq + it.g * p.G + hh) * attn::kD + c * 32;
+            const int i = r / p.Gi, hh = r - i * p.Gi;
+            bf16* dst = p.out + ((size_t)(it.b * p.n_q + i) * p.Hq + it.g * p.Gi + hh) * attn::kD + c * 32;
 #pragma unroll
             for (int q = 0; q < 32; q += 8) {
               uint4 v;
@@ -885,7 +706,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               *reinterpret_cast<uint4*>(dst + q) = v;
             }
           } else {
-            float* dst = p.part_o + (cta * p.M + r) * attn::kD + c * 32;
+            float* dst = p.part_o + (cta * p.Mi + r) * attn::kD + c * 32;
 #pragma unroll
             for (int q = 0; q < 32; q += 4)
               *reinterpret_cast<float4*>(dst + q) = make_float4(__uint_as_float(o[q]), __uint_as_float(o[q + 1]),
@@ -893,7 +714,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
       }
-      if (!single && r < p.M) p.part_ml[cta * p.M + r] = make_float2(m_run, l_run);
+      if (!single && r < p.Mi) p.part_ml[cta * p.Mi + r] = make_float2(m_run, l_run);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[slot]);
@@ -914,34 +735,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   }
 }
 
-// Merge the split partials of every (sequence, kv head) that was split.
+// Merge the split partials of every (sequence, kv-head group) that was split.
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const AttnParams p) {
   const int g = blockIdx.x, b = blockIdx.y;
-  const int C = max(0, min(p.ctx_len[b], p.max_ctx));
-  const int n_ctx_tiles = (C + attn_tc::kTileK - 1) / attn_tc::kTileK;
-  const int nsplit = max(1, (n_ctx_tiles + attn::kTilesPerSplit - 1) / attn::kTilesPerSplit);
+  __shared__ int s_cap;
+  if (threadIdx.x < 32) {
+    // the same split plan as the attention kernel
+    const long long tot = launch_tiles_warp(p, threadIdx.x);
+    if (threadIdx.x == 0) s_cap = split_cap(p, tot);
+  }
+  __syncthreads();
+  const int nsplit = seq_split(p, b, s_cap).nsplit;
   if (nsplit == 1) return;
-  const size_t group = (size_t)b * p.Hkv + g;
-  for (int idx = threadIdx.x; idx < p.M * (attn::kD / 4); idx += blockDim.x) {
+  const size_t group = (size_t)b * p.n_groups + g;
+  for (int idx = threadIdx.x; idx < p.Mi * (attn::kD / 4); idx += blockDim.x) {
     const int row = idx / (attn::kD / 4), d4 = idx - row * (attn::kD / 4);
     float M = -CUDART_INF_F;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, p.part_ml[(group * p.max_splits + sp) * p.M + row].x);
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, p.part_ml[(group * p.max_splits + sp) * p.Mi + row].x);
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -CUDART_INF_F) {
       for (int sp = 0; sp < nsplit; ++sp) {
         const size_t c2 = group * p.max_splits + sp;
-        const float2 ml = p.part_ml[c2 * p.M + row];
+        const float2 ml = p.part_ml[c2 * p.Mi + row];
         const float w = (ml.x == -CUDART_INF_F) ? 0.f : exp2f(ml.x - M);
         L += ml.y * w;
-        const float4 v = reinterpret_cast<const float4*>(p.part_o + (c2 * p.M + row) * attn::kD)[d4];
+        const float4 v = reinterpret_cast<const float4*>(p.part_o + (c2 * p.Mi + row) * attn::kD)[d4];
         acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int i = row / p.G, hh = row - i * p.G;
-    bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.G + hh) * attn::kD + d4 * 4;
+    const int i = row / p.Gi, hh = row - i * p.Gi;
+    bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.Gi + hh) * attn::kD + d4 * 4;
     reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
     reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
   }
@@ -1031,7 +857,9 @@ attn_generic_kernel(const T* __restrict__ q, const T* __restrict__ k_blk, const 
 // ===========================================================================
 static bool bf16_fast_ok(const AttnArgs& a) {
   const int M = a.n_q * (a.Hq / a.Hkv);
+  // (the kernel takes row maxima of unscaled scores: the scale must be > 0)
   return a.dtype == 1 && a.D == 128 && M <= 16 * attn::kMaxWarps && a.n_kv >= 1 && a.n_kv <= attn::kTileK &&
+         a.scale > 0.f && a.scale < 3.0e38f &&
          a.B <= attn_tc::kMaxSeqs &&
          (a.page_size == 8 || a.page_size == 16 || a.page_size == 32 || a.page_size == 64) &&
          a.num_pages * (long)a.page_size < (1L << 31) &&
@@ -1040,16 +868,42 @@ static bool bf16_fast_ok(const AttnArgs& a) {
          (reinterpret_cast<uintptr_t>(a.v_blk) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 15) == 0;
 }
 
-static int attn_max_splits(int max_ctx) {
-  const int tiles = (max_ctx + attn::kTileK - 1) / attn::kTileK;
-  return std::max(1, (tiles + attn::kTilesPerSplit - 1) / attn::kTilesPerSplit);
+// Kv heads per work item: two heads share one item (and one TMA box per page
+// and d-half, twice the size of a one-head box) when their packed query rows
+// fit the 128 MMA rows and the pages and the block fit the paired box layout.
+static int attn_hpi(int n_q, int n_kv, int Hq, int Hkv, int page_size) {
+  const int G = Hq / Hkv;
+  const bool pair = Hkv % 2 == 0 && 2 * n_q * G <= 128 && page_size >= 16 && n_kv <= attn::kTileK / 2;
+  return pair ? 2 : 1;
 }
 
-size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int dtype) {
+static int attn_max_splits(int max_ctx, int TK) {
+  const int tiles = (max_ctx + TK - 1) / TK;
+  return std::max(1, (tiles + attn::kMinSplitTiles - 1) / attn::kMinSplitTiles);
+}
+
+size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int page_size, int dtype) {
   if (dtype != 1 || D != 128) return 0;
-  const int M = n_q * (Hq / Hkv);
-  const size_t ctas = (size_t)B * Hkv * attn_max_splits(max_ctx);
-  return align_up(ctas * M * 128 * sizeof(float)) + align_up(ctas * M * sizeof(float2));
+  const int hpi = attn_hpi(n_q, n_kv, Hq, Hkv, page_size);
+  const int Mi = hpi * n_q * (Hq / Hkv);
+  const size_t ctas = (size_t)B * (Hkv / hpi) * attn_max_splits(max_ctx, attn::kTileK / hpi);
+  return align_up(ctas * Mi * 128 * sizeof(float)) + align_up(ctas * Mi * sizeof(float2));
+}
+
+template <int kThreadsT, int HPI>
+static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                                  const CUtensorMap& kbmap, const CUtensorMap& vbmap, const AttnParams& p, int Ms,
+                                  int S, size_t smem, int32_t* sched, cudaStream_t st) {
+  static size_t smem_set = 0;   // largest dynamic shared memory opted into so far
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kThreadsT, HPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S,
+                                                                        sched);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
@@ -1069,15 +923,6 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
     return cudaGetLastError();
   }
   using namespace attn;
-  CUtensorMap kmap, vmap;
-  const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.num_pages * a.page_size};
-  const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};
-  const uint32_t box[3] = {64, 1, (uint32_t)a.page_size};
-  if (!encode_tensor_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_pool), dims,
-                         strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_pool), dims,
-                         strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorNotSupported;   // tensor-map encoding refused the pool layout
   AttnParams p;
   p.q = (const bf16*)a.q;
   p.k_blk = (const bf16*)a.k_blk;
@@ -1088,54 +933,64 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   p.B = a.B; p.n_q = a.n_q; p.n_kv = a.n_kv; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = a.Hq / a.Hkv;
   p.M = a.n_q * p.G;
   p.page_size = a.page_size; p.max_pages = a.max_pages; p.num_pages = a.num_pages;
-  p.max_splits = attn_max_splits(a.max_ctx);
+  p.hpi = attn_hpi(a.n_q, a.n_kv, a.Hq, a.Hkv, a.page_size);
+  p.Gi = p.hpi * p.G;
+  p.Mi = p.hpi * p.M;
+  p.n_groups = a.Hkv / p.hpi;
+  p.TK = kTileK / p.hpi;
+  p.br = p.hpi == 1 ? a.page_size : std::min(a.page_size, 32);
+  p.max_splits = attn_max_splits(a.max_ctx, p.TK);
   p.max_ctx = a.max_ctx;
   p.scale_log2 = a.scale * kLog2e;
-  const int M = p.M;
-  const size_t ctas = (size_t)a.B * a.Hkv * p.max_splits;
+  const int M = p.Mi;
+  const size_t ctas = (size_t)a.B * p.n_groups * p.max_splits;
   char* ws = (char*)a.scratch;
   p.part_o = (float*)ws;
   p.part_ml = (float2*)(ws + align_up(ctas * M * 128 * sizeof(float)));
   p.counters = a.counters;
   p.err = a.err;
-  CUtensorMap qmap, kbmap, vbmap;
+  // K/V pools and the block rows as [row][head][d]: a box of {64 d, hpi heads,
+  // br rows} lands as [row][head][64 d]
+  CUtensorMap kmap, vmap, qmap, kbmap, vbmap;
   {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.num_pages * a.page_size};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};
+    const uint32_t box[3] = {64, (uint32_t)p.hpi, (uint32_t)p.br};
     const uint64_t qd[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)a.B * a.n_q};
     const uint64_t qs[2] = {(uint64_t)kD * 2, (uint64_t)a.Hq * kD * 2};
-    const uint32_t qb[3] = {64, (uint32_t)(a.Hq / a.Hkv), (uint32_t)a.n_q};
+    const uint32_t qb[3] = {64, (uint32_t)p.Gi, (uint32_t)a.n_q};
     const uint64_t bd[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.B * a.n_kv};
     const uint64_t bs[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};
-    const uint32_t bb[3] = {64, 1, (uint32_t)a.n_kv};
-    if (!encode_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qd, qs, qb,
+    const uint32_t bb[3] = {64, (uint32_t)p.hpi, (uint32_t)a.n_kv};
+    if (!encode_tensor_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_pool), dims,
+                           strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_pool), dims,
+                           strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qd, qs, qb,
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map(&kbmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_blk), bd, bs, bb,
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map(&vbmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_blk), bd, bs, bb,
                            CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorNotSupported;
+      return cudaErrorNotSupported;   // tensor-map encoding refused a layout
   }
   const int Ms = M <= 64 ? 64 : 128;     // stored query rows per operand atom
-  const int S = Ms == 64 ? 5 : 3;        // K/V stages that fit beside Q and P
-  const size_t smem = 1024 + 6 * (size_t)Ms * 128 + (size_t)S * 2 * attn_tc::kTileBytes + attn_tc::kBarBytes;
-  // warps 0-9 (two softmax quarters, producer, MMA, epilogue 8-9) or 0-13
-  const bool wide = (M + 31) / 32 > 2;
-  static size_t smem_set[2] = {0, 0};   // largest dynamic shared memory opted into so far
-  if (smem > smem_set[wide]) {
-    cudaError_t e = wide ? cudaFuncSetAttribute(attn_tc_kernel<448>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)smem)
-                         : cudaFuncSetAttribute(attn_tc_kernel<320>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set[wide] = smem;
-  }
+  // K/V stages that fit beside the two Q buffers (at most the barrier count)
+  const size_t fixed = 1024 + 4 * (size_t)Ms * 128 + attn_tc::kBarBytes;
+  const int S = (int)std::min<size_t>(attn_tc::kMaxStages, (232448 - fixed) / (2 * attn_tc::kTileBytes));
+  const size_t smem = fixed + (size_t)S * 2 * attn_tc::kTileBytes;
+  // one head per item: warps 0-9 (two softmax quarters, producer, MMA,
+  // epilogue 8-9) or 0-13; two heads per item: warps 0-9
+  const bool wide = p.hpi == 1 && (M + 31) / 32 > 2;
+  cudaError_t e;
   if (wide)
-    attn_tc_kernel<448><<<attn_tc::kGrid, 448, smem, a.stream>>>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, a.sched);
+    e = launch_attn_tc<448, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
   else
-    attn_tc_kernel<320><<<attn_tc::kGrid, 320, smem, a.stream>>>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, a.sched);
-  cudaError_t e = cudaGetLastError();
+    e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream)
+                   : launch_attn_tc<320, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
   if (e != cudaSuccess) return e;
   if (p.max_splits > 1) {
-    attn_merge_kernel<<<dim3(a.Hkv, a.B), 256, 0, a.stream>>>(p);
+    attn_merge_kernel<<<dim3(p.n_groups, a.B), 256, 0, a.stream>>>(p);
     *launches = 2;
   }
   return cudaGetLastError();

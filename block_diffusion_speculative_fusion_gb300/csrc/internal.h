@@ -81,7 +81,7 @@ struct AttnArgs {
   cudaStream_t stream;
 };
 
-size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int dtype);
+size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int page_size, int dtype);
 cudaError_t launch_block_attn(const AttnArgs& a, int* launches);
 
 // ----------------------------------------------------------- materialise ---

@@ -99,6 +99,16 @@ def test_attn_bf16_page_sizes(page):
     _run(w, cache, blk, 2e-2)
 
 
+@pytest.mark.parametrize("ctx,hkv", [([2048], 8), ([1024, 333, 2049], 3)])
+def test_attn_bf16_one_kv_head_per_item(ctx, hkv):
+    # B * n_kv below one box of rows (B = 1) and an odd kv-head count both take
+    # the one-head-per-item layout of the tensor-core kernel
+    import dataclasses
+    wl = W.LLAMA8B_B1 if hkv == 8 else dataclasses.replace(W.QWEN3_4B_B8, Hq=12, Hkv=3)
+    w, cache, blk = _case(wl, ctx, seed=9)
+    _run(w, cache, blk, 2e-2)
+
+
 def test_attn_bf16_masks_garbage_past_context():
     w, cache, blk = _case(W.LLAMA8B_B64, [17, 1030, 64], seed=6, headroom=80, nan_tail=True)
     _run(w, cache, blk, 2e-2)
