@@ -84,7 +84,7 @@ constexpr uint32_t kPCol = 384;      // P_t (bf16 pairs) at kPCol + 32 (t % 2)
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kGrid = 152;                  // persistent CTAs: one per SM
 constexpr int kMaxSeqs = 1024;              // sequences per call on this path
-constexpr int kPtMax = 256;                 // page-table entries of one item
+constexpr int kPtMax = 512;                 // page-table entries of one item
 constexpr int kClaimAhead = 3;              // tiles before an item's end at which the next is claimed
 constexpr int kBarBytes = 41 * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
                           (2 * 2 * 128 + 2 * 3 * 128) * 4 + 64;
@@ -157,6 +157,11 @@ __device__ __forceinline__ void decode_item(const AttnParams& p, const int* cum,
   it.n_tiles = it.n_tiles_ctx + ((it.split == it.nsplit - 1 && p.n_kv > 0) ? 1 : 0);
 }
 
+// Barrier `id` among `n` threads (whole warps) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // 2^x on the special-function unit (flush-to-zero; P is rounded to bf16 anyway).
 __device__ __forceinline__ float ex2_ftz(float x) {
   float y;
@@ -224,6 +229,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sm + 1);
   int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
   int* cap_sm = reinterpret_cast<int*>(tmem_base_sm + 3);
+  volatile int* last_sm = reinterpret_cast<volatile int*>(tmem_base_sm + 4);   // epilogue: merge this item
 
   if (tid == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
@@ -718,6 +724,63 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[slot]);
+      if (!single) {
+        // Completion ticket of the (sequence, group): the CTA whose split
+        // finishes last merges every split's partial (still in L2) into the
+        // output. Partials are published (fence) before the ticket is taken.
+        __threadfence();
+        named_bar_sync(1, W * 32);
+        const size_t grp = (size_t)it.b * p.n_groups + it.g;
+        if (quarter == 0 && lane == 0) {
+          const int prev = atomicAdd(&p.counters[grp], 1);
+          const int last = prev == it.nsplit - 1;
+          if (last) p.counters[grp] = 0;   // every split has arrived: ready for the next launch
+          *last_sm = last;
+        }
+        named_bar_sync(1, W * 32);
+        if (*last_sm && r < p.Mi) {
+          __threadfence();
+          const float2* ml = p.part_ml + grp * p.max_splits * p.Mi + r;
+          float mx = -CUDART_INF_F;
+          for (int sp = 0; sp < it.nsplit; ++sp) mx = fmaxf(mx, __ldcg(ml + (size_t)sp * p.Mi).x);
+          float L = 0.f;
+          for (int sp = 0; sp < it.nsplit; ++sp) {
+            const float2 v = __ldcg(ml + (size_t)sp * p.Mi);
+            L += v.x == -CUDART_INF_F ? 0.f : v.y * exp2f(v.x - mx);
+          }
+          const float inv_l = L > 0.f ? 1.f / L : 0.f;
+          const int i = r / p.Gi, hh = r - i * p.Gi;
+          bf16* dst = p.out + ((size_t)(it.b * p.n_q + i) * p.Hq + it.g * p.Gi + hh) * attn::kD;
+          for (int c = 0; c < attn::kD; c += 32) {
+            float acc[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+            for (int sp = 0; sp < it.nsplit; ++sp) {
+              const float2 v = __ldcg(ml + (size_t)sp * p.Mi);
+              const float w = v.x == -CUDART_INF_F ? 0.f : exp2f(v.x - mx) * inv_l;
+              const float4* src =
+                  reinterpret_cast<const float4*>(p.part_o + ((grp * p.max_splits + sp) * p.Mi + r) * attn::kD + c);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 x = __ldcg(src + q);
+                acc[4 * q + 0] += w * x.x;
+                acc[4 * q + 1] += w * x.y;
+                acc[4 * q + 2] += w * x.z;
+                acc[4 * q + 3] += w * x.w;
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) {
+              uint4 v;
+              v.x = pack_bf16(acc[q + 0], acc[q + 1]);
+              v.y = pack_bf16(acc[q + 2], acc[q + 3]);
+              v.z = pack_bf16(acc[q + 4], acc[q + 5]);
+              v.w = pack_bf16(acc[q + 6], acc[q + 7]);
+              *reinterpret_cast<uint4*>(dst + c + q) = v;
+            }
+          }
+        }
+      }
       ++item_seq;
     }
   }
@@ -732,44 +795,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == mma_warp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
-// Merge the split partials of every (sequence, kv-head group) that was split.
-__global__ void __launch_bounds__(256)
-attn_merge_kernel(const AttnParams p) {
-  const int g = blockIdx.x, b = blockIdx.y;
-  __shared__ int s_cap;
-  if (threadIdx.x < 32) {
-    // the same split plan as the attention kernel
-    const long long tot = launch_tiles_warp(p, threadIdx.x);
-    if (threadIdx.x == 0) s_cap = split_cap(p, tot);
-  }
-  __syncthreads();
-  const int nsplit = seq_split(p, b, s_cap).nsplit;
-  if (nsplit == 1) return;
-  const size_t group = (size_t)b * p.n_groups + g;
-  for (int idx = threadIdx.x; idx < p.Mi * (attn::kD / 4); idx += blockDim.x) {
-    const int row = idx / (attn::kD / 4), d4 = idx - row * (attn::kD / 4);
-    float M = -CUDART_INF_F;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, p.part_ml[(group * p.max_splits + sp) * p.Mi + row].x);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -CUDART_INF_F) {
-      for (int sp = 0; sp < nsplit; ++sp) {
-        const size_t c2 = group * p.max_splits + sp;
-        const float2 ml = p.part_ml[c2 * p.Mi + row];
-        const float w = (ml.x == -CUDART_INF_F) ? 0.f : exp2f(ml.x - M);
-        L += ml.y * w;
-        const float4 v = reinterpret_cast<const float4*>(p.part_o + (c2 * p.Mi + row) * attn::kD)[d4];
-        acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
-      }
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int i = row / p.Gi, hh = row - i * p.Gi;
-    bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.Gi + hh) * attn::kD + d4 * 4;
-    reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
   }
 }
 
@@ -988,12 +1013,7 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   else
     e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream)
                    : launch_attn_tc<320, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
-  if (e != cudaSuccess) return e;
-  if (p.max_splits > 1) {
-    attn_merge_kernel<<<dim3(p.n_groups, a.B), 256, 0, a.stream>>>(p);
-    *launches = 2;
-  }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dflash
