@@ -92,10 +92,17 @@ class DflashStep:
     def ctx_len(self) -> torch.Tensor:
         return self.ctx[self.cur]
 
-    def copy_inputs_from_host(self):
-        """Host -> device copies of one step's inputs (pinned host memory)."""
-        for k_, v_ in self.inp.items():
+    def copy_inputs_from_host(self, inp: Optional[Dict[str, torch.Tensor]] = None):
+        """Host -> device copies of one step's inputs (pinned host memory) into
+        ``inp`` (default: the step's own input buffers), on the current stream."""
+        inp = self.inp if inp is None else inp
+        for k_, v_ in inp.items():
             v_.copy_(self.host[k_], non_blocking=True)
+
+    def second_input_set(self) -> Dict[str, torch.Tensor]:
+        """A second set of device input buffers, for copying the next step's
+        inputs while the current step runs."""
+        return {k_: torch.empty_like(v_) for k_, v_ in self.inp.items()}
 
     def input_bytes(self) -> int:
         return sum(v_.numel() * v_.element_size() for v_ in self.host.values())
@@ -103,11 +110,12 @@ class DflashStep:
     def _ws(self, name: str, slot: int) -> Optional[torch.Tensor]:
         return self.ws.get(name)
 
-    def step(self, timer=None):
-        """Enqueue one step. ``timer(name)`` (optional) is called between calls
-        to record per-kernel events."""
+    def step(self, timer=None, inp: Optional[Dict[str, torch.Tensor]] = None):
+        """Enqueue one step on the current stream, reading the inputs ``inp``
+        (default: the step's own input buffers). ``timer(name)`` (optional) is
+        called between calls to record per-kernel events."""
         wl = self.wl
-        inp = self.inp
+        inp = self.inp if inp is None else inp
         if self.stationary:
             cur, nxt = self.ctx_start, self.ctx[1]
         else:
