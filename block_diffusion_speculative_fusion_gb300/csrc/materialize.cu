@@ -29,9 +29,12 @@ __global__ void __launch_bounds__(256)
 mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restrict__ start_pos, int B,
                 int rows_max, int32_t* __restrict__ meta, int32_t* __restrict__ row_b,
                 int32_t* __restrict__ row_j, int32_t* __restrict__ new_len, int tc, int N1, int K1, int N2,
-                int K2) {
+                int K2, float rope_theta, int D, double* __restrict__ inv_freq) {
   __shared__ int32_t scan[256];
   const int tid = threadIdx.x;
+  // RoPE frequencies theta^(-2i/D), once per call, in double
+  if (rope_theta > 0.f)
+    for (int i = tid; i < D / 2; i += blockDim.x) inv_freq[i] = exp(-(2.0 * i / D) * log((double)rope_theta));
   const int per = (B + blockDim.x - 1) / blockDim.x;
   const int b0 = tid * per, b1 = min(B, b0 + per);
   int local = 0;
@@ -68,16 +71,38 @@ mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restric
 __global__ void __launch_bounds__(256)
 mat_gather_kernel(const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, const int32_t* __restrict__ meta,
                   const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j, int rows_max,
-                  size_t row_bytes) {
-  const int t = blockIdx.y;
-  if (t >= meta[0]) return;
-  const uint8_t* src = hidden + ((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes;
-  uint8_t* dst = X + (size_t)t * row_bytes;
-  const size_t nvec = row_bytes / 16;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < nvec; v += (size_t)gridDim.x * blockDim.x)
-    reinterpret_cast<uint4*>(dst)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
-  if (blockIdx.x == 0)
-    for (size_t e = nvec * 16 + threadIdx.x; e < row_bytes; e += blockDim.x) dst[e] = src[e];
+                  size_t row_bytes, const int32_t* __restrict__ start_pos, const double* __restrict__ inv_freq,
+                  float2* __restrict__ rope, int half) {
+  // grid-stride over the committed rows only (their count is on the device)
+  const long T = meta[0];
+  const long nvec = (long)(row_bytes / 16);
+  const long stride = (long)gridDim.x * blockDim.x;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * nvec; idx += stride) {
+    const long t = idx / nvec, v = idx - t * nvec;
+    const uint4* src = reinterpret_cast<const uint4*>(hidden + ((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes);
+    reinterpret_cast<uint4*>(X + (size_t)t * row_bytes)[v] = __ldg(src + v);
+  }
+  const long tail = (long)row_bytes - nvec * 16;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * tail; idx += stride) {
+    const long t = idx / tail, e = nvec * 16 + (idx - t * tail);
+    X[(size_t)t * row_bytes + e] = hidden[((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes + e];
+  }
+  // RoPE (cos, sin) of every committed row's position, pair i: the angle
+  // pos * theta^(-2i/D) in double (it reaches ~1e4 radians), reduced to
+  // [-pi, pi] by Cody-Waite subtraction of k * 2 pi with 2 pi split into a
+  // double and its remainder, then sin/cos in fp32 on the reduced angle
+  if (rope)
+    for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * half; idx += stride) {
+      const long t = idx / half;
+      const int i = (int)(idx - t * half);
+      const double a = (double)(start_pos[row_b[t]] + row_j[t]) * inv_freq[i];
+      const double k = rint(a * 0.15915494309189535);
+      double r = fma(-k, 6.283185307179586, a);
+      r = fma(-k, 2.4492935982947064e-16, r);
+      float sf, cf;
+      sincosf((float)r, &sf, &cf);
+      rope[idx] = make_float2(cf, sf);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -137,64 +162,61 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 mat_bias_kernel(const float* __restrict__ part, int splits, const T* __restrict__ b_f, T* __restrict__ h,
                 const int32_t* __restrict__ meta, int T_max, int d, int K1) {
-  const int t = blockIdx.y;
-  if (t >= meta[0]) return;
+  // grid-stride over the committed rows only; 4 consecutive features per
+  // thread (d % 4 == 0: they share one output tile, hence one segment count)
+  const int d4 = d / 4;
+  const long Tn = (long)min(meta[0], T_max) * d4;
   const int per = meta[1];
-  for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < d; f += gridDim.x * blockDim.x) {
-    float v = b_f ? to_f32(b_f[f]) : 0.f;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < Tn; idx += (long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / d4), f = 4 * (int)(idx - (long)t * d4);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (b_f) v = make_float4(to_f32(b_f[f]), to_f32(b_f[f + 1]), to_f32(b_f[f + 2]), to_f32(b_f[f + 3]));
     const int segs = part_segs(t, f, d, K1, per, splits);
-    for (int s = 0; s < segs; ++s) v += part[((size_t)s * T_max + t) * d + f];
-    h[(size_t)t * d + f] = from_f32<T>(v);
+    for (int s = 0; s < segs; ++s) {
+      const float4 x = *reinterpret_cast<const float4*>(part + ((size_t)s * T_max + t) * d + f);
+      v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+    }
+    T* o = h + (size_t)t * d + f;
+    o[0] = from_f32<T>(v.x); o[1] = from_f32<T>(v.y); o[2] = from_f32<T>(v.z); o[3] = from_f32<T>(v.w);
   }
 }
 
 // ---------------------------------------------------------------------------
-// epilogue: one CTA per committed token; one warp per (layer, K|V, kv head)
-// vector of D values. K: RMSNorm over D, then rotate-half RoPE at the token's
-// absolute position; then the cast and the paged write.
+// epilogue: one warp per (committed token, layer, K|V, kv head) vector of D
+// values, grid-stride. K: RMSNorm over D, then rotate-half RoPE at the token's
+// absolute position (cos/sin table from the gather kernel); then the cast and
+// the paged write.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256)
 mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* __restrict__ meta,
                     const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j,
                     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ page_table,
-                    const T* __restrict__ k_norm_w, float rms_eps, float rope_theta, MatPools pools,
+                    const T* __restrict__ k_norm_w, float rms_eps, const float2* __restrict__ rope, MatPools pools,
                     int T_max, int L, int Hkv, int D, int page_size, int max_pages, int num_pages, int K2) {
-  extern __shared__ float esm[];             // [D/2] cos, [D/2] sin, [warps][D] staging
-  float* cs = esm;
-  float* sn = esm + D / 2;
-  const int t = blockIdx.x;
-  if (t >= meta[0]) return;
-  const int b = row_b[t], j = row_j[t];
-  const int pos = start_pos[b] + j;
-  const int lp = pos / page_size;
-  if (pos < 0 || lp >= max_pages) return;
-  const int phys = page_table[(size_t)b * max_pages + lp];
-  if (phys < 0 || phys >= num_pages) return;
-  const size_t slot = (size_t)phys * page_size + pos % page_size;
-  const int half = D / 2;
-  if (rope_theta > 0.f) {
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-      // angle in double: positions reach ~1e4 radians at the lowest frequency
-      const double inv_freq = exp(-(2.0 * i / D) * log((double)rope_theta));
-      double sd, cd;
-      sincos((double)pos * inv_freq, &sd, &cd);
-      cs[i] = (float)cd;
-      sn[i] = (float)sd;
-    }
-  }
-  __syncthreads();
+  extern __shared__ float esm[];             // [warps][D] staging
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  float* xs = esm + D + warp * D;
-  const int N = L * 2 * Hkv * D;
+  float* xs = esm + warp * D;
+  const int NV = L * 2 * Hkv;
+  const int N = NV * D;
+  const int half = D / 2;
   const int per = meta[2];
-  for (int v = warp; v < L * 2 * Hkv; v += nwarps) {
+  const long tasks = (long)min(meta[0], T_max) * NV;
+  for (long task = (long)blockIdx.x * nwarps + warp; task < tasks; task += (long)gridDim.x * nwarps) {
+    const int t = (int)(task / NV), v = (int)(task - (long)t * NV);
+    const int b = row_b[t];
+    const int pos = start_pos[b] + row_j[t];
+    const int lp = pos / page_size;
+    if (pos < 0 || lp >= max_pages) continue;
+    const int phys = page_table[(size_t)b * max_pages + lp];
+    if (phys < 0 || phys >= num_pages) continue;
+    const size_t slot = (size_t)phys * page_size + pos % page_size;
     const int h = v % Hkv, kv = (v / Hkv) & 1, l = v / (2 * Hkv);
-    const size_t n0 = (size_t)v * D;   // column of (l, kv, h) in [L, 2, Hkv*D]
+    const int n0 = v * D;                    // column of (l, kv, h) in [L, 2, Hkv*D]
     float ss = 0.f;
     for (int d = lane; d < D; d += 32) {
       float x = 0.f;
-      const int segs = part_segs(t, (int)n0 + d, N, K2, per, splits);
+      const int segs = part_segs(t, n0 + d, N, K2, per, splits);
       for (int s = 0; s < segs; ++s) x += part[((size_t)s * T_max + t) * N + n0 + d];
       xs[d] = x;
       ss += x * x;
@@ -215,11 +237,13 @@ mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* _
     for (int d = lane; d < D; d += 32) {
       float x = xs[d] * scale;
       if (k_norm_w) x *= to_f32(k_norm_w[(size_t)l * D + d]);
-      if (rope_theta > 0.f) {
+      if (rope) {
         const int i = d < half ? d : d - half;
-        float y = xs[d < half ? d + half : d - half] * scale;
-        if (k_norm_w) y *= to_f32(k_norm_w[(size_t)l * D + (d < half ? d + half : d - half)]);
-        x = d < half ? x * cs[i] - y * sn[i] : x * cs[i] + y * sn[i];
+        const int dp = d < half ? d + half : d - half;
+        float y = xs[dp] * scale;
+        if (k_norm_w) y *= to_f32(k_norm_w[(size_t)l * D + dp]);
+        const float2 c = rope[(size_t)t * half + i];
+        x = d < half ? x * c.x - y * c.y : x * c.x + y * c.y;
       }
       dst[d] = from_f32<T>(x);
     }
@@ -252,6 +276,8 @@ size_t mat_ws_bytes(const MatPlan& p, int dtype) {
   const size_t el = dtype == 1 ? 2 : 4;
   const size_t Nmax = std::max(p.N1, p.N2);
   size_t s = align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max));
+  s += align_up(sizeof(double) * 128);             // RoPE frequencies (D <= 256)
+  s += align_up(sizeof(float2) * (size_t)p.T_max * 128);   // RoPE (cos, sin) per committed row
   s += align_up((size_t)p.T_max * p.K1 * el);     // gathered operand X
   s += align_up((size_t)p.T_max * p.N1 * el);     // h_ctx
   s += align_up((size_t)std::max(p.S1, p.S2) * p.T_max * Nmax * sizeof(float));
@@ -277,6 +303,10 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   int32_t* row_b = meta + 64;
   int32_t* row_j = row_b + p.T_max;
   ws += align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max));
+  double* inv_freq = (double*)ws;
+  ws += align_up(sizeof(double) * 128);
+  float2* rope = a.rope_theta > 0.f ? (float2*)ws : nullptr;
+  ws += align_up(sizeof(float2) * (size_t)p.T_max * 128);
   T* X = (T*)ws;
   ws += align_up((size_t)p.T_max * p.K1 * el);
   T* h = (T*)ws;
@@ -285,26 +315,26 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   cudaStream_t st = a.stream;
   int n = 0;
   mat_plan_kernel<<<1, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, meta, row_b, row_j, a.new_len,
-                                     p.tc ? 1 : 0, p.N1, p.K1, p.N2, p.K2);
+                                     p.tc ? 1 : 0, p.N1, p.K1, p.N2, p.K2, a.rope_theta, a.D, inv_freq);
   ++n;
   const size_t row_bytes = (size_t)p.K1 * el;
-  dim3 gg((unsigned)std::min<size_t>(8, (row_bytes / 16 + 255) / 256 + 1), p.T_max);
-  mat_gather_kernel<<<gg, 256, 0, st>>>((const uint8_t*)a.hidden, (uint8_t*)X, meta, row_b, row_j, a.rows_max,
-                                        row_bytes);
+  // grid-stride kernels over the committed rows: a few waves of the 152 SMs
+  const int gs = 4 * 152;
+  mat_gather_kernel<<<gs, 256, 0, st>>>((const uint8_t*)a.hidden, (uint8_t*)X, meta, row_b, row_j, a.rows_max,
+                                        row_bytes, a.start_pos, inv_freq, rope, a.D / 2);
   ++n;
   cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, 1, a.err, st);
   if (e != cudaSuccess) return e;
   ++n;
-  dim3 gb((p.N1 + 255) / 256, p.T_max);
-  mat_bias_kernel<T><<<gb, 256, 0, st>>>(part, p.S1, (const T*)a.b_f, h, meta, p.T_max, p.N1, p.K1);
+  mat_bias_kernel<T><<<gs, 256, 0, st>>>(part, p.S1, (const T*)a.b_f, h, meta, p.T_max, p.N1, p.K1);
   ++n;
   e = run_gemm<T>(p, p.tc, h, a.W_kv, part, meta, p.N2, p.K2, p.S2, 2, a.err, st);
   if (e != cudaSuccess) return e;
   ++n;
-  const size_t esmem = sizeof(float) * (a.D + 8 * (size_t)a.D);
-  mat_epilogue_kernel<T><<<p.T_max, 256, esmem, st>>>(
-      part, p.S2, meta, row_b, row_j, a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, a.rope_theta,
-      a.pools, p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages, p.K2);
+  const size_t esmem = sizeof(float) * 8 * (size_t)a.D;
+  mat_epilogue_kernel<T><<<gs, 256, esmem, st>>>(
+      part, p.S2, meta, row_b, row_j, a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, rope, a.pools,
+      p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages, p.K2);
   ++n;
   *launches = n;
   return cudaGetLastError();
