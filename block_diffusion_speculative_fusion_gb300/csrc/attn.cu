@@ -87,7 +87,7 @@ constexpr int kMaxSeqs = 1024;              // sequences per call on this path
 constexpr int kPtMax = 512;                 // page-table entries of one item
 constexpr int kClaimAhead = 3;              // tiles before an item's end at which the next is claimed
 constexpr int kBarBytes = 41 * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
-                          (2 * 2 * 128 + 2 * 3 * 128) * 4 + 64;
+                          (2 * 2 * 128 + 2 * 4 * 128) * 4 + 64;
 }  // namespace attn_tc
 
 // Work items are (sequence, kv-head group, key split). A split covers tiles
@@ -176,24 +176,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                const __grid_constant__ CUtensorMap vbmap, const AttnParams p, int Ms, int S, int32_t* sched) {
   using namespace attn_tc;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Roles, with W = ceil(Mi / 32) TMEM lane quarters holding real rows.
-  // One head per item (SPL = 2 softmax warps per quarter):
-  //   softmax   warps q and q + 4 for q < W (keys 0-31 / 32-63 of a tile)
+  // Roles, with W = ceil(Mi / 32) TMEM lane quarters holding real rows:
+  //   softmax   warps q and q + 4 for q < W (half h = 0, 1 of the pair)
   //   epilogue  warps 8 + q for q < W (O read-out of finished items)
   //   producer  warp 2 (W <= 2) or 12; MMA issuer the warp after it
-  // Two heads per item (SPL = 1: a thread owns its whole row):
-  //   softmax   warps q < W;  epilogue warps 4 + q;  producer 8;  MMA 9
+  // One head per item: half h takes keys 32h .. 32h + 31 of every tile (SPL = 2
+  // column halves; the row max is exchanged). Two heads per item: half h takes
+  // every other tile of an item whole (ALT = 2 tile groups) and accumulates
+  // into its own TMEM O; the epilogue merges the two.
   constexpr int TK = kTileK / HPI;          // keys per tile (of each of the HPI heads)
-  constexpr int SPL = HPI == 1 ? 2 : 1;     // softmax warps per TMEM lane quarter
+  constexpr int SPL = HPI == 1 ? 2 : 1;     // softmax warps sharing one tile's row
+  constexpr int ALT = HPI == 1 ? 1 : 2;     // softmax warp groups taking alternate tiles
   constexpr int NK = TK / SPL;              // keys of a tile per softmax thread
   constexpr int NCOL = NK * HPI;            // S columns per softmax thread (both heads)
   const int W = (p.Mi + 31) / 32;
-  const int n_sm = SPL * W;                 // softmax warps
-  const int prod_warp = SPL == 1 ? 8 : (W <= 2 ? 2 : 12), mma_warp = prod_warp + 1;
-  const int quarter = warp & 3, chalf = SPL == 1 ? 0 : (warp >> 2) & 1;
-  const bool is_softmax = SPL == 1 ? warp < 4 && quarter < W
-                                   : warp < 8 && quarter < W && warp != prod_warp && warp != mma_warp;
-  const bool is_epi = SPL == 1 ? warp >= 4 && warp < 8 && quarter < W : warp >= 8 && warp < 12 && quarter < W;
+  const int n_sm = 2 * W;                   // softmax warps
+  const int n_tile_sm = n_sm / ALT;         // softmax warps that consume one tile
+  const int prod_warp = W <= 2 ? 2 : 12, mma_warp = prod_warp + 1;
+  const int quarter = warp & 3, chalf = (warp >> 2) & 1;
+  const bool is_softmax = warp < 8 && quarter < W && warp != prod_warp && warp != mma_warp;
+  const bool is_epi = warp >= 8 && warp < 12 && quarter < W;
 
   // shared memory: [Q0][Q1: 2 atoms x Ms rows each][S stages: K | V][barriers, tables]
   // A 128-row MMA reads past the Ms stored rows into the next buffer; those
@@ -224,8 +226,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint16_t* order = reinterpret_cast<uint16_t*>(cum + (kMaxSeqs + 1));   // [B] sequence of each rank
   int* pt_s = reinterpret_cast<int*>(order + kMaxSeqs);        // [2][kPtMax] page rows of two items
   float* xch = reinterpret_cast<float*>(pt_s + 2 * kPtMax);    // [2 tiles][2 halves][128] tile maxima
-  float* ml_s = xch + 2 * 2 * 128;                             // [2 slots][3][128]: m, l half 0, l half 1
-  uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(ml_s + 2 * 3 * 128);
+  float* ml_s = xch + 2 * 2 * 128;     // [2 slots][4][128]: (m, l) of softmax half 0, then of half 1
+  uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(ml_s + 2 * 4 * 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sm + 1);
   int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
   int* cap_sm = reinterpret_cast<int*>(tmem_base_sm + 3);
@@ -238,8 +240,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], n_sm);
-      mbar_init(&p_full[i], n_sm);
+      mbar_init(&s_empty[i], n_tile_sm);
+      mbar_init(&p_full[i], n_tile_sm);
       mbar_init(&pv_done[i], 1);
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
@@ -450,21 +452,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         if (item < 0) break;
         AttnItem it;
         decode_item(p, cum, order, cap, item, it);
+        // O: one buffer per item slot (ALT = 1), or both buffers for every item (ALT = 2)
+        const int oi = ALT == 2 ? 0 : slot;
+        const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
         if (!wait_or_abort(&q_full[slot], par, abort_flag, p.err, 25)) break;
-        if (!wait_or_abort(&o_empty[slot], par ^ 1u, abort_flag, p.err, 26)) break;
+        if (!wait_or_abort(&o_empty[oi], opar ^ 1u, abort_flag, p.err, 26)) break;
         tc_fence_after();
         const uint32_t qa = smem_u32(q_s + slot * 2 * atom);
-        const uint32_t o_tmem = tmem_base + 128 + (uint32_t)(slot * attn::kD);
         auto issue_pv = [&](int t, int j) -> bool {
           if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
           tc_fence_after();
           // P_t from TMEM (8 packed columns per 16-row K step), V_t MN-major from smem
           const uint32_t pa = tmem_base + kPCol + (uint32_t)((t & 1) * 32);
           const uint32_t va = smem_u32(kv_s + (t % S) * 2 * kTileBytes + kTileBytes);
+          const uint32_t o_tmem = tmem_base + 128 + (uint32_t)((ALT == 2 ? (t & 1) : slot) * attn::kD);
 #pragma unroll
           for (int i = 0; i < kTileK / 16; ++i)
             tc_mma_bf16_ta(o_tmem, pa + (uint32_t)(i * 8), sdesc_sw128_mn(va + i * 2048, kTileBytes / 2), id_pv,
-                           (j > 0 || i > 0) ? 1u : 0u);
+                           (j >= ALT || i > 0) ? 1u : 0u);
           tc_commit(&pv_done[t & 1]);
           tc_commit(&kv_empty[t % S]);
           ++consumed;
@@ -493,7 +498,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         if (!ok) break;
         if (!issue_pv(tile_seq + it.n_tiles - 1, it.n_tiles - 1)) break;
-        tc_commit(&o_full[slot]);
+        tc_commit(&o_full[oi]);
         tile_seq += it.n_tiles;
         ++item_seq;
       }
@@ -510,10 +515,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // kv head hr; key kk of head h sits in S column (and V row) kk * HPI + h, so
     // the warp's columns are c0 .. c0 + 31 for both heads together
     const int hr = HPI == 1 ? 0 : (r % p.Gi) / p.G;
-    const int kk0 = chalf * NK;
-    const int c0 = chalf * NCOL;
+    const int kk0 = ALT == 2 ? 0 : chalf * NK;
+    const int c0 = ALT == 2 ? 0 : chalf * NCOL;
     constexpr int OCOLS = attn::kD / SPL;           // O columns this thread rescales
-    const uint32_t oc0 = (uint32_t)(chalf * OCOLS);
+    const uint32_t oc0 = (uint32_t)(ALT == 2 ? 0 : chalf * OCOLS);
     int item_seq = 0, tile_seq = 0;
     bool ok = true;
     int xs = 0;   // exchanges with the partner warp so far (both warps make the same sequence)
@@ -537,9 +542,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       AttnItem it;
       decode_item(p, cum, order, cap, item, it);
       const int t0 = it.t0;
-      const uint32_t o_col = 128 + (uint32_t)(slot * attn::kD) + oc0;
+      const uint32_t o_col = 128 + (uint32_t)((ALT == 2 ? chalf : slot) * attn::kD) + oc0;
       float m_run = -CUDART_INF_F, l_part = 0.f;
-      for (int j = 0; j < it.n_tiles; ++j) {
+      // ALT = 2: this half takes the item's tiles t with t % 2 == half
+      for (int j = ALT == 2 ? ((chalf - tile_seq) & 1) : 0; j < it.n_tiles; j += ALT) {
         const int t = tile_seq + j;
         const int sb = t & 1;
         if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[sb], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 32))) {
@@ -587,9 +593,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         const bool raise = mt > m_run + kRescaleLog2 || (m_run == -CUDART_INF_F && mt != -CUDART_INF_F);
         const float m_new = raise ? mt : m_run;
         const float alpha = raise ? (m_run == -CUDART_INF_F ? 0.f : exp2f(m_run - m_new)) : 1.f;
-        if (j >= 1 && __any_sync(0xffffffffu, raise)) {
+        if (j >= ALT && __any_sync(0xffffffffu, raise)) {
           // O must hold every earlier tile of the item before it is rescaled
-          if (!__all_sync(0xffffffffu, wait_or_abort(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1),
+          // (the last one into this O is tile t - ALT)
+          if (!__all_sync(0xffffffffu, wait_or_abort(&pv_done[(t - ALT) & 1], (uint32_t)(((t - ALT) >> 1) & 1),
                                                      abort_flag, p.err, 33))) {
             ok = false;
             break;
@@ -660,10 +667,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // hand the row max and this half's row sums to the epilogue warps; the
       // slot is free again once the epilogue of item_seq - 2 released O (the
       // MMA only started this item after that)
-      float* mls = ml_s + slot * 384;
-      if (chalf == 0) mls[r] = m_run;
-      mls[128 * (1 + chalf) + r] = l_part;
-      if (SPL == 1) mls[256 + r] = 0.f;
+      float* mls = ml_s + slot * 512;
+      mls[256 * chalf + r] = m_run;
+      mls[256 * chalf + 128 + r] = l_part;
       __syncwarp();
       if (lane == 0) mbar_arrive(&l_full[slot]);
       tile_seq += it.n_tiles;
@@ -684,20 +690,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (item < 0) break;
       AttnItem it;
       decode_item(p, cum, order, cap, item, it);
+      const int oi = ALT == 2 ? 0 : slot;
+      const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
       if (!__all_sync(0xffffffffu, wait_or_abort(&l_full[slot], par, abort_flag, p.err, 39))) break;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&o_full[slot], par, abort_flag, p.err, 35))) break;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&o_full[oi], opar, abort_flag, p.err, 35))) break;
       tc_fence_after();
-      const float* mls = ml_s + slot * 384;
-      const float m_run = mls[r];
-      const float l_run = mls[128 + r] + mls[256 + r];
+      const float* mls = ml_s + slot * 512;
+      const float ma = mls[r], la = mls[128 + r], mb = mls[256 + r], lb = mls[384 + r];
+      // one O (ALT = 1: the halves' sums share one max) or two O merged (ALT = 2)
+      float m_run, l_run, wa = 1.f, wb = 0.f;
+      if (ALT == 1) {
+        m_run = ma;
+        l_run = la + lb;
+      } else {
+        m_run = fmaxf(ma, mb);
+        wa = la > 0.f ? exp2f(ma - m_run) : 0.f;
+        wb = lb > 0.f ? exp2f(mb - m_run) : 0.f;
+        l_run = la * wa + lb * wb;
+      }
       const bool single = (it.nsplit == 1);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const size_t cta = ((size_t)it.b * p.n_groups + it.g) * p.max_splits + it.split;
-      const uint32_t o_col = 128 + (uint32_t)(slot * attn::kD);
+      const uint32_t o_col = 128 + (uint32_t)((ALT == 2 ? 0 : slot) * attn::kD);
       for (int c = 0; c < attn::kD / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tmem_base + lane_off + o_col + c * 32, o);
-        tmem_ld_wait();
+        if (ALT == 2) {
+          uint32_t ob[32];
+          tmem_ld32(tmem_base + lane_off + o_col + attn::kD + c * 32, ob);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            // a half that took no tile has l = 0 and an O that was never written
+            const float xa = wa != 0.f ? __uint_as_float(o[q]) * wa : 0.f;
+            const float xb = wb != 0.f ? __uint_as_float(ob[q]) * wb : 0.f;
+            o[q] = __float_as_uint(xa + xb);
+          }
+        } else {
+          tmem_ld_wait();
+        }
         if (r < p.Mi) {
           if (single) {
             const int i = r / p.Gi, hh = r - i * p.Gi;
@@ -723,7 +754,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (!single && r < p.Mi) p.part_ml[cta * p.Mi + r] = make_float2(m_run, l_run);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[slot]);
+      if (lane == 0) mbar_arrive(&o_empty[oi]);
       if (!single) {
         // Completion ticket of the (sequence, group): the CTA whose split
         // finishes last merges every split's partial (still in L2) into the
@@ -1004,12 +1035,12 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   const size_t fixed = 1024 + 4 * (size_t)Ms * 128 + attn_tc::kBarBytes;
   const int S = (int)std::min<size_t>(attn_tc::kMaxStages, (232448 - fixed) / (2 * attn_tc::kTileBytes));
   const size_t smem = fixed + (size_t)S * 2 * attn_tc::kTileBytes;
-  // one head per item: warps 0-9 (two softmax quarters, producer, MMA,
-  // epilogue 8-9) or 0-13; two heads per item: warps 0-9
-  const bool wide = p.hpi == 1 && (M + 31) / 32 > 2;
+  // warps 0-9 (two softmax quarters, producer, MMA, epilogue 8-9) or 0-13
+  const bool wide = (M + 31) / 32 > 2;
   cudaError_t e;
   if (wide)
-    e = launch_attn_tc<448, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
+    e = p.hpi == 2 ? launch_attn_tc<448, 2>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream)
+                   : launch_attn_tc<448, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
   else
     e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream)
                    : launch_attn_tc<320, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
