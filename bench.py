@@ -83,6 +83,26 @@ class Clocks:
 
 
 # ---------------------------------------------------------------------------
+# replicas: every rank runs its own batch; the job's time is the slowest rank's
+# ---------------------------------------------------------------------------
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The maximum of ``x`` over all ranks (x itself when there is one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(steps: int, ms_max: float, world: int) -> float:
+    """Steps per second of the whole job: all ranks' steps over the slowest
+    rank's time (weak scaling: every rank has a full batch)."""
+    return world * steps / (ms_max / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_step_estimate(wl, ctx_all, commit_rows, n_attn=2, n_verify=2, n_rows=4, seed=0):
@@ -272,15 +292,11 @@ def run_ours(args, wl):
     barrier()
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    ms_max = ms_total
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = max_over_ranks(ms_total, world, dev)
     commit_sum = float(st.out["commit_len"].sum().item())   # committed rows per step (every step alike)
     per_kernel = {k: (sum(a.elapsed_time(b) for a, b in v) / len(v)) * 1e3 for k, v in ev.items() if v}
     ms_per_step = ms_max / args.steps
-    value = world * args.steps / (ms_max / 1e3)
+    value = replica_throughput(args.steps, ms_max, world)
     tokens_per_s = value * commit_sum
 
     # ---------------- roofline of the dominant kernel (block attention) ----------------
@@ -346,12 +362,8 @@ def run_ours(args, wl):
     e2e_run(args.steps, start=e0)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = replica_throughput(args.steps, e2e_ms, world)
 
     # ---------------- CPU baseline: the oracle on a bounded sample ----------------
     cpu = None
