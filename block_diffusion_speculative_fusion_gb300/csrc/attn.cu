@@ -71,9 +71,9 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 // P_t (bf16) to shared memory, and the MMA thread accumulates O += P_t V_t
 // (M = 128, N = 128, V read MN-major) into the item's TMEM O buffer. The
 // running max is only raised (O rescaled in TMEM) when a tile's max exceeds it
-// by more than 2^8, so rescaling is rare. Q and O are double-buffered per item
-// so that one item's output overlaps the next item's MMAs; the K/V ring runs
-// across item boundaries.
+// by more than 2^8, so rescaling is rare. The K/V ring runs across item
+// boundaries; one item's epilogue overlaps the next item's MMAs where the O
+// buffers allow it.
 // ===========================================================================
 namespace attn_tc {
 constexpr int kTileK = 64;
@@ -197,14 +197,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const bool is_softmax = warp < 8 && quarter < W && warp != prod_warp && warp != mma_warp;
   const bool is_epi = warp >= 8 && warp < 12 && quarter < W;
 
-  // shared memory: [Q0][Q1: 2 atoms x Ms rows each][S stages: K | V][barriers, tables]
-  // A 128-row MMA reads past the Ms stored rows into the next buffer; those
+  // shared memory: [Q: 2 atoms x Ms rows][S stages: K | V][barriers, tables]; one Q buffer is
+  // reused by consecutive items (the next item's Q loads once the last S of the
+  // current item has read it), which leaves room for one more K/V stage
+  // A 128-row MMA reads past the Ms stored rows into the next atom; those
   // padding rows only produce padding rows of S, P and O, which are never used.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int atom = Ms * 128;                 // one 64-wide column block of Ms rows
-  uint8_t* q_s = smem;                       // Q buffer i at + 2 i atom: d 0-63, then d 64-127
-  uint8_t* kv_s = smem + 4 * atom;           // stage s: K at s*2*T, V at s*2*T + T
+  uint8_t* q_s = smem;                       // Q: d 0-63, then d 64-127
+  uint8_t* kv_s = smem + 2 * atom;           // stage s: K at s*2*T, V at s*2*T + T
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + S * 2 * kTileBytes);
   uint64_t* kv_full = bars;          // [5]
   uint64_t* kv_empty = bars + 5;     // [5]
@@ -337,10 +339,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     };
     // Q of item `item` into Q buffer `slot` (lane 0); false on abort
     auto load_q = [&](int item, int seq) -> bool {
-      const int slot = seq & 1;
+      const int slot = 0;
       bool w = true;
       if (lane == 0) {
-        w = wait_or_abort(&q_empty[slot], (uint32_t)(((seq >> 1) & 1) ^ 1), abort_flag, p.err, 22);
+        w = wait_or_abort(&q_empty[slot], (uint32_t)((seq & 1) ^ 1), abort_flag, p.err, 22);
         if (w) {
           AttnItem it;
           decode_item(p, cum, order, cap, item, it);
@@ -417,12 +419,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         if (ok && j == j_claim) {
           if (lane == 0) nxt = atomicAdd(&sched[0], 1);
           nxt = __shfl_sync(0xffffffffu, nxt, 0);
-          if (nxt < n_items) {
-            load_pages(nxt, slot ^ 1);
-            ok = load_q(nxt, item_seq + 1);
-          }
+          if (nxt < n_items) load_pages(nxt, slot ^ 1);
         }
       }
+      // one Q buffer: the next item's Q once this item's last S no longer reads it
+      if (ok && nxt < n_items) ok = load_q(nxt, item_seq + 1);
       cur = nxt;
       ++item_seq;
     }
@@ -455,10 +456,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         // O: one buffer per item slot (ALT = 1), or both buffers for every item (ALT = 2)
         const int oi = ALT == 2 ? 0 : slot;
         const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
-        if (!wait_or_abort(&q_full[slot], par, abort_flag, p.err, 25)) break;
+        if (!wait_or_abort(&q_full[0], (uint32_t)(item_seq & 1), abort_flag, p.err, 25)) break;
         if (!wait_or_abort(&o_empty[oi], opar ^ 1u, abort_flag, p.err, 26)) break;
         tc_fence_after();
-        const uint32_t qa = smem_u32(q_s + slot * 2 * atom);
+        const uint32_t qa = smem_u32(q_s);
         auto issue_pv = [&](int t, int j) -> bool {
           if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
           tc_fence_after();
@@ -493,7 +494,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                         id_s, i > 0 ? 1u : 0u);
           }
           tc_commit(&s_full[t & 1]);
-          if (j == it.n_tiles - 1) tc_commit(&q_empty[slot]);   // Q is no longer read
+          if (j == it.n_tiles - 1) tc_commit(&q_empty[0]);   // Q is no longer read
           if (j >= 1) ok = issue_pv(t - 1, j - 1);
         }
         if (!ok) break;
@@ -1031,8 +1032,8 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
       return cudaErrorNotSupported;   // tensor-map encoding refused a layout
   }
   const int Ms = M <= 64 ? 64 : 128;     // stored query rows per operand atom
-  // K/V stages that fit beside the two Q buffers (at most the barrier count)
-  const size_t fixed = 1024 + 4 * (size_t)Ms * 128 + attn_tc::kBarBytes;
+  // K/V stages that fit beside the Q buffer (at most the barrier count)
+  const size_t fixed = 1024 + 2 * (size_t)Ms * 128 + attn_tc::kBarBytes;
   const int S = (int)std::min<size_t>(attn_tc::kMaxStages, (232448 - fixed) / (2 * attn_tc::kTileBytes));
   const size_t smem = fixed + (size_t)S * 2 * attn_tc::kTileBytes;
   // warps 0-9 (two softmax quarters, producer, MMA, epilogue 8-9) or 0-13
