@@ -4,20 +4,25 @@
 // contiguous), bf16 in, fp32 out.
 //
 // Weights are the A operand (M = 128 output features per tile) and the rows
-// are the B operand (N = up to 256 rows per tile), so a decode-sized T reads
-// each weight byte once while the MMA's N shrinks to the rows present.
+// are the B operand. A tile covers up to 512 rows (a pass) as two MMA groups
+// of up to 256 rows that share each k-block's weight tile, so a decode-sized
+// T (up to 512 committed rows) reads each weight byte from HBM once. The rows
+// of a pass are loaded with 256-, 64- and 16-row boxes, so a short second
+// group costs only the rows it has; the ring of stages is laid out at run time
+// for the number of rows present.
 //
 // Persistent CTAs (one per SM) split the (tile, 64-wide k-block) space into
 // equal contiguous ranges (stream-K style); a range that covers part of a tile
 // writes that tile's partial sum to its own segment slot, and the consumers sum
 // a tile's segments in a fixed order, so results are deterministic.
 //
-// Per CTA: warp 0 = TMA producer (4-stage ring of 128B-swizzled tiles), warp 1
-// = TMEM allocator and single-thread MMA issuer, warps 2-5 = epilogue (TMEM ->
-// registers -> global). Two 256-column TMEM accumulators let the epilogue of
-// one range piece overlap the MMAs of the next. Every mbarrier wait is bounded:
-// a wait that gives up records an error code, the CTA drains its own copies and
-// MMAs (again bounded), frees TMEM and returns.
+// Per CTA: warp 0 = TMA producer, warp 1 = TMEM allocator and single-thread
+// MMA issuer, warps 2-5 = epilogue (TMEM -> registers -> global). With one
+// group per pass, two 256-column TMEM accumulators let the epilogue of one
+// range piece overlap the MMAs of the next; with two groups they are the two
+// groups' accumulators. Every mbarrier wait is bounded: a wait that gives up
+// records an error code, the CTA drains its own copies and MMAs (again
+// bounded), frees TMEM and returns.
 #include <algorithm>
 
 #include "common.cuh"
@@ -29,17 +34,18 @@ namespace dflash {
 
 namespace tc {
 using namespace tcplan;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int B_BYTES = BN * BK * 2;    // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB: one k-block of 128 weight rows
+constexpr int MAX_STAGES = 4;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;          // two 256-column fp32 accumulators
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int SMEM_BYTES = 232448;      // all of it: the ring is sized at run time
+constexpr int RING_BYTES = SMEM_BYTES - 1024 - 256;
 }  // namespace tc
 
 struct TcWork {
-  int T, per, G, total, MT, KB;
+  int T, per, P, total, MT, KB;
+  int rows_max;       // rows of the largest pass, rounded up to 16
+  int stage_bytes, stages, nbuf;
 };
 
 __device__ __forceinline__ TcWork tc_work(const int32_t* meta, int per_idx, int MT, int KB, int T_max) {
@@ -48,21 +54,41 @@ __device__ __forceinline__ TcWork tc_work(const int32_t* meta, int per_idx, int 
   w.per = meta[per_idx];
   w.MT = MT;
   w.KB = KB;
-  w.G = (w.T + tc::BN - 1) / tc::BN;
-  w.total = MT * w.G * KB;
+  w.P = (w.T + tc::BP - 1) / tc::BP;
+  w.total = MT * w.P * KB;
+  w.rows_max = min(tc::BP, (w.T + 15) / 16 * 16);
+  w.stage_bytes = (tc::A_BYTES + w.rows_max * tc::BK * 2 + 1023) / 1024 * 1024;
+  w.stages = min(tc::MAX_STAGES, tc::RING_BYTES / w.stage_bytes);
+  w.nbuf = w.rows_max <= tc::BN ? 2 : 1;
   return w;
 }
 
+struct TcPiece {
+  int tile, kb0, kb1, m_tile, r0, rows, ng;
+};
+__device__ __forceinline__ TcPiece tc_piece(const TcWork& w, int pos, int hi) {
+  TcPiece c;
+  c.tile = pos / w.KB;
+  c.kb0 = pos - c.tile * w.KB;
+  c.kb1 = min(w.KB, c.kb0 + (hi - pos));
+  c.m_tile = c.tile % w.MT;
+  c.r0 = (c.tile / w.MT) * tc::BP;
+  c.rows = min(tc::BP, w.T - c.r0);
+  c.ng = (c.rows + tc::BN - 1) / tc::BN;
+  return c;
+}
+
 __global__ void __launch_bounds__(tc::THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap_l,
+               const __grid_constant__ CUtensorMap xmap_m, const __grid_constant__ CUtensorMap xmap_s,
                float* __restrict__ part, const int32_t* __restrict__ meta, int per_idx, int T_max, int N, int MT,
-               int KB, int b_rows, int* err) {
+               int KB, int box_l, int box_m, int* err) {
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;       // [2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* tfull = empty + MAX_STAGES;   // [2]
   uint64_t* tempty = tfull + 2;           // [2]
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -73,11 +99,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
   const int lo = blockIdx.x * w.per;
   const int hi = min(w.total, lo + w.per);
   if (w.per <= 0 || lo >= hi) return;
+  const int S = w.stages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int producer_issued = 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -104,19 +131,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
       int issued = 0;
       bool ok = true;
       for (int pos = lo; pos < hi && ok;) {
-        const int tile = pos / w.KB, kb0 = pos - tile * w.KB;
-        const int kb1 = min(w.KB, kb0 + (hi - pos));
-        const int m_tile = tile % w.MT, group = tile / w.MT;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const TcPiece c = tc_piece(w, pos, hi);
+        const int rows16 = (c.rows + 15) / 16 * 16;
+        for (int kb = c.kb0; kb < c.kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, abort_flag, err, 2)) { ok = false; break; }
-          uint8_t* sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(A_BYTES + b_rows * BK * 2));
-          tma_load_2d(sa, &wmap, &full[stage], kb * BK, m_tile * BM);
-          tma_load_2d(sa + A_BYTES, &xmap, &full[stage], kb * BK, group * BN);
+          uint8_t* sa = smem + stage * w.stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(A_BYTES + rows16 * BK * 2));
+          tma_load_2d(sa, &wmap, &full[stage], kb * BK, c.m_tile * BM);
+          // the pass's rows in the largest boxes that fit (all multiples of 16)
+          for (int r = 0; r < rows16;) {
+            const int left = rows16 - r;
+            const CUtensorMap* map = left >= box_l ? &xmap_l : (left >= box_m ? &xmap_m : &xmap_s);
+            const int n = left >= box_l ? box_l : (left >= box_m ? box_m : 16);
+            tma_load_2d(sa + A_BYTES + r * BK * 2, map, &full[stage], kb * BK, c.r0 + r);
+            r += n;
+          }
           ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
-        pos += kb1 - kb0;
+        pos += c.kb1 - c.kb0;
       }
       producer_issued = issued;
     }
@@ -126,38 +159,41 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      int buf = 0;
+      uint32_t buf_phase = 0;
       int consumed = 0;
       bool ok = true;
       for (int pos = lo; pos < hi && ok;) {
-        const int tile = pos / w.KB, kb0 = pos - tile * w.KB;
-        const int kb1 = min(w.KB, kb0 + (hi - pos));
-        const int group = tile / w.MT;
-        const int rows = min(BN, w.T - group * BN);
-        const int n_mma = (rows + 15) / 16 * 16;
-        const uint32_t idesc = idesc_bf16(BM, n_mma);
-        if (!wait_or_abort(&tempty[acc], acc_phase ^ 1u, abort_flag, err, 4)) break;
+        const TcPiece c = tc_piece(w, pos, hi);
+        if (!wait_or_abort(&tempty[buf], buf_phase ^ 1u, abort_flag, err, 4)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = c.kb0; kb < c.kb1; ++kb) {
           if (!wait_or_abort(&full[stage], phase, abort_flag, err, 5)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sa = smem_u32(smem + stage * w.stage_bytes);
           const uint64_t adesc = sdesc_sw128(sa);
-          const uint64_t bdesc = sdesc_sw128(sa + A_BYTES);
+          for (int g = 0; g < c.ng; ++g) {
+            const int rows_g = min(BN, c.rows - g * BN);
+            const uint32_t idesc = idesc_bf16(BM, (rows_g + 15) / 16 * 16);
+            const uint64_t bdesc = sdesc_sw128(sa + A_BYTES + g * BN * BK * 2);
+            const uint32_t d_tmem = tmem_base + (uint32_t)((buf + g) * BN);
 #pragma unroll
-          for (int j = 0; j < BK / 16; ++j)   // 16 bf16 = 32 bytes of K per instruction
-            tc_mma_bf16(d_tmem, adesc + (uint64_t)(j * 2), bdesc + (uint64_t)(j * 2), idesc,
-                        (kb > kb0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < BK / 16; ++j)   // 16 bf16 = 32 bytes of K per instruction
+              tc_mma_bf16(d_tmem, adesc + (uint64_t)(j * 2), bdesc + (uint64_t)(j * 2), idesc,
+                          (kb > c.kb0 || j > 0) ? 1u : 0u);
+          }
           tc_commit(&empty[stage]);       // stage is free once these MMAs have read it
           ++consumed;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&tfull[acc]);           // accumulator ready for the epilogue
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-        pos += kb1 - kb0;
+        tc_commit(&tfull[buf]);           // accumulators ready for the epilogue
+        if (w.nbuf == 2) {
+          if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
+        } else {
+          buf_phase ^= 1u;
+        }
+        pos += c.kb1 - c.kb0;
       }
       *consumed_sm = consumed;
       // every MMA issued by this thread has completed before TMEM is released
@@ -168,32 +204,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
   } else {
     // ------------------------------ epilogue (warps 2..5) ------------------------------
     const int quarter = warp & 3;         // TMEM lanes [32 q, 32 q + 32) belong to warp q mod 4
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    int buf = 0;
+    uint32_t buf_phase = 0;
     for (int pos = lo; pos < hi;) {
-      const int tile = pos / w.KB, kb0 = pos - tile * w.KB;
-      const int kb1 = min(w.KB, kb0 + (hi - pos));
-      const int m_tile = tile % w.MT, group = tile / w.MT;
-      const int seg = blockIdx.x - (tile * w.KB) / w.per;
-      const int rows = min(BN, w.T - group * BN);
-      if (!wait_or_abort(&tfull[acc], acc_phase, abort_flag, err, 7)) break;
+      const TcPiece c = tc_piece(w, pos, hi);
+      const int seg = blockIdx.x - (c.tile * w.KB) / w.per;
+      if (!wait_or_abort(&tfull[buf], buf_phase, abort_flag, err, 7)) break;
       tc_fence_after();
-      const int f = m_tile * BM + quarter * 32 + lane;
-      float* dst = part + ((size_t)seg * T_max + (size_t)group * BN) * N + f;
-      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      for (int c0 = 0; c0 < rows; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tbase + (uint32_t)c0, r);
-        tmem_ld_wait();
+      const int f = c.m_tile * BM + quarter * 32 + lane;
+      for (int g = 0; g < c.ng; ++g) {
+        const int rows_g = min(BN, c.rows - g * BN);
+        float* dst = part + ((size_t)seg * T_max + (size_t)(c.r0 + g * BN)) * N + f;
+        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf + g) * BN);
+        for (int c0 = 0; c0 < rows_g; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tbase + (uint32_t)c0, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          if (c0 + c < rows) dst[(size_t)(c0 + c) * N] = __uint_as_float(r[c]);
+          for (int q = 0; q < 16; ++q)
+            if (c0 + q < rows_g) dst[(size_t)(c0 + q) * N] = __uint_as_float(r[q]);
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-      pos += kb1 - kb0;
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (w.nbuf == 2) {
+        if (++buf == 2) { buf = 0; buf_phase ^= 1u; }
+      } else {
+        buf_phase ^= 1u;
+      }
+      pos += c.kb1 - c.kb0;
     }
   }
   tc_fence_before();
@@ -202,7 +242,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
   // wait for them (bounded) so that none lands after this CTA has exited.
   if (warp == 0 && lane == 0 && *abort_flag)
     for (int i = *consumed_sm; i < producer_issued; ++i)
-      mbar_wait_bounded(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), err, 3);
+      mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), err, 3);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -226,7 +266,7 @@ int gemm_tc_splits(int /*T_max*/, int N, int /*K*/) {
 cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int32_t* meta, int T_max, int N, int K,
                            int per_idx, int* err, cudaStream_t st) {
   using namespace tc;
-  CUtensorMap wmap, xmap;
+  CUtensorMap wmap, xmap_l, xmap_m, xmap_s;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
     const uint64_t strides[1] = {(uint64_t)K * 2};
@@ -235,13 +275,18 @@ cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int3
                            CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorNotSupported;
   }
-  // rows per B box: a full tile, or all of a small T_max (16-row granularity)
-  const int b_rows = std::min(BN, (T_max + 15) / 16 * 16);
+  // row boxes of 256 (or all of a small T_max), 64 and 16 rows
+  const int t16 = (T_max + 15) / 16 * 16;
+  const int box_l = std::min(BN, t16), box_m = std::min(64, t16);
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)T_max};
     const uint64_t strides[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {BK, (uint32_t)b_rows};
-    if (!encode_tensor_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box,
+    const uint32_t bl[2] = {BK, (uint32_t)box_l}, bm[2] = {BK, (uint32_t)box_m}, bs[2] = {BK, 16};
+    if (!encode_tensor_map(&xmap_l, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, bl,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&xmap_m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, bm,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&xmap_s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, bs,
                            CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorNotSupported;
   }
@@ -251,8 +296,8 @@ cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int3
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  gemm_tc_kernel<<<GRID, THREADS, SMEM_BYTES, st>>>(wmap, xmap, part, meta, per_idx, T_max, N, N / BM, K / BK,
-                                                    b_rows, err);
+  gemm_tc_kernel<<<GRID, THREADS, SMEM_BYTES, st>>>(wmap, xmap_l, xmap_m, xmap_s, part, meta, per_idx, T_max, N,
+                                                    N / BM, K / BK, box_l, box_m, err);
   return cudaGetLastError();
 }
 

@@ -122,16 +122,17 @@ cudaError_t launch_materialize(const MatArgs& a, int* launches);
 // tcgen05 GEMM: part[seg][t][n] = sum over one K segment of X[t][k] W[n][k], bf16 in, fp32 out.
 namespace tcplan {
 constexpr int BM = 128;      // output features per tile (MMA M)
-constexpr int BN = 256;      // rows per tile (MMA N upper bound)
+constexpr int BN = 256;      // rows per MMA group (MMA N upper bound)
+constexpr int BP = 512;      // rows per tile: two MMA groups share each weight k-block
 constexpr int BK = 64;       // K per k-block: one 128-byte swizzle atom of bf16
 constexpr int GRID = 152;    // persistent CTAs: one per SM of a GB300
 constexpr int MIN_PER = 8;   // smallest k-block range per CTA
 }  // namespace tcplan
 
-// k-block range per CTA when T rows are valid (tiles = N/BM x ceil(T/BN)).
+// k-block range per CTA when T rows are valid (tiles = N/BM x ceil(T/BP)).
 inline __host__ __device__ int gemm_tc_per(int T, int N, int K) {
   const int MT = N / tcplan::BM, KB = K / tcplan::BK;
-  const int G = (T + tcplan::BN - 1) / tcplan::BN;
+  const int G = (T + tcplan::BP - 1) / tcplan::BP;
   const long total = (long)MT * G * KB;
   long per = (total + tcplan::GRID - 1) / tcplan::GRID;
   if (per < tcplan::MIN_PER) per = tcplan::MIN_PER;
@@ -145,7 +146,7 @@ inline __host__ __device__ int gemm_tc_tile_segs(int tile, int KB, int per) {
 // the output element (t, n).
 inline __host__ __device__ int part_segs(int t, int n, int N, int K, int per, int S) {
   if (per <= 0) return S;
-  const int tile = (t / tcplan::BN) * (N / tcplan::BM) + n / tcplan::BM;
+  const int tile = (t / tcplan::BP) * (N / tcplan::BM) + n / tcplan::BM;
   return gemm_tc_tile_segs(tile, K / tcplan::BK, per);
 }
 
