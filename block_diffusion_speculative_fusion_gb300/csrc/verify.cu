@@ -16,6 +16,7 @@
 namespace dflash {
 
 constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 4;    // resident CTAs per SM the streaming kernels are planned for
 constexpr int kMaxRows = 256;    // n_max + 1 limit (drafts per verify <= 255)
 constexpr int kMaxDrawChunks = 1024;   // vocabulary <= 1024 x 16384
 
@@ -121,7 +122,7 @@ __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2)
 // Greedy rule
 // ===========================================================================
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 greedy_kernel(const T* __restrict__ logits, const int64_t* __restrict__ cand,
               const int32_t* __restrict__ n_draft, int R, int V, int nch, int chunk,
               VI* __restrict__ parts, int32_t* __restrict__ counters,
@@ -218,8 +219,8 @@ __device__ __forceinline__ void pair_weights(const uint4& vt, const uint4& vd, c
   const float inv_st = 1.f / j.st, inv_sd = 1.f / j.sd;
 #pragma unroll
   for (int q = 0; q < N; ++q) {
-    pv[q] = exp2f(fmaf(ft[q], k2, -j.mt)) * inv_st;
-    w[q] = use_p ? pv[q] : fmaxf(0.f, pv[q] - exp2f(fmaf(fd[q], k2, -j.md)) * inv_sd);
+    pv[q] = ex2_ftz(fmaf(ft[q], k2, -j.mt)) * inv_st;
+    w[q] = use_p ? pv[q] : fmaxf(0.f, pv[q] - ex2_ftz(fmaf(fd[q], k2, -j.md)) * inv_sd);
   }
 }
 
@@ -368,11 +369,12 @@ sample_draw_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const flo
       const int e = es + 2 * l + q;
       float wt = 0.f;
       if (e < V) {
-        const float pt = exp2f(fmaf(to_f32(zt_row[e]), k2, -j.mt)) / j.st;
+        // the same arithmetic as the segment sums of pass 1
+        const float pt = ex2_ftz(fmaf(to_f32(zt_row[e]), k2, -j.mt)) * (1.f / j.st);
         if (usep_r || degenerate) {
           wt = pt;
         } else {
-          const float qd = exp2f(fmaf(to_f32(zd_row[e]), k2, -j.md)) / j.sd;
+          const float qd = ex2_ftz(fmaf(to_f32(zd_row[e]), k2, -j.md)) * (1.f / j.sd);
           wt = fmaxf(0.f, pt - qd);
         }
       }
@@ -439,7 +441,7 @@ sample_draw_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const flo
 // ===========================================================================
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
                     const int64_t* __restrict__ cand, const int32_t* __restrict__ n_draft,
                     const float* __restrict__ u_acc, int n_max, int V, int nch, int chunk,
@@ -552,7 +554,7 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
 // DLoop gate
 // ===========================================================================
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
             const uint8_t* __restrict__ active, int k, int V, int nch, int chunk, float k2,
             float inv_t, float g, MS* __restrict__ parts, float* __restrict__ zx,
@@ -617,12 +619,12 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
 static int vec_elems(int dtype) { return dtype == 0 ? 4 : 8; }
 
 // Chunks per row: the grid (rows x chunks) is sized to one wave of resident
-// CTAs (8 per SM) so that no partial wave trails the kernel; each thread
+// CTAs (kCtasPerSm per SM) so that no partial wave trails the kernel; each thread
 // handles at least one 16-byte vector per chunk.
 ChunkPlan plan_chunks(int rows, int V, int dtype, int num_sms) {
   const int per_thread_vec = kThreads * vec_elems(dtype);
   const int units = (V + per_thread_vec - 1) / per_thread_vec;   // vector rounds for a whole row
-  const long wave = 8L * num_sms;
+  const long wave = (long)kCtasPerSm * num_sms;
   long nch = wave / (rows > 0 ? rows : 1);
   if (nch < 1) nch = 1;
   if (nch > units) nch = units;
