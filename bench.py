@@ -445,6 +445,122 @@ def run_kernel(args, wl):
     print(json.dumps(out), flush=True)
 
 
+def _time_calls(fn, steps, warmup):
+    """Mean device time of ``fn()`` in microseconds (CUDA events on the current stream)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / steps
+
+
+def report_config(wl, args):
+    """Per-kernel times and roofline fractions of one workload (one JSON line)."""
+    import dataclasses as dc
+    import torch
+    from block_diffusion_speculative_fusion_gb300 import api, synth
+    from block_diffusion_speculative_fusion_gb300.step import DflashStep
+    hbm, tf, _, _ = _peaks()
+    dev = "cuda:0"
+    el = 2 if wl.dtype == "bf16" else 4
+    out = {"config": wl.name, "B": wl.B, "k": wl.k, "V": wl.V}
+    gbs = lambda nbytes, us: nbytes / us / 1e3
+    if wl.stages == 1:
+        # ---- one serving step through the step harness (stationary contexts) ----
+        st = DflashStep(wl, seed=0, device=dev, headroom_steps=2, stationary=True)
+        us_step = _time_calls(st.step, args.steps, args.warmup)
+        rows = float(st.out["commit_len"].sum().item())
+        out.update({"steps_per_s": 1e6 / us_step, "us_per_step": us_step, "verified_tokens_per_s": rows * 1e6 / us_step,
+                    "committed_rows_per_step": rows})
+        inp = st.inp
+        us_attn = _time_calls(lambda: api.block_attn(inp["q0"], inp["k_blk0"], inp["v_blk0"], st.k_pools[0],
+                                                     st.v_pools[0], st.page_table, st.ctx_start, max_ctx=st.max_ctx,
+                                                     out=st.attn_out[0]), args.steps, args.warmup)
+        ab = attn_bytes(float(st.ctx0.sum()), wl)
+        out["attn_us_per_layer"] = us_attn
+        out["attn_frac_hbm"] = gbs(ab, us_attn) / hbm
+        ng = wl.n_greedy
+        R = wl.n_draft + 1
+        if ng > 0:
+            us_g = _time_calls(lambda: api.verify_greedy(inp["target_logits"][:ng], inp["cand"][:ng],
+                                                         inp["n_draft"][:ng], out=st.out_g), args.steps, args.warmup)
+            out["verify_greedy_us"] = us_g
+            out["verify_greedy_frac_hbm"] = gbs(ng * R * wl.V * el, us_g) / hbm
+        if ng < wl.B:
+            ns = wl.B - ng
+            us_s = _time_calls(lambda: api.verify_sample(
+                inp["target_logits"][ng:], inp["draft_logits"][ng:], inp["cand"][ng:], inp["u_acc"][ng:],
+                inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:], out=st.out_s), args.steps, args.warmup)
+            out["verify_sample_us"] = us_s
+            out["verify_sample_frac_hbm"] = gbs(ns * (2 * R - 1 + 2) * wl.V * el, us_s) / hbm
+        del st
+    else:
+        # ---- DLoop: S stages of (attention in L layers + gate), then one sampled verify ----
+        n_q = wl.k
+        ctx = synth.ctx_lengths(wl, 0)
+        cache = synth.paged_cache(wl, headroom=wl.stages + n_q, seed=0, layers=1, ctx_len=ctx, device=dev)
+        pt, cl = cache.page_table.to(dev), cache.ctx_len.to(dev)
+        total_us = 0.0
+        for s in range(1, wl.stages + 1):
+            blk = {k_: v_.to(dev) for k_, v_ in synth.block_qkv(wl, 0, seed=0, n_kv_blk=n_q + s - 1).items()}
+            o = torch.empty_like(blk["q"])
+            us_a = _time_calls(lambda: api.block_attn(blk["q"], blk["k_blk"], blk["v_blk"], cache.k_pools[0],
+                                                      cache.v_pools[0], pt, cl, out=o), args.steps, args.warmup)
+            gb = {k_: v_.to(dev) for k_, v_ in synth.gate_batch(wl, s - 1, seed=0).items()}
+            us_gate = _time_calls(lambda: api.gate(gb["draft_logits"], gb["tokens"], wl.temperature, wl.gate_g,
+                                                   active=gb["active"]), args.steps, args.warmup)
+            out[f"stage{s}_attn_us_per_layer"] = us_a
+            out[f"stage{s}_gate_us"] = us_gate
+            total_us += wl.L * us_a + us_gate
+            if s == 1:
+                out["attn_frac_hbm"] = gbs(attn_bytes(float(ctx.sum()), dc.replace(wl, k=n_q)), us_a) / hbm
+                out["gate_frac_hbm"] = gbs(wl.B * wl.n_draft * wl.V * el, us_gate) / hbm
+        vb = {k_: v_.to(dev) for k_, v_ in synth.verify_batch(wl, seed=0).items()}
+        us_v = _time_calls(lambda: api.verify_sample(vb["target_logits"], vb["draft_logits"], vb["cand"], vb["u_acc"],
+                                                     vb["u_final"], wl.temperature, vb["n_draft"]),
+                           args.steps, args.warmup)
+        n = wl.n_max
+        out["verify_sample_us"] = us_v
+        out["verify_sample_frac_hbm"] = gbs(wl.B * (2 * n + 1 + 2) * wl.V * el, us_v) / hbm
+        out["looped_step_us_all_stages"] = total_us + us_v
+    if wl.dtype == "bf16" and wl.stages == 1 and wl.ctx_lo == wl.ctx_hi:
+        # ---- prefill-sized materialisation: every context row of every sequence ----
+        rows = wl.ctx_lo
+        w = {k_: (v_.to(dev) if v_ is not None else None) for k_, v_ in synth.ctx_weights(wl, 0).items()}
+        hid = synth.captured_hidden(wl, rows, 0, B=wl.B).to(dev)
+        pc = synth.paged_cache(wl, headroom=0, seed=0, layers=wl.L, ctx_len=torch.full((wl.B,), rows, dtype=torch.int32),
+                               device=dev)
+        commit = torch.full((wl.B,), rows, dtype=torch.int32, device=dev)
+        start = torch.zeros(wl.B, dtype=torch.int32, device=dev)
+        pools_k = [t.to(dev) for t in pc.k_pools]
+        pools_v = [t.to(dev) for t in pc.v_pools]
+        ptab = pc.page_table.to(dev)
+        us_m = _time_calls(lambda: api.materialize_ctx_kv(hid, commit, start, w["W_f"], w["b_f"], w["W_kv"],
+                                                          w["k_norm_w"], wl.rms_eps, wl.rope_theta, pools_k, pools_v,
+                                                          ptab), max(3, args.steps // 4), 2)
+        T = wl.B * rows
+        flops = 2.0 * T * (wl.m * wl.d * wl.d + wl.d * wl.kv_out)
+        out["prefill_materialize_rows"] = T
+        out["prefill_materialize_us"] = us_m
+        out["prefill_materialize_tflops"] = flops / us_m / 1e6
+        out["prefill_materialize_frac_bf16_peak"] = flops / us_m / 1e6 / tf
+    print(json.dumps(out), flush=True)
+
+
+def run_all_configs(args):
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_diffusion_speculative_fusion_gb300 import workloads as W
+    for wl in W.ALL:
+        report_config(wl, args)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -455,11 +571,15 @@ def main():
     ap.add_argument("--kernel", choices=["attn", "verify", "materialize"], default=None,
                     help="time one call of the step in isolation (profiling aid)")
     ap.add_argument("--batch", type=int, default=None, help="override B (with --kernel)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="per-kernel times and roofline fractions of every workload, one JSON line each")
     args = ap.parse_args()
     from block_diffusion_speculative_fusion_gb300 import workloads as W
     wl = W.LLAMA8B_B64
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.all_configs:
+        run_all_configs(args)
     elif args.kernel:
         run_kernel(args, wl)
     else:
