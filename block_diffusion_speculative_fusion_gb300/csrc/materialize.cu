@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(256)
 mat_gather_kernel(const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, const int32_t* __restrict__ meta,
                   const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j, int rows_max,
                   size_t row_bytes, const int32_t* __restrict__ start_pos, const double* __restrict__ inv_freq,
-                  float2* __restrict__ rope, int half) {
+                  float2* __restrict__ rope, int half, const int32_t* __restrict__ page_table, int page_size,
+                  int max_pages, int num_pages, long long* __restrict__ slots) {
   // grid-stride over the committed rows only (their count is on the device)
   const long T = meta[0];
   const long nvec = (long)(row_bytes / 16);
@@ -86,6 +87,18 @@ mat_gather_kernel(const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, c
   for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * tail; idx += stride) {
     const long t = idx / tail, e = nvec * 16 + (idx - t * tail);
     X[(size_t)t * row_bytes + e] = hidden[((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes + e];
+  }
+  // the pool slot of every committed row (-1: position outside the page table)
+  for (long t = blockIdx.x * (long)blockDim.x + threadIdx.x; t < T; t += stride) {
+    const int b = row_b[t];
+    const int pos = start_pos[b] + row_j[t];
+    const int lp = pos / page_size;
+    long long sl = -1;
+    if (pos >= 0 && lp < max_pages) {
+      const int phys = page_table[(size_t)b * max_pages + lp];
+      if (phys >= 0 && phys < num_pages) sl = (long long)phys * page_size + pos % page_size;
+    }
+    slots[t] = sl;
   }
   // RoPE (cos, sin) of every committed row's position, pair i: the angle
   // pos * theta^(-2i/D) in double (it reaches ~1e4 radians), reduced to
@@ -187,6 +200,100 @@ mat_bias_kernel(const float* __restrict__ part, int splits, const T* __restrict_
 // absolute position (cos/sin table from the gather kernel); then the cast and
 // the paged write.
 // ---------------------------------------------------------------------------
+// D = 128 fast path: lane l owns elements 4l .. 4l + 3 of the vector (one float4
+// of each partial sum), the RoPE partner d + 64 of lane l < 16 sits in lane l + 16
+// and is fetched by a shuffle; stores are 8 bytes per lane.
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float4 v) {
+  *reinterpret_cast<float4*>(dst) = v;
+}
+template <>
+__device__ __forceinline__ void store4<bf16>(bf16* dst, float4 v) {
+  uint2 u;
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+template <typename T>
+__device__ __forceinline__ void epi128_finish(float4 x, int v, long long slot, int t, int Hkv, const T* k_norm_w,
+                                              float rms_eps, const float2* rope, const MatPools& pools, int lane) {
+  constexpr int D = 128, half = 64;
+  const int d0 = 4 * lane;
+  const int h = v % Hkv, kv = (v / Hkv) & 1, l = v / (2 * Hkv);
+  T* dst = (kv == 0 ? (T*)pools.k[l] : (T*)pools.v[l]) + ((size_t)slot * Hkv + h) * D + d0;
+  if (kv == 0) {
+    if (k_norm_w) {
+      float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float sc = 1.f / sqrtf(ss / D + rms_eps);
+      const T* wv = k_norm_w + (size_t)l * D + d0;
+      x.x *= sc * to_f32(wv[0]);
+      x.y *= sc * to_f32(wv[1]);
+      x.z *= sc * to_f32(wv[2]);
+      x.w *= sc * to_f32(wv[3]);
+    }
+    if (rope) {
+      float4 y;
+      y.x = __shfl_xor_sync(0xffffffffu, x.x, 16);
+      y.y = __shfl_xor_sync(0xffffffffu, x.y, 16);
+      y.z = __shfl_xor_sync(0xffffffffu, x.z, 16);
+      y.w = __shfl_xor_sync(0xffffffffu, x.w, 16);
+      const float2* c = rope + (size_t)t * half + (d0 & (half - 1));
+      const float2 c0 = c[0], c1 = c[1], c2 = c[2], c3 = c[3];
+      if (d0 < half)
+        x = make_float4(x.x * c0.x - y.x * c0.y, x.y * c1.x - y.y * c1.y, x.z * c2.x - y.z * c2.y,
+                        x.w * c3.x - y.w * c3.y);
+      else
+        x = make_float4(x.x * c0.x + y.x * c0.y, x.y * c1.x + y.y * c1.y, x.z * c2.x + y.z * c2.y,
+                        x.w * c3.x + y.w * c3.y);
+    }
+  }
+  if (slot >= 0) store4<T>(dst, x);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+mat_epilogue_d128_kernel(const float* __restrict__ part, int splits, const int32_t* __restrict__ meta,
+                         const long long* __restrict__ slots, const T* __restrict__ k_norm_w, float rms_eps,
+                         const float2* __restrict__ rope, MatPools pools, int T_max, int L, int Hkv, int K2) {
+  constexpr int D = 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int NV = L * 2 * Hkv;
+  const int N = NV * D;
+  const int per = meta[2];
+  const long tasks = (long)min(meta[0], T_max) * NV;
+  const long stride = (long)gridDim.x * nwarps;
+  auto load = [&](long task, int& t, int& v, long long& slot) -> float4 {
+    t = (int)(task / NV);
+    v = (int)(task - (long)t * NV);
+    slot = slots[t];
+    // a 128-wide vector lies in one 128-feature GEMM tile: one segment count
+    const int segs = part_segs(t, v * D, N, K2, per, splits);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sg = 0; sg < segs; ++sg) {
+      const float4 y = *reinterpret_cast<const float4*>(part + ((size_t)sg * T_max + t) * N + v * D + 4 * lane);
+      x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+    }
+    return x;
+  };
+  // two tasks in flight per warp: the second one's loads overlap the first one's math
+  for (long task = (long)blockIdx.x * nwarps + warp; task < tasks; task += 2 * stride) {
+    int t0, v0, t1 = 0, v1 = 0;
+    long long s0, s1 = -1;
+    const float4 x0 = load(task, t0, v0, s0);
+    const bool two = task + stride < tasks;
+    float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (two) x1 = load(task + stride, t1, v1, s1);
+    epi128_finish<T>(x0, v0, s0, t0, Hkv, k_norm_w, rms_eps, rope, pools, lane);
+    if (two) epi128_finish<T>(x1, v1, s1, t1, Hkv, k_norm_w, rms_eps, rope, pools, lane);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* __restrict__ meta,
@@ -278,6 +385,7 @@ size_t mat_ws_bytes(const MatPlan& p, int dtype) {
   size_t s = align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max));
   s += align_up(sizeof(double) * 128);             // RoPE frequencies (D <= 256)
   s += align_up(sizeof(float2) * (size_t)p.T_max * 128);   // RoPE (cos, sin) per committed row
+  s += align_up(sizeof(long long) * (size_t)p.T_max);       // pool slot per committed row
   s += align_up((size_t)p.T_max * p.K1 * el);     // gathered operand X
   s += align_up((size_t)p.T_max * p.N1 * el);     // h_ctx
   s += align_up((size_t)std::max(p.S1, p.S2) * p.T_max * Nmax * sizeof(float));
@@ -307,6 +415,8 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   ws += align_up(sizeof(double) * 128);
   float2* rope = a.rope_theta > 0.f ? (float2*)ws : nullptr;
   ws += align_up(sizeof(float2) * (size_t)p.T_max * 128);
+  long long* slots = (long long*)ws;
+  ws += align_up(sizeof(long long) * (size_t)p.T_max);
   T* X = (T*)ws;
   ws += align_up((size_t)p.T_max * p.K1 * el);
   T* h = (T*)ws;
@@ -321,7 +431,8 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   // grid-stride kernels over the committed rows: a few waves of the 152 SMs
   const int gs = 4 * 152;
   mat_gather_kernel<<<gs, 256, 0, st>>>((const uint8_t*)a.hidden, (uint8_t*)X, meta, row_b, row_j, a.rows_max,
-                                        row_bytes, a.start_pos, inv_freq, rope, a.D / 2);
+                                        row_bytes, a.start_pos, inv_freq, rope, a.D / 2, a.page_table, a.page_size,
+                                        a.max_pages, a.num_pages, slots);
   ++n;
   cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, 1, a.err, st);
   if (e != cudaSuccess) return e;
@@ -331,10 +442,15 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   e = run_gemm<T>(p, p.tc, h, a.W_kv, part, meta, p.N2, p.K2, p.S2, 2, a.err, st);
   if (e != cudaSuccess) return e;
   ++n;
-  const size_t esmem = sizeof(float) * 8 * (size_t)a.D;
-  mat_epilogue_kernel<T><<<gs, 256, esmem, st>>>(
-      part, p.S2, meta, row_b, row_j, a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, rope, a.pools,
-      p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages, p.K2);
+  if (a.D == 128) {
+    mat_epilogue_d128_kernel<T><<<gs, 256, 0, st>>>(part, p.S2, meta, slots, (const T*)a.k_norm_w, a.rms_eps,
+                                                   rope, a.pools, p.T_max, a.L, a.Hkv, p.K2);
+  } else {
+    const size_t esmem = sizeof(float) * 8 * (size_t)a.D;
+    mat_epilogue_kernel<T><<<gs, 256, esmem, st>>>(
+        part, p.S2, meta, row_b, row_j, a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, rope, a.pools,
+        p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages, p.K2);
+  }
   ++n;
   *launches = n;
   return cudaGetLastError();
