@@ -4,17 +4,21 @@
 // contiguous), bf16 in, fp32 out.
 //
 // Weights are the A operand (M = 128 output features per tile) and the rows
-// are the B operand. A tile covers up to 512 rows (a pass) as two MMA groups
-// of up to 256 rows that share each k-block's weight tile, so a decode-sized
-// T (up to 512 committed rows) reads each weight byte from HBM once. The rows
+// are the B operand. When all T rows fit 512, a tile covers them as two MMA
+// groups of up to 256 rows that share each k-block's weight tile, so a
+// decode-sized T reads each weight byte from HBM once; larger T uses tiles of
+// 256 rows, whose smaller stages make a deeper ring. The rows
 // of a pass are loaded with 256-, 64- and 16-row boxes, so a short second
 // group costs only the rows it has; the ring of stages is laid out at run time
 // for the number of rows present.
 //
-// Persistent CTAs (one per SM) split the (tile, 64-wide k-block) space into
-// equal contiguous ranges (stream-K style); a range that covers part of a tile
-// writes that tile's partial sum to its own segment slot, and the consumers sum
-// a tile's segments in a fixed order, so results are deterministic.
+// Persistent CTAs (one per SM): when there are at least GRID tiles, whole
+// waves of GRID tiles go one per CTA (concurrent tiles then share their rows
+// and weights in L2); the remaining tiles' (tile, 64-wide k-block) space is
+// split into equal contiguous ranges (stream-K style). A range that covers
+// part of a tile writes that tile's partial sum to its own segment slot, and
+// the consumers sum a tile's segments in a fixed order, so results are
+// deterministic.
 //
 // Per CTA: warp 0 = TMA producer, warp 1 = TMEM allocator and single-thread
 // MMA issuer, warps 2-5 = epilogue (TMEM -> registers -> global). With one
@@ -35,7 +39,7 @@ namespace dflash {
 namespace tc {
 using namespace tcplan;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB: one k-block of 128 weight rows
-constexpr int MAX_STAGES = 4;
+constexpr int MAX_STAGES = 12;   // barrier area: 8 * (2 * 12 + 5) + 12 bytes <= 256
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;          // two 256-column fp32 accumulators
 constexpr int SMEM_BYTES = 232448;      // all of it: the ring is sized at run time
@@ -43,7 +47,9 @@ constexpr int RING_BYTES = SMEM_BYTES - 1024 - 256;
 }  // namespace tc
 
 struct TcWork {
-  int T, per, P, total, MT, KB;
+  int T, per, PR, P, total, MT, KB;
+  int full, waves;    // tiles handed out whole (waves of GRID), and how many waves
+  int lo, hi;         // this CTA's k-block range over the split tiles
   int rows_max;       // rows of the largest pass, rounded up to 16
   int stage_bytes, stages, nbuf;
 };
@@ -54,9 +60,14 @@ __device__ __forceinline__ TcWork tc_work(const int32_t* meta, int per_idx, int 
   w.per = meta[per_idx];
   w.MT = MT;
   w.KB = KB;
-  w.P = (w.T + tc::BP - 1) / tc::BP;
+  w.PR = gemm_tc_pass_rows(w.T);
+  w.P = (w.T + w.PR - 1) / w.PR;
   w.total = MT * w.P * KB;
-  w.rows_max = min(tc::BP, (w.T + 15) / 16 * 16);
+  w.full = gemm_tc_full_tiles(w.T, MT * tc::BM);
+  w.waves = w.full / tc::GRID;
+  w.lo = w.full * KB + (int)blockIdx.x * w.per;
+  w.hi = min(w.total, w.lo + w.per);
+  w.rows_max = min(w.PR, (w.T + 15) / 16 * 16);
   w.stage_bytes = (tc::A_BYTES + w.rows_max * tc::BK * 2 + 1023) / 1024 * 1024;
   w.stages = min(tc::MAX_STAGES, tc::RING_BYTES / w.stage_bytes);
   w.nbuf = w.rows_max <= tc::BN ? 2 : 1;
@@ -64,18 +75,31 @@ __device__ __forceinline__ TcWork tc_work(const int32_t* meta, int per_idx, int 
 }
 
 struct TcPiece {
-  int tile, kb0, kb1, m_tile, r0, rows, ng;
+  int tile, kb0, kb1, m_tile, r0, rows, ng, seg;
 };
-__device__ __forceinline__ TcPiece tc_piece(const TcWork& w, int pos, int hi) {
-  TcPiece c;
-  c.tile = pos / w.KB;
-  c.kb0 = pos - c.tile * w.KB;
-  c.kb1 = min(w.KB, c.kb0 + (hi - pos));
+// The pieces of this CTA in order: its whole tiles (one per wave), then its
+// k-block range over the split tiles. `wave` and `pos` carry the position.
+__device__ __forceinline__ bool tc_next(const TcWork& w, int& wave, int& pos, TcPiece& c) {
+  if (wave < w.waves) {
+    c.tile = wave * tc::GRID + (int)blockIdx.x;
+    c.kb0 = 0;
+    c.kb1 = w.KB;
+    c.seg = 0;
+    ++wave;
+  } else if (pos < w.hi) {
+    c.tile = pos / w.KB;
+    c.kb0 = pos - c.tile * w.KB;
+    c.kb1 = min(w.KB, c.kb0 + (w.hi - pos));
+    c.seg = (int)blockIdx.x - ((c.tile - w.full) * w.KB) / w.per;
+    pos += c.kb1 - c.kb0;
+  } else {
+    return false;
+  }
   c.m_tile = c.tile % w.MT;
-  c.r0 = (c.tile / w.MT) * tc::BP;
-  c.rows = min(tc::BP, w.T - c.r0);
+  c.r0 = (c.tile / w.MT) * w.PR;
+  c.rows = min(w.PR, w.T - c.r0);
   c.ng = (c.rows + tc::BN - 1) / tc::BN;
-  return c;
+  return true;
 }
 
 __global__ void __launch_bounds__(tc::THREADS, 1)
@@ -96,9 +120,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
   int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
 
   const TcWork w = tc_work(meta, per_idx, MT, KB, T_max);
-  const int lo = blockIdx.x * w.per;
-  const int hi = min(w.total, lo + w.per);
-  if (w.per <= 0 || lo >= hi) return;
+  if (w.per <= 0 || (w.waves == 0 && w.lo >= w.hi)) return;
   const int S = w.stages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -130,8 +152,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int pos = lo; pos < hi && ok;) {
-        const TcPiece c = tc_piece(w, pos, hi);
+      int wave = 0, pos = w.lo;
+      TcPiece c;
+      while (ok && tc_next(w, wave, pos, c)) {
         const int rows16 = (c.rows + 15) / 16 * 16;
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, abort_flag, err, 2)) { ok = false; break; }
@@ -149,7 +172,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
           ++issued;
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
-        pos += c.kb1 - c.kb0;
       }
       producer_issued = issued;
     }
@@ -163,8 +185,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
       uint32_t buf_phase = 0;
       int consumed = 0;
       bool ok = true;
-      for (int pos = lo; pos < hi && ok;) {
-        const TcPiece c = tc_piece(w, pos, hi);
+      int wave = 0, pos = w.lo;
+      TcPiece c;
+      while (ok && tc_next(w, wave, pos, c)) {
         if (!wait_or_abort(&tempty[buf], buf_phase ^ 1u, abort_flag, err, 4)) break;
         tc_fence_after();
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
@@ -193,7 +216,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
         } else {
           buf_phase ^= 1u;
         }
-        pos += c.kb1 - c.kb0;
       }
       *consumed_sm = consumed;
       // every MMA issued by this thread has completed before TMEM is released
@@ -206,9 +228,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
     const int quarter = warp & 3;         // TMEM lanes [32 q, 32 q + 32) belong to warp q mod 4
     int buf = 0;
     uint32_t buf_phase = 0;
-    for (int pos = lo; pos < hi;) {
-      const TcPiece c = tc_piece(w, pos, hi);
-      const int seg = blockIdx.x - (c.tile * w.KB) / w.per;
+    int wave = 0, pos = w.lo;
+    TcPiece c;
+    while (tc_next(w, wave, pos, c)) {
+      const int seg = c.seg;
       if (!wait_or_abort(&tfull[buf], buf_phase, abort_flag, err, 7)) break;
       tc_fence_after();
       const int f = c.m_tile * BM + quarter * 32 + lane;
@@ -233,7 +256,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
       } else {
         buf_phase ^= 1u;
       }
-      pos += c.kb1 - c.kb0;
     }
   }
   tc_fence_before();
@@ -258,10 +280,7 @@ bool gemm_tc_supported(int K, int N) { return K % tc::BK == 0 && N % tc::BM == 0
 // Upper bound of the segment count of any tile: a CTA range covers at least
 // ceil(MT * KB / GRID) k-blocks, so a tile of KB k-blocks meets at most
 // ceil(GRID / MT) + 1 ranges.
-int gemm_tc_splits(int /*T_max*/, int N, int /*K*/) {
-  const int MT = N / tc::BM;
-  return (tc::GRID + MT - 1) / MT + 1;
-}
+int gemm_tc_splits(int /*T_max*/, int N, int /*K*/) { return gemm_tc_slots(N); }
 
 cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int32_t* meta, int T_max, int N, int K,
                            int per_idx, int* err, cudaStream_t st) {

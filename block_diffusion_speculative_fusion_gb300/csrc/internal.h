@@ -111,7 +111,7 @@ struct MatArgs {
 };
 
 struct MatPlan {
-  int T_max, K1, N1, K2, N2, S1, S2;
+  int B, T_max, K1, N1, K2, N2, S1, S2;
   bool tc;   // GEMMs on tcgen05 tensor cores
 };
 
@@ -123,31 +123,71 @@ cudaError_t launch_materialize(const MatArgs& a, int* launches);
 namespace tcplan {
 constexpr int BM = 128;      // output features per tile (MMA M)
 constexpr int BN = 256;      // rows per MMA group (MMA N upper bound)
-constexpr int BP = 512;      // rows per tile: two MMA groups share each weight k-block
+constexpr int BP = 512;      // rows per tile at most: two MMA groups share each weight k-block
 constexpr int BK = 64;       // K per k-block: one 128-byte swizzle atom of bf16
 constexpr int GRID = 152;    // persistent CTAs: one per SM of a GB300
 constexpr int MIN_PER = 8;   // smallest k-block range per CTA
 }  // namespace tcplan
 
-// k-block range per CTA when T rows are valid (tiles = N/BM x ceil(T/BP)).
+// Rows per tile for T rows: all of them as two MMA groups sharing each weight
+// k-block when they fit one tile (decode-sized commits read every weight byte
+// once), else 256 (one group per tile, which leaves room for a deeper ring).
+inline __host__ __device__ int gemm_tc_pass_rows(int T) { return T <= tcplan::BP ? tcplan::BP : tcplan::BN; }
+// Tiles of a GEMM over T rows: N/BM x ceil(T/rows per tile). When the rows
+// take more than one pass and there are at least GRID tiles, whole waves of
+// GRID tiles are handed out one per CTA (the CTAs of a wave then work on a few
+// passes at once and share their rows and weights in L2); the rest are split
+// over the CTAs in contiguous k-block ranges (stream-K).
+inline __host__ __device__ int gemm_tc_tiles(int T, int N) {
+  const int PR = gemm_tc_pass_rows(T);
+  return (N / tcplan::BM) * ((T + PR - 1) / PR);
+}
+inline __host__ __device__ int gemm_tc_full_tiles(int T, int N) {
+  if (T <= gemm_tc_pass_rows(T)) return 0;
+  return (gemm_tc_tiles(T, N) / tcplan::GRID) * tcplan::GRID;
+}
+// Partial-sum slots per output element: ceil(GRID / MT) + 1.
+inline __host__ __device__ int gemm_tc_slots(int N) {
+  const int MT = N / tcplan::BM;
+  return (tcplan::GRID + MT - 1) / MT + 1;
+}
+// k-block range per CTA over the split tiles; at least KB / (slots - 1), so
+// that no tile spans more segments than there are slots.
 inline __host__ __device__ int gemm_tc_per(int T, int N, int K) {
-  const int MT = N / tcplan::BM, KB = K / tcplan::BK;
-  const int G = (T + tcplan::BP - 1) / tcplan::BP;
-  const long total = (long)MT * G * KB;
-  long per = (total + tcplan::GRID - 1) / tcplan::GRID;
+  const int KB = K / tcplan::BK, S = gemm_tc_slots(N);
+  const long rem = (long)(gemm_tc_tiles(T, N) - gemm_tc_full_tiles(T, N)) * KB;
+  long per = (rem + tcplan::GRID - 1) / tcplan::GRID;
+  const long floor_per = (KB + S - 2) / (S - 1);
+  if (per < floor_per) per = floor_per;
   if (per < tcplan::MIN_PER) per = tcplan::MIN_PER;
   return (int)per;
 }
-// Number of K segments (CTA ranges) that tile `tile` spans.
+// Number of K segments (CTA ranges) that split tile `tile` (counted from the
+// first split tile) spans.
 inline __host__ __device__ int gemm_tc_tile_segs(int tile, int KB, int per) {
   return ((tile + 1) * KB - 1) / per - (tile * KB) / per + 1;
 }
-// Partial-sum slots of a GEMM with segment rule `per` (0: fixed S splits) for
-// the output element (t, n).
-inline __host__ __device__ int part_segs(int t, int n, int N, int K, int per, int S) {
-  if (per <= 0) return S;
-  const int tile = (t / tcplan::BP) * (N / tcplan::BM) + n / tcplan::BM;
-  return gemm_tc_tile_segs(tile, K / tcplan::BK, per);
+// Which partial-sum slots hold an output element's sums: the per-call
+// constants of a GEMM over T rows with segment rule `per` (0: fixed S splits),
+// taken once per thread, and the count for element (t, n).
+struct SegRule {
+  int per, S, PR, MT, KB, full;
+};
+inline __host__ __device__ SegRule seg_rule(int N, int K, int per, int S, int T) {
+  SegRule r;
+  r.per = per;
+  r.S = S;
+  r.PR = gemm_tc_pass_rows(T);
+  r.MT = N / tcplan::BM;
+  r.KB = K / tcplan::BK;
+  r.full = per > 0 ? gemm_tc_full_tiles(T, N) : 0;
+  return r;
+}
+inline __host__ __device__ int seg_count(const SegRule& r, int t, int n) {
+  if (r.per <= 0) return r.S;
+  const int tile = (t / r.PR) * r.MT + n / tcplan::BM;
+  if (tile < r.full) return 1;
+  return gemm_tc_tile_segs(tile - r.full, r.KB, r.per);
 }
 
 bool gemm_tc_supported(int K, int N);

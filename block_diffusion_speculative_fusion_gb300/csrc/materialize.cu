@@ -16,6 +16,7 @@
 // GEMMs run on tcgen05 tensor cores for bf16 (gemm_tc.cu) and on CUDA cores
 // for fp32 or shapes the tensor-core kernel does not take.
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "internal.h"
@@ -28,13 +29,10 @@ namespace dflash {
 __global__ void __launch_bounds__(256)
 mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restrict__ start_pos, int B,
                 int rows_max, int32_t* __restrict__ meta, int32_t* __restrict__ row_b,
-                int32_t* __restrict__ row_j, int32_t* __restrict__ new_len, int tc, int N1, int K1, int N2,
-                int K2, float rope_theta, int D, double* __restrict__ inv_freq) {
+                int32_t* __restrict__ row_j, int32_t* __restrict__ row_start, int32_t* __restrict__ new_len, int tc,
+                int N1, int K1, int N2, int K2) {
   __shared__ int32_t scan[256];
   const int tid = threadIdx.x;
-  // RoPE frequencies theta^(-2i/D), once per call, in double
-  if (rope_theta > 0.f)
-    for (int i = tid; i < D / 2; i += blockDim.x) inv_freq[i] = exp(-(2.0 * i / D) * log((double)rope_theta));
   const int per = (B + blockDim.x - 1) / blockDim.x;
   const int b0 = tid * per, b1 = min(B, b0 + per);
   int local = 0;
@@ -50,20 +48,36 @@ mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restric
   int row = scan[tid] - local;
   for (int b = b0; b < b1; ++b) {
     const int n = max(0, min(commit_len[b], rows_max));
-    for (int j = 0; j < n; ++j, ++row) {
-      row_b[row] = b;
-      row_j[row] = j;
-    }
+    row_start[b] = row;
+    row += n;
     if (new_len) new_len[b] = start_pos[b] + n;
   }
+  const int T = scan[blockDim.x - 1];
   if (tid == blockDim.x - 1) {
-    const int T = scan[tid];
+    row_start[B] = T;
     meta[0] = T;
     // tensor-core GEMMs: k-block range per persistent CTA for T rows (0: fixed splits)
     meta[1] = tc ? gemm_tc_per(T, N1, K1) : 0;
     meta[2] = tc ? gemm_tc_per(T, N2, K2) : 0;
   }
+  __syncthreads();
+  // row list, all threads: row r belongs to the last sequence whose rows start at or before r
+  for (int r = tid; r < T; r += blockDim.x) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (row_start[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    row_b[r] = lo;
+    row_j[r] = r - row_start[lo];
+  }
 }
+
+// RoPE frequencies theta^(-2i/D) for i < D/2, computed on the host in double
+// and passed by value (D <= 256)
+struct RopeFreq {
+  double f[128];
+};
 
 // ---------------------------------------------------------------------------
 // gather: hidden[b, j, :] -> X[t, :]
@@ -71,17 +85,33 @@ mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restric
 __global__ void __launch_bounds__(256)
 mat_gather_kernel(const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, const int32_t* __restrict__ meta,
                   const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j, int rows_max,
-                  size_t row_bytes, const int32_t* __restrict__ start_pos, const double* __restrict__ inv_freq,
+                  size_t row_bytes, const int32_t* __restrict__ start_pos, const __grid_constant__ RopeFreq inv_freq,
                   float2* __restrict__ rope, int half, const int32_t* __restrict__ page_table, int page_size,
                   int max_pages, int num_pages, long long* __restrict__ slots) {
   // grid-stride over the committed rows only (their count is on the device)
   const long T = meta[0];
   const long nvec = (long)(row_bytes / 16);
   const long stride = (long)gridDim.x * blockDim.x;
-  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * nvec; idx += stride) {
-    const long t = idx / nvec, v = idx - t * nvec;
-    const uint4* src = reinterpret_cast<const uint4*>(hidden + ((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes);
-    reinterpret_cast<uint4*>(X + (size_t)t * row_bytes)[v] = __ldg(src + v);
+  // four 16-byte copies in flight per thread
+  constexpr int U = 4;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * nvec; idx += U * stride) {
+    uint4 val[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long i = idx + k * stride;
+      if (i < T * nvec) {
+        const long t = i / nvec, v = i - t * nvec;
+        val[k] = __ldg(reinterpret_cast<const uint4*>(hidden + ((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes) + v);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long i = idx + k * stride;
+      if (i < T * nvec) {
+        const long t = i / nvec, v = i - t * nvec;
+        reinterpret_cast<uint4*>(X + (size_t)t * row_bytes)[v] = val[k];
+      }
+    }
   }
   const long tail = (long)row_bytes - nvec * 16;
   for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * tail; idx += stride) {
@@ -108,7 +138,7 @@ mat_gather_kernel(const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, c
     for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * half; idx += stride) {
       const long t = idx / half;
       const int i = (int)(idx - t * half);
-      const double a = (double)(start_pos[row_b[t]] + row_j[t]) * inv_freq[i];
+      const double a = (double)(start_pos[row_b[t]] + row_j[t]) * inv_freq.f[i];
       const double k = rint(a * 0.15915494309189535);
       double r = fma(-k, 6.283185307179586, a);
       r = fma(-k, 2.4492935982947064e-16, r);
@@ -179,18 +209,53 @@ mat_bias_kernel(const float* __restrict__ part, int splits, const T* __restrict_
   // thread (d % 4 == 0: they share one output tile, hence one segment count)
   const int d4 = d / 4;
   const long Tn = (long)min(meta[0], T_max) * d4;
-  const int per = meta[1];
-  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < Tn; idx += (long)gridDim.x * blockDim.x) {
-    const int t = (int)(idx / d4), f = 4 * (int)(idx - (long)t * d4);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (b_f) v = make_float4(to_f32(b_f[f]), to_f32(b_f[f + 1]), to_f32(b_f[f + 2]), to_f32(b_f[f + 3]));
-    const int segs = part_segs(t, f, d, K1, per, splits);
-    for (int s = 0; s < segs; ++s) {
-      const float4 x = *reinterpret_cast<const float4*>(part + ((size_t)s * T_max + t) * d + f);
-      v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+  const SegRule rule = seg_rule(d, K1, meta[1], splits, min(meta[0], T_max));
+  const long stride = (long)gridDim.x * blockDim.x;
+  // two items of 4 features per thread, two segments a pass: four loads in flight
+  constexpr int U = 2;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < Tn; idx += U * stride) {
+    float4 v[U];
+    int segs[U];
+    int smax = 0;
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long i = idx + k * stride;
+      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      segs[k] = 0;
+      if (i < Tn) {
+        const int t = (int)(i / d4), f = 4 * (int)(i - (long)t * d4);
+        if (b_f) v[k] = make_float4(to_f32(b_f[f]), to_f32(b_f[f + 1]), to_f32(b_f[f + 2]), to_f32(b_f[f + 3]));
+        segs[k] = seg_count(rule, t, f);
+        smax = max(smax, segs[k]);
+      }
     }
-    T* o = h + (size_t)t * d + f;
-    o[0] = from_f32<T>(v.x); o[1] = from_f32<T>(v.y); o[2] = from_f32<T>(v.z); o[3] = from_f32<T>(v.w);
+    for (int s = 0; s < smax; s += 2) {
+      float4 x[2][U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const long i = idx + k * stride;
+        const int t = (int)(i / d4), f = 4 * (int)(i - (long)t * d4);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (s + q < segs[k]) x[q][k] = *reinterpret_cast<const float4*>(part + ((size_t)(s + q) * T_max + t) * d + f);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+          if (s + q < segs[k]) {
+            v[k].x += x[q][k].x; v[k].y += x[q][k].y; v[k].z += x[q][k].z; v[k].w += x[q][k].w;
+          }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long i = idx + k * stride;
+      if (i < Tn) {
+        const int t = (int)(i / d4), f = 4 * (int)(i - (long)t * d4);
+        T* o = h + (size_t)t * d + f;
+        o[0] = from_f32<T>(v[k].x); o[1] = from_f32<T>(v[k].y); o[2] = from_f32<T>(v[k].z); o[3] = from_f32<T>(v[k].w);
+      }
+    }
   }
 }
 
@@ -218,79 +283,108 @@ __device__ __forceinline__ void store4<bf16>(bf16* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-template <typename T>
-__device__ __forceinline__ void epi128_finish(float4 x, int v, long long slot, int t, int Hkv, const T* k_norm_w,
-                                              float rms_eps, const float2* rope, const MatPools& pools, int lane) {
-  constexpr int D = 128, half = 64;
-  const int d0 = 4 * lane;
-  const int h = v % Hkv, kv = (v / Hkv) & 1, l = v / (2 * Hkv);
-  T* dst = (kv == 0 ? (T*)pools.k[l] : (T*)pools.v[l]) + ((size_t)slot * Hkv + h) * D + d0;
-  if (kv == 0) {
-    if (k_norm_w) {
-      float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float sc = 1.f / sqrtf(ss / D + rms_eps);
-      const T* wv = k_norm_w + (size_t)l * D + d0;
-      x.x *= sc * to_f32(wv[0]);
-      x.y *= sc * to_f32(wv[1]);
-      x.z *= sc * to_f32(wv[2]);
-      x.w *= sc * to_f32(wv[3]);
-    }
-    if (rope) {
-      float4 y;
-      y.x = __shfl_xor_sync(0xffffffffu, x.x, 16);
-      y.y = __shfl_xor_sync(0xffffffffu, x.y, 16);
-      y.z = __shfl_xor_sync(0xffffffffu, x.z, 16);
-      y.w = __shfl_xor_sync(0xffffffffu, x.w, 16);
-      const float2* c = rope + (size_t)t * half + (d0 & (half - 1));
-      const float2 c0 = c[0], c1 = c[1], c2 = c[2], c3 = c[3];
-      if (d0 < half)
-        x = make_float4(x.x * c0.x - y.x * c0.y, x.y * c1.x - y.y * c1.y, x.z * c2.x - y.z * c2.y,
-                        x.w * c3.x - y.w * c3.y);
-      else
-        x = make_float4(x.x * c0.x + y.x * c0.y, x.y * c1.x + y.y * c1.y, x.z * c2.x + y.z * c2.y,
-                        x.w * c3.x + y.w * c3.y);
-    }
-  }
-  if (slot >= 0) store4<T>(dst, x);
-}
+// One unit = (committed token t, layer l, K or V, up to kEpiHeads kv heads): the
+// heads' partial-sum vectors are all loaded before any is finished, and the
+// token's RoPE coefficients and the layer's norm weights are loaded once for them.
+constexpr int kEpiHeads = 8;
+
+constexpr int kEpiCtasPerSm = 2;   // 104 registers a thread
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, kEpiCtasPerSm)
 mat_epilogue_d128_kernel(const float* __restrict__ part, int splits, const int32_t* __restrict__ meta,
                          const long long* __restrict__ slots, const T* __restrict__ k_norm_w, float rms_eps,
                          const float2* __restrict__ rope, MatPools pools, int T_max, int L, int Hkv, int K2) {
-  constexpr int D = 128;
+  constexpr int D = 128, half = 64, NH = kEpiHeads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const int NV = L * 2 * Hkv;
-  const int N = NV * D;
-  const int per = meta[2];
-  const long tasks = (long)min(meta[0], T_max) * NV;
-  const long stride = (long)gridDim.x * nwarps;
-  auto load = [&](long task, int& t, int& v, long long& slot) -> float4 {
-    t = (int)(task / NV);
-    v = (int)(task - (long)t * NV);
-    slot = slots[t];
-    // a 128-wide vector lies in one 128-feature GEMM tile: one segment count
-    const int segs = part_segs(t, v * D, N, K2, per, splits);
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sg = 0; sg < segs; ++sg) {
-      const float4 y = *reinterpret_cast<const float4*>(part + ((size_t)sg * T_max + t) * N + v * D + 4 * lane);
-      x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+  const int d0 = 4 * lane;
+  const int N = L * 2 * Hkv * D;
+  const int Tr = min(meta[0], T_max);
+  const SegRule rule = seg_rule(N, K2, meta[2], splits, Tr);
+  // heads per unit: up to kEpiHeads, fewer when that leaves warps without a unit
+  const long warps = (long)gridDim.x * nwarps;
+  int hs = NH;
+  while (hs > 1 && (long)Tr * L * 2 * ((Hkv + hs - 1) / hs) < warps) hs >>= 1;
+  const int hchunks = (Hkv + hs - 1) / hs;
+  const long units = (long)Tr * L * 2 * hchunks;
+  for (long u = (long)blockIdx.x * nwarps + warp; u < units; u += warps) {
+    long r = u;
+    const int hc = (int)(r % hchunks);
+    r /= hchunks;
+    const int kv = (int)(r & 1);
+    r >>= 1;
+    const int l = (int)(r % L);
+    const int t = (int)(r / L);
+    const int h0 = hc * hs, nh = min(hs, Hkv - h0);
+    const int v0 = (l * 2 + kv) * Hkv + h0;    // vector index of head h0: (l, K|V, h) -> features v * D
+    const long long slot = slots[t];
+    // a 128-wide vector lies in one 128-feature GEMM tile: one segment count each
+    int segs[NH];
+    int smax = 0;
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+      segs[i] = i < nh ? seg_count(rule, t, (v0 + i) * D) : 0;
+      smax = max(smax, segs[i]);
     }
-    return x;
-  };
-  // two tasks in flight per warp: the second one's loads overlap the first one's math
-  for (long task = (long)blockIdx.x * nwarps + warp; task < tasks; task += 2 * stride) {
-    int t0, v0, t1 = 0, v1 = 0;
-    long long s0, s1 = -1;
-    const float4 x0 = load(task, t0, v0, s0);
-    const bool two = task + stride < tasks;
-    float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (two) x1 = load(task + stride, t1, v1, s1);
-    epi128_finish<T>(x0, v0, s0, t0, Hkv, k_norm_w, rms_eps, rope, pools, lane);
-    if (two) epi128_finish<T>(x1, v1, s1, t1, Hkv, k_norm_w, rms_eps, rope, pools, lane);
+    // the first segment straight into the sums, the others (split tiles) added
+    const float* src0 = part + (size_t)t * N + (size_t)v0 * D + d0;
+    float4 x[NH];
+#pragma unroll
+    for (int i = 0; i < NH; ++i)
+      x[i] = segs[i] > 0 ? *reinterpret_cast<const float4*>(src0 + i * D) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sg = 1; sg < smax; ++sg) {
+      const float* src = part + ((size_t)sg * T_max + t) * N + (size_t)v0 * D + d0;
+      float4 y[NH];
+#pragma unroll
+      for (int i = 0; i < NH; ++i)
+        if (sg < segs[i]) y[i] = *reinterpret_cast<const float4*>(src + i * D);
+#pragma unroll
+      for (int i = 0; i < NH; ++i)
+        if (sg < segs[i]) {
+          x[i].x += y[i].x; x[i].y += y[i].y; x[i].z += y[i].z; x[i].w += y[i].w;
+        }
+    }
+    T* dst = (kv == 0 ? (T*)pools.k[l] : (T*)pools.v[l]) + ((size_t)slot * Hkv + h0) * D + d0;
+    if (kv == 0) {
+      float4 w = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (k_norm_w) {
+        const T* wv = k_norm_w + (size_t)l * D + d0;
+        w = make_float4(to_f32(wv[0]), to_f32(wv[1]), to_f32(wv[2]), to_f32(wv[3]));
+      }
+      float2 c0 = make_float2(1.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
+      if (rope) {
+        const float2* c = rope + (size_t)t * half + (d0 & (half - 1));
+        c0 = c[0]; c1 = c[1]; c2 = c[2]; c3 = c[3];
+      }
+      // RMSNorm over D then rotate-half RoPE: the partner of element d < 64 is
+      // d + 64, held by lane + 16
+      const float sgn = d0 < half ? -1.f : 1.f;
+#pragma unroll
+      for (int i = 0; i < NH; ++i) {
+        float4 a = x[i];
+        if (k_norm_w) {
+          float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          const float sc = 1.f / sqrtf(ss / D + rms_eps);
+          a = make_float4(a.x * (sc * w.x), a.y * (sc * w.y), a.z * (sc * w.z), a.w * (sc * w.w));
+        }
+        if (rope) {
+          float4 y;
+          y.x = __shfl_xor_sync(0xffffffffu, a.x, 16);
+          y.y = __shfl_xor_sync(0xffffffffu, a.y, 16);
+          y.z = __shfl_xor_sync(0xffffffffu, a.z, 16);
+          y.w = __shfl_xor_sync(0xffffffffu, a.w, 16);
+          a = make_float4(a.x * c0.x + sgn * y.x * c0.y, a.y * c1.x + sgn * y.y * c1.y,
+                          a.z * c2.x + sgn * y.z * c2.y, a.w * c3.x + sgn * y.w * c3.y);
+        }
+        if (i < nh && slot >= 0) store4<T>(dst + i * D, a);
+      }
+    } else if (slot >= 0) {
+#pragma unroll
+      for (int i = 0; i < NH; ++i)
+        if (i < nh) store4<T>(dst + i * D, x[i]);
+    }
   }
 }
 
@@ -307,7 +401,7 @@ mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* _
   const int NV = L * 2 * Hkv;
   const int N = NV * D;
   const int half = D / 2;
-  const int per = meta[2];
+  const SegRule rule = seg_rule(N, K2, meta[2], splits, min(meta[0], T_max));
   const long tasks = (long)min(meta[0], T_max) * NV;
   for (long task = (long)blockIdx.x * nwarps + warp; task < tasks; task += (long)gridDim.x * nwarps) {
     const int t = (int)(task / NV), v = (int)(task - (long)t * NV);
@@ -323,7 +417,7 @@ mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* _
     float ss = 0.f;
     for (int d = lane; d < D; d += 32) {
       float x = 0.f;
-      const int segs = part_segs(t, n0 + d, N, K2, per, splits);
+      const int segs = seg_count(rule, t, n0 + d);
       for (int s = 0; s < segs; ++s) x += part[((size_t)s * T_max + t) * N + n0 + d];
       xs[d] = x;
       ss += x * x;
@@ -363,6 +457,7 @@ mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* _
 // ---------------------------------------------------------------------------
 MatPlan mat_plan(int B, int rows_max, int m, int d, int L, int Hkv, int D, int dtype) {
   MatPlan p;
+  p.B = B;
   p.T_max = B * rows_max;
   p.K1 = m * d;
   p.N1 = d;
@@ -382,8 +477,7 @@ MatPlan mat_plan(int B, int rows_max, int m, int d, int L, int Hkv, int D, int d
 size_t mat_ws_bytes(const MatPlan& p, int dtype) {
   const size_t el = dtype == 1 ? 2 : 4;
   const size_t Nmax = std::max(p.N1, p.N2);
-  size_t s = align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max));
-  s += align_up(sizeof(double) * 128);             // RoPE frequencies (D <= 256)
+  size_t s = align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max + p.B + 1));
   s += align_up(sizeof(float2) * (size_t)p.T_max * 128);   // RoPE (cos, sin) per committed row
   s += align_up(sizeof(long long) * (size_t)p.T_max);       // pool slot per committed row
   s += align_up((size_t)p.T_max * p.K1 * el);     // gathered operand X
@@ -410,9 +504,11 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   int32_t* meta = (int32_t*)ws;
   int32_t* row_b = meta + 64;
   int32_t* row_j = row_b + p.T_max;
-  ws += align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max));
-  double* inv_freq = (double*)ws;
-  ws += align_up(sizeof(double) * 128);
+  int32_t* row_start = row_j + p.T_max;
+  ws += align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max + p.B + 1));
+  RopeFreq inv_freq;
+  for (int i = 0; i < 128; ++i)
+    inv_freq.f[i] = i < a.D / 2 && a.rope_theta > 0.f ? std::exp(-(2.0 * i / a.D) * std::log((double)a.rope_theta)) : 0.0;
   float2* rope = a.rope_theta > 0.f ? (float2*)ws : nullptr;
   ws += align_up(sizeof(float2) * (size_t)p.T_max * 128);
   long long* slots = (long long*)ws;
@@ -424,8 +520,8 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   float* part = (float*)ws;
   cudaStream_t st = a.stream;
   int n = 0;
-  mat_plan_kernel<<<1, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, meta, row_b, row_j, a.new_len,
-                                     p.tc ? 1 : 0, p.N1, p.K1, p.N2, p.K2, a.rope_theta, a.D, inv_freq);
+  mat_plan_kernel<<<1, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, meta, row_b, row_j, row_start,
+                                     a.new_len, p.tc ? 1 : 0, p.N1, p.K1, p.N2, p.K2);
   ++n;
   const size_t row_bytes = (size_t)p.K1 * el;
   // grid-stride kernels over the committed rows: a few waves of the 152 SMs
@@ -443,7 +539,7 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   if (e != cudaSuccess) return e;
   ++n;
   if (a.D == 128) {
-    mat_epilogue_d128_kernel<T><<<gs, 256, 0, st>>>(part, p.S2, meta, slots, (const T*)a.k_norm_w, a.rms_eps,
+    mat_epilogue_d128_kernel<T><<<kEpiCtasPerSm * 152, 256, 0, st>>>(part, p.S2, meta, slots, (const T*)a.k_norm_w, a.rms_eps,
                                                    rope, a.pools, p.T_max, a.L, a.Hkv, p.K2);
   } else {
     const size_t esmem = sizeof(float) * 8 * (size_t)a.D;
