@@ -543,6 +543,13 @@ def report_config(wl, args):
                                                      out=st.attn_out[0]), args.steps, args.warmup)
         ab = attn_bytes(float(st.ctx0.sum()), wl)
         out["attn_us_per_layer"] = us_attn
+        # the in-block causal variant on the same inputs
+        us_causal = _time_calls(lambda: api.block_attn(inp["q0"], inp["k_blk0"], inp["v_blk0"], st.k_pools[0],
+                                                       st.v_pools[0], st.page_table, st.ctx_start,
+                                                       max_ctx=st.max_ctx, out=st.attn_out[0], causal=True),
+                                args.steps, args.warmup)
+        out["attn_causal_us_per_layer"] = us_causal
+        out["attn_causal_frac_hbm"] = gbs(ab, us_causal) / hbm
         out["attn_frac_hbm"] = gbs(ab, us_attn) / hbm
         ng = wl.n_greedy
         R = wl.n_draft + 1

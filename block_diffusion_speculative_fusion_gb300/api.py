@@ -41,7 +41,7 @@ class CtxKvDims(ctypes.Structure):
 
 class AttnDims(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in ("B", "n_q", "n_kv_blk", "Hq", "Hkv", "D", "page_size",
-                                     "max_pages", "num_pages", "max_ctx", "dtype")]
+                                     "max_pages", "num_pages", "max_ctx", "dtype", "causal")]
 
 
 class VerifyDims(ctypes.Structure):
@@ -300,12 +300,14 @@ def gate(draft_logits: torch.Tensor, tokens: torch.Tensor, temperature: float = 
 def block_attn(q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor, k_pool: torch.Tensor,
                v_pool: torch.Tensor, page_table: torch.Tensor, ctx_len: torch.Tensor,
                max_ctx: Optional[int] = None, scale: Optional[float] = None,
-               out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Unmasked GQA attention of the draft block over [paged context ; block]
-    (``dflash_block_attn``). q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv, Hkv, D];
-    pools [num_pages, page, Hkv, D]; page_table [B, max_pages] int32; ctx_len [B]
-    int32. ``max_ctx`` bounds every ctx_len (defaults to the page table's
-    capacity)."""
+               out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+               causal: bool = False) -> torch.Tensor:
+    """GQA attention of the draft block over [paged context ; block]
+    (``dflash_block_attn``): unmasked, or with ``causal`` the in-block causal
+    variant (query i sees the context and block rows j <= i + n_kv - n_q).
+    q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv, Hkv, D]; pools [num_pages, page,
+    Hkv, D]; page_table [B, max_pages] int32; ctx_len [B] int32. ``max_ctx``
+    bounds every ctx_len (defaults to the page table's capacity)."""
     _dev(q, "q")
     B, n_q, Hq, D = q.shape
     n_kv, Hkv = k_blk.shape[1], k_blk.shape[2]
@@ -317,7 +319,7 @@ def block_attn(q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor, k_pool
     for name, t in (("k_blk", k_blk), ("v_blk", v_blk), ("k_pool", k_pool), ("v_pool", v_pool)):
         if t.dtype != q.dtype:
             raise TypeError(f"{name} must have the dtype of q")
-    dims = AttnDims(B, n_q, n_kv, Hq, Hkv, D, page, max_pages, num_pages, int(max_ctx), dt)
+    dims = AttnDims(B, n_q, n_kv, Hq, Hkv, D, page, max_pages, num_pages, int(max_ctx), dt, 1 if causal else 0)
     if out is None:
         out = torch.empty_like(q)
     need = lib().dflash_block_attn_workspace_size(ctypes.byref(dims))

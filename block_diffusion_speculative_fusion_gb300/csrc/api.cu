@@ -242,6 +242,9 @@ static int check_attn_dims(const dflash_attn_dims* d) {
   if (d->D > 256) return fail(DFLASH_ERR_UNSUPPORTED, "D=%d > 256", d->D);
   if ((long)d->B * d->Hkv > kMaxCounters - 2) return fail(DFLASH_ERR_UNSUPPORTED, "B*Hkv too large");
   if (d->n_q > 65535 || d->Hq > 65535 || d->B > 65535) return fail(DFLASH_ERR_UNSUPPORTED, "grid too large");
+  if (d->causal != 0 && d->causal != 1) return fail(DFLASH_ERR_INVALID_ARG, "causal=%d is not 0 or 1", d->causal);
+  if (d->causal && d->n_kv_blk < d->n_q)
+    return fail(DFLASH_ERR_INVALID_ARG, "causal needs n_kv_blk=%d >= n_q=%d", d->n_kv_blk, d->n_q);
   return DFLASH_OK;
 }
 
@@ -264,7 +267,7 @@ int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_bl
   dflash::AttnArgs a{};
   a.B = d->B; a.n_q = d->n_q; a.n_kv = d->n_kv_blk; a.Hq = d->Hq; a.Hkv = d->Hkv; a.D = d->D;
   a.page_size = d->page_size; a.max_pages = d->max_pages; a.num_pages = d->num_pages;
-  a.max_ctx = d->max_ctx; a.dtype = d->dtype;
+  a.max_ctx = d->max_ctx; a.dtype = d->dtype; a.causal = d->causal;
   a.q = q; a.k_blk = k_blk; a.v_blk = v_blk; a.k_pool = k_pool; a.v_pool = v_pool;
   a.page_table = page_table; a.ctx_len = ctx_len; a.scale = scale; a.out = out;
   a.counters = (int32_t*)workspace;

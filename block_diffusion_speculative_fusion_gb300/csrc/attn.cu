@@ -40,6 +40,7 @@ struct AttnParams {
   int32_t* counters; // [B * Hkv]
   int* err;
   int B, n_q, n_kv, Hq, Hkv, G, M, page_size, max_pages, num_pages, max_splits, max_ctx;
+  int causal;        // 1: query i sees block rows j <= i + n_kv - n_q
   // work items: hpi kv heads (1 or 2) per item, Gi = hpi * G query heads and
   // Mi = n_q * Gi packed rows per item, n_groups = Hkv / hpi items per split of
   // a sequence, TK = 64 / hpi keys per tile, br = K/V rows per TMA box
@@ -572,11 +573,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         // keys 0 .. valid - 1 of the tile are real (per head); scores stay
         // unscaled here (the scale is > 0, so the max commutes with it)
         const int valid = (j < it.n_tiles_ctx) ? min(TK, it.C - (t0 + j) * TK) : p.n_kv;
+        // keys this row sees: causal rows (packed row r is query r / Gi) stop
+        // at their own block position
+        const int seen = (p.causal && j >= it.n_tiles_ctx) ? min(valid, r / p.Gi + 1 + p.n_kv - p.n_q) : valid;
         float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-        if (valid < TK) {
+        if (seen < TK) {
 #pragma unroll
           for (int c = 0; c < NK; ++c)
-            if (kk0 + c >= valid) sv[c] = -CUDART_INF_F;
+            if (kk0 + c >= seen) sv[c] = -CUDART_INF_F;
         }
 #pragma unroll
         for (int c = 0; c < NK; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
@@ -839,7 +843,7 @@ attn_generic_kernel(const T* __restrict__ q, const T* __restrict__ k_blk, const 
                     const T* __restrict__ k_pool, const T* __restrict__ v_pool,
                     const int32_t* __restrict__ page_table, const int32_t* __restrict__ ctx_len,
                     T* __restrict__ out, int n_q, int n_kv, int Hq, int Hkv, int D, int page_size,
-                    int max_pages, int num_pages, float scale) {
+                    int max_pages, int num_pages, float scale, int causal) {
   constexpr int KC = 128;   // keys per chunk (one per thread)
   __shared__ float qs[256];
   __shared__ float ps[KC];
@@ -874,6 +878,7 @@ attn_generic_kernel(const T* __restrict__ q, const T* __restrict__ k_blk, const 
       float acc = 0.f;
       for (int d = 0; d < D; ++d) acc += qs[d] * to_f32(krow[d]);
       sc = acc * scale;
+      if (causal && key >= C && key - C > i + n_kv - n_q) sc = -CUDART_INF_F;
     }
     rowidx[tid] = vrow_kind;
     // chunk max
@@ -971,12 +976,12 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
       attn_generic_kernel<float><<<grid, 128, 0, a.stream>>>(
           (const float*)a.q, (const float*)a.k_blk, (const float*)a.v_blk, (const float*)a.k_pool,
           (const float*)a.v_pool, a.page_table, a.ctx_len, (float*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
-          a.D, a.page_size, a.max_pages, a.num_pages, a.scale);
+          a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal);
     else
       attn_generic_kernel<bf16><<<grid, 128, 0, a.stream>>>(
           (const bf16*)a.q, (const bf16*)a.k_blk, (const bf16*)a.v_blk, (const bf16*)a.k_pool,
           (const bf16*)a.v_pool, a.page_table, a.ctx_len, (bf16*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
-          a.D, a.page_size, a.max_pages, a.num_pages, a.scale);
+          a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal);
     return cudaGetLastError();
   }
   using namespace attn;
@@ -988,6 +993,7 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   p.ctx_len = a.ctx_len;
   p.out = (bf16*)a.out;
   p.B = a.B; p.n_q = a.n_q; p.n_kv = a.n_kv; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = a.Hq / a.Hkv;
+  p.causal = a.causal;
   p.M = a.n_q * p.G;
   p.page_size = a.page_size; p.max_pages = a.max_pages; p.num_pages = a.num_pages;
   p.hpi = attn_hpi(a.n_q, a.n_kv, a.Hq, a.Hkv, a.page_size);

@@ -65,6 +65,7 @@ cudaError_t launch_gate(const GateArgs& a, int num_sms);
 // ------------------------------------------------------------- attention ---
 struct AttnArgs {
   int B, n_q, n_kv, Hq, Hkv, D, page_size, max_pages, num_pages, max_ctx, dtype;
+  int causal;   // 1: query i sees block rows j <= i + n_kv - n_q
   const void* q;
   const void* k_blk;
   const void* v_blk;

@@ -143,14 +143,20 @@ typedef struct {
   int32_t num_pages;
   int32_t max_ctx;    /* upper bound on every ctx_len[b] (sizes the launch) */
   int32_t dtype;
+  int32_t causal;     /* 0: no mask; 1: in-block causal (needs n_kv_blk >= n_q), see below */
 } dflash_attn_dims;
 
 /*
- * out = softmax(scale * Q K^T) V with no mask, where for sequence b the keys and
- * values are the ctx_len[b] context rows of the paged pools followed by the
- * n_kv_blk rows of the block; q-head h reads kv-head h / (Hq / Hkv).
+ * out = softmax(scale * Q K^T) V, where for sequence b the keys and values are
+ * the ctx_len[b] context rows of the paged pools followed by the n_kv_blk rows
+ * of the block; q-head h reads kv-head h / (Hq / Hkv).
  *   [DFlash] 块扩散: the draft attends bidirectionally inside the block;
  *   [DFlash] KV 注入, step 3: Attention(Q_draft, [K_draft; K_ctx], [V_draft; V_ctx]).
+ * causal = 0: no mask (every query row sees every key).
+ * causal = 1: query row i sees every context row and the block rows
+ *   j <= i + n_kv_blk - n_q (query i sits at block row i + n_kv_blk - n_q), the
+ *   in-block causal variant of [DFlash] 块扩散的双向注意力问题 (JetSpec: block
+ *   position i sees positions 0 .. i). n_kv_blk < n_q is rejected (INVALID_ARG).
  *
  * q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv_blk, Hkv, D]
  * k_pool, v_pool  one draft layer's pools [num_pages, page_size, Hkv, D]

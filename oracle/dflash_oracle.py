@@ -134,13 +134,18 @@ def gather_ctx(pool, page_table_row, ctx_len, page_size):
     return _f64(pool)[pages, pos % page_size]
 
 
-def block_attn(q, k_blk, v_blk, k_pool, v_pool, page_table, ctx_len, page_size, scale=None):
+def block_attn(q, k_blk, v_blk, k_pool, v_pool, page_table, ctx_len, page_size, scale=None, causal=False):
     """Attention(Q_draft, [K_draft; K_ctx], [V_draft; V_ctx]) with no mask.
 
     [DFlash] 块扩散 (draft uses bidirectional, non-causal attention inside the
     block) and KV 注入 step 3 (queries of the draft tokens attend to the block's
     own K/V and to the injected context K/V). Grouped-query attention: q-head h
     reads kv-head h // (Hq / Hkv).
+
+    causal=True is the in-block causal variant of [DFlash] 块扩散的双向注意力问题
+    (JetSpec: block position i sees positions 0 .. i): query i, at block row
+    i + n_kv - n_q, keeps every context key and the block keys up to its own
+    row. Requires n_kv >= n_q.
 
     q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv, Hkv, D]; pools [pages, page, Hkv, D].
     Returns out [B, n_q, Hq, D] in float64.
@@ -157,9 +162,15 @@ def block_attn(q, k_blk, v_blk, k_pool, v_pool, page_table, ctx_len, page_size, 
         Vc = gather_ctx(v_pool, page_table[b], ctx_len[b], page_size)
         K = np.concatenate([Kc, k_blk[b]], axis=0)            # [keys, Hkv, D]
         V = np.concatenate([Vc, v_blk[b]], axis=0)
+        C = Kc.shape[0]
+        n_kv = k_blk.shape[1]
         for h in range(Hq):
             g = h // G
             s = scale * (q[b, :, h, :] @ K[:, g, :].T)         # [n_q, keys]
+            if causal:
+                assert n_kv >= n_q, "causal block attention needs n_kv >= n_q"
+                for i in range(n_q):
+                    s[i, C + i + n_kv - n_q + 1:] = -np.inf
             s = s - s.max(axis=1, keepdims=True)
             w = np.exp(s)
             w = w / w.sum(axis=1, keepdims=True)

@@ -51,6 +51,20 @@ def test_workspace_sizes_need_no_gpu(L):
     assert "bad dims" in api.last_error()
 
 
+def test_attention_causal_flag_checked_on_host(L):
+    d = api.AttnDims(2, 16, 16, 32, 8, 128, 16, 64, 256, 1024, api.BF16, 1)
+    assert L.dflash_block_attn_workspace_size(ctypes.byref(d)) > api.WS_COUNTER_BYTES
+    bad = api.AttnDims(2, 16, 16, 32, 8, 128, 16, 64, 256, 1024, api.BF16, 2)
+    assert L.dflash_block_attn_workspace_size(ctypes.byref(bad)) == 0
+    assert "causal" in api.last_error()
+    short = api.AttnDims(2, 16, 15, 32, 8, 128, 16, 64, 256, 1024, api.BF16, 1)
+    assert L.dflash_block_attn_workspace_size(ctypes.byref(short)) == 0
+    assert "n_kv_blk" in api.last_error()
+    # the unmasked form takes a block shorter than the queries
+    short0 = api.AttnDims(2, 16, 15, 32, 8, 128, 16, 64, 256, 1024, api.BF16, 0)
+    assert L.dflash_block_attn_workspace_size(ctypes.byref(short0)) > api.WS_COUNTER_BYTES
+
+
 def _p(x):
     return ctypes.c_void_p(x)
 

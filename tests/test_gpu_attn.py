@@ -46,10 +46,10 @@ def _case(wl, ctx, seed=0, n_q=None, n_kv=None, page=None, headroom=16, nan_tail
     return w, cache, blk
 
 
-def _run(w, cache, blk, atol, seqs=None):
+def _run(w, cache, blk, atol, seqs=None, causal=False):
     out = api.block_attn(blk["q"].to(DEV), blk["k_blk"].to(DEV), blk["v_blk"].to(DEV),
                          cache.k_pools[0].to(DEV), cache.v_pools[0].to(DEV), cache.page_table.to(DEV),
-                         cache.ctx_len.to(DEV))
+                         cache.ctx_len.to(DEV), causal=causal)
     torch.cuda.synchronize()
     got = f64(out)
     assert np.all(np.isfinite(got))
@@ -58,7 +58,7 @@ def _run(w, cache, blk, atol, seqs=None):
     for b in seqs:
         ref = O.block_attn(f64(blk["q"][b:b + 1]), f64(blk["k_blk"][b:b + 1]), f64(blk["v_blk"][b:b + 1]),
                            f64(cache.k_pools[0]), f64(cache.v_pools[0]), pt[b:b + 1],
-                           cache.ctx_len.numpy()[b:b + 1], w.page_size)
+                           cache.ctx_len.numpy()[b:b + 1], w.page_size, causal=causal)
         err = np.abs(got[b] - ref[0]).max()
         assert err < atol, (b, err)
     return got
@@ -141,3 +141,29 @@ def test_attn_deterministic_and_error_word_clear():
     b = api.block_attn(*args, ws=ws)
     assert torch.equal(a, b)
     assert api.device_error_word(ws) == 0
+
+
+# ---- in-block causal variant: query i sees the context and block rows up to its own ----
+def test_attn_causal_tiny_f32_generic_path():
+    w, cache, blk = _case(W.TINY_F32, [0, 5, 31, 77], seed=5)
+    _run(w, cache, blk, 1e-4, causal=True)
+
+
+@pytest.mark.parametrize("ctx", [[0, 1, 63, 64, 65], [37, 1024, 1100, 2100, 3000]])
+def test_attn_causal_bf16_paired_heads(ctx):
+    # llama8b shape: 16 queries x 4 heads per kv head, two kv heads per item
+    w, cache, blk = _case(W.LLAMA8B_B64, ctx, seed=6)
+    _run(w, cache, blk, 2e-2, causal=True)
+
+
+def test_attn_causal_bf16_one_kv_head_per_item_and_extra_block_rows():
+    # Hkv = 3 takes one kv head per item; 3 more block rows than queries
+    import dataclasses
+    wl = dataclasses.replace(W.LLAMA8B_B64, Hq=12, Hkv=3)
+    w, cache, blk = _case(wl, [1024, 333, 2049], seed=7, n_kv=19)
+    _run(w, cache, blk, 2e-2, causal=True)
+
+
+def test_attn_causal_bf16_dloop_stage_rows():
+    w, cache, blk = _case(W.DLOOP_QWEN3_4B, [1024, 17, 700, 1500], seed=8, n_kv=W.DLOOP_QWEN3_4B.k + 2)
+    _run(w, cache, blk, 2e-2, causal=True)

@@ -388,6 +388,55 @@ def test_attn_invariant_to_ctx_order_and_page_size():
     np.testing.assert_allclose(out, base, rtol=1e-12, atol=1e-12)
 
 
+def test_attn_causal_no_ctx_matches_library_causal():
+    # [DFlash] 块扩散的双向注意力问题 (JetSpec): position i sees positions 0 .. i.
+    # With no context and n_q = n_kv this is textbook causal attention.
+    rng = np.random.default_rng(11)
+    c = _attn_case(rng, B=1, n_q=5, Hq=3, Hkv=3, ctx=(0,))
+    out = O.block_attn(**c, causal=True)
+    q = torch.from_numpy(c["q"][0].transpose(1, 0, 2))
+    k = torch.from_numpy(c["k_blk"][0].transpose(1, 0, 2))
+    v = torch.from_numpy(c["v_blk"][0].transpose(1, 0, 2))
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True,
+                                                           scale=1 / math.sqrt(8)).numpy().transpose(1, 0, 2)
+    np.testing.assert_allclose(out[0], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attn_causal_row_is_unmasked_attention_over_its_prefix():
+    # query i sits at block row i + n_kv - n_q and keeps all context rows
+    rng = np.random.default_rng(12)
+    n_q, n_kv = 4, 6
+    c = _attn_case(rng, B=2, n_q=n_q, Hq=4, Hkv=2, ctx=(5, 9), page=4, n_kv=n_kv)
+    out = O.block_attn(**c, causal=True)
+    for i in range(n_q):
+        last = i + n_kv - n_q
+        ci = dict(c)
+        ci["q"] = c["q"][:, i:i + 1]
+        ci["k_blk"] = c["k_blk"][:, :last + 1]
+        ci["v_blk"] = c["v_blk"][:, :last + 1]
+        ref = O.block_attn(**ci)
+        np.testing.assert_allclose(out[:, i:i + 1], ref, rtol=1e-12, atol=1e-12)
+    # later block rows do not reach earlier queries
+    c2 = dict(c)
+    c2["k_blk"] = c["k_blk"].copy()
+    c2["v_blk"] = c["v_blk"].copy()
+    c2["k_blk"][:, n_kv - 1] += 3.0
+    c2["v_blk"][:, n_kv - 1] -= 2.0
+    out2 = O.block_attn(**c2, causal=True)
+    np.testing.assert_array_equal(out2[:, :n_q - 1], out[:, :n_q - 1])
+    assert np.abs(out2[:, n_q - 1] - out[:, n_q - 1]).max() > 1e-3
+
+
+def test_attn_causal_last_row_and_single_query_are_unmasked():
+    rng = np.random.default_rng(13)
+    c = _attn_case(rng, B=2, n_q=3, Hq=4, Hkv=2, ctx=(7, 2), page=2, n_kv=5)
+    full = O.block_attn(**c)
+    causal = O.block_attn(**c, causal=True)
+    np.testing.assert_allclose(causal[:, -1], full[:, -1], rtol=1e-12, atol=1e-12)
+    c1 = _attn_case(rng, B=1, n_q=1, ctx=(4,), n_kv=1)
+    np.testing.assert_allclose(O.block_attn(**c1, causal=True), O.block_attn(**c1), rtol=1e-12, atol=1e-12)
+
+
 def test_attn_identical_keys_average_values():
     rng = np.random.default_rng(4)
     c = _attn_case(rng, B=1, ctx=(6,), page=3)
