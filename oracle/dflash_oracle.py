@@ -327,6 +327,56 @@ def verify_sample(target_logits, draft_logits, cand, n_draft, u_acc, u_final, te
 
 
 # ---------------------------------------------------------------------------
+# Draft-side token choice over the MASK positions
+# ---------------------------------------------------------------------------
+def draft_select(draft_logits, anchor, n_draft=None, u_draft=None, temperature=0.0):
+    """Candidates of one round from the draft's MASK-position logits.
+
+    [DFlash] 推理流程 step 4 and its decode listing: the block is [anchor, MASK,
+    ..., MASK]; the logits of MASK position i give draft token i, taken as the
+    argmax (draft_tokens = argmax(logits[i]) for i = 1 .. k-1). [SpecDec] DFlash
+    section: a token is sampled from each position's distribution instead; the
+    candidates are [anchor] + draft tokens. [SGLang] 3 decode listing: the same
+    [last_bonus] + draft_tokens candidate layout.
+
+    draft_logits [B, n_max, V] (row i <-> draft position i + 1); anchor [B];
+    n_draft [B] (rows i >= n_b are not drafted); u_draft [B, n_max] uniforms.
+    temperature == 0: argmax with the lowest index on ties; q_x = 1 (the greedy
+    draft is a point mass); row_lse = LSE(z).
+    temperature > 0: x ~ softmax(z / T) by inverse CDF in ascending token order
+    (smallest y with C(y) > u * Z); q_x = softmax(z / T)[x]; row_lse =
+    LSE(z / T); flags FLAG_CDF_BOUNDARY when u is within 1e-6 of C(y-1)/Z or
+    C(y)/Z.
+    Returns cand [B, n_max+1] int64 (cand[:, 0] = anchor, -1 past n_b), q_x and
+    row_lse [B, n_max] float64 (0 past n_b), flags [B, n_max] uint8.
+    """
+    z = _f64(draft_logits)
+    B, n_max, V = z.shape
+    n_draft = np.full(B, n_max) if n_draft is None else np.asarray(n_draft)
+    cand = np.full((B, n_max + 1), -1, dtype=np.int64)
+    cand[:, 0] = np.asarray(anchor, dtype=np.int64)
+    q_x = np.zeros((B, n_max))
+    row_lse = np.zeros((B, n_max))
+    flags = np.zeros((B, n_max), dtype=np.uint8)
+    T = temperature if temperature > 0 else 1.0
+    for b in range(B):
+        for i in range(int(n_draft[b])):
+            row = z[b, i]
+            s = row / T
+            mx = s.max()
+            row_lse[b, i] = mx + np.log(np.exp(s - mx).sum())
+            if temperature > 0:
+                y, near = inverse_cdf(np.exp(s - mx), float(u_draft[b, i]))
+                cand[b, i + 1] = y
+                q_x[b, i] = np.exp(s[y] - row_lse[b, i])
+                flags[b, i] = FLAG_CDF_BOUNDARY if near else 0
+            else:
+                cand[b, i + 1] = int(np.argmax(row))    # first maximum: lowest index
+                q_x[b, i] = 1.0
+    return dict(cand=cand, q_x=q_x, row_lse=row_lse, flags=flags)
+
+
+# ---------------------------------------------------------------------------
 # DLoop block gate
 # ---------------------------------------------------------------------------
 def log_softmax_at(z, x, temperature=1.0):

@@ -10,6 +10,8 @@ import math
 import os
 
 import numpy as np
+import scipy.special
+import scipy.stats
 import pytest
 import torch
 
@@ -572,3 +574,80 @@ def test_oracle_imports_nothing_from_the_cuda_path():
             for n in names:
                 assert not n.startswith("block_diffusion_speculative_fusion_gb300"), (fn, n)
                 assert n.split(".")[0] in ("numpy", "__future__", "") or n.startswith("dflash_oracle"), (fn, n)
+
+
+# ---------------------------------------------------------------------------
+# draft-side token choice (DFlash page, inference steps and decode listing;
+# speculative-decoding page, DFlash section: one token sampled per position)
+# ---------------------------------------------------------------------------
+def test_draft_select_greedy_argmax_lowest_index_and_padding():
+    z = np.zeros((2, 3, 6), np.float32)
+    z[0, 0, [2, 4]] = 5.0          # tie: lowest index wins
+    z[0, 1, 5] = 1.0
+    z[0, 2, 0] = -1.0              # all others 0: the first 0 is index 1
+    z[1, 0, 3] = 2.0
+    r = O.draft_select(z, anchor=[7, 9], n_draft=[3, 1])
+    assert r["cand"].tolist() == [[7, 2, 5, 1], [9, 3, -1, -1]]
+    assert r["q_x"].tolist() == [[1.0, 1.0, 1.0], [1.0, 0.0, 0.0]]
+    # row_lse is the log-sum-exp of the raw logits (scipy)
+    np.testing.assert_allclose(r["row_lse"][0], scipy.special.logsumexp(z[0].astype(np.float64), axis=1),
+                               rtol=1e-14)
+    assert r["row_lse"][1, 1] == 0.0
+
+
+def test_draft_select_greedy_matches_numpy_argmax():
+    rng = np.random.default_rng(21)
+    z = rng.normal(size=(3, 5, 257)).astype(np.float32)
+    r = O.draft_select(z, anchor=[1, 2, 3])
+    np.testing.assert_array_equal(r["cand"][:, 1:], np.argmax(z, axis=2))
+
+
+def test_draft_select_sampled_closed_forms():
+    V = 10
+    # uniform logits: C(y) = (y + 1) / V, so y = floor(u V)
+    z = np.zeros((1, 4, V), np.float32)
+    u = np.array([[0.0, 0.05, 0.55, 0.999]], np.float32)
+    r = O.draft_select(z, anchor=[0], u_draft=u, temperature=1.0)
+    assert r["cand"][0, 1:].tolist() == [0, 0, 5, 9]
+    np.testing.assert_allclose(r["q_x"][0], 0.1, rtol=1e-14)
+    np.testing.assert_allclose(r["row_lse"][0], math.log(V), rtol=1e-14)
+    # u exactly on a step (0.3 = C(2)) is flagged; 0.35 is not
+    r2 = O.draft_select(np.zeros((1, 2, V)), anchor=[0], u_draft=np.array([[0.3, 0.35]]), temperature=1.0)
+    assert r2["flags"][0].tolist() == [O.FLAG_CDF_BOUNDARY, 0]
+    # one dominant logit: always that token, q = 1
+    zd = np.zeros((1, 3, V), np.float32)
+    zd[0, :, 6] = 1e4
+    r3 = O.draft_select(zd, anchor=[0], u_draft=np.array([[0.0, 0.5, 0.999999]]), temperature=1.0)
+    assert r3["cand"][0, 1:].tolist() == [6, 6, 6]
+    np.testing.assert_allclose(r3["q_x"][0], 1.0)
+
+
+def test_draft_select_sampled_probabilities_match_library_softmax():
+    rng = np.random.default_rng(22)
+    z = rng.normal(size=(2, 3, 50)) * 3
+    u = rng.random((2, 3))
+    for T in (0.7, 1.0, 2.0):
+        r = O.draft_select(z, anchor=[0, 0], u_draft=u, temperature=T)
+        p = scipy.special.softmax(z / T, axis=2)
+        for b in range(2):
+            for i in range(3):
+                x = r["cand"][b, i + 1]
+                np.testing.assert_allclose(r["q_x"][b, i], p[b, i, x], rtol=1e-12)
+                # x is the inverse-CDF point of u: C(x-1) <= u < C(x)
+                C = np.cumsum(p[b, i])
+                assert (C[x - 1] if x > 0 else 0.0) <= u[b, i] < C[x]
+        np.testing.assert_allclose(r["row_lse"], scipy.special.logsumexp(z / T, axis=2), rtol=1e-13)
+
+
+def test_draft_select_sampled_histogram_is_the_softmax():
+    # Monte Carlo: the draws over many uniforms follow softmax(z / T)
+    rng = np.random.default_rng(23)
+    V, n = 7, 20000
+    z = rng.normal(size=V) * 1.5
+    zz = np.broadcast_to(z, (1, n, V))
+    u = rng.random((1, n))
+    r = O.draft_select(zz, anchor=[0], u_draft=u, temperature=1.3)
+    counts = np.bincount(r["cand"][0, 1:], minlength=V)
+    p = scipy.special.softmax(z / 1.3)
+    stat, pval = scipy.stats.chisquare(counts, p * n)
+    assert pval > 1e-3
