@@ -550,6 +550,17 @@ def report_config(wl, args):
                                 args.steps, args.warmup)
         out["attn_causal_us_per_layer"] = us_causal
         out["attn_causal_frac_hbm"] = gbs(ab, us_causal) / hbm
+        # draft-side token choice over the MASK rows (argmax for greedy
+        # workloads, inverse-CDF sampling otherwise), one pass over B x n_max rows
+        sel = synth.draft_select_batch(wl, seed=0)
+        sel = {k_: v_.to(dev) for k_, v_ in sel.items()}
+        tsel = 0.0 if wl.n_greedy == wl.B else wl.temperature
+        sel_out = api.draft_select(sel["draft_logits"], sel["anchor"], tsel, u_draft=sel["u_draft"])
+        us_sel = _time_calls(lambda: api.draft_select(sel["draft_logits"], sel["anchor"], tsel,
+                                                      u_draft=sel["u_draft"], out=sel_out), args.steps, args.warmup)
+        out["draft_select_mode"] = "argmax" if tsel == 0.0 else f"sampled T={tsel}"
+        out["draft_select_us"] = us_sel
+        out["draft_select_frac_hbm"] = gbs(wl.B * wl.n_max * wl.V * el, us_sel) / hbm
         out["attn_frac_hbm"] = gbs(ab, us_attn) / hbm
         ng = wl.n_greedy
         R = wl.n_draft + 1

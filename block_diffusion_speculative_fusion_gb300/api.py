@@ -67,6 +67,9 @@ _SIGS = {
     "dflash_gate_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GateDims)]),
     "dflash_gate": (ctypes.c_int, [ctypes.POINTER(GateDims), ctypes.c_float, ctypes.c_float, c_p, c_p,
                                    c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_size_t, c_p]),
+    "dflash_draft_select_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
+    "dflash_draft_select": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float, c_p, c_p, c_p, c_p, c_p,
+                                           c_p, c_p, c_p, c_p, ctypes.c_size_t, c_p]),
     "dflash_block_attn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnDims)]),
     "dflash_block_attn": (ctypes.c_int, [ctypes.POINTER(AttnDims), c_p, c_p, c_p, c_p, c_p, c_p, c_p,
                                          ctypes.c_float, c_p, c_p, ctypes.c_size_t, c_p]),
@@ -288,6 +291,38 @@ def gate(draft_logits: torch.Tensor, tokens: torch.Tensor, temperature: float = 
         ctypes.byref(dims), ctypes.c_float(temperature), ctypes.c_float(g), _dev(draft_logits, "draft_logits"),
         _dev(tokens, "tokens", torch.int64, (B, k)), _opt(active, "active", torch.uint8, (B,)),
         _dev(o["c"], "c", torch.float32), _dev(o["cont"], "cont", torch.uint8),
+        _opt(o.get("row_lse"), "row_lse", torch.float32), _opt(o.get("flags"), "flags", torch.uint8),
+        w.data_ptr(), w.numel(), _stream(dev))
+    _check(rc)
+    return o
+
+
+def draft_select(draft_logits: torch.Tensor, anchor: torch.Tensor, temperature: float = 0.0,
+                 u_draft: Optional[torch.Tensor] = None, n_draft: Optional[torch.Tensor] = None,
+                 out: Optional[dict] = None, ws: Optional[torch.Tensor] = None):
+    """Candidates from the draft's MASK-position logits (``dflash_draft_select``):
+    argmax (temperature 0) or one inverse-CDF sample per row with ``u_draft``.
+    Returns cand [B, n_max+1] int64, q_x and row_lse [B, n_max] float32, flags
+    [B, n_max] uint8."""
+    _dev(draft_logits, "draft_logits")
+    B, n_max, V = draft_logits.shape
+    dev = draft_logits.device
+    dims = VerifyDims(B, n_max, V, _dtype_code(draft_logits))
+    o = out if out is not None else {}
+    if "cand" not in o:
+        o["cand"] = torch.empty((B, n_max + 1), dtype=torch.int64, device=dev)
+        o["q_x"] = torch.empty((B, n_max), dtype=torch.float32, device=dev)
+        o["row_lse"] = torch.empty((B, n_max), dtype=torch.float32, device=dev)
+        o["flags"] = torch.empty((B, n_max), dtype=torch.uint8, device=dev)
+    need = lib().dflash_draft_select_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(dev, need)
+    rc = lib().dflash_draft_select(
+        ctypes.byref(dims), ctypes.c_float(temperature), _dev(draft_logits, "draft_logits"),
+        _dev(anchor, "anchor", torch.int64, (B,)), _opt(n_draft, "n_draft", torch.int32, (B,)),
+        _opt(u_draft if temperature > 0 else None, "u_draft", torch.float32, (B, n_max)),
+        _dev(o["cand"], "cand", torch.int64, (B, n_max + 1)), _opt(o.get("q_x"), "q_x", torch.float32),
         _opt(o.get("row_lse"), "row_lse", torch.float32), _opt(o.get("flags"), "flags", torch.uint8),
         w.data_ptr(), w.numel(), _stream(dev))
     _check(rc)

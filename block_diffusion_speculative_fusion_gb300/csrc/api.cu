@@ -229,6 +229,48 @@ int dflash_gate(const dflash_gate_dims* d, float temperature, float g, const voi
   return ok(1);
 }
 
+// ------------------------------------------------------------ draft select ---
+static int check_select_dims(const dflash_verify_dims* d) {
+  if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->n_max < 1 || d->V < 1)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad dims B=%d n_max=%d V=%d", d->B, d->n_max, d->V);
+  if (bad_dtype(d->dtype)) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
+  if ((long)d->B * d->n_max > kMaxCounters)
+    return fail(DFLASH_ERR_UNSUPPORTED, "B*n_max=%ld > %d rows", (long)d->B * d->n_max, kMaxCounters);
+  if (d->V > dflash::kSelMaxVocab) return fail(DFLASH_ERR_UNSUPPORTED, "V=%d too large", d->V);
+  return DFLASH_OK;
+}
+
+size_t dflash_draft_select_workspace_size(const dflash_verify_dims* d) {
+  if (check_select_dims(d) != DFLASH_OK) return 0;
+  return DFLASH_WS_COUNTER_BYTES + dflash::draft_select_ws_bytes(d->B, d->n_max, d->V, d->dtype);
+}
+
+int dflash_draft_select(const dflash_verify_dims* d, float temperature, const void* draft_logits,
+                        const int64_t* anchor, const int32_t* n_draft, const float* u_draft, int64_t* cand,
+                        float* q_x, float* row_lse, uint8_t* flags, void* workspace, size_t ws_bytes,
+                        dflash_stream_t stream) {
+  int rc = check_select_dims(d);
+  if (rc) return rc;
+  if (!(temperature >= 0.f) || !(temperature < 3.0e38f))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be >= 0 and finite");
+  if (!draft_logits || !anchor || !cand) return fail(DFLASH_ERR_INVALID_ARG, "draft_select: a required pointer is NULL");
+  if (temperature > 0.f && !u_draft) return fail(DFLASH_ERR_INVALID_ARG, "draft_select: sampling needs u_draft");
+  rc = check_ws(workspace, ws_bytes, dflash_draft_select_workspace_size(d));
+  if (rc) return rc;
+  dflash::DraftSelectArgs a{};
+  a.B = d->B; a.n_max = d->n_max; a.V = d->V; a.dtype = d->dtype; a.temperature = temperature;
+  a.draft_logits = draft_logits; a.anchor = anchor; a.n_draft = n_draft; a.u_draft = u_draft;
+  a.cand = cand; a.q_x = q_x; a.row_lse = row_lse; a.flags = flags;
+  a.num_sms = kPlanSms;
+  a.counters = (int32_t*)workspace;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = dflash::launch_draft_select(a);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_select launch");
+  return ok(1);
+}
+
 // --------------------------------------------------------------- attention ---
 static int check_attn_dims(const dflash_attn_dims* d) {
   if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");

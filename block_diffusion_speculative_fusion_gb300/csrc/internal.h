@@ -62,6 +62,28 @@ struct GateArgs {
 size_t gate_ws_bytes(int B, int k, int V, int dtype, int num_sms);
 cudaError_t launch_gate(const GateArgs& a, int num_sms);
 
+// Draft-side token choice over the MASK rows (argmax or one inverse-CDF sample
+// per row, with q(x) and the row's log-sum-exp).
+struct DraftSelectArgs {
+  int B, n_max, V, dtype;
+  float temperature;          // 0: argmax
+  const void* draft_logits;   // [B, n_max, V]
+  const int64_t* anchor;      // [B]
+  const int32_t* n_draft;     // [B] or null
+  const float* u_draft;       // [B, n_max] (sampled)
+  int64_t* cand;              // [B, n_max + 1]
+  float* q_x;                 // [B, n_max] or null
+  float* row_lse;             // [B, n_max] or null
+  uint8_t* flags;             // [B, n_max] or null
+  int32_t* counters;          // zeroed region at the workspace start, one per row
+  void* scratch;
+  cudaStream_t stream;
+  int num_sms;                // persistent grid: resident CTAs x SMs
+};
+constexpr int kSelMaxVocab = 1024 * 256 * 32;   // chunks x tokens per chunk (fp32)
+size_t draft_select_ws_bytes(int B, int n_max, int V, int dtype);
+cudaError_t launch_draft_select(const DraftSelectArgs& a);
+
 // ------------------------------------------------------------- attention ---
 struct AttnArgs {
   int B, n_q, n_kv, Hq, Hkv, D, page_size, max_pages, num_pages, max_ctx, dtype;

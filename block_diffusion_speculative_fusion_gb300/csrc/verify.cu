@@ -562,7 +562,7 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
             float* __restrict__ row_lse, uint8_t* __restrict__ flags) {
   const int c = blockIdx.x;
   const int row = blockIdx.y;
-  const int b = row / k, i = row - b * k;
+  const int b = row / k;
   const bool on = active ? active[b] != 0 : true;
   MS ms{-CUDART_INF_F, 0.f};
   const bool need = on || row_lse != nullptr;
@@ -611,6 +611,287 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
     if (flags) flags[b] = (on && fabs(csum - (double)g) < 1e-4) ? 1 : 0;
   }
   reset_ticket(&counters[b]);
+}
+
+// ===========================================================================
+// Draft-side token choice over the MASK rows (DFlash page, inference steps:
+// each MASK position's logits give a draft token, argmax or one sample per
+// position). One CTA per row (persistent over rows): the row streams through
+// two shared-memory stage buffers in chunks of 256 segments of kSelVecs
+// 16-byte vectors; each thread keeps its segment's record (max * k2, sum of
+// 2^(z k2 - max k2)) and the running (max, lowest index). A sampled row then
+// takes one block scan over the records in token order and one warp walk over
+// the chosen segment (inverse CDF, ascending token order).
+// ===========================================================================
+constexpr int kSelVecs = 8;                      // 16-byte vectors per thread and chunk
+constexpr int kSelCtasPerSm = 3;                 // resident CTAs per SM (two 32 KB stage buffers each)
+constexpr int kSelSmem = 2 * kThreads * kSelVecs * 16;
+
+// 16-byte global -> shared copy that bypasses registers (L2 only)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, kSelCtasPerSm)
+draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor, const int32_t* __restrict__ n_draft,
+                    const float* __restrict__ u_draft, int B, int n_max, int V, int nch, float k2, int sampled,
+                    float2* __restrict__ rec, int64_t* __restrict__ cand, float* __restrict__ q_x,
+                    float* __restrict__ row_lse, uint8_t* __restrict__ flags) {
+  constexpr int N = VecTraits<T>::N;
+  constexpr int NV = kSelVecs;
+  constexpr int SEG = NV * N;                      // contiguous tokens per thread and chunk
+  constexpr int CHUNK = kThreads * SEG;            // tokens per chunk
+  constexpr int TPL = SEG / 32;                    // tokens per lane in the segment walk
+  const bool need_sum = sampled || row_lse != nullptr;   // argmax alone needs no exponentials
+  extern __shared__ __align__(16) uint4 sel_smem[];
+  const int tid = threadIdx.x, wid = tid >> 5, l = tid & 31;
+  __shared__ double s_wsum[kThreads / 32];
+  __shared__ double s_Z, s_cbefore;
+  __shared__ int s_j, s_y;
+  __shared__ float s_qx;
+  __shared__ uint8_t s_flag;
+
+  for (int row = blockIdx.x; row < B * n_max; row += gridDim.x) {
+    const int b = row / n_max, i = row - b * n_max;
+    const int nb = n_draft ? min(max(n_draft[b], 0), n_max) : n_max;
+    const size_t crow = (size_t)b * (n_max + 1);
+    if (i == 0 && tid == 0) cand[crow] = anchor[b];
+    if (i >= nb) {   // position not drafted: padding
+      if (tid == 0) {
+        cand[crow + i + 1] = -1;
+        if (q_x) q_x[row] = 0.f;
+        if (row_lse) row_lse[row] = 0.f;
+        if (flags) flags[row] = 0;
+      }
+      continue;
+    }
+    const T* zr = z + (size_t)row * V;
+    float2* rr = rec + (size_t)row * nch * kThreads;
+    const bool aligned = (reinterpret_cast<uintptr_t>(zr) & 15u) == 0;
+    // vector j of chunk c lands at stage[j] (coalesced copies)
+    auto issue = [&](int c, uint4* stage) {
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int j = k * kThreads + tid;
+        const int e = c * CHUNK + j * N;
+        if (aligned && e + N <= V) cp_async16(&stage[j], zr + e);
+        else stage[j] = load_vec_or_pad<T>(zr, e, V);    // -inf past V
+      }
+      cp_async_commit();
+    };
+    VI best{-CUDART_INF_F, INT32_MAX};
+    issue(0, sel_smem);
+    for (int c = 0; c < nch; ++c) {
+      uint4* stage = sel_smem + (c & 1) * (kThreads * NV);
+      if (c + 1 < nch) {
+        issue(c + 1, sel_smem + ((c + 1) & 1) * (kThreads * NV));
+        cp_async_wait_one();
+      } else {
+        cp_async_wait_all();
+      }
+      __syncthreads();
+      // this thread's contiguous segment, its vectors in a rotated order so that
+      // a quarter warp reads distinct banks
+      const int e0 = c * CHUNK + tid * SEG;
+      uint4 vv[NV];
+      float vmax[NV];
+      float tmax = -CUDART_INF_F;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        vv[k] = stage[tid * NV + ((k + tid) & (NV - 1))];
+        vmax[k] = vec_max<T>(vv[k]);
+        tmax = fmaxf(tmax, vmax[k]);
+      }
+      // lowest index of the segment's max, searched only when it can win
+      if (tmax != -CUDART_INF_F && tmax >= best.v) {
+        int ebest = INT32_MAX;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          const int ek = e0 + ((k + tid) & (NV - 1)) * N;
+          if (vmax[k] == tmax && ek < ebest) {
+            float f[N];
+            unpack16<T>(vv[k], f);
+            int q = N - 1;
+#pragma unroll
+            for (int qq = N - 1; qq >= 0; --qq)
+              if (f[qq] == tmax) q = qq;
+            ebest = ek + q;
+          }
+        }
+        if (vi_better(tmax, ebest, best)) best = VI{tmax, ebest};
+      }
+      if (need_sum) {
+        const float mt = tmax * k2;
+        float st = 0.f;
+        if (tmax != -CUDART_INF_F) {
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            float f[N];
+            unpack16<T>(vv[k], f);
+#pragma unroll
+            for (int q = 0; q < N; ++q) st += ex2_ftz(fmaf(f[q], k2, -mt));
+          }
+        }
+        rr[c * kThreads + tid] = make_float2(mt, st);
+      }
+      __syncthreads();   // stage c is refilled by chunk c + 2
+    }
+    // ---- the row's max and its lowest index ----
+    const VI rb = block_vi(best);
+    __shared__ VI s_best;
+    if (tid == 0) s_best = rb;
+    __syncthreads();
+    const VI arg = s_best;
+    const float m2M = arg.v * k2;
+    if (!need_sum) {
+      if (tid == 0) {
+        cand[crow + i + 1] = arg.i;
+        if (q_x) q_x[row] = 1.f;
+        if (flags) flags[row] = 0;
+      }
+      continue;
+    }
+    // ---- records in token order: thread t holds records t*nch .. t*nch + nch - 1
+    // (record j = chunk j / 256, segment j % 256), weights in row units ----
+    double loc = 0.0;
+    for (int r = 0; r < nch; ++r) {
+      const int j = tid * nch + r;
+      const float2 w2 = rr[(j / kThreads) * kThreads + (j % kThreads)];
+      if (w2.x != -CUDART_INF_F) loc += (double)w2.y * (double)exp2f(w2.x - m2M);
+    }
+    double inc = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double x = __shfl_up_sync(0xffffffffu, inc, o);
+      if (l >= o) inc += x;
+    }
+    if (l == 31) s_wsum[wid] = inc;
+    if (tid == 0) { s_j = -1; s_y = -1; }
+    __syncthreads();
+    double base = 0.0, Z = 0.0;
+    for (int q = 0; q < kThreads / 32; ++q) {
+      if (q < wid) base += s_wsum[q];
+      Z += s_wsum[q];
+    }
+    if (tid == 0) {
+      s_Z = Z;
+      if (row_lse) row_lse[row] = (float)(((double)m2M + log2(Z)) * 0.6931471805599453);
+    }
+    if (!sampled) {
+      if (tid == 0) {
+        cand[crow + i + 1] = arg.i;
+        if (q_x) q_x[row] = 1.f;
+        if (flags) flags[row] = 0;
+      }
+      __syncthreads();
+      continue;
+    }
+    const double u = (double)u_draft[row];
+    const double target = u * Z;
+    const double excl = base + inc - loc;
+    if (loc > 0.0 && excl <= target && excl + loc > target) {
+      // the crossing record is one of this thread's: walk them in order
+      double cum = excl;
+      int jsel = tid * nch + nch - 1;
+      for (int r = 0; r < nch; ++r) {
+        const int j = tid * nch + r;
+        const float2 w2 = rr[(j / kThreads) * kThreads + (j % kThreads)];
+        const double w = w2.x == -CUDART_INF_F ? 0.0 : (double)w2.y * (double)exp2f(w2.x - m2M);
+        if (w > 0.0 && cum + w > target) { jsel = j; break; }
+        cum += w;
+      }
+      s_j = jsel;
+      s_cbefore = cum;
+    }
+    __syncthreads();
+    if (wid == 0) {
+      int j = s_j;
+      const bool found = j >= 0;
+      double cbefore = s_cbefore;
+      if (!found) j = nch * kThreads - 1;     // rounding: resolved below to the last token with weight
+      const int cj = j / kThreads, tj = j % kThreads;
+      const float2 w2 = rr[cj * kThreads + tj];
+      const float mt = w2.x;
+      const double f = mt == -CUDART_INF_F ? 0.0 : (double)exp2f(mt - m2M);   // segment units -> row units
+      const int es = cj * CHUNK + tj * SEG;
+      float w[TPL];
+      float lsum = 0.f;
+#pragma unroll
+      for (int q = 0; q < TPL; ++q) {
+        const int e = es + TPL * l + q;
+        w[q] = (e < V && mt != -CUDART_INF_F) ? ex2_ftz(fmaf(to_f32(zr[e]), k2, -mt)) : 0.f;
+        lsum += w[q];
+      }
+      float incw = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float x = __shfl_up_sync(0xffffffffu, incw, o);
+        if (l >= o) incw += x;
+      }
+      const float rel = found ? (float)((target - cbefore) / f) : 0.f;
+      const float ex = incw - lsum;
+      int yl = INT32_MAX;
+      float run_sel = 0.f, wy = 0.f;
+      if (found && ex <= rel && incw > rel) {
+        float run = ex;
+        bool done = false;
+#pragma unroll
+        for (int q = 0; q < TPL; ++q) {
+          if (!done && (q == TPL - 1 || run + w[q] > rel)) {
+            yl = es + TPL * l + q;
+            run_sel = run;
+            wy = w[q];
+            done = true;
+          }
+          run += w[q];
+        }
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, yl != INT32_MAX);
+      if (hit) {
+        if (l == __ffs(hit) - 1) {
+          const double c_lo = (cbefore + f * (double)run_sel) / Z, c_hi = (cbefore + f * (double)(run_sel + wy)) / Z;
+          s_y = yl;
+          s_qx = (float)((double)wy * f / Z);
+          s_flag = (fabs(c_lo - u) < 1e-6 || fabs(c_hi - u) < 1e-6) ? 2 : 0;   // CDF_BOUNDARY
+        }
+      } else if (l == 0) {
+        s_y = -1;   // the target lies past every step (rounding)
+      }
+    }
+    __syncthreads();
+    if (s_y < 0) {
+      // rounding put the target past the last step: the last token with weight,
+      // found by a block-wide search from the end of the row
+      __shared__ int s_last;
+      if (tid == 0) s_last = -1;
+      __syncthreads();
+      for (int top = V - 1; top >= 0; top -= kThreads) {
+        const int e = top - tid;
+        const bool wt = e >= 0 && ex2_ftz(fmaf(to_f32(zr[e]), k2, -m2M)) > 0.f;
+        if (wt) atomicMax(&s_last, e);
+        if (__syncthreads_or(wt)) break;
+      }
+      if (tid == 0) {
+        const int y = s_last >= 0 ? s_last : arg.i;
+        s_y = y;
+        s_qx = (float)((double)ex2_ftz(fmaf(to_f32(zr[y]), k2, -m2M)) / s_Z);
+        s_flag = 2;
+      }
+      __syncthreads();
+    }
+    if (tid == 0) {
+      cand[crow + i + 1] = s_y;
+      if (q_x) q_x[row] = s_qx;
+      if (flags) flags[row] = s_flag;
+    }
+    __syncthreads();
+  }
 }
 
 // ===========================================================================
@@ -707,6 +988,37 @@ static cudaError_t launch_sample_t(const VerifyArgs& a, int num_sms) {
 
 cudaError_t launch_verify_sample(const VerifyArgs& a, int num_sms) {
   return a.dtype == 0 ? launch_sample_t<float>(a, num_sms) : launch_sample_t<bf16>(a, num_sms);
+}
+
+static int sel_chunk(int dtype) { return kThreads * kSelVecs * vec_elems(dtype); }
+
+size_t draft_select_ws_bytes(int B, int n_max, int V, int dtype) {
+  const size_t rows = (size_t)B * n_max;
+  const int nch = (V + sel_chunk(dtype) - 1) / sel_chunk(dtype);
+  return align_up(rows * nch * kThreads * sizeof(float2));
+}
+
+template <typename T>
+static cudaError_t launch_draft_select_t(const DraftSelectArgs& a) {
+  const int nch = (a.V + sel_chunk(a.dtype) - 1) / sel_chunk(a.dtype);
+  const long rows = (long)a.B * a.n_max;
+  const bool sampled = a.temperature > 0.f;
+  const float k2 = kLog2e / (sampled ? a.temperature : 1.f);
+  static bool smem_set = false;
+  if (!smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(draft_select_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+    if (e != cudaSuccess) return e;
+    smem_set = true;
+  }
+  const int grid = (int)std::min<long>(rows, (long)kSelCtasPerSm * a.num_sms);
+  draft_select_kernel<T><<<grid, kThreads, kSelSmem, a.stream>>>(
+      (const T*)a.draft_logits, a.anchor, a.n_draft, a.u_draft, a.B, a.n_max, a.V, nch, k2, sampled ? 1 : 0,
+      (float2*)a.scratch, a.cand, a.q_x, a.row_lse, a.flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_select(const DraftSelectArgs& a) {
+  return a.dtype == 0 ? launch_draft_select_t<float>(a) : launch_draft_select_t<bf16>(a);
 }
 
 template <typename T>

@@ -220,6 +220,25 @@ def verify_batch(wl: Workload, seed: int = 0, sigma: Optional[float] = None,
     }
 
 
+def draft_select_batch(wl: Workload, seed: int = 0, B: Optional[int] = None, n_max: Optional[int] = None,
+                       ragged: bool = False) -> Dict[str, torch.Tensor]:
+    """One draft-side token choice problem: the draft's MASK-position logits
+    [B, n_max, V] (same law as the verify's draft rows), the anchor [B], one
+    uniform per MASK position [B, n_max] and n_draft [B] (all n_max unless
+    ragged)."""
+    B = wl.B if B is None else B
+    n = wl.n_max if n_max is None else n_max
+    zd = draft_logits(wl, n, seed, "sel_zd", B=B)
+    n_draft = (_randint(0, n, (B,), seed, "sel_n").to(torch.int32) if ragged
+               else torch.full((B,), n, dtype=torch.int32))
+    return {
+        "draft_logits": zd.contiguous(),
+        "anchor": torch.randint(0, wl.V, (B,), generator=_gen(seed, "sel_anchor")),
+        "u_draft": _rand((B, n), seed, "sel_u"),
+        "n_draft": n_draft,
+    }
+
+
 def gate_batch(wl: Workload, stage: int, seed: int = 0, B: Optional[int] = None) -> Dict[str, torch.Tensor]:
     """One DLoop gate problem for draft stage ``stage``: draft logits [B, k, V] of
     the stage's k drafted tokens, the tokens drawn from softmax(logits / T), and

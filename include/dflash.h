@@ -289,6 +289,33 @@ int dflash_gate(const dflash_gate_dims* dims, float temperature, float g,
                 void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* Draft-side token choice                                                    */
+/* ------------------------------------------------------------------------- */
+/*
+ * The candidates of one round from the draft's MASK-position logits:
+ *   [DFlash] 推理流程 step 4 and its decode listing: draft token i is the argmax
+ *   of MASK position i's logits; [SpecDec] DFlash section: one token sampled
+ *   from each position's distribution; candidates = [anchor] + draft tokens.
+ * dims: B, n_max (MASK positions per sequence), V, dtype (dflash_verify_dims).
+ * draft_logits [B, n_max, V] (row i <-> draft position i + 1); anchor [B] int64;
+ * n_draft [B] int32 in [0, n_max] or NULL (n_max everywhere).
+ * temperature == 0: argmax (lowest index among ties); q_x = 1; row_lse = LSE(z).
+ * temperature > 0: x ~ softmax(z / T) by inverse CDF with u_draft[b, i] in
+ *   ascending token order (smallest y with C(y) > u * Z); q_x = softmax(z / T)[x];
+ *   row_lse = LSE(z / T); flags[b, i] = DFLASH_FLAG_CDF_BOUNDARY when u lies
+ *   within 1e-6 of C(y-1)/Z or C(y)/Z as the kernel evaluates them.
+ * u_draft [B, n_max] float (required when temperature > 0, else ignored).
+ * Outputs: cand [B, n_max+1] int64 (cand[:, 0] = anchor, -1 past n_b);
+ *   q_x, row_lse [B, n_max] float or NULL (0 past n_b); flags [B, n_max] uint8
+ *   or NULL. Rows: B * n_max <= 4095; V <= 8388608.
+ */
+size_t dflash_draft_select_workspace_size(const dflash_verify_dims* dims);
+int dflash_draft_select(const dflash_verify_dims* dims, float temperature,
+                        const void* draft_logits, const int64_t* anchor, const int32_t* n_draft,
+                        const float* u_draft, int64_t* cand, float* q_x, float* row_lse,
+                        uint8_t* flags, void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------- */
 /* Message of the last error on this thread ("" if none). */

@@ -65,6 +65,27 @@ def test_attention_causal_flag_checked_on_host(L):
     assert L.dflash_block_attn_workspace_size(ctypes.byref(short0)) > api.WS_COUNTER_BYTES
 
 
+def test_draft_select_checks_on_host(L):
+    d = api.VerifyDims(64, 16, 128256, api.BF16)
+    assert L.dflash_draft_select_workspace_size(ctypes.byref(d)) > api.WS_COUNTER_BYTES
+    big = api.VerifyDims(512, 16, 128256, api.BF16)       # 8192 rows > one counter each
+    assert L.dflash_draft_select_workspace_size(ctypes.byref(big)) == 0
+    assert "rows" in api.last_error()
+    p = [ctypes.c_void_p(0x1000 + 256 * i) for i in range(8)]
+    ws = ctypes.c_void_p(0x100000)
+    need = L.dflash_draft_select_workspace_size(ctypes.byref(d))
+    # sampling without uniforms, a negative temperature, a missing output: rejected before any launch
+    rc = L.dflash_draft_select(ctypes.byref(d), ctypes.c_float(1.0), p[0], p[1], None, None, p[2], None, None,
+                               None, ws, need, None)
+    assert rc == api.ERR_INVALID_ARG and "u_draft" in api.last_error()
+    rc = L.dflash_draft_select(ctypes.byref(d), ctypes.c_float(-1.0), p[0], p[1], None, p[3], p[2], None, None,
+                               None, ws, need, None)
+    assert rc == api.ERR_INVALID_ARG and "temperature" in api.last_error()
+    rc = L.dflash_draft_select(ctypes.byref(d), ctypes.c_float(0.0), p[0], p[1], None, None, None, None, None,
+                               None, ws, need, None)
+    assert rc == api.ERR_INVALID_ARG
+
+
 def _p(x):
     return ctypes.c_void_p(x)
 
