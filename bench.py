@@ -606,6 +606,16 @@ def report_config(wl, args):
         out["verify_sample_us"] = us_v
         out["verify_sample_frac_hbm"] = gbs(wl.B * (2 * n + 1 + 2) * wl.V * el, us_v) / hbm
         out["looped_step_us_all_stages"] = total_us + us_v
+        # the same verify fed with the gates' row LSEs: the draft rows are not streamed
+        gl = api.gate(vb["draft_logits"], vb["cand"][:, 1:].contiguous(), wl.temperature, wl.gate_g,
+                      want_row_lse=True)
+        lse = gl["row_lse"]
+        us_vl = _time_calls(lambda: api.verify_sample(vb["target_logits"], vb["draft_logits"], vb["cand"],
+                                                      vb["u_acc"], vb["u_final"], wl.temperature, vb["n_draft"],
+                                                      draft_row_lse=lse), args.steps, args.warmup)
+        out["verify_sample_gate_lse_us"] = us_vl
+        out["verify_sample_gate_lse_frac_hbm"] = gbs(wl.B * (n + 1 + 2) * wl.V * el, us_vl) / hbm
+        out["looped_step_us_all_stages_gate_lse"] = total_us + us_vl
     if wl.dtype == "bf16" and wl.stages == 1 and wl.ctx_lo == wl.ctx_hi:
         # ---- prefill-sized materialisation: every context row of every sequence ----
         rows = wl.ctx_lo

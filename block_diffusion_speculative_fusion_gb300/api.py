@@ -67,6 +67,10 @@ _SIGS = {
     "dflash_gate_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GateDims)]),
     "dflash_gate": (ctypes.c_int, [ctypes.POINTER(GateDims), ctypes.c_float, ctypes.c_float, c_p, c_p,
                                    c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_size_t, c_p]),
+    # dims, T, target, draft, draft_row_lse, cand, n_draft, u_accept, u_final, accept_len, bonus,
+    # commit_len, out_tokens, flags, probs, workspace, ws_bytes, stream
+    "dflash_verify_sample_lse": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float] + [c_p] * 14 +
+                                 [ctypes.c_size_t, c_p]),
     "dflash_draft_select_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
     "dflash_draft_select": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float, c_p, c_p, c_p, c_p, c_p,
                                            c_p, c_p, c_p, c_p, ctypes.c_size_t, c_p]),
@@ -230,9 +234,13 @@ def verify_greedy_noalloc(target_logits: torch.Tensor, cand: torch.Tensor, n_dra
 def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor, cand: torch.Tensor,
                   u_accept: torch.Tensor, u_final: torch.Tensor, temperature: float = 1.0,
                   n_draft: Optional[torch.Tensor] = None, want_probs: bool = False,
-                  out: Optional[dict] = None, ws: Optional[torch.Tensor] = None):
+                  out: Optional[dict] = None, ws: Optional[torch.Tensor] = None,
+                  draft_row_lse: Optional[torch.Tensor] = None):
     """Sampled accept rule with residual resample (``dflash_verify_sample``).
-    Returns accept_len, bonus, commit_len, out_tokens, flags[, probs]."""
+    With ``draft_row_lse`` [B, n_max] (LSE(draft row / T), e.g. the DLoop
+    gates' row_lse) the draft rows are not streamed
+    (``dflash_verify_sample_lse``). Returns accept_len, bonus, commit_len,
+    out_tokens, flags[, probs]."""
     _dev(target_logits, "target_logits")
     B, R, V = target_logits.shape
     n_max = R - 1
@@ -253,9 +261,15 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor, cand:
     if need == 0:
         raise DflashError(ERR_INVALID_ARG, last_error())
     w = ws if ws is not None else workspace(dev, need)
-    rc = lib().dflash_verify_sample(
-        ctypes.byref(dims), ctypes.c_float(temperature), _dev(target_logits, "target_logits"),
-        _dev(draft_logits, "draft_logits", None, (B, n_max, V)), _dev(cand, "cand", torch.int64, (B, R)),
+    head = [ctypes.byref(dims), ctypes.c_float(temperature), _dev(target_logits, "target_logits"),
+            _dev(draft_logits, "draft_logits", None, (B, n_max, V))]
+    if draft_row_lse is not None:
+        fn = lib().dflash_verify_sample_lse
+        head.append(_dev(draft_row_lse, "draft_row_lse", torch.float32, (B, n_max)))
+    else:
+        fn = lib().dflash_verify_sample
+    rc = fn(
+        *head, _dev(cand, "cand", torch.int64, (B, R)),
         _opt(n_draft, "n_draft", torch.int32, (B,)), _dev(u_accept, "u_accept", torch.float32, (B, n_max)),
         _dev(u_final, "u_final", torch.float32, (B,)),
         _dev(o["accept_len"], "accept_len", torch.int32), _dev(o["bonus"], "bonus", torch.int64),

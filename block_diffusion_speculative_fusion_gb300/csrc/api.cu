@@ -191,6 +191,35 @@ int dflash_verify_sample(const dflash_verify_dims* d, float temperature, const v
   return ok(2);
 }
 
+int dflash_verify_sample_lse(const dflash_verify_dims* d, float temperature, const void* target_logits,
+                             const void* draft_logits, const float* draft_row_lse, const int64_t* cand,
+                             const int32_t* n_draft, const float* u_accept, const float* u_final,
+                             int32_t* accept_len, int64_t* bonus, int32_t* commit_len, int64_t* out_tokens,
+                             uint8_t* flags, float* probs, void* workspace, size_t ws_bytes,
+                             dflash_stream_t stream) {
+  int rc = check_verify_dims(d, true);
+  if (rc) return rc;
+  if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
+  if (!target_logits || !cand || !u_final || !accept_len || !bonus || !commit_len ||
+      (d->n_max > 0 && (!draft_logits || !u_accept || !draft_row_lse)))
+    return fail(DFLASH_ERR_INVALID_ARG, "verify_sample_lse: a required pointer is NULL");
+  rc = check_ws(workspace, ws_bytes, dflash_verify_sample_workspace_size(d));
+  if (rc) return rc;
+  dflash::VerifyArgs a{};
+  a.B = d->B; a.n_max = d->n_max; a.V = d->V; a.dtype = d->dtype; a.temperature = temperature;
+  a.target_logits = target_logits; a.draft_logits = draft_logits; a.cand = cand;
+  a.n_draft = n_draft; a.u_accept = u_accept; a.u_final = u_final;
+  a.draft_lse = d->n_max > 0 ? draft_row_lse : nullptr;
+  a.accept_len = accept_len; a.bonus = bonus; a.commit_len = commit_len;
+  a.out_tokens = out_tokens; a.flags = flags; a.probs = probs;
+  a.counters = (int32_t*)workspace;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = dflash::launch_verify_sample(a, kPlanSms);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_sample_lse launch");
+  return ok(2);
+}
+
 // -------------------------------------------------------------------- gate ---
 static int check_gate_dims(const dflash_gate_dims* d) {
   if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");

@@ -26,6 +26,7 @@ struct VerifyArgs {
   const int32_t* n_draft;
   const float* u_accept;
   const float* u_final;
+  const float* draft_lse;   // [B, n_max] LSE(draft row / T), or null (streamed)
   int32_t* accept_len;
   int64_t* bonus;
   int32_t* commit_len;

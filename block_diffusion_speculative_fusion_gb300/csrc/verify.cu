@@ -442,7 +442,7 @@ sample_draw_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const flo
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
+sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const float* __restrict__ draft_lse,
                     const int64_t* __restrict__ cand, const int32_t* __restrict__ n_draft,
                     const float* __restrict__ u_acc, int n_max, int V, int nch, int chunk,
                     float k2, MS* __restrict__ parts, float* __restrict__ zx,
@@ -451,8 +451,10 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
                     int64_t* __restrict__ out_tokens, float* __restrict__ probs) {
   const int R = n_max + 1;
   const int RR = R + n_max;              // target rows then draft rows of a sequence
+  // with the draft rows' log-sum-exps supplied, only the target rows stream
+  const int RS = draft_lse ? R : RR;
   const int c = blockIdx.x;
-  const int b = blockIdx.y / RR, r = blockIdx.y - b * RR;
+  const int b = blockIdx.y / RS, r = blockIdx.y - b * RS;
   const int nb = n_draft ? n_draft[b] : n_max;
   const bool is_t = r < R;
   const int ri = is_t ? r : r - R;       // row index within its tensor
@@ -468,12 +470,22 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
     }
   }
   if (threadIdx.x == 0) parts[((size_t)b * RR + r) * nch + c] = ms;
-  if (!take_ticket_is_last_t0(&counters[b], RR * nch)) return;
+  if (!take_ticket_is_last_t0(&counters[b], RS * nch)) return;
 
   // ---- last CTA of sequence b ----
   __shared__ MS rs[2 * kMaxRows];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  for (int rr = w; rr < RR; rr += blockDim.x >> 5) {
+  if (draft_lse) {
+    // draft row i: log2 of sum 2^(z k2) is LSE(z / T) * log2(e); as a (max, sum)
+    // pair that is (lse2, 1), and q(x) = 2^(z_x k2 - lse2)
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+      rs[R + i] = MS{draft_lse[(size_t)b * n_max + i] * kLog2e, 1.f};
+      const int64_t x = cand[(size_t)b * R + i + 1];
+      zx[(size_t)b * RR + R + i] = (x >= 0 && x < V) ? ld_scalar(zd + ((size_t)b * n_max + i) * V + x)
+                                                      : -CUDART_INF_F;
+    }
+  }
+  for (int rr = w; rr < RS; rr += blockDim.x >> 5) {
     const bool t = rr < R;
     const int rix = t ? rr : rr - R;
     if (t ? rix > nb : rix >= nb) continue;
@@ -495,7 +507,7 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd,
     for (int i = 1; i <= nb; ++i) {
       const MS pt = rs[i - 1], pd = rs[R + i - 1];
       const float zxt = __ldcg(zx + (size_t)b * RR + (i - 1));
-      const float zxd = __ldcg(zx + (size_t)b * RR + R + (i - 1));
+      const float zxd = zx[(size_t)b * RR + R + (i - 1)];
       // exponents formed exactly as in the row sums
       const float at = fmaf(zxt, k2, -pt.m), ad = fmaf(zxd, k2, -pd.m);
       const float et = exp2f(at), ed = exp2f(ad);
@@ -972,9 +984,9 @@ static cudaError_t launch_sample_t(const VerifyArgs& a, int num_sms) {
   ws += align_up((size_t)a.B * nch2 * sizeof(float2));
   float2* dsegs = (float2*)ws;
   const float k2 = kLog2e / a.temperature;
-  dim3 g1(p.nch, a.B * RR);
+  dim3 g1(p.nch, a.B * (a.draft_lse ? R : RR));
   sample_stats_kernel<T><<<g1, kThreads, 0, a.stream>>>(
-      (const T*)a.target_logits, (const T*)a.draft_logits, a.cand, a.n_draft, a.u_accept,
+      (const T*)a.target_logits, (const T*)a.draft_logits, a.draft_lse, a.cand, a.n_draft, a.u_accept,
       a.n_max, a.V, p.nch, p.chunk, k2, parts, zx, a.counters, jobs, a.accept_len, a.commit_len,
       a.out_tokens, a.probs);
   cudaError_t e = cudaGetLastError();

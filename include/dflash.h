@@ -264,6 +264,29 @@ int dflash_verify_sample(const dflash_verify_dims* dims, float temperature,
                          int64_t* out_tokens, uint8_t* flags, float* probs,
                          void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
+/*
+ * dflash_verify_sample with the draft rows' log-sum-exps supplied instead of
+ * streamed. In [DLoop] 机制一 the gate score comes from the draft logits each
+ * stage already produced, and the stage's dflash_gate call (row_lse) leaves
+ * LSE(draft_logits[b, i] / T) for every row of the stage; the looped verify
+ * over the stages' concatenated rows then reads only the target rows, one
+ * draft logit per candidate and, for the bonus draw, the draft row at the
+ * rejected position.
+ * draft_row_lse [B, n_max] float: LSE(draft_logits[b, i] / T) in natural-log
+ *   units (entries i >= n_b are not read). Every other argument and output as
+ *   dflash_verify_sample; the workspace size is dflash_verify_sample's.
+ * Same rule and same results as dflash_verify_sample whenever draft_row_lse
+ * holds the rows' log-sum-exps (up to their float rounding, which the
+ * boundary flags cover).
+ */
+int dflash_verify_sample_lse(const dflash_verify_dims* dims, float temperature,
+                             const void* target_logits, const void* draft_logits,
+                             const float* draft_row_lse, const int64_t* cand,
+                             const int32_t* n_draft, const float* u_accept, const float* u_final,
+                             int32_t* accept_len, int64_t* bonus, int32_t* commit_len,
+                             int64_t* out_tokens, uint8_t* flags, float* probs,
+                             void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* DLoop block gate                                                           */
 /* ------------------------------------------------------------------------- */

@@ -107,13 +107,13 @@ def test_greedy_odd_vocab_unaligned_rows():
 # ---------------------------------------------------------------------------
 # sampled
 # ---------------------------------------------------------------------------
-def _check_sample(vb, temperature=1.0, max_flag_frac=0.5, probs_rtol=None):
+def _check_sample(vb, temperature=1.0, max_flag_frac=0.5, probs_rtol=None, draft_row_lse=None):
     """A residual spread over ~1e5 tokens has CDF steps of ~1e-5, so the 1e-6
     boundary band flags a visible share of draws; flagged sequences are valid
     draws that are reported, not compared (spec rule)."""
     g = gpu(vb)
     out = api.verify_sample(g["target_logits"], g["draft_logits"], g["cand"], g["u_acc"], g["u_final"],
-                            temperature, g["n_draft"], want_probs=True)
+                            temperature, g["n_draft"], want_probs=True, draft_row_lse=draft_row_lse)
     torch.cuda.synchronize()
     ref = O.verify_sample(f64(vb["target_logits"]), f64(vb["draft_logits"]), npy(vb["cand"]),
                           npy(vb["n_draft"]), npy(vb["u_acc"]), npy(vb["u_final"]), temperature)
@@ -314,3 +314,43 @@ def test_gate_uniform_logits_closed_form_on_gpu():
     out = api.gate(z, tok, 1.0, -0.5, want_row_lse=True)
     np.testing.assert_allclose(npy(out["c"]), -k * math.log(V), rtol=1e-6)
     assert torch.all(out["cont"] == 0)
+
+
+# ---- sampled rule fed with the draft rows' log-sum-exps (DLoop: the gates'
+# row LSEs) instead of streaming the draft rows ----
+def _exact_row_lse(vb, temperature):
+    z = f64(vb["draft_logits"]) / temperature
+    m = z.max(axis=2, keepdims=True)
+    return torch.from_numpy((m[..., 0] + np.log(np.exp(z - m).sum(axis=2))).astype(np.float32)).to(DEV)
+
+
+def test_sample_lse_tiny_f32_probs():
+    vb = synth.verify_batch(W.TINY_F32, seed=0, greedy_rows=0)
+    _check_sample(vb, probs_rtol=1e-5, draft_row_lse=_exact_row_lse(vb, 1.0))
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_sample_lse_from_gate_dloop_concatenated(temperature):
+    # the gate over the concatenated draft rows (what the stages' gate calls
+    # produce) supplies the row LSEs of the looped verify
+    wl = W.DLOOP_QWEN3_4B
+    vb = synth.verify_batch(wl, seed=1, B=8, ragged=True)
+    g = gpu(vb)
+    gt = api.gate(g["draft_logits"], g["cand"][:, 1:].contiguous(), temperature, -0.5, want_row_lse=True)
+    _check_sample(vb, temperature=temperature, draft_row_lse=gt["row_lse"])
+
+
+def test_sample_lse_matches_streamed_rule_llama8b_b32():
+    vb = synth.verify_batch(W.LLAMA8B_B64, seed=2, B=32, greedy_rows=0)
+    g = gpu(vb)
+    a = api.verify_sample(g["target_logits"], g["draft_logits"], g["cand"], g["u_acc"], g["u_final"], 1.0,
+                          g["n_draft"])
+    a = {k: v.clone() for k, v in a.items()}
+    gt = api.gate(g["draft_logits"], g["cand"][:, 1:].contiguous(), 1.0, -0.5, want_row_lse=True)
+    b = api.verify_sample(g["target_logits"], g["draft_logits"], g["cand"], g["u_acc"], g["u_final"], 1.0,
+                          g["n_draft"], draft_row_lse=gt["row_lse"])
+    torch.cuda.synchronize()
+    ok = (npy(a["flags"]) == 0) & (npy(b["flags"]) == 0)
+    for key in ("accept_len", "bonus", "commit_len", "out_tokens"):
+        np.testing.assert_array_equal(npy(a[key])[ok], npy(b[key])[ok], err_msg=key)
+    assert ok.mean() > 0.5
