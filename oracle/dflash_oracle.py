@@ -427,3 +427,130 @@ def dloop_stage_count(conts):
                 out[b] = s + 1
                 break
     return out
+
+
+# ---------------------------------------------------------------------------
+# DDTree: draft tree from the per-position marginals, greedy tree walk
+# ([SpecDec] section 6: 6.1 tree shape, 6.2 node budget, 6.3 best-first heap,
+# 6.5 greedy walk)
+# ---------------------------------------------------------------------------
+FLAG_TREE_TIE = 1     # two candidates within 1e-5 in log-probability decided a pop
+
+
+def ddtree_topk(draft_logits, K, temperature=1.0):
+    """[SpecDec] 6.1: the K most probable tokens of every drafted position.
+
+    draft_logits [B, n, V] (row i <-> position i + 1). Returns tok [B, n, K]
+    int64 sorted by probability (ties: lower token index first) and logp
+    [B, n, K] = log softmax(z / T) at those tokens, float64.
+    """
+    z = _f64(draft_logits) / temperature
+    B, n, V = z.shape
+    mx = z.max(axis=2, keepdims=True)
+    lse = mx + np.log(np.exp(z - mx).sum(axis=2, keepdims=True))
+    tok = np.zeros((B, n, K), dtype=np.int64)
+    logp = np.zeros((B, n, K))
+    for b in range(B):
+        for i in range(n):
+            order = np.lexsort((np.arange(V), -z[b, i]))[:K]   # value desc, then index asc
+            tok[b, i] = order
+            logp[b, i] = z[b, i, order] - lse[b, i, 0]
+    return tok, logp
+
+
+def ddtree_build(tok, logp, budget):
+    """[SpecDec] 6.3 best-first heap, taken step by step: the root's candidate
+    children (the position-1 top-K) go on a heap ordered by path probability;
+    each step pops the most probable candidate into the tree and pushes its
+    children (the next position's top-K, path log-probability = parent's +
+    the child's); stop when the tree holds ``budget`` nodes (the root, the
+    already verified anchor, takes no slot) or the heap is empty. A path's
+    probability is the product of the per-position marginals (6.3).
+
+    Ties (reading; the pages do not order equal probabilities): the candidate
+    with the smaller depth, then the earlier-popped parent (the root first),
+    then the lower rank among its siblings pops first. A pop decided by a gap
+    below 1e-5 in log-probability flags the sequence.
+
+    tok [B, n, K], logp [B, n, K]. Returns node_token, node_parent (index of
+    the parent node, -1 = root), node_depth (1-based position), node_rank
+    [B, budget] int (-1 past n_nodes), node_logp [B, budget] float64, n_nodes
+    [B], flags [B]. Nodes are in pop order, so every parent precedes its
+    children.
+    """
+    import heapq
+    tok = np.asarray(tok)
+    logp = _f64(logp)
+    B, n, K = tok.shape
+    node_token = np.full((B, budget), -1, dtype=np.int64)
+    node_parent = np.full((B, budget), -1, dtype=np.int32)
+    node_depth = np.full((B, budget), -1, dtype=np.int32)
+    node_rank = np.full((B, budget), -1, dtype=np.int32)
+    node_logp = np.zeros((B, budget))
+    n_nodes = np.zeros(B, dtype=np.int32)
+    flags = np.zeros(B, dtype=np.uint8)
+    for b in range(B):
+        # entry: (-path logp, depth, parent pop index (-1 = root), rank)
+        heap = [(-logp[b, 0, r], 1, -1, r) for r in range(K)] if n > 0 else []
+        heapq.heapify(heap)
+        cnt = 0
+        while heap and cnt < budget:
+            neg, d, par, r = heapq.heappop(heap)
+            if heap and abs(heap[0][0] - neg) < 1e-5 and (heap[0][1], heap[0][2], heap[0][3]) != (d, par, r):
+                flags[b] = FLAG_TREE_TIE
+            node_token[b, cnt] = tok[b, d - 1, r]
+            node_parent[b, cnt] = par
+            node_depth[b, cnt] = d
+            node_rank[b, cnt] = r
+            node_logp[b, cnt] = -neg
+            if d < n:
+                for rc in range(K):
+                    heapq.heappush(heap, (neg - logp[b, d, rc], d + 1, cnt, rc))
+            cnt += 1
+        n_nodes[b] = cnt
+    return dict(node_token=node_token, node_parent=node_parent, node_depth=node_depth, node_rank=node_rank,
+                node_logp=node_logp, n_nodes=n_nodes, flags=flags)
+
+
+def ddtree_walk_greedy(target_logits, node_token, node_parent, n_nodes):
+    """[SpecDec] 6.5 greedy tree walk with the greedy accept rule ([SGLang] 3):
+    start at the root; at the current node (row 0 for the root, row 1 + j for
+    node j: the target's distribution after the path to that node) the target
+    predicts argmax of that row (lowest index on ties); the child holding that
+    token is accepted and becomes the current node (siblings hold distinct
+    tokens, so there is at most one); stop when no child holds it. The bonus is
+    the prediction at the last accepted node.
+
+    target_logits [B, 1 + budget, V]; node_token, node_parent [B, budget];
+    n_nodes [B]. Returns accept_len [B] (accepted nodes), commit_len =
+    accept_len + 1, bonus [B], path [B, n_path_max] node indices (-1 padded),
+    out_tokens [B, budget + 1] (accepted tokens then the bonus, -1 padded).
+    """
+    z = _f64(target_logits)
+    B, R, V = z.shape
+    budget = R - 1
+    acc = np.zeros(B, dtype=np.int32)
+    bonus = np.zeros(B, dtype=np.int64)
+    path = np.full((B, budget), -1, dtype=np.int32)
+    out_tokens = np.full((B, budget + 1), -1, dtype=np.int64)
+    for b in range(B):
+        cur = -1            # the root
+        a = 0
+        while True:
+            row = 0 if cur < 0 else 1 + cur
+            tp = int(np.argmax(z[b, row]))
+            nxt = -1
+            for j in range(int(n_nodes[b])):
+                if node_parent[b, j] == cur and node_token[b, j] == tp:
+                    nxt = j
+                    break
+            if nxt < 0:
+                bonus[b] = tp
+                break
+            path[b, a] = nxt
+            out_tokens[b, a] = tp
+            a += 1
+            cur = nxt
+        acc[b] = a
+        out_tokens[b, a] = bonus[b]
+    return dict(accept_len=acc, commit_len=acc + 1, bonus=bonus, path=path, out_tokens=out_tokens)

@@ -651,3 +651,115 @@ def test_draft_select_sampled_histogram_is_the_softmax():
     p = scipy.special.softmax(z / 1.3)
     stat, pval = scipy.stats.chisquare(counts, p * n)
     assert pval > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# DDTree (speculative-decoding page, section 6)
+# ---------------------------------------------------------------------------
+def test_ddtree_topk_matches_library_sort_and_log_softmax():
+    rng = np.random.default_rng(31)
+    z = rng.normal(size=(2, 3, 40)) * 2
+    z[0, 0, [5, 9]] = 10.0                    # tie: lower index first
+    tok, logp = O.ddtree_topk(z, 4, temperature=0.8)
+    assert tok[0, 0, 0] == 5 and tok[0, 0, 1] == 9
+    ls = scipy.special.log_softmax(z / 0.8, axis=2)
+    for b in range(2):
+        for i in range(3):
+            ref = np.argsort(-z[b, i], kind="stable")[:4]
+            np.testing.assert_array_equal(tok[b, i], ref)
+            np.testing.assert_allclose(logp[b, i], ls[b, i, ref], rtol=1e-13)
+
+
+def _all_paths(logp, K, n):
+    """Brute force: every node of the K-ary tree of depth n as (rank path, joint log-prob)."""
+    out = []
+    frontier = [((), 0.0)]
+    for d in range(n):
+        nxt = []
+        for path, lp in frontier:
+            for r in range(K):
+                node = (path + (r,), lp + logp[d, r])
+                out.append(node)
+                nxt.append(node)
+        frontier = nxt
+    return out
+
+
+def _rank_paths(t, b):
+    paths = []
+    for j in range(int(t["n_nodes"][b])):
+        p, rk = [], j
+        while rk >= 0:
+            p.append(int(t["node_rank"][b, rk]))
+            rk = int(t["node_parent"][b, rk])
+        paths.append(tuple(reversed(p)))
+    return paths
+
+
+def test_ddtree_build_is_the_top_budget_nodes_by_path_probability():
+    # 6.3: the best-first tree within budget B holds the B most probable paths
+    rng = np.random.default_rng(32)
+    K, n = 3, 4
+    z = rng.normal(size=(2, n, 12)) * 2
+    tok, logp = O.ddtree_topk(z, K)
+    for budget in (1, 5, 17, 40):
+        t = O.ddtree_build(tok, logp, budget)
+        for b in range(2):
+            allp = _all_paths(logp[b], K, n)
+            best = sorted(allp, key=lambda x: -x[1])[:budget]
+            assert set(_rank_paths(t, b)) == {p for p, _ in best}
+            # pop order: non-increasing probability, parents before children
+            lp = t["node_logp"][b, :budget]
+            assert np.all(np.diff(lp) <= 1e-12)
+            assert np.all(t["node_parent"][b, :budget] < np.arange(budget))
+            np.testing.assert_allclose(sorted(lp, reverse=True), [x for _, x in best], rtol=1e-12)
+
+
+def test_ddtree_build_special_cases():
+    rng = np.random.default_rng(33)
+    z = rng.normal(size=(1, 3, 10))
+    tok, logp = O.ddtree_topk(z, 2)
+    # budget above the tree size: every node (2 + 4 + 8)
+    t = O.ddtree_build(tok, logp, 50)
+    assert t["n_nodes"][0] == 14
+    # K = 1: the greedy draft chain
+    tok1, logp1 = O.ddtree_topk(z, 1)
+    t1 = O.ddtree_build(tok1, logp1, 8)
+    assert t1["n_nodes"][0] == 3
+    np.testing.assert_array_equal(t1["node_token"][0, :3], np.argmax(z[0], axis=1))
+    np.testing.assert_array_equal(t1["node_parent"][0, :3], [-1, 0, 1])
+
+
+def test_ddtree_walk_worked_example():
+    # 6.5: root -> cat (accepted) -> sat (accepted) -> on (rejected); dog's subtree is dropped
+    cat, dog, sat, lay, on, the = 1, 2, 3, 4, 5, 6
+    node_token = np.array([[cat, dog, sat, lay, on]])
+    node_parent = np.array([[-1, -1, 0, 0, 2]])
+    V = 8
+    tl = np.zeros((1, 6, V))
+    tl[0, 0, cat] = 5      # root row: the target predicts cat
+    tl[0, 1, sat] = 5      # after cat: sat
+    tl[0, 2, lay] = 5      # after dog (not reached)
+    tl[0, 3, the] = 5      # after sat: "the", so on is rejected
+    r = O.ddtree_walk_greedy(tl, node_token, node_parent, np.array([5]))
+    assert r["accept_len"][0] == 2 and r["commit_len"][0] == 3
+    assert r["path"][0, :2].tolist() == [0, 2]
+    assert r["out_tokens"][0, :3].tolist() == [cat, sat, the] and r["bonus"][0] == the
+
+
+def test_ddtree_walk_on_a_chain_is_the_greedy_rule():
+    # a K = 1 tree is the DFlash draft: the walk equals the greedy verify rule
+    rng = np.random.default_rng(34)
+    B, n, V = 4, 5, 6
+    zt = rng.normal(size=(B, n + 1, V)) * 3
+    cand = np.zeros((B, n + 1), dtype=np.int64)
+    cand[:, 1:] = rng.integers(0, V, size=(B, n))
+    for b in range(2):     # the first two sequences follow the target for a while
+        cand[b, 1:4] = np.argmax(zt[b, :3], axis=1)
+    node_token = cand[:, 1:]
+    node_parent = np.tile(np.arange(-1, n - 1), (B, 1))
+    r = O.ddtree_walk_greedy(zt, node_token, node_parent, np.full(B, n))
+    g = O.verify_greedy(zt, cand)
+    np.testing.assert_array_equal(r["accept_len"], g["accept_len"])
+    np.testing.assert_array_equal(r["bonus"], g["bonus"])
+    np.testing.assert_array_equal(r["out_tokens"][:, :n + 1], g["out_tokens"])
