@@ -558,6 +558,27 @@ def report_config(wl, args):
         sel_out = api.draft_select(sel["draft_logits"], sel["anchor"], tsel, u_draft=sel["u_draft"])
         us_sel = _time_calls(lambda: api.draft_select(sel["draft_logits"], sel["anchor"], tsel,
                                                       u_draft=sel["u_draft"], out=sel_out), args.steps, args.warmup)
+        if wl.name.startswith("qwen3_4b"):
+            # DDTree on the same drafted positions: top-8 per position, a 512-node
+            # best-first tree, then the greedy walk of the verified tree
+            Kt, budget = 8, 512
+            tk = api.ddtree_topk(sel["draft_logits"], Kt, 1.0)
+            us_tk = _time_calls(lambda: api.ddtree_topk(sel["draft_logits"], Kt, 1.0, out=tk), args.steps, args.warmup)
+            tr = api.ddtree_build(tk["tok"], tk["logp"], budget, V=wl.V)
+            us_tb = _time_calls(lambda: api.ddtree_build(tk["tok"], tk["logp"], budget, V=wl.V, out=tr),
+                                args.steps, args.warmup)
+            torch.cuda.synchronize()
+            zt = synth.ddtree_target_logits(wl, tr["node_token"], tr["node_parent"], tr["n_nodes"], seed=0,
+                                            device=dev)
+            tv = api.ddtree_verify_greedy(zt, tr["node_token"], tr["node_parent"], tr["n_nodes"], wl.n_max, Kt)
+            us_tv = _time_calls(lambda: api.ddtree_verify_greedy(zt, tr["node_token"], tr["node_parent"], tr["n_nodes"],
+                                                                 wl.n_max, Kt, out=tv), args.steps, args.warmup)
+            out["ddtree"] = {"K": Kt, "budget": budget, "topk_us": us_tk,
+                             "topk_frac_hbm": gbs(wl.B * wl.n_max * wl.V * el, us_tk) / hbm,
+                             "build_us": us_tb, "verify_walk_us": us_tv,
+                             "verify_walk_frac_hbm": gbs(wl.B * (budget + 1) * wl.V * el, us_tv) / hbm,
+                             "mean_accept_len": float(tv["accept_len"].float().mean().item())}
+            del zt
         out["draft_select_mode"] = "argmax" if tsel == 0.0 else f"sampled T={tsel}"
         out["draft_select_us"] = us_sel
         out["draft_select_frac_hbm"] = gbs(wl.B * wl.n_max * wl.V * el, us_sel) / hbm

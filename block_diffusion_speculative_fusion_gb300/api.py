@@ -52,6 +52,10 @@ class GateDims(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in ("B", "k", "V", "dtype")]
 
 
+class TreeDims(ctypes.Structure):
+    _fields_ = [(n, c_i32) for n in ("B", "n", "V", "dtype", "K", "budget")]
+
+
 _SIGS = {
     "dflash_last_error": (ctypes.c_char_p, []),
     "dflash_last_launch_count": (ctypes.c_int, []),
@@ -71,6 +75,10 @@ _SIGS = {
     # commit_len, out_tokens, flags, probs, workspace, ws_bytes, stream
     "dflash_verify_sample_lse": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float] + [c_p] * 14 +
                                  [ctypes.c_size_t, c_p]),
+    "dflash_ddtree_topk": (ctypes.c_int, [ctypes.POINTER(TreeDims), ctypes.c_float, c_p, c_p, c_p, c_p]),
+    "dflash_ddtree_build": (ctypes.c_int, [ctypes.POINTER(TreeDims)] + [c_p] * 9),
+    "dflash_ddtree_verify_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(TreeDims)]),
+    "dflash_ddtree_verify_greedy": (ctypes.c_int, [ctypes.POINTER(TreeDims)] + [c_p] * 10 + [ctypes.c_size_t, c_p]),
     "dflash_draft_select_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
     "dflash_draft_select": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float, c_p, c_p, c_p, c_p, c_p,
                                            c_p, c_p, c_p, c_p, ctypes.c_size_t, c_p]),
@@ -340,6 +348,80 @@ def draft_select(draft_logits: torch.Tensor, anchor: torch.Tensor, temperature: 
         _opt(o.get("row_lse"), "row_lse", torch.float32), _opt(o.get("flags"), "flags", torch.uint8),
         w.data_ptr(), w.numel(), _stream(dev))
     _check(rc)
+    return o
+
+
+# ---------------------------------------------------------------------------
+# DDTree
+# ---------------------------------------------------------------------------
+def ddtree_topk(draft_logits: torch.Tensor, K: int, temperature: float = 1.0, out: Optional[dict] = None):
+    """Top-K tokens and their log-probabilities of every drafted position
+    (``dflash_ddtree_topk``): tok [B, n, K] int64, logp [B, n, K] float32."""
+    _dev(draft_logits, "draft_logits")
+    B, n, V = draft_logits.shape
+    dev = draft_logits.device
+    dims = TreeDims(B, n, V, _dtype_code(draft_logits), K, 1)
+    o = out if out is not None else {}
+    if "tok" not in o:
+        o["tok"] = torch.empty((B, n, K), dtype=torch.int64, device=dev)
+        o["logp"] = torch.empty((B, n, K), dtype=torch.float32, device=dev)
+    _check(lib().dflash_ddtree_topk(ctypes.byref(dims), ctypes.c_float(temperature), _dev(draft_logits, "draft_logits"),
+                                    _dev(o["tok"], "tok", torch.int64, (B, n, K)),
+                                    _dev(o["logp"], "logp", torch.float32, (B, n, K)), _stream(dev)))
+    return o
+
+
+def ddtree_build(tok: torch.Tensor, logp: torch.Tensor, budget: int, V: int = 1, out: Optional[dict] = None):
+    """Best-first draft tree within ``budget`` nodes (``dflash_ddtree_build``):
+    node_token, node_parent, node_depth, node_logp [B, budget], n_nodes [B],
+    flags [B]."""
+    B, n, K = tok.shape
+    dev = tok.device
+    dims = TreeDims(B, n, max(V, K), BF16, K, budget)
+    o = out if out is not None else {}
+    if "node_token" not in o:
+        o["node_token"] = torch.empty((B, budget), dtype=torch.int64, device=dev)
+        o["node_parent"] = torch.empty((B, budget), dtype=torch.int32, device=dev)
+        o["node_depth"] = torch.empty((B, budget), dtype=torch.int32, device=dev)
+        o["node_logp"] = torch.empty((B, budget), dtype=torch.float32, device=dev)
+        o["n_nodes"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["flags"] = torch.empty(B, dtype=torch.uint8, device=dev)
+    _check(lib().dflash_ddtree_build(
+        ctypes.byref(dims), _dev(tok, "tok", torch.int64, (B, n, K)), _dev(logp, "logp", torch.float32, (B, n, K)),
+        _dev(o["node_token"], "node_token", torch.int64), _dev(o["node_parent"], "node_parent", torch.int32),
+        _dev(o["node_depth"], "node_depth", torch.int32), _dev(o["node_logp"], "node_logp", torch.float32),
+        _dev(o["n_nodes"], "n_nodes", torch.int32), _opt(o.get("flags"), "flags", torch.uint8), _stream(dev)))
+    return o
+
+
+def ddtree_verify_greedy(target_logits: torch.Tensor, node_token: torch.Tensor, node_parent: torch.Tensor,
+                         n_nodes: torch.Tensor, n: int, K: int, out: Optional[dict] = None,
+                         ws: Optional[torch.Tensor] = None):
+    """Greedy walk of the verified tree (``dflash_ddtree_verify_greedy``):
+    accept_len, commit_len, bonus, path [B, budget], out_tokens [B, budget+1]."""
+    _dev(target_logits, "target_logits")
+    B, R, V = target_logits.shape
+    budget = R - 1
+    dev = target_logits.device
+    dims = TreeDims(B, n, V, _dtype_code(target_logits), K, budget)
+    o = out if out is not None else {}
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["bonus"] = torch.empty(B, dtype=torch.int64, device=dev)
+        o["commit_len"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["path"] = torch.empty((B, budget), dtype=torch.int32, device=dev)
+        o["out_tokens"] = torch.empty((B, R), dtype=torch.int64, device=dev)
+    need = lib().dflash_ddtree_verify_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(dev, need)
+    _check(lib().dflash_ddtree_verify_greedy(
+        ctypes.byref(dims), _dev(target_logits, "target_logits"),
+        _dev(node_token, "node_token", torch.int64, (B, budget)), _dev(node_parent, "node_parent", torch.int32, (B, budget)),
+        _dev(n_nodes, "n_nodes", torch.int32, (B,)), _dev(o["accept_len"], "accept_len", torch.int32),
+        _dev(o["bonus"], "bonus", torch.int64), _dev(o["commit_len"], "commit_len", torch.int32),
+        _opt(o.get("path"), "path", torch.int32), _opt(o.get("out_tokens"), "out_tokens", torch.int64),
+        w.data_ptr(), w.numel(), _stream(dev)))
     return o
 
 

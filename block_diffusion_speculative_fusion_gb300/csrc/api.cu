@@ -300,6 +300,83 @@ int dflash_draft_select(const dflash_verify_dims* d, float temperature, const vo
   return ok(1);
 }
 
+// ------------------------------------------------------------------ DDTree ---
+static int check_tree_dims(const dflash_tree_dims* d) {
+  if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->n < 1 || d->V < 1 || d->K < 1 || d->budget < 1)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad tree dims B=%d n=%d V=%d K=%d budget=%d", d->B, d->n, d->V, d->K,
+                d->budget);
+  if (bad_dtype(d->dtype)) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", d->dtype);
+  if (d->K > dflash::kTreeMaxK || d->K > d->V)
+    return fail(DFLASH_ERR_UNSUPPORTED, "K=%d outside [1, min(V, %d)]", d->K, dflash::kTreeMaxK);
+  if (d->budget > dflash::kTreeMaxBudget) return fail(DFLASH_ERR_UNSUPPORTED, "budget=%d > %d", d->budget,
+                                                      dflash::kTreeMaxBudget);
+  if (d->n > 255) return fail(DFLASH_ERR_UNSUPPORTED, "n=%d > 255", d->n);
+  if (d->B > kMaxCounters) return fail(DFLASH_ERR_UNSUPPORTED, "B=%d too large", d->B);
+  if ((long)d->B * (d->budget + 1) > 65535L) return fail(DFLASH_ERR_UNSUPPORTED, "B*(budget+1) > 65535");
+  return DFLASH_OK;
+}
+
+int dflash_ddtree_topk(const dflash_tree_dims* d, float temperature, const void* draft_logits, int64_t* topk_tok,
+                       float* topk_logp, dflash_stream_t stream) {
+  int rc = check_tree_dims(d);
+  if (rc) return rc;
+  if (!(temperature > 0.f) || !(temperature < 3.0e38f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
+  if (!draft_logits || !topk_tok || !topk_logp) return fail(DFLASH_ERR_INVALID_ARG, "ddtree_topk: a pointer is NULL");
+  dflash::TreeArgs a{};
+  a.B = d->B; a.n = d->n; a.V = d->V; a.dtype = d->dtype; a.K = d->K; a.budget = d->budget;
+  a.temperature = temperature; a.logits = draft_logits; a.topk_tok = topk_tok; a.topk_logp = topk_logp;
+  a.stream = (cudaStream_t)stream; a.num_sms = kPlanSms;
+  cudaError_t e = dflash::launch_ddtree_topk(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ddtree_topk launch");
+  return ok(1);
+}
+
+int dflash_ddtree_build(const dflash_tree_dims* d, const int64_t* topk_tok, const float* topk_logp,
+                        int64_t* node_token, int32_t* node_parent, int32_t* node_depth, float* node_logp,
+                        int32_t* n_nodes, uint8_t* flags, dflash_stream_t stream) {
+  int rc = check_tree_dims(d);
+  if (rc) return rc;
+  if (!topk_tok || !topk_logp || !node_token || !node_parent || !node_depth || !node_logp || !n_nodes)
+    return fail(DFLASH_ERR_INVALID_ARG, "ddtree_build: a required pointer is NULL");
+  dflash::TreeArgs a{};
+  a.B = d->B; a.n = d->n; a.V = d->V; a.dtype = d->dtype; a.K = d->K; a.budget = d->budget;
+  a.topk_tok = const_cast<int64_t*>(topk_tok); a.topk_logp = const_cast<float*>(topk_logp);
+  a.node_token = node_token; a.node_parent = node_parent; a.node_depth = node_depth; a.node_logp = node_logp;
+  a.n_nodes = n_nodes; a.flags = flags; a.stream = (cudaStream_t)stream; a.num_sms = kPlanSms;
+  cudaError_t e = dflash::launch_ddtree_build(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ddtree_build launch");
+  return ok(1);
+}
+
+size_t dflash_ddtree_verify_workspace_size(const dflash_tree_dims* d) {
+  if (check_tree_dims(d) != DFLASH_OK) return 0;
+  return DFLASH_WS_COUNTER_BYTES + dflash::ddtree_verify_ws_bytes(d->B, d->budget, d->V, d->dtype, kPlanSms);
+}
+
+int dflash_ddtree_verify_greedy(const dflash_tree_dims* d, const void* target_logits, const int64_t* node_token,
+                                const int32_t* node_parent, const int32_t* n_nodes, int32_t* accept_len,
+                                int64_t* bonus, int32_t* commit_len, int32_t* path, int64_t* out_tokens,
+                                void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_tree_dims(d);
+  if (rc) return rc;
+  if (!target_logits || !node_token || !node_parent || !n_nodes || !accept_len || !bonus || !commit_len)
+    return fail(DFLASH_ERR_INVALID_ARG, "ddtree_verify_greedy: a required pointer is NULL");
+  rc = check_ws(workspace, ws_bytes, dflash_ddtree_verify_workspace_size(d));
+  if (rc) return rc;
+  dflash::TreeArgs a{};
+  a.B = d->B; a.n = d->n; a.V = d->V; a.dtype = d->dtype; a.K = d->K; a.budget = d->budget;
+  a.logits = target_logits; a.node_token = const_cast<int64_t*>(node_token);
+  a.node_parent = const_cast<int32_t*>(node_parent); a.n_nodes = const_cast<int32_t*>(n_nodes);
+  a.accept_len = accept_len; a.bonus = bonus; a.commit_len = commit_len; a.path = path; a.out_tokens = out_tokens;
+  a.counters = (int32_t*)workspace;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream; a.num_sms = kPlanSms;
+  cudaError_t e = dflash::launch_ddtree_verify(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ddtree_verify launch");
+  return ok(1);
+}
+
 // --------------------------------------------------------------- attention ---
 static int check_attn_dims(const dflash_attn_dims* d) {
   if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");

@@ -85,6 +85,37 @@ constexpr int kSelMaxVocab = 1024 * 256 * 32;   // chunks x tokens per chunk (fp
 size_t draft_select_ws_bytes(int B, int n_max, int V, int dtype);
 cudaError_t launch_draft_select(const DraftSelectArgs& a);
 
+// DDTree: per-position top-K, best-first tree within a node budget, greedy walk.
+constexpr int kTreeMaxK = 16;
+constexpr int kTreeMaxBudget = 4096;
+struct TreeArgs {
+  int B, n, V, dtype, K, budget;
+  float temperature;
+  const void* logits;         // topk: draft logits [B, n, V]; verify: target logits [B, budget + 1, V]
+  int64_t* topk_tok;          // [B, n, K]
+  float* topk_logp;           // [B, n, K]
+  int64_t* node_token;        // [B, budget]
+  int32_t* node_parent;       // [B, budget]
+  int32_t* node_depth;        // [B, budget]
+  float* node_logp;           // [B, budget]
+  int32_t* n_nodes;           // [B]
+  uint8_t* flags;             // [B] or null
+  int32_t* accept_len;        // [B]
+  int64_t* bonus;             // [B]
+  int32_t* commit_len;        // [B]
+  int32_t* path;              // [B, budget] or null
+  int64_t* out_tokens;        // [B, budget + 1] or null
+  int32_t* counters;          // zeroed region at the workspace start
+  void* scratch;
+  cudaStream_t stream;
+  int num_sms;
+};
+cudaError_t launch_ddtree_topk(const TreeArgs& a);
+size_t ddtree_build_smem(int budget, int n, int K);
+cudaError_t launch_ddtree_build(const TreeArgs& a);
+size_t ddtree_verify_ws_bytes(int B, int budget, int V, int dtype, int num_sms);
+cudaError_t launch_ddtree_verify(const TreeArgs& a);
+
 // ------------------------------------------------------------- attention ---
 struct AttnArgs {
   int B, n_q, n_kv, Hq, Hkv, D, page_size, max_pages, num_pages, max_ctx, dtype;

@@ -12,111 +12,13 @@
 //   gate         -- DLoop page, mechanism 1 (c_s = sum log p_draft(x_i) >= g)
 #include "common.cuh"
 #include "internal.h"
+#include "stream.cuh"
 
 namespace dflash {
 
-constexpr int kThreads = 256;
 constexpr int kCtasPerSm = 4;    // resident CTAs per SM the streaming kernels are planned for
 constexpr int kMaxRows = 256;    // n_max + 1 limit (drafts per verify <= 255)
 constexpr int kMaxDrawChunks = 1024;   // vocabulary <= 1024 x 16384
-
-// Visit elements [e0, e1) of row z: 16-byte vectors in the aligned middle,
-// scalars at both ends. fv(u, first_index) gets one raw 16-byte vector, fs(v, i)
-// one value. A thread visits its vectors in ascending index order.
-template <typename T, int UNROLL, typename FV, typename FS>
-__device__ __forceinline__ void for_range(const T* z, int e0, int e1, FV&& fv, FS&& fs) {
-  constexpr int N = VecTraits<T>::N;
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(z + e0);
-  int head = (int)(((16u - (unsigned)(addr & 15u)) & 15u) / sizeof(T));
-  head = min(head, e1 - e0);
-  const int a = e0 + head;
-  const int nvec = (e1 - a) / N;
-  const int b = a + nvec * N;
-  for (int e = e0 + (int)threadIdx.x; e < a; e += blockDim.x) fs(ld_scalar(z + e), e);
-  for (int e = b + (int)threadIdx.x; e < e1; e += blockDim.x) fs(ld_scalar(z + e), e);
-  const uint4* vp = reinterpret_cast<const uint4*>(z + a);
-  int v = threadIdx.x;
-  for (; v + (UNROLL - 1) * (int)blockDim.x < nvec; v += UNROLL * blockDim.x) {
-    uint4 r[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) r[u] = ld_stream16(vp + v + u * blockDim.x);
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) fv(r[u], a + (v + u * (int)blockDim.x) * N);
-  }
-  for (; v < nvec; v += blockDim.x) fv(ld_stream16(vp + v), a + v * N);
-}
-
-// ---------------------------------------------------------------------------
-// Block reductions (deterministic tree order)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ VI block_vi(VI x) {
-  __shared__ VI sh[kThreads / 32];
-  x = warp_vi(x);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) sh[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    x = (l < (int)(blockDim.x >> 5)) ? sh[l] : VI{-CUDART_INF_F, INT32_MAX};
-    x = warp_vi(x);
-  }
-  return x;  // valid in thread 0
-}
-
-__device__ __forceinline__ MS block_ms(MS x) {
-  __shared__ MS sh[kThreads / 32];
-  x = warp_ms(x);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) sh[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    x = (l < (int)(blockDim.x >> 5)) ? sh[l] : MS{-CUDART_INF_F, 0.f};
-    x = warp_ms(x);
-  }
-  return x;  // valid in thread 0
-}
-
-// 2^x on the special-function unit, flushing denormal results to zero (terms
-// below 2^-126 of a row maximum do not change a sum that contains 1).
-__device__ __forceinline__ float ex2_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Streaming statistics of elements [e0, e1) of one row in log2 units:
-// m = max(z) * k2, s = sum 2^(fma(z, k2, -m)). The same code serves target and
-// draft rows, so identical rows give bit-identical statistics.
-template <typename T>
-__device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2) {
-  constexpr int N = VecTraits<T>::N;
-  float zmax = -CUDART_INF_F;   // running max in logit units (exact comparisons)
-  MS acc{-CUDART_INF_F, 0.f};
-  auto raise_to = [&](float v) {
-    const float m2 = v * k2;
-    acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f(acc.m - m2);
-    acc.m = m2;
-    zmax = v;
-  };
-  auto add_vec = [&](const uint4& u, int) {
-    const float vm = vec_max<T>(u);
-    if (vm > zmax) raise_to(vm);
-    if (zmax == -CUDART_INF_F) return;
-    float f[N];
-    unpack16<T>(u, f);
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < N; ++j) s += ex2_ftz(fmaf(f[j], k2, -acc.m));
-    acc.s += s;
-  };
-  auto add_one = [&](float v, int) {
-    if (v > zmax) raise_to(v);
-    if (zmax != -CUDART_INF_F) acc.s += ex2_ftz(fmaf(v, k2, -acc.m));
-  };
-  for_range<T, 8>(z, e0, e1, add_vec, add_one);
-  return block_ms(acc);
-}
 
 // ===========================================================================
 // Greedy rule
@@ -224,16 +126,6 @@ __device__ __forceinline__ void pair_weights(const uint4& vt, const uint4& vd, c
   }
 }
 
-template <typename T>
-__device__ __forceinline__ uint4 load_vec_or_pad(const T* row, int e, int V) {
-  constexpr int N = VecTraits<T>::N;
-  if (e + N <= V && (reinterpret_cast<uintptr_t>(row + e) & 15u) == 0)
-    return __ldg(reinterpret_cast<const uint4*>(row + e));
-  T tmp[N];
-#pragma unroll
-  for (int q = 0; q < N; ++q) tmp[q] = (e + q < V) ? row[e + q] : from_f32<T>(-CUDART_INF_F);
-  return *reinterpret_cast<const uint4*>(tmp);
-}
 
 // Pass 2 grid: CTA (c, b) owns tokens [c * kDrawChunk, (c + 1) * kDrawChunk) of
 // sequence b's drawn row; thread t owns the contiguous segment of kDrawSeg
@@ -639,15 +531,6 @@ constexpr int kSelVecs = 8;                      // 16-byte vectors per thread a
 constexpr int kSelCtasPerSm = 3;                 // resident CTAs per SM (two 32 KB stage buffers each)
 constexpr int kSelSmem = 2 * kThreads * kSelVecs * 16;
 
-// 16-byte global -> shared copy that bypasses registers (L2 only)
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
-               "l"(gmem_src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, kSelCtasPerSm)

@@ -239,6 +239,32 @@ def draft_select_batch(wl: Workload, seed: int = 0, B: Optional[int] = None, n_m
     }
 
 
+def ddtree_target_logits(wl: Workload, node_token: torch.Tensor, node_parent: torch.Tensor, n_nodes: torch.Tensor,
+                         seed: int = 0, p_follow: float = 0.7, device: str = "cpu") -> torch.Tensor:
+    """Target logits [B, budget + 1, V] for a draft tree: row 0 is the target
+    after the anchor, row 1 + j after the path to node j. Each row is N(0, 1)
+    noise plus a peak of 10 on one token: with probability ``p_follow`` the
+    token of the row's first child in the tree (so walks run several levels),
+    else a uniformly drawn token."""
+    B, budget = node_token.shape
+    R = budget + 1
+    z = _randn((B, R, wl.V), seed, "tree_zt", device=device)
+    follow = _rand((B, R), seed, "tree_follow") < p_follow
+    peak = torch.randint(0, wl.V, (B, R), generator=_gen(seed, "tree_tok"))
+    tok = node_token.cpu()
+    par = node_parent.cpu()
+    nn = n_nodes.cpu()
+    for b in range(B):
+        first = {}
+        for j in range(int(nn[b])):
+            first.setdefault(int(par[b, j]), int(tok[b, j]))
+        for r in range(R):
+            if bool(follow[b, r]) and (r - 1) in first:
+                peak[b, r] = first[r - 1]
+    z.scatter_add_(2, peak.to(z.device)[:, :, None], torch.full((B, R, 1), 10.0, device=z.device))
+    return z.to(io_dtype(wl))
+
+
 def gate_batch(wl: Workload, stage: int, seed: int = 0, B: Optional[int] = None) -> Dict[str, torch.Tensor]:
     """One DLoop gate problem for draft stage ``stage``: draft logits [B, k, V] of
     the stage's k drafted tokens, the tokens drawn from softmax(logits / T), and

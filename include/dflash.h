@@ -339,6 +339,66 @@ int dflash_draft_select(const dflash_verify_dims* dims, float temperature,
                         uint8_t* flags, void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* DDTree: draft tree from the per-position marginals                         */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t B;       /* sequences */
+  int32_t n;       /* drafted positions (tree depth), <= 255 */
+  int32_t V;       /* vocabulary */
+  int32_t dtype;   /* type of the logits */
+  int32_t K;       /* candidates per position, 1..16 */
+  int32_t budget;  /* tree nodes (the root, the verified anchor, takes none), 1..4096 */
+} dflash_tree_dims;
+
+/*
+ * [SpecDec] 6.1: the K most probable tokens of every drafted position.
+ * draft_logits [B, n, V] (row i <-> position i + 1); temperature > 0.
+ * topk_tok [B, n, K] int64 sorted by probability (ties: lower token index
+ * first); topk_logp [B, n, K] float = log softmax(z / T) at those tokens.
+ * No workspace.
+ */
+int dflash_ddtree_topk(const dflash_tree_dims* dims, float temperature, const void* draft_logits,
+                       int64_t* topk_tok, float* topk_logp, dflash_stream_t stream);
+
+/*
+ * [SpecDec] 6.2 and 6.3: the best-first tree within `budget` nodes. The root's
+ * candidate children are the position-1 top-K; each step takes the candidate
+ * of highest path log-probability (the sum of its positions' topk_logp) into
+ * the tree and makes its children (the next position's top-K) candidates;
+ * it stops at `budget` nodes or when no candidate is left. Equal
+ * probabilities: smaller depth, then earlier parent, then lower rank first.
+ * Outputs per sequence, in the order the nodes were taken (a parent precedes
+ * its children): node_token [B, budget] int64, node_parent [B, budget] int32
+ * (index of the parent node, -1 = root), node_depth [B, budget] int32
+ * (position 1..n), node_logp [B, budget] float (-1 / -1 / -1 / 0 past
+ * n_nodes), n_nodes [B] int32, flags [B] uint8 or NULL (1: at some step a
+ * candidate of different log-probability trailed the taken one by less than
+ * 1e-5; exact ties follow the order above). No workspace.
+ */
+int dflash_ddtree_build(const dflash_tree_dims* dims, const int64_t* topk_tok, const float* topk_logp,
+                        int64_t* node_token, int32_t* node_parent, int32_t* node_depth, float* node_logp,
+                        int32_t* n_nodes, uint8_t* flags, dflash_stream_t stream);
+
+/*
+ * [SpecDec] 6.5 greedy tree walk with the greedy accept rule ([SGLang] 3):
+ * from the root, the target's prediction (argmax, lowest index on ties) at the
+ * current node selects the child holding that token, which is accepted and
+ * becomes current; the walk stops at the first node with no such child, whose
+ * prediction is the bonus.
+ * target_logits [B, budget + 1, V]: row 0 after the anchor (the root), row
+ * 1 + j after the path to node j (rows past n_nodes are not read).
+ * accept_len, commit_len (= accept_len + 1) [B] int32; bonus [B] int64;
+ * path [B, budget] int32 or NULL (accepted node indices, -1 padded);
+ * out_tokens [B, budget + 1] int64 or NULL (accepted tokens then the bonus).
+ */
+size_t dflash_ddtree_verify_workspace_size(const dflash_tree_dims* dims);
+int dflash_ddtree_verify_greedy(const dflash_tree_dims* dims, const void* target_logits,
+                                const int64_t* node_token, const int32_t* node_parent,
+                                const int32_t* n_nodes, int32_t* accept_len, int64_t* bonus,
+                                int32_t* commit_len, int32_t* path, int64_t* out_tokens,
+                                void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------- */
 /* Message of the last error on this thread ("" if none). */

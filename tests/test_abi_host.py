@@ -86,6 +86,18 @@ def test_draft_select_checks_on_host(L):
     assert rc == api.ERR_INVALID_ARG
 
 
+def test_ddtree_dims_checked_on_host(L):
+    d = api.TreeDims(8, 15, 151936, api.BF16, 8, 512)
+    assert L.dflash_ddtree_verify_workspace_size(ctypes.byref(d)) > api.WS_COUNTER_BYTES
+    assert L.dflash_ddtree_verify_workspace_size(ctypes.byref(api.TreeDims(8, 15, 151936, api.BF16, 3, 512))) > 0
+    for bad, word in ((api.TreeDims(8, 15, 151936, api.BF16, 17, 512), "K=17"),
+                      (api.TreeDims(8, 15, 10, api.BF16, 16, 512), "K=16"),
+                      (api.TreeDims(8, 15, 151936, api.BF16, 8, 5000), "budget"),
+                      (api.TreeDims(8, 300, 151936, api.BF16, 8, 512), "n=")):
+        assert L.dflash_ddtree_verify_workspace_size(ctypes.byref(bad)) == 0
+        assert word in api.last_error(), api.last_error()
+
+
 def _p(x):
     return ctypes.c_void_p(x)
 
