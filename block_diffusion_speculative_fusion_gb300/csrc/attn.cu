@@ -78,16 +78,17 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 // ===========================================================================
 namespace attn_tc {
 constexpr int kTileK = 64;
-constexpr int kMaxStages = 5;
+constexpr int kMaxStages = 6;
 constexpr int kTileBytes = 2 * 64 * 128;   // K (or V) of one tile: two d-halves x 64 keys x 128 B
-constexpr int kTmemCols = 512;   // S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384), P0/P1 [384,448)
+constexpr int kTmemCols = 512;   // S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384), P0/P1 [384,448), Q [448,512)
 constexpr uint32_t kPCol = 384;      // P_t (bf16 pairs) at kPCol + 32 (t % 2)
+constexpr uint32_t kQCol = 448;      // Q of the current item (bf16 pairs, A operand of S = Q K^T)
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kGrid = 152;                  // persistent CTAs: one per SM
 constexpr int kMaxSeqs = 1024;              // sequences per call on this path
 constexpr int kPtMax = 512;                 // page-table entries of one item
 constexpr int kClaimAhead = 3;              // tiles before an item's end at which the next is claimed
-constexpr int kBarBytes = 41 * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
+constexpr int kBarBytes = (2 * kMaxStages + 31) * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
                           (2 * 2 * 128 + 2 * 4 * 128) * 4 + 64;
 }  // namespace attn_tc
 
@@ -198,33 +199,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const bool is_softmax = warp < 8 && quarter < W && warp != prod_warp && warp != mma_warp;
   const bool is_epi = warp >= 8 && warp < 12 && quarter < W;
 
-  // shared memory: [Q: 2 atoms x Ms rows][S stages: K | V][barriers, tables]; one Q buffer is
-  // reused by consecutive items (the next item's Q loads once the last S of the
-  // current item has read it), which leaves room for one more K/V stage
-  // A 128-row MMA reads past the Ms stored rows into the next atom; those
-  // padding rows only produce padding rows of S, P and O, which are never used.
+  // shared memory: [S stages: K | V][barriers, tables]. Q lives in TMEM (columns
+  // kQCol..kQCol+63, the S MMA's A operand): the epilogue warps write the next
+  // item's Q rows there once the current item's last S has read them.
+  // A 128-row MMA reads all 128 lanes; lanes past the item's rows only produce
+  // padding rows of S, P and O, which are never used.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int atom = Ms * 128;                 // one 64-wide column block of Ms rows
-  uint8_t* q_s = smem;                       // Q: d 0-63, then d 64-127
-  uint8_t* kv_s = smem + 2 * atom;           // stage s: K at s*2*T, V at s*2*T + T
+  (void)Ms;
+  uint8_t* kv_s = smem;                      // stage s: K at s*2*T, V at s*2*T + T
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + S * 2 * kTileBytes);
-  uint64_t* kv_full = bars;          // [5]
-  uint64_t* kv_empty = bars + 5;     // [5]
-  uint64_t* s_full = bars + 10;      // [2]
-  uint64_t* s_empty = bars + 12;     // [2]
-  uint64_t* p_full = bars + 14;      // [2]
-  uint64_t* pv_done = bars + 16;     // [2]
-  uint64_t* q_full = bars + 18;      // [2]
-  uint64_t* q_empty = bars + 20;     // [2]
-  uint64_t* it_full = bars + 22;     // [2]
-  uint64_t* it_empty = bars + 24;    // [2]
-  uint64_t* o_full = bars + 26;      // [2]  MMA -> epilogue: last P V of the item done
-  uint64_t* o_empty = bars + 28;     // [2]  epilogue -> MMA: O buffer read out
-  uint64_t* mma_done = bars + 30;
-  uint64_t* xbar = bars + 31;        // [4 quarters][2]: the two softmax warps of a quarter
-  uint64_t* l_full = bars + 39;      // [2]  softmax -> epilogue: row max and sums of the item
-  int* ring = reinterpret_cast<int*>(bars + 41);               // [2] item ids
+  constexpr int KS = kMaxStages;
+  uint64_t* kv_full = bars;               // [KS]
+  uint64_t* kv_empty = bars + KS;         // [KS]
+  uint64_t* s_full = bars + 2 * KS;       // [2]
+  uint64_t* s_empty = s_full + 2;         // [2]
+  uint64_t* p_full = s_full + 4;          // [2]
+  uint64_t* pv_done = s_full + 6;         // [2]
+  uint64_t* q_full = s_full + 8;          // [2]  epilogue warps -> MMA: Q of the item in TMEM
+  uint64_t* q_empty = s_full + 10;        // [2]  MMA -> epilogue warps: the item's last S has read Q
+  uint64_t* it_full = s_full + 12;        // [2]
+  uint64_t* it_empty = s_full + 14;       // [2]
+  uint64_t* o_full = s_full + 16;         // [2]  MMA -> epilogue: last P V of the item done
+  uint64_t* o_empty = s_full + 18;        // [2]  epilogue -> MMA: O buffer read out
+  uint64_t* mma_done = s_full + 20;
+  uint64_t* xbar = s_full + 21;           // [4 quarters][2]: the two softmax warps of a quarter
+  uint64_t* l_full = s_full + 29;         // [2]  softmax -> epilogue: row max and sums of the item
+  int* ring = reinterpret_cast<int*>(s_full + 31);             // [2] item ids
   int* cum = ring + 2;                                         // [B + 1] item prefix per rank
   uint16_t* order = reinterpret_cast<uint16_t*>(cum + (kMaxSeqs + 1));   // [B] sequence of each rank
   int* pt_s = reinterpret_cast<int*>(order + kMaxSeqs);        // [2][kPtMax] page rows of two items
@@ -246,7 +247,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       mbar_init(&s_empty[i], n_tile_sm);
       mbar_init(&p_full[i], n_tile_sm);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&q_full[i], 1);
+      mbar_init(&q_full[i], W);
       mbar_init(&q_empty[i], 1);
       mbar_init(&it_full[i], 1);
       mbar_init(&it_empty[i], 1 + n_sm + W);
@@ -308,8 +309,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 
   if (warp == prod_warp) {
     // ------------------------------ producer ------------------------------
-    // The next item's page rows and Q are fetched while the current item's last
-    // tiles stream, so that item boundaries leave no gap in the K/V stream.
+    // The next item's page rows are fetched while the current item's last tiles
+    // stream, so that item boundaries leave no gap in the K/V stream.
     const int ps = p.page_size;
     int item_seq = 0, tile_seq = 0;
     bool ok = true;
@@ -338,31 +339,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       __syncwarp();
     };
-    // Q of item `item` into Q buffer `slot` (lane 0); false on abort
-    auto load_q = [&](int item, int seq) -> bool {
-      const int slot = 0;
-      bool w = true;
-      if (lane == 0) {
-        w = wait_or_abort(&q_empty[slot], (uint32_t)((seq & 1) ^ 1), abort_flag, p.err, 22);
-        if (w) {
-          AttnItem it;
-          decode_item(p, cum, order, cap, item, it);
-          uint8_t* qb = q_s + slot * 2 * atom;
-          // one TMA box [n_q][Gi][64] per d-half lands in the packed row order r = i * Gi + hh
-          mbar_arrive_expect_tx(&q_full[slot], (uint32_t)(2 * p.Mi * 128));
-          tma_load_3d(qb, &qmap, &q_full[slot], 0, it.g * p.Gi, it.b * p.n_q);
-          tma_load_3d(qb + atom, &qmap, &q_full[slot], 64, it.g * p.Gi, it.b * p.n_q);
-        }
-      }
-      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-    };
     int cur = 0;
     if (lane == 0) cur = atomicAdd(&sched[0], 1);
     cur = __shfl_sync(0xffffffffu, cur, 0);
-    if (cur < n_items) {
-      load_pages(cur, 0);
-      ok = load_q(cur, 0);
-    }
+    if (cur < n_items) load_pages(cur, 0);
     while (ok) {
       const bool last = cur >= n_items;
       const int slot = item_seq & 1;
@@ -423,8 +403,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (nxt < n_items) load_pages(nxt, slot ^ 1);
         }
       }
-      // one Q buffer: the next item's Q once this item's last S no longer reads it
-      if (ok && nxt < n_items) ok = load_q(nxt, item_seq + 1);
       cur = nxt;
       ++item_seq;
     }
@@ -460,7 +438,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         if (!wait_or_abort(&q_full[0], (uint32_t)(item_seq & 1), abort_flag, p.err, 25)) break;
         if (!wait_or_abort(&o_empty[oi], opar ^ 1u, abort_flag, p.err, 26)) break;
         tc_fence_after();
-        const uint32_t qa = smem_u32(q_s);
         auto issue_pv = [&](int t, int j) -> bool {
           if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
           tc_fence_after();
@@ -490,8 +467,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 #pragma unroll
           for (int i = 0; i < attn::kD / 16; ++i) {
             const uint32_t off = (uint32_t)((i >> 2) * (kTileBytes / 2) + (i & 3) * 32);
-            const uint32_t qoff = (uint32_t)((i >> 2) * atom + (i & 3) * 32);
-            tc_mma_bf16(tmem_base + (uint32_t)((t & 1) * kTileK), sdesc_sw128(qa + qoff), sdesc_sw128(ka + off),
+            // Q from TMEM: 8 packed columns per 16-wide K step
+            tc_mma_bf16_ta(tmem_base + (uint32_t)((t & 1) * kTileK), tmem_base + kQCol + (uint32_t)(i * 8),
+                           sdesc_sw128(ka + off),
                         id_s, i > 0 ? 1u : 0u);
           }
           tc_commit(&s_full[t & 1]);
@@ -682,17 +660,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
   } else if (is_epi) {
     // ------------------------------ epilogue ------------------------------
+    // Per item: put the next item's Q rows into TMEM (once this item's last S
+    // has read the buffer), then read this item's O out.
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // the ring entry of item number `seq`: an item, -1 (no more) or -2 (gave up)
+    auto read_item = [&](int seq) -> int {
+      const int sl = seq & 1;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[sl], (uint32_t)((seq >> 1) & 1), abort_flag, p.err, 38)))
+        return -2;
+      const int v = *reinterpret_cast<volatile int*>(&ring[sl]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[sl]);
+      return v;
+    };
+    // this lane's packed query row r of item `item` (r = i * Gi + head) into
+    // TMEM columns kQCol..kQCol+63; rows past Mi stay unwritten (padding lanes)
+    auto put_q = [&](int item, int seq) -> bool {
+      AttnItem qi;
+      decode_item(p, cum, order, cap, item, qi);
+      uint32_t qv[64];
+      if (r < p.Mi) {
+        const int i = r / p.Gi, hh = r - i * p.Gi;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)(qi.b * p.n_q + i) * p.Hq + qi.g * p.Gi + hh) * attn::kD);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint4 v = __ldg(src + k);
+          qv[4 * k] = v.x; qv[4 * k + 1] = v.y; qv[4 * k + 2] = v.z; qv[4 * k + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) qv[k] = 0u;
+      }
+      // the previous item's last S must have read the buffer
+      if (seq > 0 &&
+          !__all_sync(0xffffffffu, wait_or_abort(&q_empty[0], (uint32_t)((seq - 1) & 1), abort_flag, p.err, 40)))
+        return false;
+      tc_fence_after();
+      tmem_st32(tmem_base + lane_off + kQCol, qv);
+      tmem_st32(tmem_base + lane_off + kQCol + 32, qv + 32);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[0]);
+      return true;
+    };
     int item_seq = 0;
-    while (true) {
+    int item = read_item(0);
+    bool qok = item >= 0 ? put_q(item, 0) : false;
+    while (item >= 0 && qok) {
+      const int nxt = read_item(item_seq + 1);
+      if (nxt == -2) break;
+      if (nxt >= 0 && !put_q(nxt, item_seq + 1)) break;
       const int slot = item_seq & 1;
       const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
-      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[slot], par, abort_flag, p.err, 38))) break;
-      const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&it_empty[slot]);
-      if (item < 0) break;
       AttnItem it;
       decode_item(p, cum, order, cap, item, it);
       const int oi = ALT == 2 ? 0 : slot;
@@ -817,6 +839,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
       }
+      item = nxt;
       ++item_seq;
     }
   }
@@ -1039,7 +1062,7 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   }
   const int Ms = M <= 64 ? 64 : 128;     // stored query rows per operand atom
   // K/V stages that fit beside the Q buffer (at most the barrier count)
-  const size_t fixed = 1024 + 2 * (size_t)Ms * 128 + attn_tc::kBarBytes;
+  const size_t fixed = 1024 + attn_tc::kBarBytes;   // Q lives in TMEM
   const int S = (int)std::min<size_t>(attn_tc::kMaxStages, (232448 - fixed) / (2 * attn_tc::kTileBytes));
   const size_t smem = fixed + (size_t)S * 2 * attn_tc::kTileBytes;
   // warps 0-9 (two softmax quarters, producer, MMA, epilogue 8-9) or 0-13
