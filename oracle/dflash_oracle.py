@@ -469,8 +469,9 @@ def ddtree_build(tok, logp, budget):
 
     Ties (reading; the pages do not order equal probabilities): the candidate
     with the smaller depth, then the earlier-popped parent (the root first),
-    then the lower rank among its siblings pops first. A pop decided by a gap
-    below 1e-5 in log-probability flags the sequence.
+    then the lower rank among its siblings pops first. A pop that a distinct
+    candidate trails by less than 1e-5 in log-probability flags the sequence
+    (exact ties are decided by the order and are not flagged).
 
     tok [B, n, K], logp [B, n, K]. Returns node_token, node_parent (index of
     the parent node, -1 = root), node_depth (1-based position), node_rank
@@ -496,7 +497,10 @@ def ddtree_build(tok, logp, budget):
         cnt = 0
         while heap and cnt < budget:
             neg, d, par, r = heapq.heappop(heap)
-            if heap and abs(heap[0][0] - neg) < 1e-5 and (heap[0][1], heap[0][2], heap[0][3]) != (d, par, r):
+            # exact ties are decided by the order above; a distinct candidate
+            # closer than 1e-5 could swap places under another rounding
+            others = [h[0] for h in heap if h[0] != neg]
+            if others and min(others) - neg < 1e-5:
                 flags[b] = FLAG_TREE_TIE
             node_token[b, cnt] = tok[b, d - 1, r]
             node_parent[b, cnt] = par
