@@ -17,6 +17,7 @@ seeded generators in ``synth``.
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Dict, List, Optional
 
 import torch
@@ -81,6 +82,17 @@ class DflashStep:
         self.out_s = {k_: v_[ng:] for k_, v_ in self.out.items()}
         # one workspace per call kind (calls run in order on one stream)
         self.ws = {}
+        # the greedy and the sampled sub-batches are independent sequences:
+        # their verify calls run concurrently, the greedy one on a forked
+        # stream with its own workspace (counters must not be shared)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_fork = torch.cuda.Event()
+        self.ev_join = torch.cuda.Event()
+        self.ws_greedy = None
+        if 0 < ng < B:
+            d = api.VerifyDims(ng, wl.n_draft, wl.V, api.BF16 if wl.dtype == "bf16" else api.F32)
+            need = api.lib().dflash_verify_greedy_workspace_size(ctypes.byref(d))
+            self.ws_greedy = torch.zeros(need, dtype=torch.uint8, device=dev)
         self.launches_per_step = 0
         self.events: Optional[List] = None
 
@@ -133,14 +145,24 @@ class DflashStep:
         ng = wl.n_greedy
         if timer:
             timer("verify_start")
+        concurrent = self.ws_greedy is not None
+        main = torch.cuda.current_stream(self.dev)
+        if concurrent:
+            self.ev_fork.record(main)
+            self.side.wait_event(self.ev_fork)
         if ng > 0:
-            api.verify_greedy(inp["target_logits"][:ng], inp["cand"][:ng], inp["n_draft"][:ng], out=self.out_g)
+            with torch.cuda.stream(self.side if concurrent else main):
+                api.verify_greedy(inp["target_logits"][:ng], inp["cand"][:ng], inp["n_draft"][:ng], out=self.out_g,
+                                  ws=self.ws_greedy)
             launches += api.last_launch_count()
         if ng < wl.B:
             api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"][ng:], inp["cand"][ng:],
                               inp["u_acc"][ng:], inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:],
                               out=self.out_s)
             launches += api.last_launch_count()
+        if concurrent:
+            self.ev_join.record(self.side)
+            main.wait_event(self.ev_join)
         if timer:
             timer("verify_end")
             timer("mat_start")
