@@ -1,14 +1,15 @@
-// Draft block attention: softmax(scale * Q K^T) V with no mask, GQA, where the
-// keys/values of sequence b are its ctx_len[b] context rows in the paged pools
-// followed by the block's own rows.
-//   DFlash page, section 块扩散 (bidirectional attention inside the block) and
-//   KV 注入 step 3 (Attention(Q_draft, [K_draft; K_ctx], [V_draft; V_ctx])).
+// Draft block attention: softmax(scale * Q K^T) V, GQA, where the keys/values
+// of sequence b are its ctx_len[b] context rows in the paged pools followed by
+// the block's own rows; no mask, or the in-block causal mask.
+//   DFlash page, section 块扩散 (bidirectional attention inside the block),
+//   KV 注入 step 3 (Attention(Q_draft, [K_draft; K_ctx], [V_draft; V_ctx])) and
+//   块扩散的双向注意力问题 (the causal variant: block position i sees 0 .. i).
 //
 // bf16 / D = 128 path (the serving shapes): a persistent, warp-specialised
 // tcgen05 kernel (below). The n_q * (Hq/Hkv) query rows that share a kv head
 // are packed into the MMA's M dimension (GQA packing), so each K/V byte is read
-// from HBM once per kv head. Context pages arrive by TMA into a ring of 64-key
-// stages; S and O live in TMEM; the online softmax runs in fp32.
+// from HBM once per kv head. Context pages arrive by TMA into a ring of 64-row
+// stages; Q, S, P and O live in TMEM; the online softmax runs in fp32.
 //
 // Generic path (fp32, or shapes outside the bf16 kernel): one CTA per query
 // row with fp32 CUDA-core arithmetic; used for the tiny fp32 configuration.
@@ -61,17 +62,19 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 // tcgen05 path: persistent, warp-specialised, TMEM accumulators.
 //   softmax     warps q and q + 4 for q < W = ceil(M / 32): TMEM lane quarter q
 //               (packed query row 32 q + lane), key columns 0-31 / 32-63
-//   producer    warp 2 (W <= 2) or 12: claims work items, loads Q and the
-//               page rows, streams context K/V pages by TMA into a ring of
-//               64-key stages
+//   producer    warp 2 (W <= 2) or 12: claims work items, fetches their page
+//               rows, streams context K/V pages by TMA into a ring of
+//               64-row stages
 //   MMA         the warp after the producer: TMEM allocator, one issuing thread
-//   epilogue    warps 8 + q: read O out of TMEM, normalise, store
+//   epilogue    warps 8 + q: write the next item's Q rows into TMEM, read O out
+//               of TMEM, normalise, store
 // A work item is (sequence, kv head, key split); items are handed out longest
-// first from a global counter. Per 64-key tile t: S_t = Q K_t^T (M = 128,
-// N = 64) into TMEM buffer t % 2; the softmax threads read their S row, write
-// P_t (bf16) to shared memory, and the MMA thread accumulates O += P_t V_t
-// (M = 128, N = 128, V read MN-major) into the item's TMEM O buffer. The
-// running max is only raised (O rescaled in TMEM) when a tile's max exceeds it
+// first from a global counter. Per 64-row tile t: S_t = Q K_t^T (M = 128,
+// N = 64, Q from TMEM) into TMEM buffer t % 2; the softmax threads read their
+// S row and write P_t (bf16 pairs) back into TMEM, and the MMA thread
+// accumulates O += P_t V_t (M = 128, N = 128, P from TMEM, V read MN-major)
+// into the item's TMEM O buffer. The running max is only raised (O rescaled
+// in TMEM) when a tile's max exceeds it
 // by more than 2^8, so rescaling is rare. The K/V ring runs across item
 // boundaries; one item's epilogue overlaps the next item's MMAs where the O
 // buffers allow it.
@@ -174,8 +177,8 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 template <int kThreadsT, int HPI>
 __global__ void __launch_bounds__(kThreadsT, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kbmap,
-               const __grid_constant__ CUtensorMap vbmap, const AttnParams p, int Ms, int S, int32_t* sched) {
+               const __grid_constant__ CUtensorMap kbmap, const __grid_constant__ CUtensorMap vbmap,
+               const AttnParams p, int S, int32_t* sched) {
   using namespace attn_tc;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Roles, with W = ceil(Mi / 32) TMEM lane quarters holding real rows:
@@ -206,7 +209,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   // padding rows of S, P and O, which are never used.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  (void)Ms;
   uint8_t* kv_s = smem;                      // stage s: K at s*2*T, V at s*2*T + T
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + S * 2 * kTileBytes);
   constexpr int KS = kMaxStages;
@@ -976,8 +978,8 @@ size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_c
 }
 
 template <int kThreadsT, int HPI>
-static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
-                                  const CUtensorMap& kbmap, const CUtensorMap& vbmap, const AttnParams& p, int Ms,
+static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& kbmap,
+                                  const CUtensorMap& vbmap, const AttnParams& p,
                                   int S, size_t smem, int32_t* sched, cudaStream_t st) {
   static size_t smem_set = 0;   // largest dynamic shared memory opted into so far
   if (smem > smem_set) {
@@ -986,8 +988,7 @@ static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vm
     if (e != cudaSuccess) return e;
     smem_set = smem;
   }
-  attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S,
-                                                                        sched);
+  attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, kbmap, vbmap, p, S, sched);
   return cudaGetLastError();
 }
 
@@ -1037,14 +1038,11 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   p.err = a.err;
   // K/V pools and the block rows as [row][head][d]: a box of {64 d, hpi heads,
   // br rows} lands as [row][head][64 d]
-  CUtensorMap kmap, vmap, qmap, kbmap, vbmap;
+  CUtensorMap kmap, vmap, kbmap, vbmap;
   {
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.num_pages * a.page_size};
     const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};
     const uint32_t box[3] = {64, (uint32_t)p.hpi, (uint32_t)p.br};
-    const uint64_t qd[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)a.B * a.n_q};
-    const uint64_t qs[2] = {(uint64_t)kD * 2, (uint64_t)a.Hq * kD * 2};
-    const uint32_t qb[3] = {64, (uint32_t)p.Gi, (uint32_t)a.n_q};
     const uint64_t bd[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.B * a.n_kv};
     const uint64_t bs[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};
     const uint32_t bb[3] = {64, (uint32_t)p.hpi, (uint32_t)a.n_kv};
@@ -1052,15 +1050,12 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
                            strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_pool), dims,
                            strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qd, qs, qb,
-                           CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map(&kbmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_blk), bd, bs, bb,
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map(&vbmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_blk), bd, bs, bb,
                            CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorNotSupported;   // tensor-map encoding refused a layout
   }
-  const int Ms = M <= 64 ? 64 : 128;     // stored query rows per operand atom
   // K/V stages that fit beside the Q buffer (at most the barrier count)
   const size_t fixed = 1024 + attn_tc::kBarBytes;   // Q lives in TMEM
   const int S = (int)std::min<size_t>(attn_tc::kMaxStages, (232448 - fixed) / (2 * attn_tc::kTileBytes));
@@ -1069,11 +1064,11 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   const bool wide = (M + 31) / 32 > 2;
   cudaError_t e;
   if (wide)
-    e = p.hpi == 2 ? launch_attn_tc<448, 2>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream)
-                   : launch_attn_tc<448, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
+    e = p.hpi == 2 ? launch_attn_tc<448, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream)
+                   : launch_attn_tc<448, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream);
   else
-    e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream)
-                   : launch_attn_tc<320, 1>(kmap, vmap, qmap, kbmap, vbmap, p, Ms, S, smem, a.sched, a.stream);
+    e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream)
+                   : launch_attn_tc<320, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream);
   return e;
 }
 
