@@ -157,12 +157,6 @@ __device__ __forceinline__ int key_depth(uint64_t k) { return (int)((k >> 17) & 
 __device__ __forceinline__ int key_parent(uint64_t k) { return (int)((k >> 4) & 0x1fff) - 1; }
 __device__ __forceinline__ int key_rank(uint64_t k) { return (int)(k & 0xf); }
 
-// top two distinct values: (v1 > v2), -inf when absent
-__device__ __forceinline__ void top2_add(float& v1, float& v2, float v) {
-  if (v > v1) { v2 = v1; v1 = v; }
-  else if (v < v1 && v > v2) v2 = v;
-}
-
 // One warp per sequence, everything warp-synchronous; the frontier (at most
 // one candidate more than the nodes taken), the taken nodes' log-probs and the
 // sequence's top-K table live in shared memory.
@@ -190,30 +184,29 @@ ddtree_build_kernel(const int64_t* __restrict__ tok, const float* __restrict__ l
   __syncwarp();
   int cnt = 0;
   bool tie = false;
+  // Near ties: a distinct candidate within 1e-5 of a pop either pops later,
+  // with all pops in between inside that gap (consecutive pops closer than
+  // 1e-5 but not equal), or is still waiting when the budget runs out (checked
+  // after the loop); exact ties follow the key order and are not flagged.
+  float prev = CUDART_INF_F;
   while (f > 0 && cnt < budget) {
-    // the first key in pop order (and its slot), and the top two distinct log-probs
+    // the first key in pop order, and its slot
     uint64_t bk = ~0ull;
     int bi = -1;
-    float v1 = -CUDART_INF_F, v2 = -CUDART_INF_F;
     for (int j = l; j < f; j += 32) {
       const uint64_t k = fr[j];
       if (k < bk) { bk = k; bi = j; }
-      top2_add(v1, v2, key_lp(k));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const uint64_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (ok < bk) { bk = ok; bi = oi; }
-      const float u1 = __shfl_xor_sync(0xffffffffu, v1, o), u2 = __shfl_xor_sync(0xffffffffu, v2, o);
-      top2_add(v1, v2, u1);
-      top2_add(v1, v2, u2);
     }
     const float lp = key_lp(bk);
     const int depth = key_depth(bk), parent = key_parent(bk), rank = key_rank(bk);
-    // a distinct candidate closer than 1e-5 could swap places under another
-    // rounding (exact ties follow the key order)
-    if (v2 != -CUDART_INF_F && lp - v2 < 1e-5f) tie = true;
+    if (prev != lp && prev - lp < 1e-5f) tie = true;
+    prev = lp;
     const bool sib = rank + 1 < K, child = depth < n;
     __syncwarp();
     if (l == 0) {
@@ -235,6 +228,17 @@ ddtree_build_kernel(const int64_t* __restrict__ tok, const float* __restrict__ l
     f = f - 1 + (sib ? 1 : 0) + (child ? 1 : 0);
     ++cnt;
     __syncwarp();
+  }
+  if (f > 0 && cnt > 0) {
+    // the budget ran out: the nearest distinct candidate left behind
+    float v = -CUDART_INF_F;
+    for (int j = l; j < f; j += 32) {
+      const float x = key_lp(fr[j]);
+      if (x != prev) v = fmaxf(v, x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (v != -CUDART_INF_F && prev - v < 1e-5f) tie = true;
   }
   for (int j = cnt + l; j < budget; j += 32) {
     const size_t o = (size_t)b * budget + j;
