@@ -148,15 +148,39 @@ sample_draw_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const flo
   const bool usep_r = (j.mode == 1);
   const T* zt_row = zt + ((size_t)b * R + j.row) * V;
   const T* zd_row = zd + ((size_t)b * n_max + min(j.row, max(n_max - 1, 0))) * V;
-  const int e0 = c * kDrawChunk + (int)threadIdx.x * kDrawSeg;
   // ---- pass 1: segment sums of the drawn weights (residual, or p) and of p ----
+  // The chunk of both rows is staged in shared memory with coalesced copies
+  // (vector v of the chunk at stage[v]); each thread then reads its own
+  // contiguous segment, its vectors in a rotated order so that a quarter warp
+  // hits distinct banks.
+  extern __shared__ __align__(16) uint4 draw_stage[];   // [2][kThreads * NV]
+  {
+    uint4* st_t = draw_stage;
+    uint4* st_d = draw_stage + kThreads * NV;
+    const bool al_t = (reinterpret_cast<uintptr_t>(zt_row) & 15u) == 0;
+    const bool al_d = (reinterpret_cast<uintptr_t>(zd_row) & 15u) == 0;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int v = k * kThreads + (int)threadIdx.x;
+      const int e = c * kDrawChunk + v * N;
+      if (al_t && e + N <= V) cp_async16(&st_t[v], zt_row + e);
+      else st_t[v] = load_vec_or_pad<T>(zt_row, e, V);
+      if (!usep_r) {
+        if (al_d && e + N <= V) cp_async16(&st_d[v], zd_row + e);
+        else st_d[v] = load_vec_or_pad<T>(zd_row, e, V);
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+  }
   float sr = 0.f, sp = 0.f;
   {
     uint4 vt[NV], vd[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-      vt[i] = load_vec_or_pad<T>(zt_row, e0 + i * N, V);
-      if (!usep_r) vd[i] = load_vec_or_pad<T>(zd_row, e0 + i * N, V);
+      const int v = (int)threadIdx.x * NV + ((i + (int)threadIdx.x) & (NV - 1));
+      vt[i] = draw_stage[v];
+      if (!usep_r) vd[i] = draw_stage[kThreads * NV + v];
     }
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -874,7 +898,14 @@ static cudaError_t launch_sample_t(const VerifyArgs& a, int num_sms) {
       a.out_tokens, a.probs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  sample_draw_kernel<T><<<dim3(nch2, a.B), kThreads, 0, a.stream>>>(
+  constexpr int kDrawSmem = 2 * kDrawChunk * (int)sizeof(T);   // the chunk of both rows
+  static bool draw_smem_set = false;
+  if (!draw_smem_set) {
+    e = cudaFuncSetAttribute(sample_draw_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDrawSmem);
+    if (e != cudaSuccess) return e;
+    draw_smem_set = true;
+  }
+  sample_draw_kernel<T><<<dim3(nch2, a.B), kThreads, kDrawSmem, a.stream>>>(
       (const T*)a.target_logits, (const T*)a.draft_logits, a.u_final, a.n_max, a.V, nch2, k2, jobs, dparts, dsegs,
       a.counters, a.bonus, a.out_tokens, a.flags, a.probs);
   (void)R;
