@@ -478,7 +478,7 @@ def run_kernel(args, wl):
                            st.ctx[0], max_ctx=st.max_ctx, out=st.attn_out[0])
         elif args.kernel == "verify":
             api.verify_greedy(inp["target_logits"][:ng], inp["cand"][:ng], inp["n_draft"][:ng], out=st.out_g)
-            api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"][ng:], inp["cand"][ng:],
+            api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"], inp["cand"][ng:],
                               inp["u_acc"][ng:], inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:],
                               out=st.out_s)
         else:
@@ -593,7 +593,7 @@ def report_config(wl, args):
         if ng < wl.B:
             ns = wl.B - ng
             us_s = _time_calls(lambda: api.verify_sample(
-                inp["target_logits"][ng:], inp["draft_logits"][ng:], inp["cand"][ng:], inp["u_acc"][ng:],
+                inp["target_logits"][ng:], inp["draft_logits"], inp["cand"][ng:], inp["u_acc"][ng:],
                 inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:], out=st.out_s), args.steps, args.warmup)
             out["verify_sample_us"] = us_s
             out["verify_sample_frac_hbm"] = gbs(ns * (2 * R - 1 + 2) * wl.V * el, us_s) / hbm

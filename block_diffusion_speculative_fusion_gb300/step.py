@@ -57,6 +57,9 @@ class DflashStep:
                 host[f"{k_}{layer}"] = v_
         vb = synth.verify_batch(wl, seed, n_max=wl.n_draft)
         host.update(vb)
+        # the draft logits are read by the sampled rule only: the step's input is
+        # the sampled sub-batch's rows (the greedy sequences' candidates are given)
+        host["draft_logits"] = vb["draft_logits"][wl.n_greedy:].contiguous()
         host["hidden"] = synth.captured_hidden(wl, wl.n_draft + 1, seed)
         if pinned_inputs:
             host = {k_: v_.pin_memory() for k_, v_ in host.items()}
@@ -156,7 +159,7 @@ class DflashStep:
                                   ws=self.ws_greedy)
             launches += api.last_launch_count()
         if ng < wl.B:
-            api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"][ng:], inp["cand"][ng:],
+            api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"], inp["cand"][ng:],
                               inp["u_acc"][ng:], inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:],
                               out=self.out_s)
             launches += api.last_launch_count()
