@@ -86,9 +86,10 @@ class DflashStep:
         # one workspace per call kind (calls run in order on one stream)
         self.ws = {}
         # the greedy and the sampled sub-batches are independent sequences:
-        # their verify calls run concurrently, the greedy one on a forked
-        # stream with its own workspace (counters must not be shared)
-        self.side = torch.cuda.Stream(device=dev)
+        # their verify calls run concurrently, the sampled one (two dependent
+        # launches, the longer path) on a forked stream of higher priority, the
+        # greedy one with its own workspace (counters must not be shared)
+        self.side = torch.cuda.Stream(device=dev, priority=-1)
         self.ev_fork = torch.cuda.Event()
         self.ev_join = torch.cuda.Event()
         self.ws_greedy = None
@@ -153,15 +154,15 @@ class DflashStep:
         if concurrent:
             self.ev_fork.record(main)
             self.side.wait_event(self.ev_fork)
-        if ng > 0:
-            with torch.cuda.stream(self.side if concurrent else main):
-                api.verify_greedy(inp["target_logits"][:ng], inp["cand"][:ng], inp["n_draft"][:ng], out=self.out_g,
-                                  ws=self.ws_greedy)
-            launches += api.last_launch_count()
         if ng < wl.B:
-            api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"], inp["cand"][ng:],
-                              inp["u_acc"][ng:], inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:],
-                              out=self.out_s)
+            with torch.cuda.stream(self.side if concurrent else main):
+                api.verify_sample(inp["target_logits"][ng:], inp["draft_logits"], inp["cand"][ng:],
+                                  inp["u_acc"][ng:], inp["u_final"][ng:], wl.temperature, inp["n_draft"][ng:],
+                                  out=self.out_s)
+            launches += api.last_launch_count()
+        if ng > 0:
+            api.verify_greedy(inp["target_logits"][:ng], inp["cand"][:ng], inp["n_draft"][:ng], out=self.out_g,
+                              ws=self.ws_greedy)
             launches += api.last_launch_count()
         if concurrent:
             self.ev_join.record(self.side)
