@@ -635,8 +635,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           // V rows of keys past the valid ones may hold anything (P is 0 there,
           // but 0 * NaN is NaN): zero them. V row n holds key n / HPI.
           uint8_t* vs = kv_s + (t % S) * 2 * kTileBytes + kTileBytes;
-          const int me = (chalf * W + quarter) * 32 + lane;
-          for (int n = me; n < kTileK; n += n_sm * 32) {
+          // the warps that take this tile: its group (ALT = 2), or both halves
+          const int me = ALT == 2 ? quarter * 32 + lane : (chalf * W + quarter) * 32 + lane;
+          for (int n = me; n < kTileK; n += n_tile_sm * 32) {
             if (n / HPI < valid) continue;
             for (int ch = 0; ch < 16; ++ch)
               *reinterpret_cast<uint4*>((ch < 8 ? vs : vs + kTileBytes / 2) + swz(n, ch & 7)) =
