@@ -76,8 +76,11 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 // into the item's TMEM O buffer. The running max is only raised (O rescaled
 // in TMEM) when a tile's max exceeds it
 // by more than 2^8, so rescaling is rare. The K/V ring runs across item
-// boundaries; one item's epilogue overlaps the next item's MMAs where the O
-// buffers allow it.
+// boundaries. The MMA thread issues P_{t-1} V_{t-1} as soon as P_{t-1} is
+// ready, also while it still waits for tile t to land, so that a stage goes
+// back to the producer without waiting for the next tile; a new item's S MMAs
+// start while the epilogue still reads the previous item's O, and only its
+// first P V waits for the O buffer.
 // ===========================================================================
 namespace attn_tc {
 constexpr int kTileK = 64;
@@ -438,10 +441,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         const int oi = ALT == 2 ? 0 : slot;
         const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
         if (!wait_or_abort(&q_full[0], (uint32_t)(item_seq & 1), abort_flag, p.err, 25)) break;
-        if (!wait_or_abort(&o_empty[oi], opar ^ 1u, abort_flag, p.err, 26)) break;
         tc_fence_after();
-        auto issue_pv = [&](int t, int j) -> bool {
-          if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
+        // The item's S MMAs go ahead while the epilogue still reads the previous
+        // item's O; only its first P V waits for the O buffer (o_ready).
+        bool o_ready = false;
+        // O += P_t V_t once P_t is in TMEM; then stage t % S is free again
+        auto pv_issue = [&](int t, int j) {
           tc_fence_after();
           // P_t from TMEM (8 packed columns per 16-row K step), V_t MN-major from smem
           const uint32_t pa = tmem_base + kPCol + (uint32_t)((t & 1) * 32);
@@ -454,12 +459,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           tc_commit(&pv_done[t & 1]);
           tc_commit(&kv_empty[t % S]);
           ++consumed;
+        };
+        auto issue_pv = [&](int t, int j) -> bool {
+          if (!o_ready) {
+            if (!wait_or_abort(&o_empty[oi], opar ^ 1u, abort_flag, p.err, 26)) return false;
+            o_ready = true;
+          }
+          if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
+          pv_issue(t, j);
           return true;
+        };
+        // Wait for K/V tile t; while it is in flight, issue the P V of tile t - 1
+        // as soon as its P is ready, so that stage (t - 1) % S goes back to the
+        // producer without waiting for tile t to land.
+        auto wait_tile = [&](int t, int j, bool& pv_pending) -> bool {
+          uint64_t* full = &kv_full[t % S];
+          const uint32_t par = (uint32_t)((t / S) & 1);
+          if (mbar_try_wait(full, par)) return true;
+          const uint64_t t_start = global_timer_ns();
+          while (true) {
+            for (int i = 0; i < 32; ++i) {
+              if (mbar_try_wait(full, par)) return true;
+              if (pv_pending) {
+                if (!o_ready) o_ready = mbar_try_wait(&o_empty[oi], opar ^ 1u);
+                if (o_ready && mbar_try_wait(&p_full[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1))) {
+                  pv_issue(t - 1, j - 1);
+                  pv_pending = false;
+                }
+              }
+            }
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t_start > 2000000000ull) {
+              *abort_flag = 1;
+              atomicCAS(p.err, 0, 28);
+              return false;
+            }
+          }
         };
         for (int j = 0; j < it.n_tiles && ok; ++j) {
           const int t = tile_seq + j;
           const int st = t % S;
-          if (!wait_or_abort(&kv_full[st], (uint32_t)((t / S) & 1), abort_flag, p.err, 28)) { ok = false; break; }
+          bool pv_pending = j >= 1;   // the P V of tile t - 1 is still to issue
+          if (!wait_tile(t, j, pv_pending)) { ok = false; break; }
           if (!wait_or_abort(&s_empty[t & 1], (uint32_t)(((t >> 1) & 1) ^ 1), abort_flag, p.err, 29)) {
             ok = false;
             break;
@@ -476,7 +517,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
           tc_commit(&s_full[t & 1]);
           if (j == it.n_tiles - 1) tc_commit(&q_empty[0]);   // Q is no longer read
-          if (j >= 1) ok = issue_pv(t - 1, j - 1);
+          if (pv_pending) ok = issue_pv(t - 1, j - 1);
         }
         if (!ok) break;
         if (!issue_pv(tile_seq + it.n_tiles - 1, it.n_tiles - 1)) break;
@@ -651,8 +692,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       if (!ok) break;
       // hand the row max and this half's row sums to the epilogue warps; the
-      // slot is free again once the epilogue of item_seq - 2 released O (the
-      // MMA only started this item after that)
+      // slot is free again once the epilogue has finished item_seq - 2 (it then
+      // wrote this item's Q, which the item's first S MMA waited for)
       float* mls = ml_s + slot * 512;
       mls[256 * chalf + r] = m_run;
       mls[256 * chalf + 128 + r] = l_part;
@@ -733,10 +774,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         m_run = ma;
         l_run = la + lb;
       } else {
+        // which half is "a" depends on where the item fell in the CTA's tile
+        // count: the merge is written without contraction into FMAs, so that it
+        // is symmetric in a and b and its rounding does not depend on that
         m_run = fmaxf(ma, mb);
         wa = la > 0.f ? exp2f(ma - m_run) : 0.f;
         wb = lb > 0.f ? exp2f(mb - m_run) : 0.f;
-        l_run = la * wa + lb * wb;
+        l_run = __fadd_rn(__fmul_rn(la, wa), __fmul_rn(lb, wb));
       }
       const bool single = (it.nsplit == 1);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -752,9 +796,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
             // a half that took no tile has l = 0 and an O that was never written
-            const float xa = wa != 0.f ? __uint_as_float(o[q]) * wa : 0.f;
-            const float xb = wb != 0.f ? __uint_as_float(ob[q]) * wb : 0.f;
-            o[q] = __float_as_uint(xa + xb);
+            const float xa = wa != 0.f ? __fmul_rn(__uint_as_float(o[q]), wa) : 0.f;
+            const float xb = wb != 0.f ? __fmul_rn(__uint_as_float(ob[q]), wb) : 0.f;
+            o[q] = __float_as_uint(__fadd_rn(xa, xb));
           }
         } else {
           tmem_ld_wait();
