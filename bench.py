@@ -465,6 +465,14 @@ def run_kernel(args, wl):
     __graft_entry__.build()
     from block_diffusion_speculative_fusion_gb300 import api, synth
     from block_diffusion_speculative_fusion_gb300.step import DflashStep
+    if args.kernel == "prefill":
+        # the prefill-sized materialisation GEMMs (Llama-3.1-8B shape, T = 2048 rows)
+        from block_diffusion_speculative_fusion_gb300 import workloads as W
+        call, T, flops = prefill_materialize_call(W.LLAMA8B_B1, "cuda:0")
+        us = _time_calls(call, args.steps, args.warmup)
+        print(json.dumps({"kernel": "prefill", "workload": W.LLAMA8B_B1.name, "rows": T, "us_per_call": us,
+                          "tflops": flops / us / 1e6, "frac_bf16_peak": flops / us / 1e6 / _peaks()[1]}), flush=True)
+        return
     if args.batch:
         wl = dataclasses.replace(wl, B=args.batch, n_greedy=min(wl.n_greedy, args.batch // 2))
     one = dataclasses.replace(wl, L=1) if args.kernel in ("attn", "verify") else wl
@@ -639,26 +647,36 @@ def report_config(wl, args):
         out["looped_step_us_all_stages_gate_lse"] = total_us + us_vl
     if wl.dtype == "bf16" and wl.stages == 1 and wl.ctx_lo == wl.ctx_hi:
         # ---- prefill-sized materialisation: every context row of every sequence ----
-        rows = wl.ctx_lo
-        w = {k_: (v_.to(dev) if v_ is not None else None) for k_, v_ in synth.ctx_weights(wl, 0).items()}
-        hid = synth.captured_hidden(wl, rows, 0, B=wl.B).to(dev)
-        pc = synth.paged_cache(wl, headroom=0, seed=0, layers=wl.L, ctx_len=torch.full((wl.B,), rows, dtype=torch.int32),
-                               device=dev)
-        commit = torch.full((wl.B,), rows, dtype=torch.int32, device=dev)
-        start = torch.zeros(wl.B, dtype=torch.int32, device=dev)
-        pools_k = [t.to(dev) for t in pc.k_pools]
-        pools_v = [t.to(dev) for t in pc.v_pools]
-        ptab = pc.page_table.to(dev)
-        us_m = _time_calls(lambda: api.materialize_ctx_kv(hid, commit, start, w["W_f"], w["b_f"], w["W_kv"],
-                                                          w["k_norm_w"], wl.rms_eps, wl.rope_theta, pools_k, pools_v,
-                                                          ptab), max(3, args.steps // 4), 2)
-        T = wl.B * rows
-        flops = 2.0 * T * (wl.m * wl.d * wl.d + wl.d * wl.kv_out)
+        call_m, T, flops = prefill_materialize_call(wl, dev)
+        us_m = _time_calls(call_m, max(3, args.steps // 4), 2)
         out["prefill_materialize_rows"] = T
         out["prefill_materialize_us"] = us_m
         out["prefill_materialize_tflops"] = flops / us_m / 1e6
         out["prefill_materialize_frac_bf16_peak"] = flops / us_m / 1e6 / tf
     print(json.dumps(out), flush=True)
+
+
+def prefill_materialize_call(wl, dev):
+    """The context-KV materialisation of every context row of every sequence
+    (prefill-sized T = B x context): returns (call, T, flops of both GEMMs)."""
+    import torch
+    from block_diffusion_speculative_fusion_gb300 import api, synth
+    rows = wl.ctx_lo
+    w = {k_: (v_.to(dev) if v_ is not None else None) for k_, v_ in synth.ctx_weights(wl, 0).items()}
+    hid = synth.captured_hidden(wl, rows, 0, B=wl.B).to(dev)
+    pc = synth.paged_cache(wl, headroom=0, seed=0, layers=wl.L, ctx_len=torch.full((wl.B,), rows, dtype=torch.int32),
+                           device=dev)
+    commit = torch.full((wl.B,), rows, dtype=torch.int32, device=dev)
+    start = torch.zeros(wl.B, dtype=torch.int32, device=dev)
+    pools_k = [t.to(dev) for t in pc.k_pools]
+    pools_v = [t.to(dev) for t in pc.v_pools]
+    ptab = pc.page_table.to(dev)
+
+    def call():
+        api.materialize_ctx_kv(hid, commit, start, w["W_f"], w["b_f"], w["W_kv"], w["k_norm_w"], wl.rms_eps,
+                               wl.rope_theta, pools_k, pools_v, ptab)
+    T = wl.B * rows
+    return call, T, 2.0 * T * (wl.m * wl.d * wl.d + wl.d * wl.kv_out)
 
 
 def run_all_configs(args):
@@ -677,7 +695,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps one by one (no CUDA graph)")
-    ap.add_argument("--kernel", choices=["attn", "verify", "materialize"], default=None,
+    ap.add_argument("--kernel", choices=["attn", "verify", "materialize", "prefill"], default=None,
                     help="time one call of the step in isolation (profiling aid)")
     ap.add_argument("--batch", type=int, default=None, help="override B (with --kernel)")
     ap.add_argument("--all-configs", action="store_true",
