@@ -163,6 +163,9 @@ typedef struct {
  * page_table [B, max_pages] int32; ctx_len [B] int32, 0 <= ctx_len[b] <= max_ctx
  * scale: softmax scale (1/sqrt(D) for the standard form)
  * out [B, n_q, Hq, D]
+ * Repeated calls on the same inputs return identical bits: the bf16 kernel
+ * hands work items to whichever CTA is free, and its arithmetic does not
+ * depend on that assignment.
  */
 size_t dflash_block_attn_workspace_size(const dflash_attn_dims* dims);
 int dflash_block_attn(const dflash_attn_dims* dims,
