@@ -1026,13 +1026,9 @@ template <int kThreadsT, int HPI>
 static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& kbmap,
                                   const CUtensorMap& vbmap, const AttnParams& p,
                                   int S, size_t smem, int32_t* sched, cudaStream_t st) {
-  static size_t smem_set = 0;   // largest dynamic shared memory opted into so far
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<kThreadsT, HPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set = smem;
-  }
+  static SmemOptIn opt_in;
+  cudaError_t e = opt_in.ensure(attn_tc_kernel<kThreadsT, HPI>, smem);
+  if (e != cudaSuccess) return e;
   attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, kbmap, vbmap, p, S, sched);
   return cudaGetLastError();
 }

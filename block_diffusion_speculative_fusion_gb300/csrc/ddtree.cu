@@ -362,11 +362,10 @@ size_t ddtree_build_smem(int budget, int n, int K) {
 
 cudaError_t launch_ddtree_build(const TreeArgs& a) {
   const size_t smem = ddtree_build_smem(a.budget, a.n, a.K);
-  static size_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(ddtree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static SmemOptIn opt_in;
+  if (smem > 48 * 1024) {
+    cudaError_t e = opt_in.ensure(ddtree_build_kernel, smem);
     if (e != cudaSuccess) return e;
-    smem_set = smem;
   }
   ddtree_build_kernel<<<a.B, 32, smem, a.stream>>>(a.topk_tok, a.topk_logp, a.n, a.K, a.budget, a.node_token,
                                                    a.node_parent, a.node_depth, a.node_logp, a.n_nodes, a.flags);

@@ -309,12 +309,9 @@ cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int3
                            CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorNotSupported;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static SmemOptIn opt_in;
+  cudaError_t e = opt_in.ensure(gemm_tc_kernel, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   gemm_tc_kernel<<<GRID, THREADS, SMEM_BYTES, st>>>(wmap, xmap_l, xmap_m, xmap_s, part, meta, per_idx, T_max, N,
                                                     N / BM, K / BK, box_l, box_m, err);
   return cudaGetLastError();

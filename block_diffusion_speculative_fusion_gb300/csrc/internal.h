@@ -5,9 +5,36 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace dflash {
 
 inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
+
+// Opt a kernel into `bytes` of dynamic shared memory on the calling thread's
+// current device. The attribute belongs to each device's context, so it is set
+// once per device (and again only to raise it), under a lock so that concurrent
+// callers cannot lower it for each other. One object per kernel.
+class SmemOptIn {
+ public:
+  template <class Kernel>
+  cudaError_t ensure(Kernel* kernel, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool tracked = dev >= 0 && dev < kDevices;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (tracked && bytes <= set_[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && tracked) set_[dev] = bytes;
+    return e;
+  }
+
+ private:
+  static constexpr int kDevices = 64;
+  std::mutex mu_;
+  size_t set_[kDevices] = {};
+};
 
 struct ChunkPlan {
   int chunk;   // elements per chunk (multiple of one 16-byte vector per thread)

@@ -899,12 +899,9 @@ static cudaError_t launch_sample_t(const VerifyArgs& a, int num_sms) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   constexpr int kDrawSmem = 2 * kDrawChunk * (int)sizeof(T);   // the chunk of both rows
-  static bool draw_smem_set = false;
-  if (!draw_smem_set) {
-    e = cudaFuncSetAttribute(sample_draw_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDrawSmem);
-    if (e != cudaSuccess) return e;
-    draw_smem_set = true;
-  }
+  static SmemOptIn opt_in;
+  e = opt_in.ensure(sample_draw_kernel<T>, kDrawSmem);
+  if (e != cudaSuccess) return e;
   sample_draw_kernel<T><<<dim3(nch2, a.B), kThreads, kDrawSmem, a.stream>>>(
       (const T*)a.target_logits, (const T*)a.draft_logits, a.u_final, a.n_max, a.V, nch2, k2, jobs, dparts, dsegs,
       a.counters, a.bonus, a.out_tokens, a.flags, a.probs);
@@ -930,12 +927,9 @@ static cudaError_t launch_draft_select_t(const DraftSelectArgs& a) {
   const long rows = (long)a.B * a.n_max;
   const bool sampled = a.temperature > 0.f;
   const float k2 = kLog2e / (sampled ? a.temperature : 1.f);
-  static bool smem_set = false;
-  if (!smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(draft_select_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
-    if (e != cudaSuccess) return e;
-    smem_set = true;
-  }
+  static SmemOptIn opt_in;
+  cudaError_t e = opt_in.ensure(draft_select_kernel<T>, kSelSmem);
+  if (e != cudaSuccess) return e;
   const int grid = (int)std::min<long>(rows, (long)kSelCtasPerSm * a.num_sms);
   draft_select_kernel<T><<<grid, kThreads, kSelSmem, a.stream>>>(
       (const T*)a.draft_logits, a.anchor, a.n_draft, a.u_draft, a.B, a.n_max, a.V, nch, k2, sampled ? 1 : 0,
