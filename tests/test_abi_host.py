@@ -138,3 +138,54 @@ def test_binding_requires_cuda_tensors(L):
     import torch
     with pytest.raises((ValueError, TypeError)):
         api.verify_greedy(torch.zeros(1, 2, 8), torch.zeros(1, 2, dtype=torch.int64))
+
+
+def test_attention_dims_checked_on_host(L):
+    ok = api.AttnDims(2, 16, 16, 32, 8, 128, 16, 64, 256, 1024, api.BF16, 0)
+    assert L.dflash_block_attn_workspace_size(ctypes.byref(ok)) > api.WS_COUNTER_BYTES
+    for bad, word in ((api.AttnDims(2, 16, 16, 30, 8, 128, 16, 64, 256, 1024, api.BF16, 0), "multiple of Hkv"),
+                      (api.AttnDims(2, 16, 16, 32, 8, 128, 16, 64, 256, 1025, api.BF16, 0), "max_ctx"),
+                      (api.AttnDims(2, 16, 16, 32, 8, 128, 16, 64, 256, 1024, 3, 0), "dtype"),
+                      (api.AttnDims(0, 16, 16, 32, 8, 128, 16, 64, 256, 1024, api.BF16, 0), "dims")):
+        assert L.dflash_block_attn_workspace_size(ctypes.byref(bad)) == 0
+        assert word in api.last_error(), api.last_error()
+    wide = api.AttnDims(2, 16, 16, 32, 8, 512, 16, 64, 256, 1024, api.BF16, 0)
+    assert L.dflash_block_attn_workspace_size(ctypes.byref(wide)) == 0 and "D=512" in api.last_error()
+    # a call with a missing pointer fails before anything is launched
+    need = L.dflash_block_attn_workspace_size(ctypes.byref(ok))
+    fake = _p(0x10000)
+    rc = L.dflash_block_attn(ctypes.byref(ok), fake, fake, fake, fake, fake, fake, None, ctypes.c_float(0.088),
+                             fake, fake, need, None)
+    assert rc == api.ERR_INVALID_ARG and "NULL" in api.last_error()
+    wide_rc = L.dflash_block_attn(ctypes.byref(wide), *([fake] * 7), ctypes.c_float(0.1), fake, fake, need, None)
+    assert wide_rc == api.ERR_UNSUPPORTED
+
+
+def test_materialize_dims_and_arguments_checked_on_host(L):
+    ok = api.CtxKvDims(64, 16, 5, 4096, 5, 8, 128, 16, 640, 40960, api.BF16)
+    need = L.dflash_materialize_workspace_size(ctypes.byref(ok))
+    assert need > api.WS_COUNTER_BYTES
+    for bad, word, code in ((api.CtxKvDims(64, 16, 5, 4096, 5, 8, 127, 16, 640, 40960, api.BF16), "even", None),
+                            (api.CtxKvDims(64, 16, 5, 4096, 17, 8, 128, 16, 640, 40960, api.BF16), "L=17", None),
+                            (api.CtxKvDims(64, 16, 5, 4100, 5, 8, 128, 16, 640, 40960, api.BF16), "16 bytes", None),
+                            (api.CtxKvDims(64, 2000, 5, 4096, 5, 8, 128, 16, 640, 40960, api.BF16), "65535", None)):
+        assert L.dflash_materialize_workspace_size(ctypes.byref(bad)) == 0
+        assert word in api.last_error(), api.last_error()
+    fake = _p(0x10000)
+    pools = (ctypes.c_void_p * 5)(*([0x10000] * 5))
+    pp = ctypes.cast(pools, ctypes.c_void_p)
+    eps, theta = ctypes.c_float(1e-6), ctypes.c_float(5e5)
+    # new_len aliasing start_pos would read and write the same array
+    rc = L.dflash_materialize_ctx_kv(ctypes.byref(ok), fake, fake, _p(0x20000), fake, None, fake, None, eps, theta,
+                                     pp, pp, fake, _p(0x20000), fake, need, None)
+    assert rc == api.ERR_INVALID_ARG and "alias" in api.last_error()
+    rc = L.dflash_materialize_ctx_kv(ctypes.byref(ok), fake, fake, fake, fake, None, fake, None, eps,
+                                     ctypes.c_float(-1.0), pp, pp, fake, None, fake, need, None)
+    assert rc == api.ERR_INVALID_ARG and "rope_theta" in api.last_error()
+    rc = L.dflash_materialize_ctx_kv(ctypes.byref(ok), None, fake, fake, fake, None, fake, None, eps, theta,
+                                     pp, pp, fake, None, fake, need, None)
+    assert rc == api.ERR_INVALID_ARG and "NULL" in api.last_error()
+    holes = (ctypes.c_void_p * 5)(0x10000, 0x10000, None, 0x10000, 0x10000)
+    rc = L.dflash_materialize_ctx_kv(ctypes.byref(ok), fake, fake, fake, fake, None, fake, None, eps, theta,
+                                     ctypes.cast(holes, ctypes.c_void_p), pp, fake, None, fake, need, None)
+    assert rc == api.ERR_INVALID_ARG and "layer 2" in api.last_error()
