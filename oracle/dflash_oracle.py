@@ -119,11 +119,6 @@ def materialize_ctx_kv(hidden, commit_len, start_pos, W_f, b_f, W_kv, k_norm_w,
     return k_out, v_out
 
 
-def context_hidden(hidden_rows, W_f, b_f):
-    """h_ctx for a set of rows ([DFlash] KV 注入 step 2)."""
-    return _f64(hidden_rows) @ _f64(W_f).T + _f64(b_f)
-
-
 # ---------------------------------------------------------------------------
 # (b) draft block attention
 # ---------------------------------------------------------------------------

@@ -108,14 +108,20 @@ def test_ddtree_topk_temperature():
 
 @pytest.mark.parametrize("budget", [64, 512])
 def test_ddtree_walk_matches_oracle(budget):
+    # The tree both walks read is the oracle's own (oracle top-K, oracle
+    # best-first build), so the walk is compared independently of the GPU build.
     wl = W.QWEN3_4B_B8
     B, n, K = 3, 15, 8
-    zd, tk, tr = _tree_case(wl, B=B, n=n, K=K, budget=budget, seed=20 + budget)
-    zt = synth.ddtree_target_logits(wl, tr["node_token"], tr["node_parent"], tr["n_nodes"], seed=21, p_follow=0.9)
-    out = api.ddtree_verify_greedy(zt.to(DEV), tr["node_token"], tr["node_parent"], tr["n_nodes"], n, K)
+    zd = synth.draft_logits(wl, n, 20 + budget, "tree_zd", B=B)
+    tok, logp = O.ddtree_topk(f64(zd), K, 1.0)
+    ref_tree = O.ddtree_build(tok, logp, budget)
+    node_token = torch.from_numpy(ref_tree["node_token"])
+    node_parent = torch.from_numpy(ref_tree["node_parent"])
+    n_nodes = torch.from_numpy(ref_tree["n_nodes"])
+    zt = synth.ddtree_target_logits(wl, node_token, node_parent, n_nodes, seed=21, p_follow=0.9)
+    out = api.ddtree_verify_greedy(zt.to(DEV), node_token.to(DEV), node_parent.to(DEV), n_nodes.to(DEV), n, K)
     torch.cuda.synchronize()
-    ref = O.ddtree_walk_greedy(f64(zt), tr["node_token"].cpu().numpy(), tr["node_parent"].cpu().numpy(),
-                               tr["n_nodes"].cpu().numpy())
+    ref = O.ddtree_walk_greedy(f64(zt), ref_tree["node_token"], ref_tree["node_parent"], ref_tree["n_nodes"])
     for key in ("accept_len", "commit_len", "bonus", "path", "out_tokens"):
         np.testing.assert_array_equal(out[key].cpu().numpy(), ref[key], err_msg=key)
     assert ref["accept_len"].max() >= 2     # the synthetic target follows the tree for a few levels
