@@ -164,6 +164,31 @@ def oracle_step_estimate(wl, ctx_all, commit_rows, n_attn=2, n_verify=2, n_rows=
                            "sample_cpu_s": t_attn + t_g + t_s + t_m}
 
 
+def workload_config(wl, world=1):
+    """The ``config`` object of the JSON line: the workload, identical in both arms."""
+    return {"workload": wl.name, "B": wl.B, "k": wl.k, "L": wl.L, "V": wl.V, "d": wl.d,
+            "Hq/Hkv/D": f"{wl.Hq}/{wl.Hkv}/{wl.D}", "ctx": f"U[{wl.ctx_lo},{wl.ctx_hi}]",
+            "page": wl.page_size, "verify": f"greedy {wl.n_greedy} + sampled {wl.B - wl.n_greedy}",
+            "l2": "inputs larger than L2: ~5.7 GB of context K/V read per step (no flush needed)",
+            "parallelism": f"replicas x{world}"}
+
+
+def oracle_committed_rows(wl, seed=0):
+    """Rows the step commits (sum of commit_len over the batch), from the
+    oracle's accept rules on the step's verify inputs."""
+    import numpy as np
+    import oracle as O
+    from block_diffusion_speculative_fusion_gb300 import synth
+    vb = synth.verify_batch(wl, seed, n_max=wl.n_draft)
+    f = lambda t: t.float().numpy().astype(np.float64)
+    ng = wl.n_greedy
+    g = O.verify_greedy(f(vb["target_logits"][:ng]), vb["cand"][:ng].numpy(), vb["n_draft"][:ng].numpy())
+    s_ = O.verify_sample(f(vb["target_logits"][ng:]), f(vb["draft_logits"][ng:]), vb["cand"][ng:].numpy(),
+                         vb["n_draft"][ng:].numpy(), vb["u_acc"][ng:].numpy(), vb["u_final"][ng:].numpy(),
+                         wl.temperature)
+    return int(g["commit_len"].sum() + s_["commit_len"].sum())
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -180,7 +205,7 @@ def run_reference(args, wl):
     if rank != 0:
         return
     ctx_all = synth.ctx_lengths(wl, 0)
-    commit_rows = wl.B * 4          # expected committed rows per step (mean accept length ~3)
+    commit_rows = oracle_committed_rows(wl, 0)      # the step's committed rows (the GPU arm's count)
     for _ in range(args.warmup):
         oracle_step_estimate(wl, ctx_all, commit_rows, n_attn=1, n_verify=1, n_rows=2)
     est = []
@@ -195,8 +220,7 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "k": wl.k, "V": wl.V, "ctx": f"U[{wl.ctx_lo},{wl.ctx_hi}]",
-                   "page": wl.page_size},
+        "config": workload_config(wl, args.gpus),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -236,6 +260,97 @@ def traffic_from_profile(kernel_file):
         return None
 
 
+def cuda_kernel_times(torch, fn, reps):
+    """Device time of every kernel ``fn`` launches, from one CUPTI pass (torch
+    profiler) over ``reps`` calls: {kernel name: [durations in us, in launch
+    order]}. None when the profiler is unavailable."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+    except Exception:   # noqa: BLE001
+        return None
+    try:
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize()
+    except Exception:   # noqa: BLE001 - reported as missing, not fatal
+        return None
+    out = {}
+    evs = [e for e in prof.events() if str(getattr(e, "device_type", "")).endswith("CUDA")]
+    evs.sort(key=lambda e: e.time_range.start)
+    for e in evs:
+        dur = e.time_range.end - e.time_range.start
+        name = e.name.split("(")[0].split("<")[0].strip().split(" ")[-1].split("::")[-1]
+        out.setdefault(name, []).append(float(dur))
+    return out
+
+
+def step_rooflines(torch, st, wl, hbm, tf, reps=4):
+    """Per-kernel roofline of the step's kernels, each from its own device
+    time (CUPTI, eager launches outside the timed region) and its algorithmic
+    bytes: attention, the greedy and sampled verify kernels, the decode-sized
+    materialisation GEMMs and the rest of the materialisation."""
+    times = cuda_kernel_times(torch, st.step, reps)
+    if not times:
+        return {"note": "torch profiler (CUPTI) unavailable"}
+    el = 2
+    V, R, n = wl.V, wl.n_draft + 1, wl.n_draft
+    ng, ns = wl.n_greedy, wl.B - wl.n_greedy
+    acc = st.out["accept_len"][ng:].cpu()
+    T = float(st.out["commit_len"].sum().item())
+    rejected = int((acc < n).sum())
+    md, N2 = wl.m * wl.d, wl.kv_out
+    byts = {
+        "greedy_kernel": ng * R * V * el,
+        "sample_stats_kernel": ns * (R + n) * V * el,
+        "sample_draw_kernel": (2 * rejected + (ns - rejected)) * V * el,
+    }
+    mean = lambda v: sum(v) / len(v)
+    res = {}
+    for name, nbytes in byts.items():
+        if name in times:
+            us = mean(times[name])
+            res[name] = {"us": us, "bytes": nbytes, "GBps": nbytes / us / 1e3, "frac_hbm": nbytes / us / 1e3 / hbm,
+                         "bound": "hbm"}
+    if "gemm_tc_kernel" in times:
+        g = times["gemm_tc_kernel"]
+        g1, g2 = mean(g[0::2]), mean(g[1::2])
+        b1 = wl.d * md * el + T * md * el + T * wl.d * el
+        b2 = N2 * wl.d * el + T * wl.d * el + T * N2 * el
+        res["gemm_tc_kernel (decode, fusion)"] = {"us": g1, "bytes": b1, "frac_hbm": b1 / g1 / 1e3 / hbm,
+                                                  "bound": "hbm", "rows": T}
+        res["gemm_tc_kernel (decode, K/V)"] = {"us": g2, "bytes": b2, "frac_hbm": b2 / g2 / 1e3 / hbm,
+                                               "bound": "hbm", "rows": T}
+    mat = [k_ for k_ in times if k_.startswith("mat_")]
+    res["mat_other_us_per_step"] = {k_: sum(times[k_]) / reps for k_ in mat}
+    if "attn_tc_kernel" in times:
+        res["attn_tc_kernel_us"] = mean(times["attn_tc_kernel"])
+    return res
+
+
+def prefill_roofline(torch, wl, tf, tf_sus):
+    """The prefill-sized materialisation GEMMs (every context row of every
+    sequence at once) against the dense bf16 tensor-core peak, from device
+    kernel times (CUPTI)."""
+    call, T, _ = prefill_materialize_call(wl, "cuda:0")
+    for _ in range(2):
+        call()
+    times = cuda_kernel_times(torch, call, 3)
+    if not times or "gemm_tc_kernel" not in times:
+        return {"note": "torch profiler (CUPTI) unavailable"}
+    g = times["gemm_tc_kernel"]
+    f1 = 2.0 * T * wl.m * wl.d * wl.d
+    f2 = 2.0 * T * wl.d * wl.kv_out
+    u1, u2 = sum(g[0::2]) / len(g[0::2]), sum(g[1::2]) / len(g[1::2])
+    other = {k_: sum(v) / 3 for k_, v in times.items() if k_ != "gemm_tc_kernel"}
+    return {"workload": wl.name, "rows": T, "bound": "tensor", "unit": "TFLOP/s",
+            "gemm_fusion": {"us": u1, "tflops": f1 / u1 / 1e6, "frac": f1 / u1 / 1e6 / tf},
+            "gemm_kv": {"us": u2, "tflops": f2 / u2 / 1e6, "frac": f2 / u2 / 1e6 / tf},
+            "peak": tf, "peak_kind": "bf16_tflops (burst: the GEMMs are timed alone)",
+            "other_kernels_us": other}
+
+
 def capture_steps(torch, st, n):
     """One CUDA graph holding n steps, with a timing event (an external event
     node) around every call of the path. Returns (graph, events, None) or
@@ -256,11 +371,8 @@ def capture_steps(torch, st, n):
         else:
             ev[kind].append((pending.pop(kind), e))
 
-    g = torch.cuda.CUDAGraph()
     try:
-        with torch.cuda.graph(g):
-            for _ in range(n):
-                st.step(timer=timer)
+        g = st.capture(n, timer=timer)
     except Exception as exc:   # noqa: BLE001 - reported in the JSON line, the stream path runs instead
         torch.cuda.synchronize()
         return None, None, f"capture failed: {type(exc).__name__}: {exc}"[:200]
@@ -352,6 +464,11 @@ def run_ours(args, wl):
             launch_note = f"stream launches (graph event times {calls_us:.0f} us vs step {step_us:.0f} us)"
             ms_total, per_kernel, clk = timed_region(False)
     ms_max = max_over_ranks(ms_total, world, dev)
+    # a kernel that gave up a bounded wait (or met a bad page entry) leaves a
+    # code in its workspace: such a run's numbers are not valid
+    dev_errors = st.error_words()
+    if any(dev_errors):
+        raise RuntimeError(f"device error words after the timed region: {dev_errors}")
     commit_sum = float(st.out["commit_len"].sum().item())   # committed rows per step (every step alike)
     ms_per_step = ms_max / args.steps
     value = replica_throughput(args.steps, ms_max, world)
@@ -367,6 +484,23 @@ def run_ours(args, wl):
             "frac": achieved / hbm, "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind ==
             "measured" else "fallback 6.8 TB/s", "traffic": traffic_from_profile("attn.cu"),
             "algorithmic_bytes_per_launch": ab, "us_per_launch": attn_us}
+
+    # ---------------- per-kernel rooflines (CUPTI device times, outside the timed region) ----------------
+    roof_all = None
+    if rank == 0:
+        roof_all = step_rooflines(torch, st, wl, hbm, tf)
+        from block_diffusion_speculative_fusion_gb300 import workloads as W
+        roof_all["prefill_gemms"] = prefill_roofline(torch, W.LLAMA8B_B1, tf, tf_sus)
+        # step-level verify and materialisation, from the graph's own events
+        el, V, R, n = 2, wl.V, wl.n_draft + 1, wl.n_draft
+        ng, ns = wl.n_greedy, wl.B - wl.n_greedy
+        vbytes = ng * R * V * el + ns * (R + n) * V * el + ns * 2 * V * el
+        mbytes = (wl.d * wl.m * wl.d + wl.kv_out * wl.d) * el + commit_sum * (wl.m * wl.d + wl.kv_out) * el
+        roof_all["verify_in_step"] = {"us": per_kernel.get("verify"), "bytes": vbytes,
+                                      "frac_hbm": vbytes / per_kernel["verify"] / 1e3 / hbm}
+        roof_all["materialize_in_step"] = {"us": per_kernel.get("mat"), "bytes": mbytes,
+                                           "frac_hbm": mbytes / per_kernel["mat"] / 1e3 / hbm}
+        st.reset()
 
     # ---------------- end to end through the public API with host buffers ----------------
     # Every step copies its inputs from pinned host memory and reads its
@@ -436,20 +570,18 @@ def run_ours(args, wl):
             "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "k": wl.k, "L": wl.L, "V": wl.V, "d": wl.d,
-                       "Hq/Hkv/D": f"{wl.Hq}/{wl.Hkv}/{wl.D}", "ctx": f"U[{wl.ctx_lo},{wl.ctx_hi}]",
-                       "page": wl.page_size, "verify": f"greedy {wl.n_greedy} + sampled {wl.B - wl.n_greedy}",
-                       "l2": "inputs larger than L2: ~5.7 GB of context K/V read per step",
-                       "launch": launch_note,
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(wl, world),
+            "launch": launch_note,
             "verified_tokens_per_s": tokens_per_s, "committed_rows_per_step": commit_sum,
             "kernels_us_per_step": {"attn_per_layer": per_kernel.get("attn"),
                                     "attn_total": per_kernel.get("attn", 0) * wl.L,
                                     "verify": per_kernel.get("verify"), "materialize": per_kernel.get("mat")},
             "roofline": roof,
+            "roofline_all": roof_all,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": st.launches_per_step * args.steps,
+            "device_error_words": dev_errors,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -513,18 +645,39 @@ def run_kernel(args, wl):
 
 
 def _time_calls(fn, steps, warmup):
-    """Mean device time of ``fn()`` in microseconds (CUDA events on the current stream)."""
+    """Mean device time of ``fn()`` in microseconds: ``steps`` calls captured in
+    one CUDA graph and timed with CUDA events around its replay, so that the
+    figure is the kernels' time and not the per-call host cost of the binding
+    (stream launches only if the capture fails)."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g):
+            for _ in range(steps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        _time_calls.mode = "cuda graph"
+    except Exception:   # noqa: BLE001 - timed with stream launches instead
+        torch.cuda.synchronize()
+        g = None
+        _time_calls.mode = "stream launches"
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(steps):
-        fn()
+    if g is not None:
+        g.replay()
+    else:
+        for _ in range(steps):
+            fn()
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / steps
+
+
+_time_calls.mode = "cuda graph"
 
 
 def report_config(wl, args):
@@ -607,44 +760,70 @@ def report_config(wl, args):
             out["verify_sample_frac_hbm"] = gbs(ns * (2 * R - 1 + 2) * wl.V * el, us_s) / hbm
         del st
     else:
-        # ---- DLoop: S stages of (attention in L layers + gate), then one sampled verify ----
-        n_q = wl.k
+        # ---- DLoop looped step (DLoop page, mechanism 1 and the looped verify): stage s
+        # drafts only where every earlier gate continued; the gates chain on the device
+        # (stage s's active mask is stage s-1's cont) and count the drafted tokens; one
+        # sampled verify then checks the S_b * k concatenated candidates, fed the gates'
+        # row LSEs. Attention runs for every sequence at every stage (the kernel has no
+        # per-sequence mask), so the stage cost does not shrink as sequences stop. ----
+        n_q, k, S, n_max = wl.k, wl.n_draft, wl.stages, wl.n_max
         ctx = synth.ctx_lengths(wl, 0)
-        cache = synth.paged_cache(wl, headroom=wl.stages + n_q, seed=0, layers=1, ctx_len=ctx, device=dev)
+        cache = synth.paged_cache(wl, headroom=S + n_q, seed=0, layers=1, ctx_len=ctx, device=dev)
         pt, cl = cache.page_table.to(dev), cache.ctx_len.to(dev)
-        total_us = 0.0
-        for s in range(1, wl.stages + 1):
-            blk = {k_: v_.to(dev) for k_, v_ in synth.block_qkv(wl, 0, seed=0, n_kv_blk=n_q + s - 1).items()}
-            o = torch.empty_like(blk["q"])
-            us_a = _time_calls(lambda: api.block_attn(blk["q"], blk["k_blk"], blk["v_blk"], cache.k_pools[0],
-                                                      cache.v_pools[0], pt, cl, out=o), args.steps, args.warmup)
-            gb = {k_: v_.to(dev) for k_, v_ in synth.gate_batch(wl, s - 1, seed=0).items()}
-            us_gate = _time_calls(lambda: api.gate(gb["draft_logits"], gb["tokens"], wl.temperature, wl.gate_g,
-                                                   active=gb["active"]), args.steps, args.warmup)
-            out[f"stage{s}_attn_us_per_layer"] = us_a
-            out[f"stage{s}_gate_us"] = us_gate
-            total_us += wl.L * us_a + us_gate
-            if s == 1:
-                out["attn_frac_hbm"] = gbs(attn_bytes(float(ctx.sum()), dc.replace(wl, k=n_q)), us_a) / hbm
-                out["gate_frac_hbm"] = gbs(wl.B * wl.n_draft * wl.V * el, us_gate) / hbm
+        blks = [{k_: v_.to(dev) for k_, v_ in synth.block_qkv(wl, 0, seed=0, n_kv_blk=n_q + s - 1).items()}
+                for s in range(1, S + 1)]
+        attn_out = [torch.empty_like(b_["q"]) for b_ in blks]
         vb = {k_: v_.to(dev) for k_, v_ in synth.verify_batch(wl, seed=0).items()}
+        row_lse = torch.zeros(wl.B, n_max, dtype=torch.float32, device=dev)
+        n_verify = torch.zeros(wl.B, dtype=torch.int32, device=dev)
+        gouts = [{} for _ in range(S)]
+        vout = {}
+
+        def looped_step():
+            n_verify.zero_()
+            active = None
+            for s in range(S):
+                b_ = blks[s]
+                for _ in range(wl.L):
+                    api.block_attn(b_["q"], b_["k_blk"], b_["v_blk"], cache.k_pools[0], cache.v_pools[0], pt, cl,
+                                   out=attn_out[s])
+                api.gate_stage(vb["draft_logits"], vb["cand"], s, k, wl.temperature, wl.gate_g, active=active,
+                               row_lse=row_lse, n_verify=n_verify, out=gouts[s])
+                active = gouts[s]["cont"]
+            api.verify_sample(vb["target_logits"], vb["draft_logits"], vb["cand"], vb["u_acc"], vb["u_final"],
+                              wl.temperature, n_verify, draft_row_lse=row_lse, out=vout)
+
+        us_loop = _time_calls(looped_step, args.steps, args.warmup)
+        n_ver = n_verify.float()
+        out["looped_step_us"] = us_loop
+        out["looped_steps_per_s"] = 1e6 / us_loop
+        out["looped_mean_stages"] = float(n_ver.mean().item()) / k
+        out["looped_verified_tokens_per_s"] = float(vout["commit_len"].float().sum().item()) * 1e6 / us_loop
+        for s in range(S):
+            b_ = blks[s]
+            us_a = _time_calls(lambda: api.block_attn(b_["q"], b_["k_blk"], b_["v_blk"], cache.k_pools[0],
+                                                      cache.v_pools[0], pt, cl, out=attn_out[s]),
+                               args.steps, args.warmup)
+            us_g = _time_calls(lambda: api.gate_stage(vb["draft_logits"], vb["cand"], s, k, wl.temperature,
+                                                      wl.gate_g, out=gouts[s]), args.steps, args.warmup)
+            out[f"stage{s + 1}_attn_us_per_layer"] = us_a
+            out[f"stage{s + 1}_gate_us"] = us_g
+            if s == 0:
+                out["attn_frac_hbm"] = gbs(attn_bytes(float(ctx.sum()), dc.replace(wl, k=n_q)), us_a) / hbm
+                out["gate_frac_hbm"] = gbs(wl.B * k * wl.V * el, us_g) / hbm
+        n = n_max
         us_v = _time_calls(lambda: api.verify_sample(vb["target_logits"], vb["draft_logits"], vb["cand"], vb["u_acc"],
                                                      vb["u_final"], wl.temperature, vb["n_draft"]),
                            args.steps, args.warmup)
-        n = wl.n_max
-        out["verify_sample_us"] = us_v
-        out["verify_sample_frac_hbm"] = gbs(wl.B * (2 * n + 1 + 2) * wl.V * el, us_v) / hbm
-        out["looped_step_us_all_stages"] = total_us + us_v
-        # the same verify fed with the gates' row LSEs: the draft rows are not streamed
-        gl = api.gate(vb["draft_logits"], vb["cand"][:, 1:].contiguous(), wl.temperature, wl.gate_g,
-                      want_row_lse=True)
-        lse = gl["row_lse"]
+        out["verify_sample_all_stages_us"] = us_v
+        out["verify_sample_all_stages_frac_hbm"] = gbs(wl.B * (2 * n + 1 + 2) * wl.V * el, us_v) / hbm
+        full_lse = api.gate(vb["draft_logits"], vb["cand"][:, 1:].contiguous(), wl.temperature, wl.gate_g,
+                            want_row_lse=True)["row_lse"]
         us_vl = _time_calls(lambda: api.verify_sample(vb["target_logits"], vb["draft_logits"], vb["cand"],
                                                       vb["u_acc"], vb["u_final"], wl.temperature, vb["n_draft"],
-                                                      draft_row_lse=lse), args.steps, args.warmup)
-        out["verify_sample_gate_lse_us"] = us_vl
+                                                      draft_row_lse=full_lse), args.steps, args.warmup)
+        out["verify_sample_gate_lse_all_stages_us"] = us_vl
         out["verify_sample_gate_lse_frac_hbm"] = gbs(wl.B * (n + 1 + 2) * wl.V * el, us_vl) / hbm
-        out["looped_step_us_all_stages_gate_lse"] = total_us + us_vl
     if wl.dtype == "bf16" and wl.stages == 1 and wl.ctx_lo == wl.ctx_hi:
         # ---- prefill-sized materialisation: every context row of every sequence ----
         call_m, T, flops = prefill_materialize_call(wl, dev)
@@ -653,6 +832,7 @@ def report_config(wl, args):
         out["prefill_materialize_us"] = us_m
         out["prefill_materialize_tflops"] = flops / us_m / 1e6
         out["prefill_materialize_frac_bf16_peak"] = flops / us_m / 1e6 / tf
+    out["timing"] = _time_calls.mode
     print(json.dumps(out), flush=True)
 
 

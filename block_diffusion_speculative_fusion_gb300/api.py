@@ -22,6 +22,8 @@ F32, BF16 = 0, 1
 FLAG_ACCEPT_BOUNDARY, FLAG_CDF_BOUNDARY, FLAG_DEGENERATE, FLAG_INVALID = 1, 2, 4, 8
 FLAG_GATE_BOUNDARY = 1
 WS_COUNTER_BYTES = 16384
+WS_ERROR_WORD_OFFSET = WS_COUNTER_BYTES - 4
+DEVERR_BAD_PAGE = 100
 
 
 class DflashError(RuntimeError):
@@ -59,6 +61,8 @@ class TreeDims(ctypes.Structure):
 _SIGS = {
     "dflash_last_error": (ctypes.c_char_p, []),
     "dflash_last_launch_count": (ctypes.c_int, []),
+    "dflash_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "dflash_wait_limit_ns": (ctypes.c_uint64, []),
     "dflash_verify_greedy_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyDims)]),
     "dflash_verify_greedy": (ctypes.c_int, [ctypes.POINTER(VerifyDims), c_p, c_p, c_p, c_p, c_p, c_p,
                                             c_p, c_p, c_p, ctypes.c_size_t, c_p]),
@@ -71,6 +75,9 @@ _SIGS = {
     "dflash_gate_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GateDims)]),
     "dflash_gate": (ctypes.c_int, [ctypes.POINTER(GateDims), ctypes.c_float, ctypes.c_float, c_p, c_p,
                                    c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_size_t, c_p]),
+    # dims, stage, n_max, T, g, draft_logits, cand, active, c_s, cont, row_lse, flags, n_verify, ws, bytes, stream
+    "dflash_gate_stage": (ctypes.c_int, [ctypes.POINTER(GateDims), ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                         ctypes.c_float] + [c_p] * 9 + [ctypes.c_size_t, c_p]),
     # dims, T, target, draft, draft_row_lse, cand, n_draft, u_accept, u_final, accept_len, bonus,
     # commit_len, out_tokens, flags, probs, workspace, ws_bytes, stream
     "dflash_verify_sample_lse": (ctypes.c_int, [ctypes.POINTER(VerifyDims), ctypes.c_float] + [c_p] * 14 +
@@ -118,6 +125,16 @@ def last_error() -> str:
 
 def last_launch_count() -> int:
     return int(lib().dflash_last_launch_count())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of the tensor-core kernels' bounded waits (``dflash_set_wait_limit_ns``);
+    0 restores the 2 s default."""
+    _check(lib().dflash_set_wait_limit_ns(int(ns)))
+
+
+def wait_limit_ns() -> int:
+    return int(lib().dflash_wait_limit_ns())
 
 
 def _check(rc: int):
@@ -319,6 +336,37 @@ def gate(draft_logits: torch.Tensor, tokens: torch.Tensor, temperature: float = 
     return o
 
 
+def gate_stage(draft_logits: torch.Tensor, cand: torch.Tensor, stage: int, k: int, temperature: float = 1.0,
+               g: float = -0.5, active: Optional[torch.Tensor] = None, row_lse: Optional[torch.Tensor] = None,
+               n_verify: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+               ws: Optional[torch.Tensor] = None):
+    """One DLoop stage's gate on the looped layout (``dflash_gate_stage``):
+    draft_logits [B, n_max, V], cand [B, n_max + 1]; stage s's rows are
+    s*k .. s*k + k - 1. ``row_lse`` [B, n_max] and ``n_verify`` [B] are
+    accumulated across stages. Returns c, cont, flags."""
+    _dev(draft_logits, "draft_logits")
+    B, n_max, V = draft_logits.shape
+    dev = draft_logits.device
+    dims = GateDims(B, k, V, _dtype_code(draft_logits))
+    o = out if out is not None else {}
+    o.setdefault("c", torch.empty(B, dtype=torch.float32, device=dev))
+    o.setdefault("cont", torch.empty(B, dtype=torch.uint8, device=dev))
+    o.setdefault("flags", torch.empty(B, dtype=torch.uint8, device=dev))
+    need = lib().dflash_gate_workspace_size(ctypes.byref(dims))
+    if need == 0:
+        raise DflashError(ERR_INVALID_ARG, last_error())
+    w = ws if ws is not None else workspace(dev, need)
+    rc = lib().dflash_gate_stage(
+        ctypes.byref(dims), int(stage), int(n_max), ctypes.c_float(temperature), ctypes.c_float(g),
+        _dev(draft_logits, "draft_logits"), _dev(cand, "cand", torch.int64, (B, n_max + 1)),
+        _opt(active, "active", torch.uint8, (B,)), _dev(o["c"], "c", torch.float32),
+        _dev(o["cont"], "cont", torch.uint8), _opt(row_lse, "row_lse", torch.float32, (B, n_max)),
+        _opt(o.get("flags"), "flags", torch.uint8), _opt(n_verify, "n_verify", torch.int32, (B,)),
+        w.data_ptr(), w.numel(), _stream(dev))
+    _check(rc)
+    return o
+
+
 def draft_select(draft_logits: torch.Tensor, anchor: torch.Tensor, temperature: float = 0.0,
                  u_draft: Optional[torch.Tensor] = None, n_draft: Optional[torch.Tensor] = None,
                  out: Optional[dict] = None, ws: Optional[torch.Tensor] = None):
@@ -469,9 +517,22 @@ def block_attn(q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor, k_pool
 
 
 def device_error_word(ws: torch.Tensor) -> int:
-    """The sticky device-side error word of a workspace (0: no kernel gave up
-    waiting for a copy)."""
-    return int(ws[WS_COUNTER_BYTES - 4:WS_COUNTER_BYTES].view(torch.int32).item())
+    """The sticky device-side error word of a workspace (0: no error; 1-99: a
+    kernel gave up a bounded wait; DEVERR_BAD_PAGE: attention met a page-table
+    entry outside the pools). Synchronises with the device to read it."""
+    return int(ws[WS_ERROR_WORD_OFFSET:WS_COUNTER_BYTES].view(torch.int32).item())
+
+
+def clear_counters(ws: torch.Tensor) -> None:
+    """Zero a workspace's counter region (after a nonzero error word), on the
+    current stream."""
+    ws[:WS_COUNTER_BYTES].zero_()
+
+
+def error_words() -> Dict[Tuple[int, int], int]:
+    """Error word of every cached workspace (see ``workspace``), keyed by
+    (device, slot)."""
+    return {k: device_error_word(v) for k, v in _WS.items()}
 
 
 # ---------------------------------------------------------------------------

@@ -1,6 +1,7 @@
 // C ABI of libdflash: host-side validation, workspace layout and dispatch.
 // Nothing here allocates device memory; every call is asynchronous on the
 // caller's stream.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -13,6 +14,9 @@ namespace {
 
 thread_local std::string g_err;
 thread_local int g_launches = 0;
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
 // Kernel plans are sized for the 152-SM GB300 so that workspace sizes depend on
 // the dims alone (no device query, callable without a GPU).
@@ -63,10 +67,21 @@ int check_verify_dims(const dflash_verify_dims* d, bool sampled) {
 
 }  // namespace
 
+namespace dflash {
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+}  // namespace dflash
+
 extern "C" {
 
 const char* dflash_last_error(void) { return g_err.c_str(); }
 int dflash_last_launch_count(void) { return g_launches; }
+
+int dflash_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : (unsigned long long)ns, std::memory_order_relaxed);
+  g_err.clear();
+  return DFLASH_OK;
+}
+uint64_t dflash_wait_limit_ns(void) { return g_wait_ns.load(std::memory_order_relaxed); }
 
 // ------------------------------------------------------------------ verify ---
 size_t dflash_verify_greedy_workspace_size(const dflash_verify_dims* d) {
@@ -248,6 +263,8 @@ int dflash_gate(const dflash_gate_dims* d, float temperature, float g, const voi
   if (rc) return rc;
   dflash::GateArgs a{};
   a.B = d->B; a.k = d->k; a.V = d->V; a.dtype = d->dtype; a.temperature = temperature; a.g = g;
+  a.layout = dflash::GateLayout{d->k, 0, d->k, 0, d->k, 0, 1};
+  a.n_verify = nullptr;
   a.draft_logits = draft_logits; a.tokens = tokens; a.active = active;
   a.c_s = c_s; a.cont = cont; a.row_lse = row_lse; a.flags = flags;
   a.counters = (int32_t*)workspace;
@@ -255,6 +272,35 @@ int dflash_gate(const dflash_gate_dims* d, float temperature, float g, const voi
   a.stream = (cudaStream_t)stream;
   cudaError_t e = dflash::launch_gate(a, kPlanSms);
   if (e != cudaSuccess) return cuda_fail(e, "gate launch");
+  return ok(1);
+}
+
+int dflash_gate_stage(const dflash_gate_dims* d, int32_t stage, int32_t n_max, float temperature, float g,
+                      const void* draft_logits, const int64_t* cand, const uint8_t* active, float* c_s,
+                      uint8_t* cont, float* row_lse, uint8_t* flags, int32_t* n_verify, void* workspace,
+                      size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_gate_dims(d);
+  if (rc) return rc;
+  if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
+  if (stage < 0 || n_max < 1 || (long)(stage + 1) * d->k > (long)n_max)
+    return fail(DFLASH_ERR_INVALID_ARG, "stage %d of %d tokens does not fit n_max=%d", stage, d->k, n_max);
+  if (n_max + 1 > 256) return fail(DFLASH_ERR_UNSUPPORTED, "n_max=%d > 255", n_max);
+  if (!draft_logits || !cand || !c_s || !cont)
+    return fail(DFLASH_ERR_INVALID_ARG, "gate_stage: a required pointer is NULL");
+  rc = check_ws(workspace, ws_bytes, dflash_gate_workspace_size(d));
+  if (rc) return rc;
+  dflash::GateArgs a{};
+  a.B = d->B; a.k = d->k; a.V = d->V; a.dtype = d->dtype; a.temperature = temperature; a.g = g;
+  // stage rows s*k .. of [B, n_max, V]; tokens after the anchor in [B, n_max + 1]
+  a.layout = dflash::GateLayout{n_max, stage * d->k, n_max + 1, 1 + stage * d->k, n_max, stage * d->k, 0};
+  a.n_verify = n_verify;
+  a.draft_logits = draft_logits; a.tokens = cand; a.active = active;
+  a.c_s = c_s; a.cont = cont; a.row_lse = row_lse; a.flags = flags;
+  a.counters = (int32_t*)workspace;
+  a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
+  a.stream = (cudaStream_t)stream;
+  cudaError_t e = dflash::launch_gate(a, kPlanSms);
+  if (e != cudaSuccess) return cuda_fail(e, "gate_stage launch");
   return ok(1);
 }
 

@@ -47,6 +47,7 @@ struct AttnParams {
   // a sequence, TK = 64 / hpi keys per tile, br = K/V rows per TMA box
   int hpi, Gi, Mi, n_groups, TK, br;
   float scale_log2;  // softmax scale * log2(e)
+  unsigned long long wait_ns;   // limit of every bounded wait on a work barrier
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -94,7 +95,7 @@ constexpr int kGrid = 152;                  // persistent CTAs: one per SM
 constexpr int kMaxSeqs = 1024;              // sequences per call on this path
 constexpr int kPtMax = 512;                 // page-table entries of one item
 constexpr int kClaimAhead = 3;              // tiles before an item's end at which the next is claimed
-constexpr int kBarBytes = (2 * kMaxStages + 31) * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
+constexpr int kBarBytes = (2 * kMaxStages + 33) * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
                           (2 * 2 * 128 + 2 * 4 * 128) * 4 + 64;
 }  // namespace attn_tc
 
@@ -165,11 +166,6 @@ __device__ __forceinline__ void decode_item(const AttnParams& p, const int* cum,
   it.n_tiles = it.n_tiles_ctx + ((it.split == it.nsplit - 1 && p.n_kv > 0) ? 1 : 0);
 }
 
-// Barrier `id` among `n` threads (whole warps) of the CTA.
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // 2^x on the special-function unit (flush-to-zero; P is rounded to bf16 anyway).
 __device__ __forceinline__ float ex2_ftz(float x) {
   float y;
@@ -230,7 +226,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint64_t* mma_done = s_full + 20;
   uint64_t* xbar = s_full + 21;           // [4 quarters][2]: the two softmax warps of a quarter
   uint64_t* l_full = s_full + 29;         // [2]  softmax -> epilogue: row max and sums of the item
-  int* ring = reinterpret_cast<int*>(s_full + 31);             // [2] item ids
+  uint64_t* mg_in = s_full + 31;          // epilogue warps -> ticket taker: split partials published
+  uint64_t* mg_out = s_full + 32;         // ticket taker -> epilogue warps: last_sm holds the ticket
+  int* ring = reinterpret_cast<int*>(s_full + 33);             // [2] item ids
   int* cum = ring + 2;                                         // [B + 1] item prefix per rank
   uint16_t* order = reinterpret_cast<uint16_t*>(cum + (kMaxSeqs + 1));   // [B] sequence of each rank
   int* pt_s = reinterpret_cast<int*>(order + kMaxSeqs);        // [2][kPtMax] page rows of two items
@@ -262,6 +260,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     mbar_init(mma_done, 1);
     for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 2);
+    mbar_init(mg_in, W);
+    mbar_init(mg_out, 1);
     *abort_flag = 0;
     *consumed_sm = 0;
     fence_barrier_init();
@@ -337,11 +337,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         const bool use = u * 32 + lane < n_lp && lp * ps < it.C && lp < p.max_pages;
         phys[u] = use ? __ldg(ptb + lp) : 0;
       }
+      bool bad = false;
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
-        const int ph = (phys[u] >= 0 && phys[u] < p.num_pages) ? phys[u] : 0;
+        // an entry outside [0, num_pages) for a position inside the context is
+        // an input error: record it and read page 0 instead (never out of bounds)
+        const bool in_range = phys[u] >= 0 && phys[u] < p.num_pages;
+        const int ph = in_range ? phys[u] : 0;
+        bad |= !in_range;
         if (u * 32 + lane < n_lp) pt_s[tb * kPtMax + u * 32 + lane] = ph * ps;
       }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(p.err, 0, kDevErrBadPage);
       __syncwarp();
     };
     int cur = 0;
@@ -352,7 +358,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const bool last = cur >= n_items;
       const int slot = item_seq & 1;
       bool w = true;
-      if (lane == 0) w = wait_or_abort(&it_empty[slot], (uint32_t)(((item_seq >> 1) & 1) ^ 1), abort_flag, p.err, 21);
+      if (lane == 0) w = wait_or_abort(&it_empty[slot], (uint32_t)(((item_seq >> 1) & 1) ^ 1), abort_flag, p.err, 21, p.wait_ns);
       if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) break;
       if (lane == 0) {
         ring[slot] = last ? -1 : cur;
@@ -372,7 +378,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           const int st = tile_seq % S;
           uint8_t* ks = kv_s + st * 2 * kTileBytes;
           uint8_t* vs = ks + kTileBytes;
-          if (!wait_or_abort(&kv_empty[st], (uint32_t)(((tile_seq / S) & 1) ^ 1), abort_flag, p.err, 23)) {
+          if (!wait_or_abort(&kv_empty[st], (uint32_t)(((tile_seq / S) & 1) ^ 1), abort_flag, p.err, 23, p.wait_ns)) {
             ok = false;
           } else if (j < it.n_tiles_ctx) {
             mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
@@ -431,7 +437,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       while (ok) {
         const int slot = item_seq & 1;
         const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
-        if (!wait_or_abort(&it_full[slot], par, abort_flag, p.err, 24)) break;
+        if (!wait_or_abort(&it_full[slot], par, abort_flag, p.err, 24, p.wait_ns)) break;
         const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
         mbar_arrive(&it_empty[slot]);
         if (item < 0) break;
@@ -440,7 +446,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         // O: one buffer per item slot (ALT = 1), or both buffers for every item (ALT = 2)
         const int oi = ALT == 2 ? 0 : slot;
         const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
-        if (!wait_or_abort(&q_full[0], (uint32_t)(item_seq & 1), abort_flag, p.err, 25)) break;
+        if (!wait_or_abort(&q_full[0], (uint32_t)(item_seq & 1), abort_flag, p.err, 25, p.wait_ns)) break;
         tc_fence_after();
         // The item's S MMAs go ahead while the epilogue still reads the previous
         // item's O; only its first P V waits for the O buffer (o_ready).
@@ -462,10 +468,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         };
         auto issue_pv = [&](int t, int j) -> bool {
           if (!o_ready) {
-            if (!wait_or_abort(&o_empty[oi], opar ^ 1u, abort_flag, p.err, 26)) return false;
+            if (!wait_or_abort(&o_empty[oi], opar ^ 1u, abort_flag, p.err, 26, p.wait_ns)) return false;
             o_ready = true;
           }
-          if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27)) return false;
+          if (!wait_or_abort(&p_full[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 27, p.wait_ns)) return false;
           pv_issue(t, j);
           return true;
         };
@@ -489,7 +495,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               }
             }
             if (*abort_flag) return false;
-            if (global_timer_ns() - t_start > 2000000000ull) {
+            if (global_timer_ns() - t_start > p.wait_ns) {
               *abort_flag = 1;
               atomicCAS(p.err, 0, 28);
               return false;
@@ -501,7 +507,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           const int st = t % S;
           bool pv_pending = j >= 1;   // the P V of tile t - 1 is still to issue
           if (!wait_tile(t, j, pv_pending)) { ok = false; break; }
-          if (!wait_or_abort(&s_empty[t & 1], (uint32_t)(((t >> 1) & 1) ^ 1), abort_flag, p.err, 29)) {
+          if (!wait_or_abort(&s_empty[t & 1], (uint32_t)(((t >> 1) & 1) ^ 1), abort_flag, p.err, 29, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -552,12 +558,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       ++xs;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
-      return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err, 37));
+      return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err, 37, p.wait_ns));
     };
     while (ok) {
       const int slot = item_seq & 1;
       const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
-      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[slot], par, abort_flag, p.err, 31))) break;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[slot], par, abort_flag, p.err, 31, p.wait_ns))) break;
       const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&it_empty[slot]);
@@ -571,7 +577,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       for (int j = ALT == 2 ? ((chalf - tile_seq) & 1) : 0; j < it.n_tiles; j += ALT) {
         const int t = tile_seq + j;
         const int sb = t & 1;
-        if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[sb], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 32))) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[sb], (uint32_t)((t >> 1) & 1), abort_flag, p.err, 32, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -623,7 +629,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           // O must hold every earlier tile of the item before it is rescaled
           // (the last one into this O is tile t - ALT)
           if (!__all_sync(0xffffffffu, wait_or_abort(&pv_done[(t - ALT) & 1], (uint32_t)(((t - ALT) >> 1) & 1),
-                                                     abort_flag, p.err, 33))) {
+                                                     abort_flag, p.err, 33, p.wait_ns))) {
             ok = false;
             break;
           }
@@ -650,7 +656,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         l_part = l_part * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         // P buffer t & 1 was last read by the P V of tile t - 2
         if (t >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&pv_done[sb], (uint32_t)(((t - 2) >> 1) & 1),
-                                                           abort_flag, p.err, 34))) {
+                                                           abort_flag, p.err, 34, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -711,7 +717,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // the ring entry of item number `seq`: an item, -1 (no more) or -2 (gave up)
     auto read_item = [&](int seq) -> int {
       const int sl = seq & 1;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[sl], (uint32_t)((seq >> 1) & 1), abort_flag, p.err, 38)))
+      if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[sl], (uint32_t)((seq >> 1) & 1), abort_flag, p.err, 38, p.wait_ns)))
         return -2;
       const int v = *reinterpret_cast<volatile int*>(&ring[sl]);
       __syncwarp();
@@ -739,7 +745,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       // the previous item's last S must have read the buffer
       if (seq > 0 &&
-          !__all_sync(0xffffffffu, wait_or_abort(&q_empty[0], (uint32_t)((seq - 1) & 1), abort_flag, p.err, 40)))
+          !__all_sync(0xffffffffu, wait_or_abort(&q_empty[0], (uint32_t)((seq - 1) & 1), abort_flag, p.err, 40, p.wait_ns)))
         return false;
       tc_fence_after();
       tmem_st32(tmem_base + lane_off + kQCol, qv);
@@ -750,7 +756,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (lane == 0) mbar_arrive(&q_full[0]);
       return true;
     };
-    int item_seq = 0;
+    int item_seq = 0, n_merge = 0;
     int item = read_item(0);
     bool qok = item >= 0 ? put_q(item, 0) : false;
     while (item >= 0 && qok) {
@@ -763,8 +769,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       decode_item(p, cum, order, cap, item, it);
       const int oi = ALT == 2 ? 0 : slot;
       const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&l_full[slot], par, abort_flag, p.err, 39))) break;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&o_full[oi], opar, abort_flag, p.err, 35))) break;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&l_full[slot], par, abort_flag, p.err, 39, p.wait_ns))) break;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&o_full[oi], opar, abort_flag, p.err, 35, p.wait_ns))) break;
       tc_fence_after();
       const float* mls = ml_s + slot * 512;
       const float ma = mls[r], la = mls[128 + r], mb = mls[256 + r], lb = mls[384 + r];
@@ -833,16 +839,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         // Completion ticket of the (sequence, group): the CTA whose split
         // finishes last merges every split's partial (still in L2) into the
         // output. Partials are published (fence) before the ticket is taken.
+        // The epilogue warps meet on two mbarriers with bounded waits (not a
+        // bar.sync), so that a warp that gave up a wait strands no other.
         __threadfence();
-        named_bar_sync(1, W * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mg_in);
+        const uint32_t mpar = (uint32_t)(n_merge & 1);
+        ++n_merge;
         const size_t grp = (size_t)it.b * p.n_groups + it.g;
-        if (quarter == 0 && lane == 0) {
-          const int prev = atomicAdd(&p.counters[grp], 1);
-          const int last = prev == it.nsplit - 1;
-          if (last) p.counters[grp] = 0;   // every split has arrived: ready for the next launch
-          *last_sm = last;
+        if (quarter == 0) {
+          if (!__all_sync(0xffffffffu, wait_or_abort(mg_in, mpar, abort_flag, p.err, 41, p.wait_ns))) break;
+          if (lane == 0) {
+            const int prev = atomicAdd(&p.counters[grp], 1);
+            const int last = prev == it.nsplit - 1;
+            if (last) p.counters[grp] = 0;   // every split has arrived: ready for the next launch
+            *last_sm = last;
+            mbar_arrive(mg_out);             // release: publishes last_sm
+          }
         }
-        named_bar_sync(1, W * 32);
+        if (!__all_sync(0xffffffffu, wait_or_abort(mg_out, mpar, abort_flag, p.err, 42, p.wait_ns))) break;
         if (*last_sm && r < p.Mi) {
           __threadfence();
           const float2* ml = p.part_ml + grp * p.max_splits * p.Mi + r;
@@ -913,7 +928,7 @@ attn_generic_kernel(const T* __restrict__ q, const T* __restrict__ k_blk, const 
                     const T* __restrict__ k_pool, const T* __restrict__ v_pool,
                     const int32_t* __restrict__ page_table, const int32_t* __restrict__ ctx_len,
                     T* __restrict__ out, int n_q, int n_kv, int Hq, int Hkv, int D, int page_size,
-                    int max_pages, int num_pages, float scale, int causal) {
+                    int max_pages, int num_pages, float scale, int causal, int* __restrict__ err) {
   constexpr int KC = 128;   // keys per chunk (one per thread)
   __shared__ float qs[256];
   __shared__ float ps[KC];
@@ -936,8 +951,12 @@ attn_generic_kernel(const T* __restrict__ q, const T* __restrict__ k_blk, const 
     if (key < T_total) {
       if (key < C) {
         const int lp = key / page_size;
-        int phys = (lp < max_pages) ? page_table[(size_t)b * max_pages + lp] : 0;
-        if (phys < 0 || phys >= num_pages) phys = 0;
+        int phys = (lp < max_pages) ? page_table[(size_t)b * max_pages + lp] : -1;
+        if (phys < 0 || phys >= num_pages) {
+          // input error (recorded); page 0 is read instead, never out of bounds
+          if (err) atomicCAS(err, 0, kDevErrBadPage);
+          phys = 0;
+        }
         const size_t row = (size_t)phys * page_size + key % page_size;
         krow = k_pool + (row * Hkv + g) * D;
         vrow_kind = (int)row;
@@ -1041,12 +1060,12 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
       attn_generic_kernel<float><<<grid, 128, 0, a.stream>>>(
           (const float*)a.q, (const float*)a.k_blk, (const float*)a.v_blk, (const float*)a.k_pool,
           (const float*)a.v_pool, a.page_table, a.ctx_len, (float*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
-          a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal);
+          a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal, a.err);
     else
       attn_generic_kernel<bf16><<<grid, 128, 0, a.stream>>>(
           (const bf16*)a.q, (const bf16*)a.k_blk, (const bf16*)a.v_blk, (const bf16*)a.k_pool,
           (const bf16*)a.v_pool, a.page_table, a.ctx_len, (bf16*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
-          a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal);
+          a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal, a.err);
     return cudaGetLastError();
   }
   using namespace attn;
@@ -1070,6 +1089,7 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   p.max_splits = attn_max_splits(a.max_ctx, p.TK);
   p.max_ctx = a.max_ctx;
   p.scale_log2 = a.scale * kLog2e;
+  p.wait_ns = wait_limit_ns();
   const int M = p.Mi;
   const size_t ctas = (size_t)a.B * p.n_groups * p.max_splits;
   char* ws = (char*)a.scratch;

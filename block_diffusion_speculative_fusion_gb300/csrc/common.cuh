@@ -91,18 +91,31 @@ __device__ __forceinline__ bool take_ticket_is_last_t0(int32_t* counter, int gro
 }
 
 // ---------------------------------------------------------------------------
-// Online max / scaled-sum pairs in log2 units: a row's statistics are
-// m = max(z) * k2 (rounded once) and s = sum 2^(z * k2 - m) with every exponent
-// formed by one fused multiply-add, so that the same expression evaluated later
-// for one element of the row is consistent with the sum.
+// Online max / scaled-sum pairs in log2 units: a row's statistics are an
+// integer-valued offset m = rint(max(z) * k2) and s = sum 2^(fma(z, k2, -m)),
+// every exponent formed by one fused multiply-add, so that the same expression
+// evaluated later for one element of the row is consistent with the sum.
+// Because the offsets are integers, rescaling a partial sum to another offset
+// multiplies it by an exact power of two: merging partials adds no rounding
+// beyond the one addition (a non-integer offset would put an exp2 rounding
+// into every merge of the reduction tree).
 // ---------------------------------------------------------------------------
 struct MS { float m; float s; };
+
+// 2^k for an integer-valued k <= 0, exact (0 below the normal range).
+__device__ __forceinline__ float pow2i(float k) {
+  const int ki = (int)k;
+  return ki < -126 ? 0.f : __int_as_float((ki + 127) << 23);
+}
+
+// The integer-valued log2 offset of a row whose largest logit is v.
+__device__ __forceinline__ float ms_offset(float v, float k2) { return rintf(v * k2); }
 
 __device__ __forceinline__ MS ms_merge(MS a, MS b) {
   const float M = fmaxf(a.m, b.m);
   if (M == -CUDART_INF_F) return MS{M, 0.f};
-  const float sa = (a.m == -CUDART_INF_F) ? 0.f : a.s * exp2f(a.m - M);
-  const float sb = (b.m == -CUDART_INF_F) ? 0.f : b.s * exp2f(b.m - M);
+  const float sa = (a.m == -CUDART_INF_F) ? 0.f : a.s * pow2i(a.m - M);
+  const float sb = (b.m == -CUDART_INF_F) ? 0.f : b.s * pow2i(b.m - M);
   return MS{M, sa + sb};
 }
 

@@ -49,8 +49,8 @@ ddtree_topk_kernel(const T* __restrict__ z, int rows, int V, int K, float k2, in
     float zmax = -CUDART_INF_F;
     MS acc{-CUDART_INF_F, 0.f};
     auto raise_to = [&](float v) {
-      const float m2 = v * k2;
-      acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f(acc.m - m2);
+      const float m2 = ms_offset(v, k2);
+      acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * pow2i(acc.m - m2);
       acc.m = m2;
       zmax = v;
     };

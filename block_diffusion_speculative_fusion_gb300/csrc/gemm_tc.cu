@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap_l,
                const __grid_constant__ CUtensorMap xmap_m, const __grid_constant__ CUtensorMap xmap_s,
                float* __restrict__ part, const int32_t* __restrict__ meta, int per_idx, int T_max, int N, int MT,
-               int KB, int box_l, int box_m, int* err) {
+               int KB, int box_l, int box_m, int* err, unsigned long long wait_ns) {
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -157,7 +157,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
       while (ok && tc_next(w, wave, pos, c)) {
         const int rows16 = (c.rows + 15) / 16 * 16;
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
-          if (!wait_or_abort(&empty[stage], phase ^ 1u, abort_flag, err, 2)) { ok = false; break; }
+          if (!wait_or_abort(&empty[stage], phase ^ 1u, abort_flag, err, 2, wait_ns)) { ok = false; break; }
           uint8_t* sa = smem + stage * w.stage_bytes;
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(A_BYTES + rows16 * BK * 2));
           tma_load_2d(sa, &wmap, &full[stage], kb * BK, c.m_tile * BM);
@@ -188,10 +188,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
       int wave = 0, pos = w.lo;
       TcPiece c;
       while (ok && tc_next(w, wave, pos, c)) {
-        if (!wait_or_abort(&tempty[buf], buf_phase ^ 1u, abort_flag, err, 4)) break;
+        if (!wait_or_abort(&tempty[buf], buf_phase ^ 1u, abort_flag, err, 4, wait_ns)) break;
         tc_fence_after();
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
-          if (!wait_or_abort(&full[stage], phase, abort_flag, err, 5)) { ok = false; break; }
+          if (!wait_or_abort(&full[stage], phase, abort_flag, err, 5, wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * w.stage_bytes);
           const uint64_t adesc = sdesc_sw128(sa);
@@ -232,7 +232,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
     TcPiece c;
     while (tc_next(w, wave, pos, c)) {
       const int seg = c.seg;
-      if (!wait_or_abort(&tfull[buf], buf_phase, abort_flag, err, 7)) break;
+      // a warp-wide decision: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, wait_or_abort(&tfull[buf], buf_phase, abort_flag, err, 7, wait_ns))) break;
       tc_fence_after();
       const int f = c.m_tile * BM + quarter * 32 + lane;
       for (int g = 0; g < c.ng; ++g) {
@@ -313,7 +314,7 @@ cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int3
   cudaError_t e = opt_in.ensure(gemm_tc_kernel, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   gemm_tc_kernel<<<GRID, THREADS, SMEM_BYTES, st>>>(wmap, xmap_l, xmap_m, xmap_s, part, meta, per_idx, T_max, N,
-                                                    N / BM, K / BK, box_l, box_m, err);
+                                                    N / BM, K / BK, box_l, box_m, err, wait_limit_ns());
   return cudaGetLastError();
 }
 

@@ -11,6 +11,15 @@ namespace dflash {
 
 inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
 
+// Limit in nanoseconds of the bounded waits on work barriers in the
+// tensor-core kernels (attention, context GEMMs); read at each launch.
+// Default 2 s; dflash_set_wait_limit_ns changes it for the whole process.
+unsigned long long wait_limit_ns();
+
+// Device error word code: a page-table entry outside [0, num_pages) inside a
+// context (attention reads page 0 for it).
+constexpr int kDevErrBadPage = 100;
+
 // Opt a kernel into `bytes` of dynamic shared memory on the calling thread's
 // current device. The attribute belongs to each device's context, so it is set
 // once per device (and again only to raise it), under a lock so that concurrent
@@ -72,8 +81,19 @@ cudaError_t launch_verify_greedy(const VerifyArgs& a, int num_sms);
 cudaError_t launch_verify_sample(const VerifyArgs& a, int num_sms);
 
 // ------------------------------------------------------------------ gate ---
+// Where a gate call finds its rows: sequence b's i-th row of the stage is row
+// z_row0 + i of z_rows rows of that sequence; its token is tokens[b *
+// tok_stride + tok0 + i]; its LSE goes to row_lse[b * lse_stride + lse0 + i].
+// The plain gate is z_rows = tok_stride = lse_stride = k and zero offsets.
+struct GateLayout {
+  int z_rows, z_row0, tok_stride, tok0, lse_stride, lse0;
+  int lse_inactive;   // 1: row LSEs of inactive sequences are computed too
+};
+
 struct GateArgs {
   int B, k, V, dtype;
+  GateLayout layout;
+  int32_t* n_verify;  // [B] or nullptr: += k for every active sequence
   float temperature, g;
   const void* draft_logits;
   const int64_t* tokens;

@@ -76,7 +76,7 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 }
 
 // Streaming statistics of elements [e0, e1) of one row in log2 units:
-// m = max(z) * k2, s = sum 2^(fma(z, k2, -m)). The same code serves target and
+// m = rint(max(z) * k2), s = sum 2^(fma(z, k2, -m)). The same code serves target and
 // draft rows, so identical rows give bit-identical statistics.
 template <typename T>
 __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2) {
@@ -84,8 +84,8 @@ __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2)
   float zmax = -CUDART_INF_F;   // running max in logit units (exact comparisons)
   MS acc{-CUDART_INF_F, 0.f};
   auto raise_to = [&](float v) {
-    const float m2 = v * k2;
-    acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * exp2f(acc.m - m2);
+    const float m2 = ms_offset(v, k2);
+    acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * pow2i(acc.m - m2);
     acc.m = m2;
     zmax = v;
   };

@@ -68,16 +68,20 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Bounded wait that also gives up when another role of the CTA has aborted.
+// Bounded wait on a work barrier that also gives up when another role of the
+// CTA has aborted. limit_ns comes from the host (dflash_set_wait_limit_ns); the
+// waits that drain a CTA's own copies and MMAs before it exits keep their fixed
+// 2 s limit (mbar_wait_bounded), so a short work limit never lets a CTA leave
+// with a copy still landing in its shared memory.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                              int code) {
+                                              int code, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > 2000000000ull) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       if (err) atomicCAS(err, 0, code);
       return false;

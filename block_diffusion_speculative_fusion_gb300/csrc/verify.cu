@@ -424,24 +424,28 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const fl
       const MS pt = rs[i - 1], pd = rs[R + i - 1];
       const float zxt = __ldcg(zx + (size_t)b * RR + (i - 1));
       const float zxd = zx[(size_t)b * RR + R + (i - 1)];
-      // exponents formed exactly as in the row sums
-      const float at = fmaf(zxt, k2, -pt.m), ad = fmaf(zxd, k2, -pd.m);
-      const float et = exp2f(at), ed = exp2f(ad);
-      const float px = et / pt.s, qx = ed / pd.s;
+      // The candidate's exponents in fp64, with the same scale k2 and offsets
+      // m as the fp32 row sums (z * k2 is exact in fp64 for bf16 or fp32 z):
+      // p(x) = 2^(z_t k2 - m_t) / s_t, q(x) likewise, p/q = 2^(at - ad) s_d / s_t.
+      // Only the row sums' rounding (~1e-7 relative) remains in the ratio that
+      // the 1e-6 boundary band is measured against.
+      const double k2d = (double)k2;
+      const double at = (double)zxt * k2d - (double)pt.m, ad = (double)zxd * k2d - (double)pd.m;
+      const double et = exp2(at), ed = exp2(ad);
+      const double px = et / (double)pt.s, qx = ed / (double)pd.s;
       if (probs) {
-        probs[(size_t)b * (2 * n_max + 1) + (i - 1)] = px;
-        probs[(size_t)b * (2 * n_max + 1) + n_max + (i - 1)] = qx;
+        probs[(size_t)b * (2 * n_max + 1) + (i - 1)] = (float)px;
+        probs[(size_t)b * (2 * n_max + 1) + n_max + (i - 1)] = (float)qx;
       }
-      float ratio;
-      if (ed == 0.f) {
+      double ratio;
+      if (!(ed > 0.0) || !(qx > 0.0)) {
         flags |= 8;                      // DFLASH_FLAG_INVALID
-        ratio = CUDART_INF_F;
+        ratio = (double)CUDART_INF_F;
       } else {
-        // p/q = 2^(at - ad) * sd / st
-        ratio = exp2f(at - ad) * (pd.s / pt.s);
+        ratio = exp2(at - ad) * ((double)pd.s / (double)pt.s);
       }
-      const float u = u_acc[(size_t)b * n_max + (i - 1)];
-      if (ratio < 1.f && fabsf(u - ratio) < 1e-6f) flags |= 1;   // ACCEPT_BOUNDARY
+      const double u = (double)u_acc[(size_t)b * n_max + (i - 1)];
+      if (ratio < 1.0 && fabs(u - ratio) < 1e-6) flags |= 1;   // ACCEPT_BOUNDARY
       if (u < ratio) {
         ++a;
       } else {
@@ -485,21 +489,21 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
             const uint8_t* __restrict__ active, int k, int V, int nch, int chunk, float k2,
-            float inv_t, float g, MS* __restrict__ parts, float* __restrict__ zx,
+            float inv_t, float g, GateLayout lay, MS* __restrict__ parts, float* __restrict__ zx,
             int32_t* __restrict__ counters, float* __restrict__ c_s, uint8_t* __restrict__ cont,
-            float* __restrict__ row_lse, uint8_t* __restrict__ flags) {
+            float* __restrict__ row_lse, uint8_t* __restrict__ flags, int32_t* __restrict__ n_verify) {
   const int c = blockIdx.x;
-  const int row = blockIdx.y;
-  const int b = row / k;
+  const int row = blockIdx.y;             // b * k + i: the i-th row of this stage of sequence b
+  const int b = row / k, i = row - b * k;
   const bool on = active ? active[b] != 0 : true;
   MS ms{-CUDART_INF_F, 0.f};
-  const bool need = on || row_lse != nullptr;
+  const bool need = on || (row_lse != nullptr && lay.lse_inactive);
   if (need) {
-    const T* zr = z + (size_t)row * V;
+    const T* zr = z + ((size_t)b * lay.z_rows + lay.z_row0 + i) * V;
     const int e0 = c * chunk, e1 = min(V, e0 + chunk);
     ms = row_chunk_ms<T>(zr, e0, e1, k2);
     if (threadIdx.x == 0) {
-      const int64_t x = tokens[row];
+      const int64_t x = tokens[(size_t)b * lay.tok_stride + lay.tok0 + i];
       if (x >= e0 && x < e1) zx[row] = ld_scalar(zr + x);
     }
   }
@@ -526,7 +530,7 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
     for (int ii = 0; ii < k; ++ii) {
       const MS r = rs[ii];
       // natural-log values from log2-unit statistics: ln v = ln 2 * log2 v
-      if (need && row_lse) row_lse[(size_t)b * k + ii] = (r.m + log2f(r.s)) * 0.6931471805599453f;
+      if (need && row_lse) row_lse[(size_t)b * lay.lse_stride + lay.lse0 + ii] = (r.m + log2f(r.s)) * 0.6931471805599453f;
       if (on) {
         const float zxv = __ldcg(zx + (size_t)b * k + ii);
         // log2 q(x) = (z_x k2 - m) - log2(sum)
@@ -537,6 +541,8 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
     c_s[b] = cval;
     cont[b] = (on && csum >= (double)g) ? 1 : 0;
     if (flags) flags[b] = (on && fabs(csum - (double)g) < 1e-4) ? 1 : 0;
+    // looped draft: the stage's k tokens join the verify whatever its gate says
+    if (n_verify && on) n_verify[b] += k;
   }
   reset_ticket(&counters[b]);
 }
@@ -646,7 +652,7 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
         if (vi_better(tmax, ebest, best)) best = VI{tmax, ebest};
       }
       if (need_sum) {
-        const float mt = tmax * k2;
+        const float mt = tmax == -CUDART_INF_F ? -CUDART_INF_F : ms_offset(tmax, k2);
         float st = 0.f;
         if (tmax != -CUDART_INF_F) {
 #pragma unroll
@@ -667,7 +673,7 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
     if (tid == 0) s_best = rb;
     __syncthreads();
     const VI arg = s_best;
-    const float m2M = arg.v * k2;
+    const float m2M = ms_offset(arg.v, k2);   // integer-valued: record rescales are exact
     if (!need_sum) {
       if (tid == 0) {
         cand[crow + i + 1] = arg.i;
@@ -682,7 +688,7 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
     for (int r = 0; r < nch; ++r) {
       const int j = tid * nch + r;
       const float2 w2 = rr[(j / kThreads) * kThreads + (j % kThreads)];
-      if (w2.x != -CUDART_INF_F) loc += (double)w2.y * (double)exp2f(w2.x - m2M);
+      if (w2.x != -CUDART_INF_F) loc += (double)w2.y * (double)pow2i(w2.x - m2M);
     }
     double inc = loc;
 #pragma unroll
@@ -721,7 +727,7 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
       for (int r = 0; r < nch; ++r) {
         const int j = tid * nch + r;
         const float2 w2 = rr[(j / kThreads) * kThreads + (j % kThreads)];
-        const double w = w2.x == -CUDART_INF_F ? 0.0 : (double)w2.y * (double)exp2f(w2.x - m2M);
+        const double w = w2.x == -CUDART_INF_F ? 0.0 : (double)w2.y * (double)pow2i(w2.x - m2M);
         if (w > 0.0 && cum + w > target) { jsel = j; break; }
         cum += w;
       }
@@ -737,7 +743,7 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
       const int cj = j / kThreads, tj = j % kThreads;
       const float2 w2 = rr[cj * kThreads + tj];
       const float mt = w2.x;
-      const double f = mt == -CUDART_INF_F ? 0.0 : (double)exp2f(mt - m2M);   // segment units -> row units
+      const double f = mt == -CUDART_INF_F ? 0.0 : (double)pow2i(mt - m2M);   // segment units -> row units
       const int es = cj * CHUNK + tj * SEG;
       float w[TPL];
       float lsum = 0.f;
@@ -951,8 +957,8 @@ static cudaError_t launch_gate_t(const GateArgs& a, int num_sms) {
   dim3 grid(p.nch, a.B * a.k);
   gate_kernel<T><<<grid, kThreads, 0, a.stream>>>(
       (const T*)a.draft_logits, a.tokens, a.active, a.k, a.V, p.nch, p.chunk,
-      kLog2e / a.temperature, 1.f / a.temperature, a.g, parts, zx, a.counters, a.c_s, a.cont,
-      a.row_lse, a.flags);
+      kLog2e / a.temperature, 1.f / a.temperature, a.g, a.layout, parts, zx, a.counters, a.c_s, a.cont,
+      a.row_lse, a.flags, a.n_verify);
   return cudaGetLastError();
 }
 

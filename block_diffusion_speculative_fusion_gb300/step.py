@@ -101,6 +101,32 @@ class DflashStep:
         self.events: Optional[List] = None
 
     # ------------------------------------------------------------------
+    def capture(self, n_steps: int, timer=None, after_step=None):
+        """One CUDA graph holding ``n_steps`` consecutive steps, in the launch
+        form the benchmark times: the verify fork onto the side stream and its
+        join are captured with the launches. ``after_step(i)`` may enqueue more
+        work after step i (copies of its outputs) inside the graph. Run one
+        step eagerly first, so that every workspace exists before capture."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_steps):
+                self.step(timer=timer)
+                if after_step is not None:
+                    after_step(i)
+        return g
+
+    def workspaces(self) -> List[torch.Tensor]:
+        """The device workspaces this step's calls use."""
+        out = [w for (dev, _), w in api._WS.items() if dev == (self.dev.index or 0)]
+        if self.ws_greedy is not None:
+            out.append(self.ws_greedy)
+        return out
+
+    def error_words(self) -> List[int]:
+        """Device error words of the step's workspaces (all 0 unless a kernel
+        gave up a bounded wait or met a bad page-table entry)."""
+        return [api.device_error_word(w) for w in self.workspaces()]
+
     def reset(self):
         self.ctx[0].copy_(self.ctx0.to(self.dev))
         self.cur = 0

@@ -273,3 +273,41 @@ def gate_batch(wl: Workload, stage: int, seed: int = 0, B: Optional[int] = None)
     z = draft_logits(wl, wl.n_draft, seed, f"gate{stage}", B=B)
     tok = _gumbel_pick(z, wl.temperature, seed, f"gate{stage}_pick")
     return {"draft_logits": z, "tokens": tok, "active": torch.ones((B,), dtype=torch.uint8)}
+
+
+def plant_needles(wl: Workload, blk: Dict[str, torch.Tensor], cache: PagedCache, seed: int = 0,
+                  q_shift: float = 3.0, key_norm: float = 35.0, v_offset: float = 2.0,
+                  layer: int = 0) -> List[List[int]]:
+    """Attention inputs in which every context page that holds a needle, and
+    the block's first and last rows, carry a visible share of the output.
+
+    Per sequence b: a random unit direction u_b is added to every query row
+    (q += q_shift * u_b, all heads); "needle" keys equal key_norm * u_b (all kv
+    heads) at context positions 0, C/3, C/2, 2C/3, C-1 and at block rows 0 and
+    n_kv-1, each with its own value row N(0, 0.5^2) + v_offset. Needle scores
+    then stand ~q_shift * key_norm / sqrt(D) above the N(0, 1) background, so
+    each needle takes several percent of every row's attention and shifts the
+    output by far more than the 2e-2 tolerance if its page (or block row) is
+    skipped. Edits ``blk`` and ``cache`` (layer ``layer``) in place; returns
+    the needle positions of each sequence."""
+    B, n_kv = blk["k_blk"].shape[0], blk["k_blk"].shape[1]
+    g = _gen(seed, "needles")
+    dt = blk["q"].dtype
+    u = torch.randn(B, wl.D, generator=g)
+    u = u / u.norm(dim=1, keepdim=True)
+    blk["q"].copy_((blk["q"].float() + q_shift * u[:, None, None, :]).to(dt))
+    kp, vp = cache.k_pools[layer], cache.v_pools[layer]
+    P = wl.page_size
+    where = []
+    for b in range(B):
+        C = int(cache.ctx_len[b])
+        pos = sorted({p for p in (0, C // 3, C // 2, (2 * C) // 3, C - 1) if 0 <= p < C})
+        where.append(pos)
+        for p in pos:
+            page = int(cache.page_table[b, p // P])
+            kp[page, p % P] = (key_norm * u[b]).to(kp.dtype).expand(wl.Hkv, wl.D)
+            vp[page, p % P] = (v_offset + 0.5 * torch.randn(wl.Hkv, wl.D, generator=g)).to(vp.dtype)
+        for r in sorted({0, n_kv - 1}):
+            blk["k_blk"][b, r] = (key_norm * u[b]).to(dt).expand(wl.Hkv, wl.D)
+            blk["v_blk"][b, r] = (v_offset + 0.5 * torch.randn(wl.Hkv, wl.D, generator=g)).to(dt)
+    return where

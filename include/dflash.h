@@ -76,6 +76,32 @@ enum { DFLASH_FLAG_GATE_BOUNDARY = 1 };
 
 #define DFLASH_WS_COUNTER_BYTES 16384
 
+/*
+ * Device-side error word. The last 4 bytes of a workspace's counter region
+ * (byte offset DFLASH_WS_ERROR_WORD_OFFSET) hold an int32 that a kernel sets
+ * when something goes wrong on the device; the first code written stays and
+ * nothing clears it. It cannot be returned by the (asynchronous) call itself:
+ * a caller that wants to know reads it once the stream has passed the call
+ * (for example a 4-byte cudaMemcpy). Values:
+ *   0                        no error
+ *   1 .. 99                  a tensor-core kernel gave up a bounded wait (the
+ *                            value names the wait; see dflash_set_wait_limit_ns).
+ *                            The kernel returned early: that call's outputs are
+ *                            invalid and completion counters of the workspace
+ *                            may be left part-counted, so zero the whole counter
+ *                            region (DFLASH_WS_COUNTER_BYTES) before the next call.
+ *   DFLASH_DEVERR_BAD_PAGE   dflash_block_attn met a page-table entry outside
+ *                            [0, num_pages) for a position inside a context; it
+ *                            read page 0 for that position (never out of bounds),
+ *                            so that call's output is invalid. Counters stay
+ *                            consistent; clear the word to reuse the workspace.
+ * Calls that can set it: dflash_block_attn (any dtype) and
+ * dflash_materialize_ctx_kv (bf16 tensor-core GEMMs). The verify, gate,
+ * draft-select and DDTree kernels have no waits and never set it.
+ */
+#define DFLASH_WS_ERROR_WORD_OFFSET (DFLASH_WS_COUNTER_BYTES - 4)
+enum { DFLASH_DEVERR_BAD_PAGE = 100 };
+
 /* ------------------------------------------------------------------------- */
 /* (a) Target-context KV materialisation                                      */
 /* ------------------------------------------------------------------------- */
@@ -160,7 +186,10 @@ typedef struct {
  *
  * q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv_blk, Hkv, D]
  * k_pool, v_pool  one draft layer's pools [num_pages, page_size, Hkv, D]
- * page_table [B, max_pages] int32; ctx_len [B] int32, 0 <= ctx_len[b] <= max_ctx
+ * page_table [B, max_pages] int32; ctx_len [B] int32, 0 <= ctx_len[b] <= max_ctx.
+ *   Entries for positions inside a context must lie in [0, num_pages); an entry
+ *   outside is read as page 0 and sets DFLASH_DEVERR_BAD_PAGE in the workspace's
+ *   error word. Entries past a context are not read.
  * scale: softmax scale (1/sqrt(D) for the standard form)
  * out [B, n_q, Hq, D]
  * Repeated calls on the same inputs return identical bits: the bf16 kernel
@@ -314,6 +343,34 @@ int dflash_gate(const dflash_gate_dims* dims, float temperature, float g,
                 float* c_s, uint8_t* cont, float* row_lse, uint8_t* flags,
                 void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
+/*
+ * One stage of the DLoop looped draft, read from the looped layout that the
+ * verify of all stages takes, so that the stages chain on the device with no
+ * host synchronisation. [DLoop] 机制一: a stage's block is drafted only while
+ * every earlier gate said continue; the stage whose gate says stop is still
+ * verified. [DLoop] looped verify: the S_b drafted blocks are concatenated
+ * into one candidate list of S_b * k tokens checked by the sampled rule.
+ *
+ * dims: B, k (tokens of one stage), V, dtype. 0 <= stage, (stage + 1) * k <= n_max.
+ * draft_logits [B, n_max, V]: stage s's rows are rows s*k .. s*k + k - 1
+ * cand [B, n_max + 1] int64: cand[:, 0] the anchor, stage s's tokens at 1 + s*k ..
+ * active [B] uint8 or NULL (all): sequences still drafting at this stage, i.e.
+ *   the previous stage's cont (stage 0: NULL or all ones)
+ * c_s, cont [B]; flags [B] or NULL: as dflash_gate (0 for inactive sequences)
+ * row_lse [B, n_max] float or NULL: LSE(row / T) of this stage's rows of the
+ *   active sequences, written at columns s*k .. s*k + k - 1 (other entries are
+ *   left as they are): after the last stage it is the draft_row_lse of
+ *   dflash_verify_sample_lse
+ * n_verify [B] int32 or NULL: every active sequence adds k (its block joins the
+ *   verify whether or not its gate continues); zero it before stage 0, and after
+ *   the last stage it is the n_draft of the looped verify (S_b * k)
+ * The workspace is dflash_gate_workspace_size(dims).
+ */
+int dflash_gate_stage(const dflash_gate_dims* dims, int32_t stage, int32_t n_max, float temperature,
+                      float g, const void* draft_logits, const int64_t* cand, const uint8_t* active,
+                      float* c_s, uint8_t* cont, float* row_lse, uint8_t* flags, int32_t* n_verify,
+                      void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Draft-side token choice                                                    */
 /* ------------------------------------------------------------------------- */
@@ -404,6 +461,19 @@ int dflash_ddtree_verify_greedy(const dflash_tree_dims* dims, const void* target
 /* ------------------------------------------------------------------------- */
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------- */
+/*
+ * Limit, in nanoseconds, of every bounded wait of the tensor-core kernels
+ * (dflash_block_attn for bf16, dflash_materialize_ctx_kv for bf16) on the
+ * barriers between their roles (copy landed, MMA done, buffer free). A wait
+ * that runs out sets the error word (see DFLASH_WS_ERROR_WORD_OFFSET) and the
+ * kernel returns early after draining its own copies and MMAs under a fixed
+ * 2 s limit. The value is process-wide and read when a call launches (a kernel
+ * captured in a CUDA graph keeps the value it was captured with). ns = 0
+ * restores the default of 2 000 000 000 (2 s), far above any wait of a working
+ * launch. Always returns DFLASH_OK.
+ */
+int dflash_set_wait_limit_ns(uint64_t ns);
+uint64_t dflash_wait_limit_ns(void);
 /* Message of the last error on this thread ("" if none). */
 const char* dflash_last_error(void);
 /* Number of kernel launches (memsets included) the last successful call on this

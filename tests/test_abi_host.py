@@ -189,3 +189,19 @@ def test_materialize_dims_and_arguments_checked_on_host(L):
     rc = L.dflash_materialize_ctx_kv(ctypes.byref(ok), fake, fake, fake, fake, None, fake, None, eps, theta,
                                      ctypes.cast(holes, ctypes.c_void_p), pp, fake, None, fake, need, None)
     assert rc == api.ERR_INVALID_ARG and "layer 2" in api.last_error()
+
+
+def test_wait_limit_is_settable_and_zero_restores_default(L):
+    default = L.dflash_wait_limit_ns()
+    assert default == 2_000_000_000
+    assert L.dflash_set_wait_limit_ns(5000) == 0
+    assert L.dflash_wait_limit_ns() == 5000
+    assert L.dflash_set_wait_limit_ns(0) == 0
+    assert L.dflash_wait_limit_ns() == default
+
+
+def test_error_word_offset_matches_header():
+    hdr = open(os.path.join(ROOT, "include", "dflash.h")).read()
+    assert "#define DFLASH_WS_ERROR_WORD_OFFSET (DFLASH_WS_COUNTER_BYTES - 4)" in hdr
+    assert "DFLASH_DEVERR_BAD_PAGE = 100" in hdr
+    assert api.WS_ERROR_WORD_OFFSET == api.WS_COUNTER_BYTES - 4 and api.DEVERR_BAD_PAGE == 100

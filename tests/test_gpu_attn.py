@@ -176,3 +176,39 @@ def test_attn_causal_bf16_one_kv_head_per_item_and_extra_block_rows():
 def test_attn_causal_bf16_dloop_stage_rows():
     w, cache, blk = _case(W.DLOOP_QWEN3_4B, [1024, 17, 700, 1500], seed=8, n_kv=W.DLOOP_QWEN3_4B.k + 2)
     _run(w, cache, blk, 2e-2, causal=True)
+
+
+# ---- inputs that bite: needle keys in the pages (and block rows) carry a
+# visible share of every output, so a skipped page, block row or a wrong split
+# weight moves the output far past the tolerance ----
+def _needle_full_size(seed):
+    wl = W.LLAMA8B_B64
+    ctx_len = synth.ctx_lengths(wl, 0)
+    cache = synth.paged_cache(wl, headroom=16, seed=seed, layers=1, ctx_len=ctx_len)
+    blk = synth.block_qkv(wl, 0, seed=seed)
+    synth.plant_needles(wl, blk, cache, seed=seed)
+    order = np.argsort(ctx_len.numpy())
+    seqs = sorted({int(order[0]), int(order[1]), int(order[len(order) // 2]), int(order[-2]), int(order[-1]), 5, 40})
+    return wl, cache, blk, seqs
+
+
+def test_attn_full_size_needles_llama8b_b64():
+    wl, cache, blk, seqs = _needle_full_size(seed=13)
+    got = _run(wl, cache, blk, 2e-2, seqs=seqs, repeat=3)
+    assert np.abs(got).max() > 0.5          # the needles do dominate the outputs
+
+
+def test_attn_full_size_needles_causal_llama8b_b64():
+    wl, cache, blk, seqs = _needle_full_size(seed=14)
+    _run(wl, cache, blk, 2e-2, seqs=seqs[:4], causal=True)
+
+
+@pytest.mark.parametrize("ctx", [[1024, 1025, 2048, 3000, 4097, 8192, 17, 500]])
+def test_attn_needles_split_boundaries(ctx):
+    # contexts near 1024-key multiples, split when the launch's mean work is small
+    import dataclasses
+    wl = dataclasses.replace(W.LLAMA8B_B64, B=len(ctx))
+    cache = synth.paged_cache(wl, headroom=16, seed=15, layers=1, ctx_len=torch.tensor(ctx, dtype=torch.int32))
+    blk = synth.block_qkv(wl, 0, seed=15)
+    synth.plant_needles(wl, blk, cache, seed=15)
+    _run(wl, cache, blk, 2e-2)

@@ -115,3 +115,59 @@ def test_materialize_bf16_qwen3_4b_prefill_rows():
     # one sequence committing a long prompt-like block in a single call
     wl = dataclasses.replace(W.QWEN3_4B_B8, k=256)
     _run_case(wl, [256, 200], [0, 4096], seed=4)
+
+
+def _prefill_case(wl, B, rows, n_check, seed):
+    """Every row of every sequence committed in one call (prefill-sized
+    T = B * rows), then n_check seeded rows compared with the oracle. Each row's
+    K/V depends only on its own hidden row and position, so the oracle runs on
+    just those rows (each as a one-row sequence at its position)."""
+    w = synth.ctx_weights(wl, seed)
+    hidden = synth.captured_hidden(wl, rows, seed, B=B)
+    wb = dataclasses.replace(wl, B=B)
+    pt, num_pages, _ = synth.page_table(wb, torch.zeros(B, dtype=torch.int32), rows, seed)
+    dt = synth.io_dtype(wl)
+    shape = (num_pages, wl.page_size, wl.Hkv, wl.D)
+    kd = [torch.zeros(shape, dtype=dt, device=DEV) for _ in range(wl.L)]
+    vd = [torch.zeros(shape, dtype=dt, device=DEV) for _ in range(wl.L)]
+    commit = torch.full((B,), rows, dtype=torch.int32, device=DEV)
+    start = torch.zeros(B, dtype=torch.int32, device=DEV)
+    new_len = torch.empty(B, dtype=torch.int32, device=DEV)
+    api.materialize_ctx_kv(hidden.to(DEV), commit, start, w["W_f"].to(DEV), w["b_f"].to(DEV), w["W_kv"].to(DEV),
+                           w["k_norm_w"].to(DEV), wl.rms_eps, wl.rope_theta, kd, vd, pt.to(DEV), new_len)
+    torch.cuda.synchronize()
+    assert torch.all(new_len.cpu() == rows)
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(B * rows, size=n_check, replace=False)
+    bs, js = pick // rows, pick % rows
+    # the picked rows as one-row sequences at their positions, one private page each
+    P = wl.page_size
+    tab = np.full((n_check, max(js) // P + 1), -1, dtype=np.int32)
+    tab[np.arange(n_check), js // P] = np.arange(n_check)
+    pool0 = [np.zeros((n_check, P, wl.Hkv, wl.D)) for _ in range(wl.L)]
+    rk, rv = O.materialize_ctx_kv(f64(hidden[torch.from_numpy(bs), torch.from_numpy(js)])[:, None],
+                                  [1] * n_check, js.tolist(), f64(w["W_f"]), f64(w["b_f"]), f64(w["W_kv"]),
+                                  f64(w["k_norm_w"]), wl.rms_eps, wl.rope_theta, pool0,
+                                  [p.copy() for p in pool0], tab, P)
+    slots = torch.from_numpy(pt.numpy()[bs, js // P].astype(np.int64) * P + js % P)
+    worst = 0.0
+    for layer in range(wl.L):
+        gk = f64(kd[layer].view(-1, wl.Hkv, wl.D)[slots.to(DEV)])
+        gv = f64(vd[layer].view(-1, wl.Hkv, wl.D)[slots.to(DEV)])
+        ok_ = rk[layer][np.arange(n_check), js % P]
+        ov = rv[layer][np.arange(n_check), js % P]
+        worst = max(worst, np.abs(gk - ok_).max(), np.abs(gv - ov).max())
+    assert worst < 2e-2, worst
+    return worst
+
+
+def test_materialize_prefill_llama8b_t2048():
+    # the Llama-3.1-8B workload's prefill: one sequence, T = 2048 rows; the
+    # K/V GEMM (N = 10240) hands out whole waves of 152 tiles
+    _prefill_case(W.LLAMA8B_B1, B=1, rows=2048, n_check=256, seed=11)
+
+
+def test_materialize_prefill_qwen3_4b_t8192():
+    # the Qwen3-4B workload's prefill: 8 sequences x 1024 rows, T = 8192; both
+    # GEMMs run several waves of whole tiles before the stream-K remainder
+    _prefill_case(W.QWEN3_4B_B8, B=8, rows=1024, n_check=256, seed=12)

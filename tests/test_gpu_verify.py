@@ -264,6 +264,76 @@ def test_sample_identity_monte_carlo_on_gpu(V):
     assert abs(accepted / n - beta) < 5 * math.sqrt(beta * (1 - beta) / n)
 
 
+def _boundary_distance(ref, vb, b):
+    """How far sequence b's uniforms sit from the oracle's decision boundaries:
+    every evaluated accept test with p/q < 1, and the two CDF steps around the
+    drawn token (speculative-decoding page, section 3)."""
+    d = ref["debug"][b]
+    u = npy(vb["u_acc"])[b].astype(np.float64)
+    dist = np.inf
+    for i, (px, qx) in enumerate(zip(d["p_x"], d["q_x"])):
+        if qx > 0 and px / qx < 1.0:
+            dist = min(dist, abs(u[i] - px / qx))
+    fd = d["final_dist"]
+    y = int(ref["bonus"][b])
+    c_hi = fd[:y + 1].sum()
+    uf = float(npy(vb["u_final"])[b])
+    return min(dist, abs(c_hi - fd[y] - uf), abs(c_hi - uf))
+
+
+def _full_size_sample_case(name):
+    if name == "llama8b_b32_sigma2":
+        return synth.verify_batch(W.LLAMA8B_B64, seed=0, B=32, greedy_rows=0)
+    if name.startswith("qwen3_4b_b8_sigma"):
+        return synth.verify_batch(W.QWEN3_4B_B8, seed=0, sigma=float(name.split("sigma")[1]))
+    return synth.verify_batch(W.DLOOP_QWEN3_4B, seed=3, B=32, ragged=True)
+
+
+@pytest.mark.parametrize("name", ["llama8b_b32_sigma2", "qwen3_4b_b8_sigma0.5", "qwen3_4b_b8_sigma2",
+                                  "qwen3_4b_b8_sigma4", "dloop_b32_concatenated_ragged"])
+def test_sample_full_size_probs_ratio_and_flag_bands(name):
+    """bf16 full-size sampled verify: p(x), q(x) of every evaluated draft and
+    the drawn distribution's mass Z within 1e-5 relative; the accept ratio p/q
+    within 3e-7 of the oracle's (under a third of the 1e-6 flag band); and the flags
+    decided by the band: a sequence whose uniforms lie more than 1.5e-6 from
+    every oracle boundary is unflagged on the GPU and bit-exact, one within
+    0.5e-6 of a boundary is flagged on the GPU too."""
+    vb = _full_size_sample_case(name)
+    out, ref = _check_sample(vb, max_flag_frac=1.0)
+    pr = npy(out["probs"]).astype(np.float64)
+    n_max = vb["u_acc"].shape[1]
+    gflags = npy(out["flags"])
+    worst_ratio, worst_rel = 0.0, 0.0
+    near = far = 0
+    for b in range(len(gflags)):
+        d = ref["debug"][b]
+        k = len(d["p_x"])
+        gp, gq = pr[b, :k], pr[b, n_max:n_max + k]
+        np.testing.assert_allclose(gp, d["p_x"], rtol=1e-5, atol=1e-30)
+        np.testing.assert_allclose(gq, d["q_x"], rtol=1e-5, atol=1e-30)
+        worst_rel = max(worst_rel, float(np.max(np.abs(gp / np.maximum(d["p_x"], 1e-300) - 1.0), initial=0.0)))
+        Z = d["Z"] if d["Z"] is not None else 1.0
+        np.testing.assert_allclose(pr[b, 2 * n_max], Z, rtol=1e-5)
+        for i in range(k):
+            r_o = d["p_x"][i] / d["q_x"][i]
+            if r_o < 1.0:
+                worst_ratio = max(worst_ratio, abs(gp[i] / gq[i] - r_o))
+        dist = _boundary_distance(ref, vb, b)
+        if dist > 1.5e-6:
+            far += 1
+            assert gflags[b] == 0, (b, dist, gflags[b])
+            for key in ("accept_len", "bonus", "commit_len", "out_tokens"):
+                np.testing.assert_array_equal(npy(out[key])[b], ref[key][b], err_msg=f"{key} seq {b}")
+        elif dist < 0.5e-6:
+            near += 1
+            assert gflags[b] != 0, (b, dist)
+    print(f"[{name}] sequences {len(gflags)}: far {far}, near {near}, oracle-flagged "
+          f"{int((ref['flags'] != 0).sum())}, GPU-flagged {int((gflags != 0).sum())}; "
+          f"max |ratio - oracle| {worst_ratio:.3e}, max rel p(x) {worst_rel:.3e}")
+    # the fp32 probabilities (ratio formed in fp64) err far inside the band
+    assert worst_ratio < 3e-7, worst_ratio
+
+
 def test_verify_is_deterministic():
     vb = gpu(synth.verify_batch(W.QWEN3_4B_B8, seed=9))
     a = api.verify_sample(vb["target_logits"], vb["draft_logits"], vb["cand"], vb["u_acc"], vb["u_final"])
@@ -354,3 +424,59 @@ def test_sample_lse_matches_streamed_rule_llama8b_b32():
     for key in ("accept_len", "bonus", "commit_len", "out_tokens"):
         np.testing.assert_array_equal(npy(a[key])[ok], npy(b[key])[ok], err_msg=key)
     assert ok.mean() > 0.5
+
+
+# ---------------------------------------------------------------------------
+# DLoop looped step: gates chained on the device, then one verify of the
+# S_b * k concatenated candidates
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", [5, 6])
+def test_dloop_looped_chain_matches_oracle(seed):
+    """DLoop page, mechanism 1 and the looped verify: stage s is drafted only
+    while every earlier gate continued (the next stage's active mask is this
+    stage's cont, on the device); the stage that stops is still verified; the
+    verify checks the S_b * k concatenated candidates with the sampled rule,
+    fed the gates' row LSEs. Compared with oracle.gate per stage,
+    oracle.dloop_stage_count and oracle.verify_sample over n_b = S_b * k."""
+    wl = W.DLOOP_QWEN3_4B
+    B, k, S, T = wl.B, wl.n_draft, wl.stages, wl.temperature
+    n_max = S * k
+    vb = synth.verify_batch(wl, seed=seed)
+    g = gpu(vb)
+    row_lse = torch.zeros(B, n_max, dtype=torch.float32, device=DEV)
+    n_verify = torch.zeros(B, dtype=torch.int32, device=DEV)
+    conts, cvals, gflags = [], [], []
+    active = None
+    for s in range(S):
+        o = api.gate_stage(g["draft_logits"], g["cand"], s, k, T, wl.gate_g, active=active, row_lse=row_lse,
+                           n_verify=n_verify)
+        conts.append(o["cont"].clone())
+        cvals.append(o["c"].clone())
+        gflags.append(o["flags"].clone())
+        active = conts[-1]
+    out = api.verify_sample(g["target_logits"], g["draft_logits"], g["cand"], g["u_acc"], g["u_final"], T,
+                            n_verify, draft_row_lse=row_lse)
+    torch.cuda.synchronize()
+    # ---- the oracle's chain ----
+    zd = f64(vb["draft_logits"])
+    cand = npy(vb["cand"])
+    act = np.ones(B, dtype=np.uint8)
+    conts_o, flagged = [], np.zeros(B, bool)
+    for s in range(S):
+        ref = O.gate(zd[:, s * k:(s + 1) * k], cand[:, 1 + s * k:1 + (s + 1) * k], act, T, wl.gate_g)
+        flagged |= (ref["flags"] != 0) | (npy(gflags[s]) != 0)
+        ok = ~flagged
+        np.testing.assert_allclose(npy(cvals[s])[ok], ref["c"][ok], atol=1e-4, rtol=0)
+        np.testing.assert_array_equal(npy(conts[s])[ok], ref["cont"][ok], err_msg=f"cont stage {s}")
+        conts_o.append(ref["cont"])
+        act = ref["cont"].astype(np.uint8)
+    S_b = O.dloop_stage_count(np.array(conts_o))
+    ok = ~flagged
+    np.testing.assert_array_equal(npy(n_verify)[ok], (S_b * k)[ok])
+    assert 1 < len(set(S_b[ok].tolist()))            # the gates both stop and continue
+    ref_v = O.verify_sample(f64(vb["target_logits"]), zd, cand, S_b * k, npy(vb["u_acc"]), npy(vb["u_final"]), T)
+    ok &= ref_v["flags"] == 0
+    ok &= npy(out["flags"]) == 0
+    assert ok.mean() > 0.5
+    for key in ("accept_len", "bonus", "commit_len", "out_tokens"):
+        np.testing.assert_array_equal(npy(out[key])[ok], ref_v[key][ok], err_msg=key)
