@@ -270,14 +270,22 @@ def cuda_kernel_times(torch, fn, reps):
         return None
     try:
         torch.cuda.synchronize()
+        if not getattr(cuda_kernel_times, "warm", False):
+            # the first session in a process can miss kernels while CUPTI starts
+            with profile(activities=[ProfilerActivity.CUDA]):
+                fn()
+                torch.cuda.synchronize()
+            cuda_kernel_times.warm = True
         with profile(activities=[ProfilerActivity.CUDA]) as prof:
             for _ in range(reps):
                 fn()
             torch.cuda.synchronize()
-    except Exception:   # noqa: BLE001 - reported as missing, not fatal
-        return None
+    except Exception as exc:   # noqa: BLE001 - reported, not fatal
+        return {"_error": f"{type(exc).__name__}: {exc}"[:300]}
     out = {}
     evs = [e for e in prof.events() if str(getattr(e, "device_type", "")).endswith("CUDA")]
+    if not evs:
+        return {"_error": f"no device events among {len(prof.events())} profiler events"}
     evs.sort(key=lambda e: e.time_range.start)
     for e in evs:
         dur = e.time_range.end - e.time_range.start
@@ -292,8 +300,8 @@ def step_rooflines(torch, st, wl, hbm, tf, reps=4):
     bytes: attention, the greedy and sampled verify kernels, the decode-sized
     materialisation GEMMs and the rest of the materialisation."""
     times = cuda_kernel_times(torch, st.step, reps)
-    if not times:
-        return {"note": "torch profiler (CUPTI) unavailable"}
+    if not times or "_error" in times:
+        return {"note": "torch profiler (CUPTI) unavailable", "detail": (times or {}).get("_error")}
     el = 2
     V, R, n = wl.V, wl.n_draft + 1, wl.n_draft
     ng, ns = wl.n_greedy, wl.B - wl.n_greedy
@@ -338,7 +346,7 @@ def prefill_roofline(torch, wl, tf, tf_sus):
         call()
     times = cuda_kernel_times(torch, call, 3)
     if not times or "gemm_tc_kernel" not in times:
-        return {"note": "torch profiler (CUPTI) unavailable"}
+        return {"note": "torch profiler (CUPTI) unavailable", "detail": (times or {}).get("_error")}
     g = times["gemm_tc_kernel"]
     f1 = 2.0 * T * wl.m * wl.d * wl.d
     f2 = 2.0 * T * wl.d * wl.kv_out

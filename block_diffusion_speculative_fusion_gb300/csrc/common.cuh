@@ -119,6 +119,36 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b) {
   return MS{M, sa + sb};
 }
 
+// The same pair with the sum carried as an unevaluated fp32 pair hi + lo, for
+// reduction trees whose partial sums must not lose digits (a 256-thread tree
+// in plain fp32 errs by up to 8 ulps). Merges use an exact power-of-two
+// rescale and an error-free two-sum, fp32 arithmetic only (fp64 is slow here).
+struct MS2 { float m; float hi; float lo; };
+
+__device__ __forceinline__ MS2 ms2_merge(MS2 a, MS2 b) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -CUDART_INF_F) return MS2{M, 0.f, 0.f};
+  const float fa = (a.m == -CUDART_INF_F) ? 0.f : pow2i(a.m - M);
+  const float fb = (b.m == -CUDART_INF_F) ? 0.f : pow2i(b.m - M);
+  const float ah = a.hi * fa, al = a.lo * fa, bh = b.hi * fb, bl = b.lo * fb;   // exact
+  const float s = ah + bh;
+  const float bp = s - ah;
+  const float e = (ah - (s - bp)) + (bh - bp);     // s + e == ah + bh exactly
+  const float lo = (al + bl) + e;
+  const float hi = s + lo;
+  return MS2{M, hi, lo - (hi - s)};
+}
+
+__device__ __forceinline__ MS2 warp_ms2(MS2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS2 w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.hi, o),
+          __shfl_xor_sync(0xffffffffu, v.lo, o)};
+    v = ms2_merge(v, w);
+  }
+  return v;
+}
+
 __device__ __forceinline__ MS warp_ms(MS v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

@@ -67,6 +67,22 @@ __device__ __forceinline__ MS block_ms(MS x) {
   return x;  // valid in thread 0
 }
 
+// Block tree of (max, sum) pairs with compensated fp32 sums; the result
+// (valid in thread 0) is rounded to one fp32 sum.
+__device__ __forceinline__ MS block_ms2(MS2 x) {
+  __shared__ MS2 sh2[kThreads / 32];
+  x = warp_ms2(x);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sh2[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    x = (l < (int)(blockDim.x >> 5)) ? sh2[l] : MS2{-CUDART_INF_F, 0.f, 0.f};
+    x = warp_ms2(x);
+  }
+  return MS{x.m, x.hi + x.lo};
+}
+
 // 2^x on the special-function unit, flushing denormal results to zero (terms
 // below 2^-126 of a row maximum do not change a sum that contains 1).
 __device__ __forceinline__ float ex2_ftz(float x) {
@@ -78,14 +94,27 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 // Streaming statistics of elements [e0, e1) of one row in log2 units:
 // m = rint(max(z) * k2), s = sum 2^(fma(z, k2, -m)). The same code serves target and
 // draft rows, so identical rows give bit-identical statistics.
+// The thread's running sum is compensated (Kahan): a thread adds some 60
+// vector sums of a 128k-token row, whose plain fp32 sum errs by ~sqrt(60) ulps
+// (~5e-7 relative), as much as the 1e-6 decision band of the sampled rule; the
+// block combines the threads' sums as compensated fp32 pairs.
 template <typename T>
 __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2) {
   constexpr int N = VecTraits<T>::N;
   float zmax = -CUDART_INF_F;   // running max in logit units (exact comparisons)
   MS acc{-CUDART_INF_F, 0.f};
+  float comp = 0.f;             // Kahan compensation of acc.s
+  auto kadd = [&](float x) {
+    const float y = x - comp;
+    const float t = acc.s + y;
+    comp = (t - acc.s) - y;
+    acc.s = t;
+  };
   auto raise_to = [&](float v) {
     const float m2 = ms_offset(v, k2);
-    acc.s = (acc.m == -CUDART_INF_F) ? 0.f : acc.s * pow2i(acc.m - m2);
+    const float f = (acc.m == -CUDART_INF_F) ? 0.f : pow2i(acc.m - m2);   // exact power of two
+    acc.s *= f;
+    comp *= f;
     acc.m = m2;
     zmax = v;
   };
@@ -98,14 +127,14 @@ __device__ __forceinline__ MS row_chunk_ms(const T* z, int e0, int e1, float k2)
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < N; ++j) s += ex2_ftz(fmaf(f[j], k2, -acc.m));
-    acc.s += s;
+    kadd(s);
   };
   auto add_one = [&](float v, int) {
     if (v > zmax) raise_to(v);
-    if (zmax != -CUDART_INF_F) acc.s += ex2_ftz(fmaf(v, k2, -acc.m));
+    if (zmax != -CUDART_INF_F) kadd(ex2_ftz(fmaf(v, k2, -acc.m)));
   };
   for_range<T, 8>(z, e0, e1, add_vec, add_one);
-  return block_ms(acc);
+  return block_ms2(MS2{acc.m, acc.s, -comp});
 }
 
 

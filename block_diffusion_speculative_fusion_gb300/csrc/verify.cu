@@ -405,45 +405,50 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const fl
     const bool t = rr < R;
     const int rix = t ? rr : rr - R;
     if (t ? rix > nb : rix >= nb) continue;
-    MS x{-CUDART_INF_F, 0.f};
+    MS2 x{-CUDART_INF_F, 0.f, 0.f};
     const MS* pr = parts + ((size_t)b * RR + rr) * nch;
     for (int cc = l; cc < nch; cc += 32) {
       const float2 raw = __ldcg(reinterpret_cast<const float2*>(pr + cc));
-      x = ms_merge(x, MS{raw.x, raw.y});
+      x = ms2_merge(x, MS2{raw.x, raw.y, 0.f});
     }
-    // fixed-order combine across lanes
-    x = warp_ms(x);
-    if (l == 0) rs[rr] = x;
+    // fixed-order combine across lanes (compensated sums, rounded once)
+    x = warp_ms2(x);
+    if (l == 0) rs[rr] = MS{x.m, x.hi + x.lo};
   }
   __syncthreads();
-  __shared__ int s_a;
+  // Every candidate's p(x), q(x) and p/q at once, one thread each. The
+  // numerator of p(x) is the very term the row sum holds for x (same exponent
+  // fma, same ex2), so where x carries most of its row the approximation
+  // errors of numerator and sum cancel; the fp32 exponent's rounding
+  // residual r (z * k2 is exact in fp64 for bf16 or fp32 z) is put back as a
+  // factor 1 + r ln 2. The quotients are formed in fp64.
+  __shared__ double s_ratio[kMaxRows];
+  __shared__ float s_px[kMaxRows], s_qx[kMaxRows];
+  __shared__ uint8_t s_inv[kMaxRows];
+  for (int i = (int)threadIdx.x + 1; i <= nb; i += blockDim.x) {
+    const MS pt = rs[i - 1], pd = rs[R + i - 1];
+    const float zxt = __ldcg(zx + (size_t)b * RR + (i - 1));
+    const float zxd = zx[(size_t)b * RR + R + (i - 1)];
+    const double k2d = (double)k2;
+    const float at = fmaf(zxt, k2, -pt.m), ad = fmaf(zxd, k2, -pd.m);   // as in the row sums
+    const double rt = ((double)zxt * k2d - (double)pt.m) - (double)at;
+    const double rd = ((double)zxd * k2d - (double)pd.m) - (double)ad;
+    const double px = (double)ex2_ftz(at) * (1.0 + rt * 0.6931471805599453) / (double)pt.s;
+    const double qx = (double)ex2_ftz(ad) * (1.0 + rd * 0.6931471805599453) / (double)pd.s;
+    s_px[i - 1] = (float)px;
+    s_qx[i - 1] = (float)qx;
+    // q(x) = 0: the candidate was not drawn from q (infinite ratio, flagged)
+    s_inv[i - 1] = qx > 0.0 ? 0 : 1;
+    s_ratio[i - 1] = qx > 0.0 ? px / qx : (double)CUDART_INF_F;
+  }
+  __syncthreads();
+  __shared__ int s_a, s_eval;
   if (threadIdx.x == 0) {
     int a = 0, flags = 0;
     bool rejected = false;
     for (int i = 1; i <= nb; ++i) {
-      const MS pt = rs[i - 1], pd = rs[R + i - 1];
-      const float zxt = __ldcg(zx + (size_t)b * RR + (i - 1));
-      const float zxd = zx[(size_t)b * RR + R + (i - 1)];
-      // The candidate's exponents in fp64, with the same scale k2 and offsets
-      // m as the fp32 row sums (z * k2 is exact in fp64 for bf16 or fp32 z):
-      // p(x) = 2^(z_t k2 - m_t) / s_t, q(x) likewise, p/q = 2^(at - ad) s_d / s_t.
-      // Only the row sums' rounding (~1e-7 relative) remains in the ratio that
-      // the 1e-6 boundary band is measured against.
-      const double k2d = (double)k2;
-      const double at = (double)zxt * k2d - (double)pt.m, ad = (double)zxd * k2d - (double)pd.m;
-      const double et = exp2(at), ed = exp2(ad);
-      const double px = et / (double)pt.s, qx = ed / (double)pd.s;
-      if (probs) {
-        probs[(size_t)b * (2 * n_max + 1) + (i - 1)] = (float)px;
-        probs[(size_t)b * (2 * n_max + 1) + n_max + (i - 1)] = (float)qx;
-      }
-      double ratio;
-      if (!(ed > 0.0) || !(qx > 0.0)) {
-        flags |= 8;                      // DFLASH_FLAG_INVALID
-        ratio = (double)CUDART_INF_F;
-      } else {
-        ratio = exp2(at - ad) * ((double)pd.s / (double)pt.s);
-      }
+      const double ratio = s_ratio[i - 1];
+      if (s_inv[i - 1]) flags |= 8;      // DFLASH_FLAG_INVALID
       const double u = (double)u_acc[(size_t)b * n_max + (i - 1)];
       if (ratio < 1.0 && fabs(u - ratio) < 1e-6) flags |= 1;   // ACCEPT_BOUNDARY
       if (u < ratio) {
@@ -453,11 +458,7 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const fl
         break;
       }
     }
-    if (probs)
-      for (int i = a + (rejected ? 1 : 0) + 1; i <= n_max; ++i) {
-        probs[(size_t)b * (2 * n_max + 1) + (i - 1)] = 0.f;
-        probs[(size_t)b * (2 * n_max + 1) + n_max + (i - 1)] = 0.f;
-      }
+    s_eval = a + (rejected ? 1 : 0);
     SampleJob j;
     j.row = a;
     j.mode = rejected ? 0 : 1;
@@ -473,6 +474,12 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const fl
     s_a = a;
   }
   __syncthreads();
+  if (probs)
+    for (int i = threadIdx.x; i < n_max; i += blockDim.x) {
+      const bool ev = i < s_eval;      // candidates the rule evaluated; 0 past them
+      probs[(size_t)b * (2 * n_max + 1) + i] = ev ? s_px[i] : 0.f;
+      probs[(size_t)b * (2 * n_max + 1) + n_max + i] = ev ? s_qx[i] : 0.f;
+    }
   if (out_tokens) {
     // accepted drafts now; the bonus slot and padding are written by the draw
     const int a = s_a;
@@ -514,14 +521,14 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (need) {
     for (int ii = w; ii < k; ii += blockDim.x >> 5) {
-      MS x{-CUDART_INF_F, 0.f};
+      MS2 x{-CUDART_INF_F, 0.f, 0.f};
       const MS* pr = parts + ((size_t)b * k + ii) * nch;
       for (int cc = l; cc < nch; cc += 32) {
         const float2 raw = __ldcg(reinterpret_cast<const float2*>(pr + cc));
-        x = ms_merge(x, MS{raw.x, raw.y});
+        x = ms2_merge(x, MS2{raw.x, raw.y, 0.f});
       }
-      x = warp_ms(x);
-      if (l == 0) rs[ii] = x;
+      x = warp_ms2(x);
+      if (l == 0) rs[ii] = MS{x.m, x.hi + x.lo};
     }
   }
   __syncthreads();
