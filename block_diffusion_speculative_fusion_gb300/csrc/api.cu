@@ -465,7 +465,6 @@ int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_bl
   a.q = q; a.k_blk = k_blk; a.v_blk = v_blk; a.k_pool = k_pool; a.v_pool = v_pool;
   a.page_table = page_table; a.ctx_len = ctx_len; a.scale = scale; a.out = out;
   a.counters = (int32_t*)workspace;
-  a.sched = (int32_t*)workspace + kMaxCounters - 2;
   a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
   a.stream = (cudaStream_t)stream;

@@ -63,14 +63,15 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 // tcgen05 path: persistent, warp-specialised, TMEM accumulators.
 //   softmax     warps q and q + 4 for q < W = ceil(M / 32): TMEM lane quarter q
 //               (packed query row 32 q + lane), key columns 0-31 / 32-63
-//   producer    warp 2 (W <= 2) or 12: claims work items, fetches their page
-//               rows, streams context K/V pages by TMA into a ring of
-//               64-row stages
+//   producer    warp 2 (W <= 2) or 12: walks the CTA's pieces of the static
+//               partition, fetches their page rows, streams context K/V pages
+//               by TMA into a ring of 64-row stages
 //   MMA         the warp after the producer: TMEM allocator, one issuing thread
 //   epilogue    warps 8 + q: write the next item's Q rows into TMEM, read O out
 //               of TMEM, normalise, store
-// A work item is (sequence, kv head, key split); items are handed out longest
-// first from a global counter. Per 64-row tile t: S_t = Q K_t^T (M = 128,
+// A work item (piece) is a run of tiles of one (sequence, kv-head group),
+// from a static partition that gives every CTA the same number of tiles
+// (see AttnItem). Per 64-row tile t: S_t = Q K_t^T (M = 128,
 // N = 64, Q from TMEM) into TMEM buffer t % 2; the softmax threads read their
 // S row and write P_t (bf16 pairs) back into TMEM, and the MMA thread
 // accumulates O += P_t V_t (M = 128, N = 128, P from TMEM, V read MN-major)
@@ -94,76 +95,98 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr int kGrid = 152;                  // persistent CTAs: one per SM
 constexpr int kMaxSeqs = 1024;              // sequences per call on this path
 constexpr int kPtMax = 512;                 // page-table entries of one item
-constexpr int kClaimAhead = 3;              // tiles before an item's end at which the next is claimed
-constexpr int kBarBytes = (2 * kMaxStages + 33) * 8 + 2 * 4 + (kMaxSeqs + 1) * 4 + kMaxSeqs * 2 + 2 * kPtMax * 4 +
+constexpr int kClaimAhead = 3;              // tiles before a piece's end at which the next one's pages are fetched
+constexpr int kBarBytes = (2 * kMaxStages + 33) * 8 + 2 * 32 + (kMaxSeqs + 1) * 4 + 2 * kPtMax * 4 +
                           (2 * 2 * 128 + 2 * 4 * 128) * 4 + 64;
 }  // namespace attn_tc
 
-// Work items are (sequence, kv-head group, key split). A split covers tiles
-// [t0, t0 + n_tiles_ctx) of the context; the last split of a sequence also
-// takes the block's own rows as one more tile.
+// Work is a static, balanced partition of the launch's tiles. Every (sequence
+// b, kv-head group g) owns nt_b consecutive tiles -- its context tiles, then
+// the block's own rows as one more tile -- in the order b-major, g-minor; the
+// resulting sequence of N tiles is cut into ranges of `share` tiles (the mean
+// work of one CTA, at least 16 tiles, at most what one page-table window
+// holds), and CTA c takes ranges c, c + grid, ... A piece is the part of one
+// range that falls in one (b, g); a (b, g) cut by range borders is computed
+// in pieces whose partial results the piece that finishes last merges.
 struct AttnItem {
-  int b, g, split, nsplit, t0, C, n_tiles_ctx, n_tiles;
+  int b, g, split, nsplit, t0, C, n_tiles_ctx, n_tiles;   // b < 0: no more pieces
 };
-
-// Largest split, in 64-key tiles, of one launch: the mean work per CTA when
-// that is more than 16 tiles (a context no longer than that is processed whole,
-// with no partial results to merge), capped by what one item's page table
-// holds. Items are then handed out longest first, which balances the CTAs
-// without cutting long contexts into short pieces.
-__device__ __forceinline__ int split_cap(const AttnParams& p, long long total_tiles) {
-  const long long share = (total_tiles + attn_tc::kGrid - 1) / attn_tc::kGrid;
-  // one page more than the split spans, for splits that start inside a page
-  const long long table = (long long)(attn_tc::kPtMax - 1) * p.page_size / p.TK;
-  return (int)max((long long)attn::kMinSplitTiles, min(share, table));
-}
 
 __device__ __forceinline__ int ctx_tiles(const AttnParams& p, int b) {
   const int C = max(0, min(p.ctx_len[b], p.max_ctx));
   return (C + p.TK - 1) / p.TK;
 }
 
-// Total tiles of the launch (every kv head of every sequence).
-__device__ __forceinline__ long long launch_tiles_warp(const AttnParams& p, int lane) {
-  long long tot = 0;
-  for (int b = lane; b < p.B; b += 32) tot += (long long)p.n_groups * (ctx_tiles(p, b) + (p.n_kv > 0 ? 1 : 0));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  return tot;
+__device__ __forceinline__ int group_tiles(const AttnParams& p, int b) {
+  return ctx_tiles(p, b) + (p.n_kv > 0 ? 1 : 0);
 }
 
-// Near-equal split of a context of nt tiles into ceil(nt / cap) parts.
-struct SeqSplit {
-  int nt, nsplit, per;
+struct AttnPlan {
+  int N, share, R;   // tiles of the launch, tiles per range, ranges
 };
-__device__ __forceinline__ SeqSplit seq_split(const AttnParams& p, int b, int cap) {
-  SeqSplit q;
-  q.nt = ctx_tiles(p, b);
-  q.nsplit = max(1, (q.nt + cap - 1) / cap);
-  q.per = (q.nt + q.nsplit - 1) / q.nsplit;
+
+// cum[b] (b = 0..B) = tiles per group of the sequences before b; whole warp.
+__device__ __forceinline__ void plan_cum_warp(const AttnParams& p, int* cum, int lane) {
+  const int per = (p.B + 31) / 32;
+  const int r0 = lane * per, r1 = min(p.B, r0 + per);
+  int tot = 0;
+  for (int b = r0; b < r1; ++b) tot += group_tiles(p, b);
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - tot;
+  for (int b = r0; b < r1; ++b) {
+    cum[b] = run;
+    run += group_tiles(p, b);
+  }
+  if (lane == 31) cum[p.B] = incl;
+}
+
+__device__ __forceinline__ AttnPlan make_plan(const AttnParams& p, const int* cum) {
+  AttnPlan q;
+  q.N = p.n_groups * cum[p.B];
+  // one page more than a piece spans, for pieces that start inside a page
+  const int window = (attn_tc::kPtMax - 1) * p.page_size / p.TK;
+  q.share = min(window, max(attn::kMinSplitTiles, (q.N + attn_tc::kGrid - 1) / attn_tc::kGrid));
+  q.R = (q.N + q.share - 1) / q.share;
   return q;
 }
 
-// Work item k (0 <= k < cum[B]): sequences in the order `order` (longest items
-// first), then kv head, then split; cum[r] = items of the sequences ranked
-// before r.
-__device__ __forceinline__ void decode_item(const AttnParams& p, const int* cum, const uint16_t* order, int cap,
-                                            int k, AttnItem& it) {
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {          // last rank r with cum[r] <= k
-    const int mid = (lo + hi + 1) >> 1;
-    if (cum[mid] <= k) lo = mid; else hi = mid - 1;
+// The next piece of this CTA: `v` is the current range, `pos` the next tile of
+// the launch sequence to hand out. Returns false when the CTA has no more work.
+__device__ __forceinline__ bool next_piece(const AttnParams& p, const int* cum, const AttnPlan& q, int& v, int& pos,
+                                           AttnItem& it) {
+  while (v < q.R) {
+    const int e = min(q.N, (v + 1) * q.share);
+    if (pos < e) {
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {      // last sequence whose tiles start at or before pos
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.n_groups * cum[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo, nt = cum[b + 1] - cum[b];
+      const int gb = p.n_groups * cum[b];
+      const int g = (pos - gb) / nt;
+      const int base = gb + g * nt;
+      const int t0 = pos - base, t1 = min(nt, e - base);
+      it.b = b;
+      it.g = g;
+      it.C = max(0, min(p.ctx_len[b], p.max_ctx));
+      it.t0 = t0;
+      it.n_tiles = t1 - t0;
+      it.n_tiles_ctx = max(0, min(t1, ctx_tiles(p, b)) - t0);
+      it.split = v - base / q.share;
+      it.nsplit = (base + nt - 1) / q.share - base / q.share + 1;
+      pos = base + t1;
+      return true;
+    }
+    v += attn_tc::kGrid;
+    pos = v * q.share;
   }
-  it.b = order[lo];
-  it.C = max(0, min(p.ctx_len[it.b], p.max_ctx));
-  const SeqSplit q = seq_split(p, it.b, cap);
-  it.nsplit = q.nsplit;
-  const int rem = k - cum[lo];
-  it.g = rem / q.nsplit;
-  it.split = rem - it.g * q.nsplit;
-  it.t0 = it.split * q.per;
-  it.n_tiles_ctx = max(0, min(q.nt, it.t0 + q.per) - it.t0);
-  it.n_tiles = it.n_tiles_ctx + ((it.split == it.nsplit - 1 && p.n_kv > 0) ? 1 : 0);
+  return false;
 }
 
 // 2^x on the special-function unit (flush-to-zero; P is rounded to bf16 anyway).
@@ -177,7 +200,7 @@ template <int kThreadsT, int HPI>
 __global__ void __launch_bounds__(kThreadsT, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const __grid_constant__ CUtensorMap kbmap, const __grid_constant__ CUtensorMap vbmap,
-               const AttnParams p, int S, int32_t* sched) {
+               const AttnParams p, int S) {
   using namespace attn_tc;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Roles, with W = ceil(Mi / 32) TMEM lane quarters holding real rows:
@@ -228,16 +251,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint64_t* l_full = s_full + 29;         // [2]  softmax -> epilogue: row max and sums of the item
   uint64_t* mg_in = s_full + 31;          // epilogue warps -> ticket taker: split partials published
   uint64_t* mg_out = s_full + 32;         // ticket taker -> epilogue warps: last_sm holds the ticket
-  int* ring = reinterpret_cast<int*>(s_full + 33);             // [2] item ids
-  int* cum = ring + 2;                                         // [B + 1] item prefix per rank
-  uint16_t* order = reinterpret_cast<uint16_t*>(cum + (kMaxSeqs + 1));   // [B] sequence of each rank
-  int* pt_s = reinterpret_cast<int*>(order + kMaxSeqs);        // [2][kPtMax] page rows of two items
+  AttnItem* ring = reinterpret_cast<AttnItem*>(s_full + 33);  // [2] pieces in flight (b < 0: none left)
+  int* cum = reinterpret_cast<int*>(ring + 2);                // [B + 1] tiles per group before sequence b
+  int* pt_s = cum + (kMaxSeqs + 1);                           // [2][kPtMax] page rows of two pieces
   float* xch = reinterpret_cast<float*>(pt_s + 2 * kPtMax);    // [2 tiles][2 halves][128] tile maxima
   float* ml_s = xch + 2 * 2 * 128;     // [2 slots][4][128]: (m, l) of softmax half 0, then of half 1
   uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(ml_s + 2 * 4 * 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sm + 1);
   int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
-  int* cap_sm = reinterpret_cast<int*>(tmem_base_sm + 3);
   volatile int* last_sm = reinterpret_cast<volatile int*>(tmem_base_sm + 4);   // epilogue: merge this item
 
   if (tid == 0) {
@@ -267,49 +288,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     fence_barrier_init();
   }
   if (warp == mma_warp) tmem_alloc(tmem_base_sm, kTmemCols);
-  // ---- work list: the split size, then sequences ranked by item size ----
-  if (warp == 0) {
-    const long long tot = launch_tiles_warp(p, lane);
-    if (lane == 0) *cap_sm = split_cap(p, tot);
-  }
-  __syncthreads();
-  const int cap = *cap_sm;
-  for (int bb = tid; bb < p.B; bb += blockDim.x) cum[bb] = seq_split(p, bb, cap).per;
-  __syncthreads();
-  for (int bb = tid; bb < p.B; bb += blockDim.x) {
-    const int key = cum[bb];
-    int rank = 0;   // larger items first; equal items in sequence order
-    for (int o = 0; o < p.B; ++o) {
-      const int ko = cum[o];
-      rank += (ko > key || (ko == key && o < bb)) ? 1 : 0;
-    }
-    order[rank] = (uint16_t)bb;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // cum[r] = sum over ranks r' < r of Hkv * splits: lane-contiguous runs, then a warp scan
-    const int per = (p.B + 31) / 32;
-    const int r0 = lane * per, r1 = min(p.B, r0 + per);
-    int tot = 0;
-    for (int rr = r0; rr < r1; ++rr) tot += p.n_groups * seq_split(p, order[rr], cap).nsplit;
-    int incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - tot;
-    for (int rr = r0; rr < r1; ++rr) {
-      cum[rr] = run;
-      run += p.n_groups * seq_split(p, order[rr], cap).nsplit;
-    }
-    if (lane == 31) cum[p.B] = incl;
-  }
+  // ---- work list: the tiles per group of every sequence, prefix-summed ----
+  if (warp == 0) plan_cum_warp(p, cum, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_sm;
-  const int n_items = cum[p.B];
+  const AttnPlan plan = make_plan(p, cum);
   int producer_issued = 0;
 
   if (warp == prod_warp) {
@@ -322,9 +307,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // page rows of item `item` into table `tb` (whole warp). Every lane issues
     // its loads together before storing any, so the fetch costs one memory
     // latency instead of one per round.
-    auto load_pages = [&](int item, int tb) {
-      AttnItem it;
-      decode_item(p, cum, order, cap, item, it);
+    auto load_pages = [&](const AttnItem& it, int tb) {
       const int lp0 = it.t0 * TK / ps;
       const int n_lp = ((it.t0 + it.n_tiles_ctx) * TK + ps - 1) / ps - lp0;
       const int32_t* ptb = p.page_table + (size_t)it.b * p.max_pages;
@@ -350,28 +333,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(p.err, 0, kDevErrBadPage);
       __syncwarp();
     };
-    int cur = 0;
-    if (lane == 0) cur = atomicAdd(&sched[0], 1);
-    cur = __shfl_sync(0xffffffffu, cur, 0);
-    if (cur < n_items) load_pages(cur, 0);
+    // this CTA's ranges: blockIdx.x, blockIdx.x + grid, ...
+    int rv = (int)blockIdx.x, rpos = (int)blockIdx.x * plan.share;
+    AttnItem cur;
+    bool have = next_piece(p, cum, plan, rv, rpos, cur);
+    if (have) load_pages(cur, 0);
     while (ok) {
-      const bool last = cur >= n_items;
       const int slot = item_seq & 1;
       bool w = true;
       if (lane == 0) w = wait_or_abort(&it_empty[slot], (uint32_t)(((item_seq >> 1) & 1) ^ 1), abort_flag, p.err, 21, p.wait_ns);
       if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) break;
       if (lane == 0) {
-        ring[slot] = last ? -1 : cur;
+        AttnItem pub = cur;
+        if (!have) pub.b = -1;
+        ring[slot] = pub;
         mbar_arrive(&it_full[slot]);    // release semantics publish the ring entry
       }
-      if (last) break;
-      AttnItem it;
-      decode_item(p, cum, order, cap, cur, it);
+      if (!have) break;
+      const AttnItem it = cur;
       const int* pt = pt_s + slot * kPtMax;
-      // the next item is claimed a few tiles before this one ends (late enough
-      // that the items still go to whichever CTA frees up first, early enough
-      // to fetch its page rows and Q before its first tile)
-      int nxt = n_items;
+      // the next piece's page rows are fetched a few tiles before this one ends
+      AttnItem nxt;
+      bool have_n = false;
       const int j_claim = max(0, it.n_tiles - kClaimAhead);
       for (int j = 0; j < it.n_tiles && ok; ++j, ++tile_seq) {
         if (lane == 0) {
@@ -409,22 +392,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (ok && j == j_claim) {
-          if (lane == 0) nxt = atomicAdd(&sched[0], 1);
-          nxt = __shfl_sync(0xffffffffu, nxt, 0);
-          if (nxt < n_items) load_pages(nxt, slot ^ 1);
+          have_n = next_piece(p, cum, plan, rv, rpos, nxt);
+          if (have_n) load_pages(nxt, slot ^ 1);
         }
       }
       cur = nxt;
+      have = have_n;
       ++item_seq;
-    }
-    // the last CTA to finish resets the work counter for the next launch
-    if (lane == 0) {
-      __threadfence();
-      if (atomicAdd(&sched[1], 1) == (int)gridDim.x - 1) {
-        sched[0] = 0;
-        sched[1] = 0;
-        __threadfence();
-      }
     }
     __syncwarp();
   } else if (warp == mma_warp) {
@@ -438,11 +412,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         const int slot = item_seq & 1;
         const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
         if (!wait_or_abort(&it_full[slot], par, abort_flag, p.err, 24, p.wait_ns)) break;
-        const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
+        const AttnItem it = ring[slot];
         mbar_arrive(&it_empty[slot]);
-        if (item < 0) break;
-        AttnItem it;
-        decode_item(p, cum, order, cap, item, it);
+        if (it.b < 0) break;
         // O: one buffer per item slot (ALT = 1), or both buffers for every item (ALT = 2)
         const int oi = ALT == 2 ? 0 : slot;
         const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
@@ -564,12 +536,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const int slot = item_seq & 1;
       const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
       if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[slot], par, abort_flag, p.err, 31, p.wait_ns))) break;
-      const int item = *reinterpret_cast<volatile int*>(&ring[slot]);
+      const AttnItem it = ring[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&it_empty[slot]);
-      if (item < 0) break;
-      AttnItem it;
-      decode_item(p, cum, order, cap, item, it);
+      if (it.b < 0) break;
       const int t0 = it.t0;
       const uint32_t o_col = 128 + (uint32_t)((ALT == 2 ? chalf : slot) * attn::kD) + oc0;
       float m_run = -CUDART_INF_F, l_part = 0.f;
@@ -714,21 +684,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // has read the buffer), then read this item's O out.
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // the ring entry of item number `seq`: an item, -1 (no more) or -2 (gave up)
-    auto read_item = [&](int seq) -> int {
+    // the ring entry of item number `seq` into `out`: 0 (a piece), -1 (no more)
+    // or -2 (gave up)
+    auto read_item = [&](int seq, AttnItem& out) -> int {
       const int sl = seq & 1;
       if (!__all_sync(0xffffffffu, wait_or_abort(&it_full[sl], (uint32_t)((seq >> 1) & 1), abort_flag, p.err, 38, p.wait_ns)))
         return -2;
-      const int v = *reinterpret_cast<volatile int*>(&ring[sl]);
+      out = ring[sl];
       __syncwarp();
       if (lane == 0) mbar_arrive(&it_empty[sl]);
-      return v;
+      return out.b < 0 ? -1 : 0;
     };
     // this lane's packed query row r of item `item` (r = i * Gi + head) into
     // TMEM columns kQCol..kQCol+63; rows past Mi stay unwritten (padding lanes)
-    auto put_q = [&](int item, int seq) -> bool {
-      AttnItem qi;
-      decode_item(p, cum, order, cap, item, qi);
+    auto put_q = [&](const AttnItem& qi, int seq) -> bool {
       uint32_t qv[64];
       if (r < p.Mi) {
         const int i = r / p.Gi, hh = r - i * p.Gi;
@@ -757,16 +726,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       return true;
     };
     int item_seq = 0, n_merge = 0;
-    int item = read_item(0);
-    bool qok = item >= 0 ? put_q(item, 0) : false;
-    while (item >= 0 && qok) {
-      const int nxt = read_item(item_seq + 1);
-      if (nxt == -2) break;
-      if (nxt >= 0 && !put_q(nxt, item_seq + 1)) break;
+    AttnItem it_cur, it_nxt;
+    int st_cur = read_item(0, it_cur);
+    bool qok = st_cur == 0 ? put_q(it_cur, 0) : false;
+    while (st_cur == 0 && qok) {
+      const int st_nxt = read_item(item_seq + 1, it_nxt);
+      if (st_nxt == -2) break;
+      if (st_nxt == 0 && !put_q(it_nxt, item_seq + 1)) break;
       const int slot = item_seq & 1;
       const uint32_t par = (uint32_t)((item_seq >> 1) & 1);
-      AttnItem it;
-      decode_item(p, cum, order, cap, item, it);
+      const AttnItem it = it_cur;
       const int oi = ALT == 2 ? 0 : slot;
       const uint32_t opar = ALT == 2 ? (uint32_t)(item_seq & 1) : par;
       if (!__all_sync(0xffffffffu, wait_or_abort(&l_full[slot], par, abort_flag, p.err, 39, p.wait_ns))) break;
@@ -901,7 +870,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
       }
-      item = nxt;
+      it_cur = it_nxt;
+      st_cur = st_nxt;
       ++item_seq;
     }
   }
@@ -1028,9 +998,11 @@ static int attn_hpi(int n_q, int n_kv, int Hq, int Hkv, int page_size) {
   return pair ? 2 : 1;
 }
 
+// Pieces of one (sequence, group) at most: its tiles (context and block) over
+// ranges of at least kMinSplitTiles, plus one for a range border inside it.
 static int attn_max_splits(int max_ctx, int TK) {
-  const int tiles = (max_ctx + TK - 1) / TK;
-  return std::max(1, (tiles + attn::kMinSplitTiles - 1) / attn::kMinSplitTiles);
+  const int tiles = (max_ctx + TK - 1) / TK + 1;
+  return (tiles + attn::kMinSplitTiles - 1) / attn::kMinSplitTiles + 1;
 }
 
 size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int page_size, int dtype) {
@@ -1044,11 +1016,11 @@ size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_c
 template <int kThreadsT, int HPI>
 static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& kbmap,
                                   const CUtensorMap& vbmap, const AttnParams& p,
-                                  int S, size_t smem, int32_t* sched, cudaStream_t st) {
+                                  int S, size_t smem, cudaStream_t st) {
   static SmemOptIn opt_in;
   cudaError_t e = opt_in.ensure(attn_tc_kernel<kThreadsT, HPI>, smem);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, kbmap, vbmap, p, S, sched);
+  attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, kbmap, vbmap, p, S);
   return cudaGetLastError();
 }
 
@@ -1125,11 +1097,11 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   const bool wide = (M + 31) / 32 > 2;
   cudaError_t e;
   if (wide)
-    e = p.hpi == 2 ? launch_attn_tc<448, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream)
-                   : launch_attn_tc<448, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream);
+    e = p.hpi == 2 ? launch_attn_tc<448, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream)
+                   : launch_attn_tc<448, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream);
   else
-    e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream)
-                   : launch_attn_tc<320, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.sched, a.stream);
+    e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream)
+                   : launch_attn_tc<320, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream);
   return e;
 }
 

@@ -177,7 +177,6 @@ struct AttnArgs {
   float scale;
   void* out;
   int32_t* counters;
-  int32_t* sched;   // two zeroed ints: persistent-kernel work counter and exit counter
   int* err;
   void* scratch;
   cudaStream_t stream;

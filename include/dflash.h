@@ -193,8 +193,8 @@ typedef struct {
  * scale: softmax scale (1/sqrt(D) for the standard form)
  * out [B, n_q, Hq, D]
  * Repeated calls on the same inputs return identical bits: the bf16 kernel
- * hands work items to whichever CTA is free, and its arithmetic does not
- * depend on that assignment.
+ * divides the work by a static partition that depends on the dims and ctx_len
+ * only, and merges split contexts in a fixed order.
  */
 size_t dflash_block_attn_workspace_size(const dflash_attn_dims* dims);
 int dflash_block_attn(const dflash_attn_dims* dims,
