@@ -23,56 +23,6 @@
 
 namespace dflash {
 
-// ---------------------------------------------------------------------------
-// plan: compact row list of the committed rows
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
-mat_plan_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restrict__ start_pos, int B,
-                int rows_max, int32_t* __restrict__ meta, int32_t* __restrict__ row_b,
-                int32_t* __restrict__ row_j, int32_t* __restrict__ row_start, int32_t* __restrict__ new_len, int tc,
-                int N1, int K1, int N2, int K2) {
-  __shared__ int32_t scan[256];
-  const int tid = threadIdx.x;
-  const int per = (B + blockDim.x - 1) / blockDim.x;
-  const int b0 = tid * per, b1 = min(B, b0 + per);
-  int local = 0;
-  for (int b = b0; b < b1; ++b) local += max(0, min(commit_len[b], rows_max));
-  scan[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < (int)blockDim.x; off <<= 1) {
-    const int v = tid >= off ? scan[tid - off] : 0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
-  }
-  int row = scan[tid] - local;
-  for (int b = b0; b < b1; ++b) {
-    const int n = max(0, min(commit_len[b], rows_max));
-    row_start[b] = row;
-    row += n;
-    if (new_len) new_len[b] = start_pos[b] + n;
-  }
-  const int T = scan[blockDim.x - 1];
-  if (tid == blockDim.x - 1) {
-    row_start[B] = T;
-    meta[0] = T;
-    // tensor-core GEMMs: k-block range per persistent CTA for T rows (0: fixed splits)
-    meta[1] = tc ? gemm_tc_per(T, N1, K1) : 0;
-    meta[2] = tc ? gemm_tc_per(T, N2, K2) : 0;
-  }
-  __syncthreads();
-  // row list, all threads: row r belongs to the last sequence whose rows start at or before r
-  for (int r = tid; r < T; r += blockDim.x) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (row_start[mid] <= r) lo = mid; else hi = mid - 1;
-    }
-    row_b[r] = lo;
-    row_j[r] = r - row_start[lo];
-  }
-}
-
 // RoPE frequencies theta^(-2i/D) for i < D/2, computed on the host in double
 // and passed by value (D <= 256)
 struct RopeFreq {
@@ -80,72 +30,115 @@ struct RopeFreq {
 };
 
 // ---------------------------------------------------------------------------
-// gather: hidden[b, j, :] -> X[t, :]
+// gather: committed rows hidden[b, j, :] -> a dense X[t, :], t in prefix order
+// of the sequences. Every CTA forms the prefix of commit_len itself (threads
+// own contiguous runs of sequences, then one block scan), so no separate plan
+// launch is needed; CTA 0 also writes the plan the later kernels read (T, the
+// GEMMs' k-block ranges) and new_len. Rows go one per CTA pass, 256 threads x
+// 16-byte vectors, ten loads in flight per thread. The same pass records each
+// row's sequence, index, pool slot and RoPE (cos, sin) coefficients.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
-mat_gather_kernel(const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, const int32_t* __restrict__ meta,
-                  const int32_t* __restrict__ row_b, const int32_t* __restrict__ row_j, int rows_max,
-                  size_t row_bytes, const int32_t* __restrict__ start_pos, const __grid_constant__ RopeFreq inv_freq,
-                  float2* __restrict__ rope, int half, const int32_t* __restrict__ page_table, int page_size,
-                  int max_pages, int num_pages, long long* __restrict__ slots) {
-  // grid-stride over the committed rows only (their count is on the device)
-  const long T = meta[0];
+mat_gather_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restrict__ start_pos, int B,
+                  int rows_max, const uint8_t* __restrict__ hidden, uint8_t* __restrict__ X, size_t row_bytes,
+                  int32_t* __restrict__ meta, int32_t* __restrict__ row_b, int32_t* __restrict__ row_j,
+                  int32_t* __restrict__ new_len, int tc, int N1, int K1, int N2, int K2,
+                  const __grid_constant__ RopeFreq inv_freq, float2* __restrict__ rope, int half,
+                  const int32_t* __restrict__ page_table, int page_size, int max_pages, int num_pages,
+                  long long* __restrict__ slots) {
+  __shared__ int scan[256];
+  __shared__ int run_start[257];
+  const int tid = threadIdx.x;
+  const int per = (B + 255) / 256;
+  const int b0 = tid * per, b1 = min(B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += max(0, min(commit_len[b], rows_max));
+  scan[tid] = local;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    const int v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  run_start[tid] = scan[tid] - local;
+  if (tid == 255) run_start[256] = scan[255];
+  __syncthreads();
+  const int T = run_start[256];
+  if (blockIdx.x == 0) {
+    if (tid == 0) {
+      meta[0] = T;
+      // tensor-core GEMMs: k-block range per persistent CTA for T rows (0: fixed splits)
+      meta[1] = tc ? gemm_tc_per(T, N1, K1) : 0;
+      meta[2] = tc ? gemm_tc_per(T, N2, K2) : 0;
+    }
+    if (new_len)
+      for (int b = b0; b < b1; ++b) new_len[b] = start_pos[b] + max(0, min(commit_len[b], rows_max));
+  }
+  const bool vec = (row_bytes % 16) == 0 && (reinterpret_cast<uintptr_t>(hidden) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(X) & 15) == 0;
   const long nvec = (long)(row_bytes / 16);
-  const long stride = (long)gridDim.x * blockDim.x;
-  // four 16-byte copies in flight per thread
-  constexpr int U = 4;
-  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * nvec; idx += U * stride) {
-    uint4 val[U];
+  for (int r = blockIdx.x; r < T; r += gridDim.x) {
+    // the sequence of row r: the last run starting at or before r, then its sequences
+    int lo = 0, hi = 255;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (run_start[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    int b = lo * per, j = r - run_start[lo];
+    for (const int be = min(B, b + per) - 1; b < be; ++b) {
+      const int n = max(0, min(commit_len[b], rows_max));
+      if (j < n) break;
+      j -= n;
+    }
+    const uint8_t* src = hidden + ((size_t)b * rows_max + j) * row_bytes;
+    uint8_t* dst = X + (size_t)r * row_bytes;
+    if (vec) {
+      constexpr int U = 10;
+      for (long v0 = 0; v0 < nvec; v0 += U * 256) {
+        uint4 val[U];
 #pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const long i = idx + k * stride;
-      if (i < T * nvec) {
-        const long t = i / nvec, v = i - t * nvec;
-        val[k] = __ldg(reinterpret_cast<const uint4*>(hidden + ((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes) + v);
-      }
-    }
+        for (int u = 0; u < U; ++u) {
+          const long v = v0 + u * 256 + tid;
+          if (v < nvec) val[u] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+        }
 #pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const long i = idx + k * stride;
-      if (i < T * nvec) {
-        const long t = i / nvec, v = i - t * nvec;
-        reinterpret_cast<uint4*>(X + (size_t)t * row_bytes)[v] = val[k];
+        for (int u = 0; u < U; ++u) {
+          const long v = v0 + u * 256 + tid;
+          if (v < nvec) reinterpret_cast<uint4*>(dst)[v] = val[u];
+        }
       }
+    } else {
+      for (size_t e = tid; e < row_bytes; e += 256) dst[e] = src[e];
     }
-  }
-  const long tail = (long)row_bytes - nvec * 16;
-  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * tail; idx += stride) {
-    const long t = idx / tail, e = nvec * 16 + (idx - t * tail);
-    X[(size_t)t * row_bytes + e] = hidden[((size_t)row_b[t] * rows_max + row_j[t]) * row_bytes + e];
-  }
-  // the pool slot of every committed row (-1: position outside the page table)
-  for (long t = blockIdx.x * (long)blockDim.x + threadIdx.x; t < T; t += stride) {
-    const int b = row_b[t];
-    const int pos = start_pos[b] + row_j[t];
-    const int lp = pos / page_size;
-    long long sl = -1;
-    if (pos >= 0 && lp < max_pages) {
-      const int phys = page_table[(size_t)b * max_pages + lp];
-      if (phys >= 0 && phys < num_pages) sl = (long long)phys * page_size + pos % page_size;
+    const int pos = start_pos[b] + j;
+    if (tid == 0) {
+      row_b[r] = b;
+      row_j[r] = j;
+      // the pool slot of the row (-1: position outside the page table)
+      const int lp = pos / page_size;
+      long long sl = -1;
+      if (pos >= 0 && lp < max_pages) {
+        const int phys = page_table[(size_t)b * max_pages + lp];
+        if (phys >= 0 && phys < num_pages) sl = (long long)phys * page_size + pos % page_size;
+      }
+      slots[r] = sl;
     }
-    slots[t] = sl;
+    // RoPE (cos, sin) of the row's position, pair i: the angle pos * theta^(-2i/D)
+    // in double (it reaches ~1e4 radians), reduced to [-pi, pi] by Cody-Waite
+    // subtraction of k * 2 pi with 2 pi split into a double and its remainder,
+    // then sin/cos in fp32 on the reduced angle
+    if (rope)
+      for (int i = tid; i < half; i += 256) {
+        const double a = (double)pos * inv_freq.f[i];
+        const double k = rint(a * 0.15915494309189535);
+        double rr = fma(-k, 6.283185307179586, a);
+        rr = fma(-k, 2.4492935982947064e-16, rr);
+        float sf, cf;
+        sincosf((float)rr, &sf, &cf);
+        rope[(size_t)r * half + i] = make_float2(cf, sf);
+      }
   }
-  // RoPE (cos, sin) of every committed row's position, pair i: the angle
-  // pos * theta^(-2i/D) in double (it reaches ~1e4 radians), reduced to
-  // [-pi, pi] by Cody-Waite subtraction of k * 2 pi with 2 pi split into a
-  // double and its remainder, then sin/cos in fp32 on the reduced angle
-  if (rope)
-    for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < T * half; idx += stride) {
-      const long t = idx / half;
-      const int i = (int)(idx - t * half);
-      const double a = (double)(start_pos[row_b[t]] + row_j[t]) * inv_freq.f[i];
-      const double k = rint(a * 0.15915494309189535);
-      double r = fma(-k, 6.283185307179586, a);
-      r = fma(-k, 2.4492935982947064e-16, r);
-      float sf, cf;
-      sincosf((float)r, &sf, &cf);
-      rope[idx] = make_float2(cf, sf);
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -504,7 +497,6 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   int32_t* meta = (int32_t*)ws;
   int32_t* row_b = meta + 64;
   int32_t* row_j = row_b + p.T_max;
-  int32_t* row_start = row_j + p.T_max;
   ws += align_up(sizeof(int32_t) * (64 + 2 * (size_t)p.T_max + p.B + 1));
   RopeFreq inv_freq;
   for (int i = 0; i < 128; ++i)
@@ -520,14 +512,12 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   float* part = (float*)ws;
   cudaStream_t st = a.stream;
   int n = 0;
-  mat_plan_kernel<<<1, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, meta, row_b, row_j, row_start,
-                                     a.new_len, p.tc ? 1 : 0, p.N1, p.K1, p.N2, p.K2);
-  ++n;
   const size_t row_bytes = (size_t)p.K1 * el;
   // grid-stride kernels over the committed rows: a few waves of the 152 SMs
   const int gs = 4 * 152;
-  mat_gather_kernel<<<gs, 256, 0, st>>>((const uint8_t*)a.hidden, (uint8_t*)X, meta, row_b, row_j, a.rows_max,
-                                        row_bytes, a.start_pos, inv_freq, rope, a.D / 2, a.page_table, a.page_size,
+  mat_gather_kernel<<<gs, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, (const uint8_t*)a.hidden,
+                                        (uint8_t*)X, row_bytes, meta, row_b, row_j, a.new_len, p.tc ? 1 : 0, p.N1,
+                                        p.K1, p.N2, p.K2, inv_freq, rope, a.D / 2, a.page_table, a.page_size,
                                         a.max_pages, a.num_pages, slots);
   ++n;
   cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, 1, a.err, st);
