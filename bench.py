@@ -613,6 +613,15 @@ def run_kernel(args, wl):
         print(json.dumps({"kernel": "prefill", "workload": W.LLAMA8B_B1.name, "rows": T, "us_per_call": us,
                           "tflops": flops / us / 1e6, "frac_bf16_peak": flops / us / 1e6 / _peaks()[1]}), flush=True)
         return
+    if args.kernel == "materialize":
+        # decode-sized: 64 sequences commit 1-8 rows each (seeded, ~4 on
+        # average like the step's accept lengths) at their context ends; the
+        # pools map only the pages those rows touch, so the call holds ~0.4 GB
+        call, T, nbytes = decode_materialize_call(wl, "cuda:0")
+        us = _time_calls(call, args.steps, args.warmup)
+        print(json.dumps({"kernel": "materialize", "workload": wl.name, "rows": T, "us_per_call": us,
+                          "bytes": nbytes, "frac_hbm": nbytes / us / 1e3 / _peaks()[0]}), flush=True)
+        return
     if args.batch:
         wl = dataclasses.replace(wl, B=args.batch, n_greedy=min(wl.n_greedy, args.batch // 2))
     one = dataclasses.replace(wl, L=1) if args.kernel in ("attn", "verify") else wl
@@ -865,6 +874,41 @@ def prefill_materialize_call(wl, dev):
                                wl.rope_theta, pools_k, pools_v, ptab)
     T = wl.B * rows
     return call, T, 2.0 * T * (wl.m * wl.d * wl.d + wl.d * wl.kv_out)
+
+
+def decode_materialize_call(wl, dev):
+    """One decode-sized materialisation at the throughput workload's shape:
+    returns (call, committed rows T, algorithmic bytes: weights, the committed
+    hidden rows and the K/V rows written)."""
+    import torch
+    from block_diffusion_speculative_fusion_gb300 import api, synth
+    gen = torch.Generator().manual_seed(3)
+    commit = torch.randint(1, 9, (wl.B,), generator=gen).to(torch.int32)
+    start = synth.ctx_lengths(wl, 0)
+    P = wl.page_size
+    lo = (start // P).tolist()
+    hi = ((start + commit - 1) // P).tolist()
+    max_pages = max(hi) + 1
+    pt = torch.full((wl.B, max_pages), -1, dtype=torch.int32)
+    n = 0
+    for b in range(wl.B):
+        k = hi[b] - lo[b] + 1
+        pt[b, lo[b]:hi[b] + 1] = torch.arange(n, n + k, dtype=torch.int32)
+        n += k
+    w = {k_: (v_.to(dev) if v_ is not None else None) for k_, v_ in synth.ctx_weights(wl, 0).items()}
+    hid = synth.captured_hidden(wl, wl.k, 0).to(dev)
+    dt = synth.io_dtype(wl)
+    kp = [torch.zeros((n, P, wl.Hkv, wl.D), dtype=dt, device=dev) for _ in range(wl.L)]
+    vp = [torch.zeros((n, P, wl.Hkv, wl.D), dtype=dt, device=dev) for _ in range(wl.L)]
+    commit_d, start_d, pt_d = commit.to(dev), start.to(dev), pt.to(dev)
+
+    def call():
+        api.materialize_ctx_kv(hid, commit_d, start_d, w["W_f"], w["b_f"], w["W_kv"], w["k_norm_w"], wl.rms_eps,
+                               wl.rope_theta, kp, vp, pt_d)
+    T = int(commit.sum())
+    el = 2
+    nbytes = (wl.d * wl.m * wl.d + wl.kv_out * wl.d) * el + T * (wl.m * wl.d + wl.kv_out) * el
+    return call, T, nbytes
 
 
 def run_all_configs(args):
