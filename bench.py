@@ -164,6 +164,20 @@ def oracle_step_estimate(wl, ctx_all, commit_rows, n_attn=2, n_verify=2, n_rows=
                            "sample_cpu_s": t_attn + t_g + t_s + t_m}
 
 
+def abi_host_cost():
+    """Host time of one enqueue through the C ABI per entry point (the C
+    harness built beside the library; small problems, no synchronisation in
+    the timed loop)."""
+    from block_diffusion_speculative_fusion_gb300 import build as _b
+    if not os.path.exists(_b.HOST_COST):
+        return {"note": "harness not built"}
+    try:
+        r = subprocess.run([_b.HOST_COST], stdout=subprocess.PIPE, stderr=subprocess.STDOUT, timeout=120, text=True)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as exc:   # noqa: BLE001 - reported, not fatal
+        return {"note": f"{type(exc).__name__}: {exc}"[:200]}
+
+
 def workload_config(wl, world=1):
     """The ``config`` object of the JSON line: the workload, identical in both arms."""
     return {"workload": wl.name, "B": wl.B, "k": wl.k, "L": wl.L, "V": wl.V, "d": wl.d,
@@ -431,18 +445,33 @@ def run_ours(args, wl):
 
     # The K timed steps are launched as one CUDA graph (the step is a fixed
     # sequence of launches on one stream), which removes the host launch gaps
-    # between kernels; every call keeps its own timing events inside the graph.
+    # between kernels. `value` is timed on a graph of the bare steps; the
+    # per-call times come from a second graph of the same steps with a timing
+    # event around every call, replayed apart (the event nodes add ~3 % to a
+    # step, so they stay out of the timed region).
     graph, gev, launch_note = (None, None, "stream launches (--no-graph)")
+    graph_plain = None
     if not args.no_graph:
         graph, gev, why = capture_steps(torch, st, args.steps)
         if graph is not None:
-            graph.replay()          # upload and one untimed pass
+            try:
+                graph_plain = st.capture(args.steps)
+            except Exception as exc:   # noqa: BLE001 - the event graph is timed instead
+                torch.cuda.synchronize()
+                graph_plain = None
+                why = f"plain capture failed: {type(exc).__name__}"
+            for g_ in (graph, graph_plain):
+                if g_ is not None:
+                    g_.replay()          # upload and one untimed pass
             torch.cuda.synchronize()
-            launch_note = f"one CUDA graph of the {args.steps} timed steps"
+            launch_note = (f"one CUDA graph of the {args.steps} timed steps" if graph_plain is not None else
+                           f"one CUDA graph of the {args.steps} timed steps, with per-call events ({why})")
         else:
             launch_note = f"stream launches ({why})"
 
-    def timed_region(use_graph):
+    def timed_region(mode):
+        """mode: 'plain' (bare-step graph), 'events' (graph with per-call
+        events) or 'stream' (stream launches with events)."""
         clocks = Clocks(local)
         barrier()
         torch.cuda.synchronize()
@@ -450,7 +479,9 @@ def run_ours(args, wl):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        if use_graph:
+        if mode == "plain":
+            graph_plain.replay()
+        elif mode == "events":
             graph.replay()
         else:
             for _ in range(args.steps):
@@ -459,18 +490,24 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
         barrier()
         clk_ = clocks.stop()
-        src = gev if use_graph else ev
+        src = gev if mode == "events" else ev
         pk = {k: (sum(a.elapsed_time(b) for a, b in v) / len(v)) * 1e3 for k, v in src.items() if v}
         return t_start.elapsed_time(t_end), pk, clk_
 
-    ms_total, per_kernel, clk = timed_region(graph is not None)
     if graph is not None:
+        ms_ev, per_kernel, clk = timed_region("events")
         # the calls' event times must fit inside the step time
         calls_us = per_kernel.get("attn", 0.0) * wl.L + per_kernel.get("verify", 0.0) + per_kernel.get("mat", 0.0)
-        step_us = ms_total / args.steps * 1e3
+        step_us = ms_ev / args.steps * 1e3
         if not (0.5 * step_us < calls_us <= 1.02 * step_us):
             launch_note = f"stream launches (graph event times {calls_us:.0f} us vs step {step_us:.0f} us)"
-            ms_total, per_kernel, clk = timed_region(False)
+            ms_total, per_kernel, clk = timed_region("stream")
+        elif graph_plain is not None:
+            ms_total, _, clk = timed_region("plain")
+        else:
+            ms_total = ms_ev
+    else:
+        ms_total, per_kernel, clk = timed_region("stream")
     ms_max = max_over_ranks(ms_total, world, dev)
     # a kernel that gave up a bounded wait (or met a bad page entry) leaves a
     # code in its workspace: such a run's numbers are not valid
@@ -565,6 +602,11 @@ def run_ours(args, wl):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = replica_throughput(args.steps, e2e_ms, world)
 
+    # ---------------- per-call host cost of the C ABI, measured from C ----------------
+    abi_host = None
+    if rank == 0:
+        abi_host = abi_host_cost()
+
     # ---------------- CPU baseline: the oracle on a bounded sample ----------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -590,6 +632,8 @@ def run_ours(args, wl):
             "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": st.launches_per_step * args.steps,
             "device_error_words": dev_errors,
+            "ms_per_step_with_call_events": ms_ev / args.steps if graph is not None else None,
+            "abi_host_us_per_call": abi_host,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

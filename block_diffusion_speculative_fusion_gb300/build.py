@@ -70,7 +70,29 @@ def build(verbose: bool = False, extra_flags=None) -> str:
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
         os.replace(tmp, LIB)
+    _build_tools(verbose)
     return LIB
+
+
+TOOLS = os.path.join(HERE, "tools")
+HOST_COST = os.path.join(OBJDIR, "abi_host_cost")
+
+
+def _build_tools(verbose: bool = False) -> None:
+    """The C harness that times the ABI's per-call host cost (bench.py runs it)."""
+    src = os.path.join(TOOLS, "abi_host_cost.c")
+    if not os.path.exists(src):
+        return
+    newest = max(os.path.getmtime(src), os.path.getmtime(LIB), os.path.getmtime(os.path.join(INCLUDE, "dflash.h")))
+    if os.path.exists(HOST_COST) and os.path.getmtime(HOST_COST) >= newest:
+        return
+    cmd = [nvcc(), "-O2", "-o", HOST_COST, src, "-I", INCLUDE, "-L", HERE, "-ldflash", "-lcudart",
+           "-Xlinker", f"-rpath={HERE}"]
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+    if r.returncode != 0:
+        raise RuntimeError("abi_host_cost build failed:\n" + r.stdout.decode(errors="replace"))
 
 
 if __name__ == "__main__":
