@@ -12,6 +12,10 @@
 // group costs only the rows it has; the ring of stages is laid out at run time
 // for the number of rows present.
 //
+// Weight tiles are loaded with an L2 evict-first policy: each weight byte is
+// read once, and without the hint the weight stream pushes the split-K
+// partial sums out of L2 before the kernels that sum them run.
+//
 // Persistent CTAs (one per SM): when there are at least GRID tiles, whole
 // waves of GRID tiles go one per CTA (concurrent tiles then share their rows
 // and weights in L2); the remaining tiles' (tile, 64-wide k-block) space is
@@ -152,6 +156,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
+      const uint64_t pol_w = l2_policy_evict_first();
       int wave = 0, pos = w.lo;
       TcPiece c;
       while (ok && tc_next(w, wave, pos, c)) {
@@ -160,7 +165,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
           if (!wait_or_abort(&empty[stage], phase ^ 1u, abort_flag, err, 2, wait_ns)) { ok = false; break; }
           uint8_t* sa = smem + stage * w.stage_bytes;
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(A_BYTES + rows16 * BK * 2));
-          tma_load_2d(sa, &wmap, &full[stage], kb * BK, c.m_tile * BM);
+          tma_load_2d_hint(sa, &wmap, &full[stage], kb * BK, c.m_tile * BM, pol_w);
           // the pass's rows in the largest boxes that fit (all multiples of 16)
           for (int r = 0; r < rows16;) {
             const int left = rows16 - r;
