@@ -24,6 +24,9 @@ FLAG_GATE_BOUNDARY = 1
 WS_COUNTER_BYTES = 16384
 WS_ERROR_WORD_OFFSET = WS_COUNTER_BYTES - 4
 DEVERR_BAD_PAGE = 100
+DEVERR_BAD_N_DRAFT = 101
+# recorded only by the debug library (select_library(debug=True))
+DEVERR_BAD_CTX_LEN, DEVERR_BAD_COMMIT_LEN, DEVERR_BAD_POSITION = 102, 103, 104
 
 
 class DflashError(RuntimeError):
@@ -99,6 +102,17 @@ _SIGS = {
 }
 
 _lib = None
+LIB_DEBUG_PATH = os.path.join(_HERE, "libdflash_debug.so")
+
+
+def select_library(debug: bool = False) -> str:
+    """Use libdflash.so, or libdflash_debug.so (built by ``build.build(debug=True)``,
+    whose kernels also record clamped inputs in the error word), for every later
+    call; returns its path."""
+    global _lib, LIB_PATH
+    LIB_PATH = LIB_DEBUG_PATH if debug else os.path.join(_HERE, "libdflash.so")
+    _lib = None
+    return LIB_PATH
 
 
 def lib() -> ctypes.CDLL:
@@ -519,7 +533,10 @@ def block_attn(q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor, k_pool
 def device_error_word(ws: torch.Tensor) -> int:
     """The sticky device-side error word of a workspace (0: no error; 1-99: a
     kernel gave up a bounded wait; DEVERR_BAD_PAGE: attention met a page-table
-    entry outside the pools). Synchronises with the device to read it."""
+    entry outside the pools; DEVERR_BAD_N_DRAFT: a verify or draft-select call
+    met an n_draft outside [0, n_max]; with the debug library also
+    DEVERR_BAD_CTX_LEN, DEVERR_BAD_COMMIT_LEN, DEVERR_BAD_POSITION).
+    Synchronises with the device to read it."""
     return int(ws[WS_ERROR_WORD_OFFSET:WS_COUNTER_BYTES].view(torch.int32).item())
 
 

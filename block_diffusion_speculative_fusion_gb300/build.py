@@ -3,6 +3,11 @@
 Each translation unit compiles in parallel with nvcc; the objects link into one
 shared library next to this file. Rebuilds only what changed. Usable as
 ``python -m block_diffusion_speculative_fusion_gb300.build``.
+
+``build(debug=True)`` makes libdflash_debug.so from the same sources with
+DFLASH_DEBUG defined: the kernels then also record, in the workspace error
+word, the inputs that release builds clamp without a record (context and
+commit lengths out of range, committed rows without a pool slot).
 """
 from __future__ import annotations
 
@@ -17,6 +22,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdflash.so")
+LIB_DEBUG = os.path.join(HERE, "libdflash_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -35,15 +41,17 @@ def _headers():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def build(verbose: bool = False, extra_flags=None) -> str:
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    objdir = OBJDIR + "_debug" if debug else OBJDIR
+    lib = LIB_DEBUG if debug else LIB
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_mtime = max([os.path.getmtime(h) for h in _headers()] + [os.path.getmtime(__file__)])
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + (["-DDFLASH_DEBUG"] if debug else []) + list(extra_flags or [])
     procs = []
     objs = []
     for src in srcs:
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), hdr_mtime):
             continue
@@ -63,15 +71,16 @@ def build(verbose: bool = False, extra_flags=None) -> str:
         msg = "\n".join(f"--- {s}\n{t}" for s, t in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
     newest = max(os.path.getmtime(o) for o in objs)
-    if procs or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
-        tmp = LIB + ".tmp"
+    if procs or not os.path.exists(lib) or os.path.getmtime(lib) < newest:
+        tmp = lib + ".tmp"
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
-        os.replace(tmp, LIB)
-    _build_tools(verbose)
-    return LIB
+        os.replace(tmp, lib)
+    if not debug:
+        _build_tools(verbose)
+    return lib
 
 
 TOOLS = os.path.join(HERE, "tools")

@@ -7,10 +7,22 @@
 #include <mutex>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/dflash.h"
 #include "internal.h"
 
 namespace {
+
+// One NVTX range per call that launches work, named after the entry point, so
+// that a profiler recording NVTX shows each call's kernels under its name
+// (header-only NVTX: without a tool attached a range costs a few nanoseconds).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 thread_local std::string g_err;
 thread_local int g_launches = 0;
@@ -93,6 +105,7 @@ int dflash_verify_greedy(const dflash_verify_dims* d, const void* target_logits,
                          const int32_t* n_draft, int32_t* accept_len, int64_t* bonus,
                          int32_t* commit_len, int64_t* out_tokens, int64_t* target_pred,
                          void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  CallRange range_("dflash_verify_greedy");
   int rc = check_verify_dims(d, false);
   if (rc) return rc;
   if (!target_logits || !cand || !accept_len || !bonus || !commit_len)
@@ -105,6 +118,7 @@ int dflash_verify_greedy(const dflash_verify_dims* d, const void* target_logits,
   a.accept_len = accept_len; a.bonus = bonus; a.commit_len = commit_len;
   a.out_tokens = out_tokens; a.target_pred = target_pred;
   a.counters = (int32_t*)workspace;
+  a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
   a.stream = (cudaStream_t)stream;
   cudaError_t e = dflash::launch_verify_greedy(a, kPlanSms);
@@ -157,6 +171,7 @@ int dflash_verify_greedy_noalloc(const dflash_verify_dims* d, const void* target
                                  const int32_t* n_draft, int32_t* accept_len, int64_t* bonus,
                                  int32_t* commit_len, int64_t* out_tokens, int64_t* target_pred,
                                  dflash_stream_t stream) {
+  CallRange range_("dflash_verify_greedy_noalloc");
   int rc = check_verify_dims(d, false);
   if (rc) return rc;
   if (!target_logits || !cand || !accept_len || !bonus || !commit_len)
@@ -184,6 +199,7 @@ int dflash_verify_sample(const dflash_verify_dims* d, float temperature, const v
                          const float* u_accept, const float* u_final, int32_t* accept_len,
                          int64_t* bonus, int32_t* commit_len, int64_t* out_tokens, uint8_t* flags,
                          float* probs, void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  CallRange range_("dflash_verify_sample");
   int rc = check_verify_dims(d, true);
   if (rc) return rc;
   if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
@@ -199,6 +215,7 @@ int dflash_verify_sample(const dflash_verify_dims* d, float temperature, const v
   a.accept_len = accept_len; a.bonus = bonus; a.commit_len = commit_len;
   a.out_tokens = out_tokens; a.flags = flags; a.probs = probs;
   a.counters = (int32_t*)workspace;
+  a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
   a.stream = (cudaStream_t)stream;
   cudaError_t e = dflash::launch_verify_sample(a, kPlanSms);
@@ -212,6 +229,7 @@ int dflash_verify_sample_lse(const dflash_verify_dims* d, float temperature, con
                              int32_t* accept_len, int64_t* bonus, int32_t* commit_len, int64_t* out_tokens,
                              uint8_t* flags, float* probs, void* workspace, size_t ws_bytes,
                              dflash_stream_t stream) {
+  CallRange range_("dflash_verify_sample_lse");
   int rc = check_verify_dims(d, true);
   if (rc) return rc;
   if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
@@ -228,6 +246,7 @@ int dflash_verify_sample_lse(const dflash_verify_dims* d, float temperature, con
   a.accept_len = accept_len; a.bonus = bonus; a.commit_len = commit_len;
   a.out_tokens = out_tokens; a.flags = flags; a.probs = probs;
   a.counters = (int32_t*)workspace;
+  a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
   a.stream = (cudaStream_t)stream;
   cudaError_t e = dflash::launch_verify_sample(a, kPlanSms);
@@ -255,6 +274,7 @@ int dflash_gate(const dflash_gate_dims* d, float temperature, float g, const voi
                 const int64_t* tokens, const uint8_t* active, float* c_s, uint8_t* cont,
                 float* row_lse, uint8_t* flags, void* workspace, size_t ws_bytes,
                 dflash_stream_t stream) {
+  CallRange range_("dflash_gate");
   int rc = check_gate_dims(d);
   if (rc) return rc;
   if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
@@ -279,6 +299,7 @@ int dflash_gate_stage(const dflash_gate_dims* d, int32_t stage, int32_t n_max, f
                       const void* draft_logits, const int64_t* cand, const uint8_t* active, float* c_s,
                       uint8_t* cont, float* row_lse, uint8_t* flags, int32_t* n_verify, void* workspace,
                       size_t ws_bytes, dflash_stream_t stream) {
+  CallRange range_("dflash_gate_stage");
   int rc = check_gate_dims(d);
   if (rc) return rc;
   if (!(temperature > 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
@@ -325,6 +346,7 @@ int dflash_draft_select(const dflash_verify_dims* d, float temperature, const vo
                         const int64_t* anchor, const int32_t* n_draft, const float* u_draft, int64_t* cand,
                         float* q_x, float* row_lse, uint8_t* flags, void* workspace, size_t ws_bytes,
                         dflash_stream_t stream) {
+  CallRange range_("dflash_draft_select");
   int rc = check_select_dims(d);
   if (rc) return rc;
   if (!(temperature >= 0.f) || !(temperature < 3.0e38f))
@@ -339,6 +361,7 @@ int dflash_draft_select(const dflash_verify_dims* d, float temperature, const vo
   a.cand = cand; a.q_x = q_x; a.row_lse = row_lse; a.flags = flags;
   a.num_sms = kPlanSms;
   a.counters = (int32_t*)workspace;
+  a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
   a.stream = (cudaStream_t)stream;
   cudaError_t e = dflash::launch_draft_select(a);
@@ -365,6 +388,7 @@ static int check_tree_dims(const dflash_tree_dims* d) {
 
 int dflash_ddtree_topk(const dflash_tree_dims* d, float temperature, const void* draft_logits, int64_t* topk_tok,
                        float* topk_logp, dflash_stream_t stream) {
+  CallRange range_("dflash_ddtree_topk");
   int rc = check_tree_dims(d);
   if (rc) return rc;
   if (!(temperature > 0.f) || !(temperature < 3.0e38f)) return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0");
@@ -381,6 +405,7 @@ int dflash_ddtree_topk(const dflash_tree_dims* d, float temperature, const void*
 int dflash_ddtree_build(const dflash_tree_dims* d, const int64_t* topk_tok, const float* topk_logp,
                         int64_t* node_token, int32_t* node_parent, int32_t* node_depth, float* node_logp,
                         int32_t* n_nodes, uint8_t* flags, dflash_stream_t stream) {
+  CallRange range_("dflash_ddtree_build");
   int rc = check_tree_dims(d);
   if (rc) return rc;
   if (!topk_tok || !topk_logp || !node_token || !node_parent || !node_depth || !node_logp || !n_nodes)
@@ -404,6 +429,7 @@ int dflash_ddtree_verify_greedy(const dflash_tree_dims* d, const void* target_lo
                                 const int32_t* node_parent, const int32_t* n_nodes, int32_t* accept_len,
                                 int64_t* bonus, int32_t* commit_len, int32_t* path, int64_t* out_tokens,
                                 void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  CallRange range_("dflash_ddtree_verify_greedy");
   int rc = check_tree_dims(d);
   if (rc) return rc;
   if (!target_logits || !node_token || !node_parent || !n_nodes || !accept_len || !bonus || !commit_len)
@@ -452,6 +478,7 @@ int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_bl
                       const void* k_pool, const void* v_pool, const int32_t* page_table,
                       const int32_t* ctx_len, float scale, void* out, void* workspace, size_t ws_bytes,
                       dflash_stream_t stream) {
+  CallRange range_("dflash_block_attn");
   int rc = check_attn_dims(d);
   if (rc) return rc;
   if (!q || !k_pool || !v_pool || !page_table || !ctx_len || !out || (d->n_kv_blk > 0 && (!k_blk || !v_blk)))
@@ -502,6 +529,7 @@ int dflash_materialize_ctx_kv(const dflash_ctx_kv_dims* d, const void* hidden, c
                               const void* k_norm_w, float rms_eps, float rope_theta, void* const* k_pools,
                               void* const* v_pools, const int32_t* page_table, int32_t* new_len,
                               void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  CallRange range_("dflash_materialize_ctx_kv");
   int rc = check_mat_dims(d);
   if (rc) return rc;
   if (!hidden || !commit_len || !start_pos || !W_f || !W_kv || !k_pools || !v_pools || !page_table)

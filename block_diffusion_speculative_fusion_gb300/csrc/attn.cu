@@ -143,6 +143,12 @@ __device__ __forceinline__ void plan_cum_warp(const AttnParams& p, int* cum, int
     run += group_tiles(p, b);
   }
   if (lane == 31) cum[p.B] = incl;
+#ifdef DFLASH_DEBUG
+  // context lengths outside [0, max_ctx] are clamped; debug builds record them
+  if (blockIdx.x == 0)
+    for (int b = r0; b < r1; ++b)
+      if (p.ctx_len[b] < 0 || p.ctx_len[b] > p.max_ctx) record_dev_error(p.err, kDevErrBadCtxLen);
+#endif
 }
 
 __device__ __forceinline__ AttnPlan make_plan(const AttnParams& p, const int* cum) {

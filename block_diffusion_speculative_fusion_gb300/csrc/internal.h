@@ -19,6 +19,15 @@ unsigned long long wait_limit_ns();
 // Device error word code: a page-table entry outside [0, num_pages) inside a
 // context (attention reads page 0 for it).
 constexpr int kDevErrBadPage = 100;
+constexpr int kDevErrBadNDraft = 101;
+constexpr int kDevErrBadCtxLen = 102;      // recorded in DFLASH_DEBUG builds only
+constexpr int kDevErrBadCommitLen = 103;   // recorded in DFLASH_DEBUG builds only
+constexpr int kDevErrBadPosition = 104;    // recorded in DFLASH_DEBUG builds only
+
+// Record an input error in the workspace error word (the first code stays).
+__device__ __forceinline__ void record_dev_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
 
 // Opt a kernel into `bytes` of dynamic shared memory on the calling thread's
 // current device. The attribute belongs to each device's context, so it is set
@@ -71,6 +80,7 @@ struct VerifyArgs {
   uint8_t* flags;
   float* probs;
   int32_t* counters;   // zeroed region at the workspace start
+  int* err;            // the workspace's error word
   void* scratch;       // workspace after the counter region
   cudaStream_t stream;
 };
@@ -124,6 +134,7 @@ struct DraftSelectArgs {
   float* row_lse;             // [B, n_max] or null
   uint8_t* flags;             // [B, n_max] or null
   int32_t* counters;          // zeroed region at the workspace start, one per row
+  int* err;                   // the workspace's error word
   void* scratch;
   cudaStream_t stream;
   int num_sms;                // persistent grid: resident CTAs x SMs

@@ -45,7 +45,7 @@ mat_gather_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restr
                   int32_t* __restrict__ new_len, int tc, int N1, int K1, int N2, int K2,
                   const __grid_constant__ RopeFreq inv_freq, float2* __restrict__ rope, int half,
                   const int32_t* __restrict__ page_table, int page_size, int max_pages, int num_pages,
-                  long long* __restrict__ slots) {
+                  long long* __restrict__ slots, int* __restrict__ err) {
   __shared__ int scan[256];
   __shared__ int run_start[257];
   const int tid = threadIdx.x;
@@ -53,6 +53,14 @@ mat_gather_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restr
   const int b0 = tid * per, b1 = min(B, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b) local += max(0, min(commit_len[b], rows_max));
+#ifdef DFLASH_DEBUG
+  // commit lengths outside [0, rows_max] are clamped; debug builds record them
+  if (blockIdx.x == 0)
+    for (int b = b0; b < b1; ++b)
+      if (commit_len[b] < 0 || commit_len[b] > rows_max) record_dev_error(err, kDevErrBadCommitLen);
+#else
+  (void)err;
+#endif
   scan[tid] = local;
   __syncthreads();
   for (int off = 1; off < 256; off <<= 1) {
@@ -123,6 +131,10 @@ mat_gather_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restr
         if (phys >= 0 && phys < num_pages) sl = (long long)phys * page_size + pos % page_size;
       }
       slots[r] = sl;
+#ifdef DFLASH_DEBUG
+      // a committed row without a pool slot is not written; debug builds record it
+      if (sl < 0) record_dev_error(err, kDevErrBadPosition);
+#endif
     }
     // RoPE (cos, sin) of the row's position, pair i: the angle pos * theta^(-2i/D)
     // in double (it reaches ~1e4 radians), reduced to [-pi, pi] by Cody-Waite
@@ -518,7 +530,7 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   mat_gather_kernel<<<gs, 256, 0, st>>>(a.commit_len, a.start_pos, a.B, a.rows_max, (const uint8_t*)a.hidden,
                                         (uint8_t*)X, row_bytes, meta, row_b, row_j, a.new_len, p.tc ? 1 : 0, p.N1,
                                         p.K1, p.N2, p.K2, inv_freq, rope, a.D / 2, a.page_table, a.page_size,
-                                        a.max_pages, a.num_pages, slots);
+                                        a.max_pages, a.num_pages, slots, a.err);
   ++n;
   cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, 1, a.err, st);
   if (e != cudaSuccess) return e;

@@ -30,11 +30,16 @@ greedy_kernel(const T* __restrict__ logits, const int64_t* __restrict__ cand,
               VI* __restrict__ parts, int32_t* __restrict__ counters,
               int32_t* __restrict__ accept_len, int64_t* __restrict__ bonus,
               int32_t* __restrict__ commit_len, int64_t* __restrict__ out_tokens,
-              int64_t* __restrict__ target_pred) {
+              int64_t* __restrict__ target_pred, int* __restrict__ err) {
   const int c = blockIdx.x;
   const int row = blockIdx.y;
   const int b = row / R, i = row - b * R;
-  const int nb = n_draft ? n_draft[b] : R - 1;
+  // drafts of sequence b, clamped to [0, R - 1] (an out-of-range count is recorded)
+  int nb = n_draft ? n_draft[b] : R - 1;
+  if (nb < 0 || nb > R - 1) {
+    if (c == 0 && i == 0 && threadIdx.x == 0) record_dev_error(err, kDevErrBadNDraft);
+    nb = min(max(nb, 0), R - 1);
+  }
   VI best{-CUDART_INF_F, INT32_MAX};
   if (i <= nb) {
     const T* z = logits + (size_t)row * V;
@@ -364,14 +369,19 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const fl
                     float k2, MS* __restrict__ parts, float* __restrict__ zx,
                     int32_t* __restrict__ counters, SampleJob* __restrict__ jobs,
                     int32_t* __restrict__ accept_len, int32_t* __restrict__ commit_len,
-                    int64_t* __restrict__ out_tokens, float* __restrict__ probs) {
+                    int64_t* __restrict__ out_tokens, float* __restrict__ probs, int* __restrict__ err) {
   const int R = n_max + 1;
   const int RR = R + n_max;              // target rows then draft rows of a sequence
   // with the draft rows' log-sum-exps supplied, only the target rows stream
   const int RS = draft_lse ? R : RR;
   const int c = blockIdx.x;
   const int b = blockIdx.y / RS, r = blockIdx.y - b * RS;
-  const int nb = n_draft ? n_draft[b] : n_max;
+  // drafts of sequence b, clamped to [0, n_max] (an out-of-range count is recorded)
+  int nb = n_draft ? n_draft[b] : n_max;
+  if (nb < 0 || nb > n_max) {
+    if (c == 0 && r == 0 && threadIdx.x == 0) record_dev_error(err, kDevErrBadNDraft);
+    nb = min(max(nb, 0), n_max);
+  }
   const bool is_t = r < R;
   const int ri = is_t ? r : r - R;       // row index within its tensor
   const bool valid = is_t ? (ri <= nb) : (ri < nb);
@@ -574,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, kSelCtasPerSm)
 draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor, const int32_t* __restrict__ n_draft,
                     const float* __restrict__ u_draft, int B, int n_max, int V, int nch, float k2, int sampled,
                     float2* __restrict__ rec, int64_t* __restrict__ cand, float* __restrict__ q_x,
-                    float* __restrict__ row_lse, uint8_t* __restrict__ flags) {
+                    float* __restrict__ row_lse, uint8_t* __restrict__ flags, int* __restrict__ err) {
   constexpr int N = VecTraits<T>::N;
   constexpr int NV = kSelVecs;
   constexpr int SEG = NV * N;                      // contiguous tokens per thread and chunk
@@ -591,7 +601,10 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
 
   for (int row = blockIdx.x; row < B * n_max; row += gridDim.x) {
     const int b = row / n_max, i = row - b * n_max;
-    const int nb = n_draft ? min(max(n_draft[b], 0), n_max) : n_max;
+    // drafts of sequence b, clamped to [0, n_max] (an out-of-range count is recorded)
+    const int nd = n_draft ? n_draft[b] : n_max;
+    if ((nd < 0 || nd > n_max) && i == 0 && tid == 0) record_dev_error(err, kDevErrBadNDraft);
+    const int nb = min(max(nd, 0), n_max);
     const size_t crow = (size_t)b * (n_max + 1);
     if (i == 0 && tid == 0) cand[crow] = anchor[b];
     if (i >= nb) {   // position not drafted: padding
@@ -880,7 +893,7 @@ static cudaError_t launch_greedy_t(const VerifyArgs& a, int num_sms) {
   greedy_kernel<T><<<grid, kThreads, 0, a.stream>>>(
       (const T*)a.target_logits, a.cand, a.n_draft, R, a.V, p.nch, p.chunk,
       (VI*)a.scratch, a.counters, a.accept_len, a.bonus, a.commit_len, a.out_tokens,
-      a.target_pred);
+      a.target_pred, a.err);
   return cudaGetLastError();
 }
 
@@ -908,7 +921,7 @@ static cudaError_t launch_sample_t(const VerifyArgs& a, int num_sms) {
   sample_stats_kernel<T><<<g1, kThreads, 0, a.stream>>>(
       (const T*)a.target_logits, (const T*)a.draft_logits, a.draft_lse, a.cand, a.n_draft, a.u_accept,
       a.n_max, a.V, p.nch, p.chunk, k2, parts, zx, a.counters, jobs, a.accept_len, a.commit_len,
-      a.out_tokens, a.probs);
+      a.out_tokens, a.probs, a.err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   constexpr int kDrawSmem = 2 * kDrawChunk * (int)sizeof(T);   // the chunk of both rows
@@ -946,7 +959,7 @@ static cudaError_t launch_draft_select_t(const DraftSelectArgs& a) {
   const int grid = (int)std::min<long>(rows, (long)kSelCtasPerSm * a.num_sms);
   draft_select_kernel<T><<<grid, kThreads, kSelSmem, a.stream>>>(
       (const T*)a.draft_logits, a.anchor, a.n_draft, a.u_draft, a.B, a.n_max, a.V, nch, k2, sampled ? 1 : 0,
-      (float2*)a.scratch, a.cand, a.q_x, a.row_lse, a.flags);
+      (float2*)a.scratch, a.cand, a.q_x, a.row_lse, a.flags, a.err);
   return cudaGetLastError();
 }
 

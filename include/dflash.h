@@ -95,12 +95,33 @@ enum { DFLASH_FLAG_GATE_BOUNDARY = 1 };
  *                            read page 0 for that position (never out of bounds),
  *                            so that call's output is invalid. Counters stay
  *                            consistent; clear the word to reuse the workspace.
- * Calls that can set it: dflash_block_attn (any dtype) and
- * dflash_materialize_ctx_kv (bf16 tensor-core GEMMs). The verify, gate,
- * draft-select and DDTree kernels have no waits and never set it.
+ *   DFLASH_DEVERR_BAD_N_DRAFT  a verify or draft-select call met an n_draft[b]
+ *                            outside [0, n_max]; it used the value clamped to
+ *                            that range (never out of bounds), so sequence b's
+ *                            outputs are those of the clamped count.
+ * Only in a library built with DFLASH_DEBUG defined (the Python build's
+ * debug library); release builds clamp these inputs without a record:
+ *   DFLASH_DEVERR_BAD_CTX_LEN    dflash_block_attn met a ctx_len[b] outside
+ *                            [0, max_ctx] (clamped to that range).
+ *   DFLASH_DEVERR_BAD_COMMIT_LEN dflash_materialize_ctx_kv met a commit_len[b]
+ *                            outside [0, rows_max] (clamped to that range).
+ *   DFLASH_DEVERR_BAD_POSITION   dflash_materialize_ctx_kv met a committed row
+ *                            whose position has no valid pool slot (a negative
+ *                            position, a page past max_pages, or a page-table
+ *                            entry outside [0, num_pages)); the row is not
+ *                            written.
+ * Calls that can set it: dflash_block_attn, dflash_materialize_ctx_kv, the
+ * verify calls (greedy, sampled, sampled with LSEs) and
+ * dflash_draft_select. The gate and DDTree kernels never set it.
  */
 #define DFLASH_WS_ERROR_WORD_OFFSET (DFLASH_WS_COUNTER_BYTES - 4)
-enum { DFLASH_DEVERR_BAD_PAGE = 100 };
+enum {
+  DFLASH_DEVERR_BAD_PAGE = 100,
+  DFLASH_DEVERR_BAD_N_DRAFT = 101,
+  DFLASH_DEVERR_BAD_CTX_LEN = 102,
+  DFLASH_DEVERR_BAD_COMMIT_LEN = 103,
+  DFLASH_DEVERR_BAD_POSITION = 104
+};
 
 /* ------------------------------------------------------------------------- */
 /* (a) Target-context KV materialisation                                      */

@@ -203,5 +203,25 @@ def test_wait_limit_is_settable_and_zero_restores_default(L):
 def test_error_word_offset_matches_header():
     hdr = open(os.path.join(ROOT, "include", "dflash.h")).read()
     assert "#define DFLASH_WS_ERROR_WORD_OFFSET (DFLASH_WS_COUNTER_BYTES - 4)" in hdr
-    assert "DFLASH_DEVERR_BAD_PAGE = 100" in hdr
-    assert api.WS_ERROR_WORD_OFFSET == api.WS_COUNTER_BYTES - 4 and api.DEVERR_BAD_PAGE == 100
+    assert api.WS_ERROR_WORD_OFFSET == api.WS_COUNTER_BYTES - 4
+    codes = {m.group(1): int(m.group(2)) for m in re.finditer(r"DFLASH_DEVERR_([A-Z_]+) = (\d+)", hdr)}
+    assert codes == {"BAD_PAGE": 100, "BAD_N_DRAFT": 101, "BAD_CTX_LEN": 102, "BAD_COMMIT_LEN": 103,
+                     "BAD_POSITION": 104}
+    for name, value in codes.items():
+        assert getattr(api, "DEVERR_" + name) == value, name
+
+
+def test_debug_library_builds_and_exports_every_symbol(L):
+    """The DFLASH_DEBUG build of the same sources (kernels that also record
+    clamped inputs in the error word) links and exports the whole ABI."""
+    path = build.build(debug=True)
+    assert path.endswith("libdflash_debug.so") and path != api.LIB_PATH
+    D = ctypes.CDLL(path)
+    missing = [n for n in sorted(_declared_functions()) if not hasattr(D, n)]
+    assert not missing, missing
+    assert api.select_library(debug=True) == path
+    try:
+        assert api.lib().dflash_wait_limit_ns() > 0
+    finally:
+        api.select_library(debug=False)
+    assert api.LIB_PATH.endswith("libdflash.so")

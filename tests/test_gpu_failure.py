@@ -148,3 +148,135 @@ def test_attention_bad_page_entry_is_recorded(wl):
     torch.cuda.synchronize()
     assert api.device_error_word(ws) == 0
     assert torch.equal(again, ref)
+
+
+# ---------------------------------------------------------------------------
+# Inputs outside their documented range: every kernel clamps them before any
+# use (never out of bounds) and records what it met in the error word; the
+# debug library also records the inputs release builds clamp silently.
+# ---------------------------------------------------------------------------
+def _ws(size_fn, dims):
+    need = getattr(api.lib(), size_fn)(ctypes.byref(dims))
+    assert need > 0
+    return torch.zeros(need, dtype=torch.uint8, device=DEV)
+
+
+def _clamped_pair(n_draft, n_max):
+    bad = n_draft.clone()
+    bad[0] = n_max + 3
+    bad[1] = -2
+    return bad, bad.clamp(0, n_max)
+
+
+def _same(a, b, keys):
+    for k in keys:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_verify_n_draft_out_of_range_is_clamped_and_recorded():
+    vb = {k: v.to(DEV) for k, v in synth.verify_batch(W.LLAMA8B_B1, seed=5, B=6, greedy_rows=3).items()}
+    B, R, V = vb["target_logits"].shape
+    n_max = R - 1
+    bad, good = _clamped_pair(vb["n_draft"], n_max)
+    dims = api.VerifyDims(B, n_max, V, api.BF16)
+    keys = ("accept_len", "bonus", "commit_len", "out_tokens")
+    # greedy
+    ws = _ws("dflash_verify_greedy_workspace_size", dims)
+    ref = {k: v.clone() for k, v in api.verify_greedy(vb["target_logits"], vb["cand"], good, ws=ws).items()}
+    torch.cuda.synchronize()
+    assert api.device_error_word(ws) == 0
+    got = api.verify_greedy(vb["target_logits"], vb["cand"], bad, ws=ws)
+    torch.cuda.synchronize()
+    assert api.device_error_word(ws) == api.DEVERR_BAD_N_DRAFT
+    _same(got, ref, keys)
+    # sampled
+    ws = _ws("dflash_verify_sample_workspace_size", dims)
+    args = (vb["target_logits"], vb["draft_logits"], vb["cand"], vb["u_acc"], vb["u_final"], 1.0)
+    ref = {k: v.clone() for k, v in api.verify_sample(*args, n_draft=good, ws=ws).items()}
+    torch.cuda.synchronize()
+    assert api.device_error_word(ws) == 0
+    got = api.verify_sample(*args, n_draft=bad, ws=ws)
+    torch.cuda.synchronize()
+    assert api.device_error_word(ws) == api.DEVERR_BAD_N_DRAFT
+    _same(got, ref, keys + ("flags",))
+    # draft-side choice over the MASK rows
+    ws = _ws("dflash_draft_select_workspace_size", dims)
+    anchor = vb["cand"][:, 0].contiguous()
+    ref = {k: v.clone() for k, v in api.draft_select(vb["draft_logits"], anchor, 0.0, n_draft=good, ws=ws).items()}
+    torch.cuda.synchronize()
+    assert api.device_error_word(ws) == 0
+    got = api.draft_select(vb["draft_logits"], anchor, 0.0, n_draft=bad, ws=ws)
+    torch.cuda.synchronize()
+    assert api.device_error_word(ws) == api.DEVERR_BAD_N_DRAFT
+    _same(got, ref, ("cand",))
+
+
+@pytest.fixture(scope="module")
+def debug_library():
+    from block_diffusion_speculative_fusion_gb300 import build
+    path = build.build(debug=True)
+    yield path
+    api.select_library(debug=False)
+
+
+@pytest.mark.parametrize("debug", [False, True], ids=["release", "debug"])
+def test_attention_context_past_max_ctx(debug_library, debug):
+    """ctx_len above max_ctx is clamped to it; only the debug library records it."""
+    api.select_library(debug=debug)
+    try:
+        w, cache, blk, args = _attn_case([900, 2500, 300], seed=41)
+        max_ctx = cache.max_pages * w.page_size
+        b = int(torch.argmax(cache.ctx_len))          # every page of its table row is assigned
+        ws = torch.zeros(1 << 26, dtype=torch.uint8, device=DEV)
+        ok_ctx = args[6].clone()
+        ok_ctx[b] = max_ctx
+        ref = api.block_attn(*args[:6], ok_ctx, max_ctx=max_ctx, ws=ws).clone()
+        torch.cuda.synchronize()
+        assert api.device_error_word(ws) == 0
+        long_ctx = ok_ctx.clone()
+        long_ctx[b] = max_ctx + 40
+        got = api.block_attn(*args[:6], long_ctx, max_ctx=max_ctx, ws=ws)
+        torch.cuda.synchronize()
+        assert api.device_error_word(ws) == (api.DEVERR_BAD_CTX_LEN if debug else 0)
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    finally:
+        api.select_library(debug=False)
+
+
+@pytest.mark.parametrize("debug", [False, True], ids=["release", "debug"])
+def test_materialize_commit_len_and_positions_out_of_range(debug_library, debug):
+    """A commit_len above rows_max is clamped and a row without a pool slot is
+    skipped; only the debug library records them."""
+    api.select_library(debug=debug)
+    try:
+        wl, d, cache = _mat_inputs(seed=42)
+        dims = api.CtxKvDims(wl.B, wl.k, wl.m, wl.d, wl.L, wl.Hkv, wl.D, wl.page_size, cache.max_pages,
+                             cache.num_pages, api.BF16)
+        ws = torch.zeros(api.lib().dflash_materialize_workspace_size(ctypes.byref(dims)), dtype=torch.uint8,
+                         device=DEV)
+        k0 = [t.clone() for t in cache.k_pools]
+        v0 = [t.clone() for t in cache.v_pools]
+        # commit_len past rows_max: the same rows as commit_len = rows_max
+        kp, vp = [t.clone() for t in k0], [t.clone() for t in v0]
+        d["commit"][3] = wl.k
+        _mat_call(wl, d, kp, vp, ws)
+        torch.cuda.synchronize()
+        assert api.device_error_word(ws) == 0
+        ref_k = [t.clone() for t in kp]
+        kq, vq = [t.clone() for t in k0], [t.clone() for t in v0]
+        d["commit"][3] = wl.k + 5
+        _mat_call(wl, d, kq, vq, ws)
+        torch.cuda.synchronize()
+        assert api.device_error_word(ws) == (api.DEVERR_BAD_COMMIT_LEN if debug else 0)
+        for layer in range(wl.L):
+            assert torch.equal(kq[layer].view(torch.int16), ref_k[layer].view(torch.int16)), layer
+        d["commit"][3] = wl.k
+        # a negative start position: its rows have no slot and are not written
+        ws.zero_()
+        kr, vr = [t.clone() for t in k0], [t.clone() for t in v0]
+        d["start"][5] = -3
+        _mat_call(wl, d, kr, vr, ws)
+        torch.cuda.synchronize()
+        assert api.device_error_word(ws) == (api.DEVERR_BAD_POSITION if debug else 0)
+    finally:
+        api.select_library(debug=False)
