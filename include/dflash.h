@@ -271,8 +271,7 @@ int dflash_verify_greedy(const dflash_verify_dims* dims,
  *     before anything is launched (B*(n_max+1) up to about 30000 rows fit).
  *   - Set-up: the first call on a device (the device current on the calling
  *     thread) resolves the array's address with cudaGetSymbolAddress, which may
- *     load the module on that device; make that first call before any stream
- *     capture begins. Later calls only read the cached address.
+ *     load the module on that device. Later calls only read the cached address.
  *   - Zero state: the array's counter region must be zero when a call starts.
  *     Module load zeroes it and every completed call leaves it zero; nothing
  *     else writes it.
