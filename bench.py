@@ -533,9 +533,12 @@ def run_ours(args, wl):
     # ---------------- per-kernel rooflines (CUPTI device times, outside the timed region) ----------------
     roof_all = None
     if rank == 0:
-        roof_all = step_rooflines(torch, st, wl, hbm, tf)
-        from block_diffusion_speculative_fusion_gb300 import workloads as W
-        roof_all["prefill_gemms"] = prefill_roofline(torch, W.LLAMA8B_B1, tf, tf_sus)
+        if args.no_cupti:
+            roof_all = {"note": "skipped (--no-cupti)"}
+        else:
+            roof_all = step_rooflines(torch, st, wl, hbm, tf)
+            from block_diffusion_speculative_fusion_gb300 import workloads as W
+            roof_all["prefill_gemms"] = prefill_roofline(torch, W.LLAMA8B_B1, tf, tf_sus)
         # step-level verify and materialisation, from the graph's own events
         el, V, R, n = 2, wl.V, wl.n_draft + 1, wl.n_draft
         ng, ns = wl.n_greedy, wl.B - wl.n_greedy
@@ -604,7 +607,7 @@ def run_ours(args, wl):
 
     # ---------------- per-call host cost of the C ABI, measured from C ----------------
     abi_host = None
-    if rank == 0:
+    if rank == 0 and not args.no_cupti:
         abi_host = abi_host_cost()
 
     # ---------------- CPU baseline: the oracle on a bounded sample ----------------
@@ -970,6 +973,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # for runs under a profiler: skip the CUPTI passes (a second CUPTI subscriber
+    # beside ncu's) and the C host-cost child process
+    ap.add_argument("--no-cupti", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps one by one (no CUDA graph)")
     ap.add_argument("--kernel", choices=["attn", "verify", "materialize", "prefill"], default=None,
                     help="time one call of the step in isolation (profiling aid)")
