@@ -9,7 +9,9 @@
 //                         that bound, K block rounds over the collected ones
 //   ddtree_build_kernel   one warp per sequence: the candidate frontier as
 //                         64-bit order keys in shared memory, each pop a
-//                         warp-wide minimum; siblings enter lazily (a node's
+//                         warp-wide minimum (each lane loads 8 of its slots at
+//                         once, then two hardware warp reductions, high word
+//                         then low word); siblings enter lazily (a node's
 //                         next sibling is pushed when it pops), which pops the
 //                         same nodes in the same order as pushing all K
 //   ddtree_verify_kernel  argmax of every node's target row (chunks, one wave)
@@ -190,18 +192,29 @@ ddtree_build_kernel(const int64_t* __restrict__ tok, const float* __restrict__ l
   // after the loop); exact ties follow the key order and are not flagged.
   float prev = CUDART_INF_F;
   while (f > 0 && cnt < budget) {
-    // the first key in pop order, and its slot
+    // the first key in pop order, and its slot (keys are distinct); each lane
+    // loads 8 of its slots before comparing, so the loads overlap
     uint64_t bk = ~0ull;
     int bi = -1;
-    for (int j = l; j < f; j += 32) {
-      const uint64_t k = fr[j];
-      if (k < bk) { bk = k; bi = j; }
-    }
+    for (int j0 = l; j0 < f; j0 += 32 * 8) {
+      uint64_t kk[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ok < bk) { bk = ok; bi = oi; }
+      for (int u = 0; u < 8; ++u) kk[u] = j0 + 32 * u < f ? fr[j0 + 32 * u] : ~0ull;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (kk[u] < bk) { bk = kk[u]; bi = j0 + 32 * u; }
+    }
+    {
+      // warp minimum of the 64-bit keys: the high words, then the low words of
+      // the lanes holding the smallest high word; the key is distinct, so one
+      // lane holds it and passes on its slot
+      const uint32_t hi = (uint32_t)(bk >> 32), lo = (uint32_t)bk;
+      const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
+      const uint32_t mlo = __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
+      const uint64_t mk = ((uint64_t)mhi << 32) | mlo;
+      const unsigned who = __ballot_sync(0xffffffffu, bk == mk);
+      bi = __shfl_sync(0xffffffffu, bi, who ? __ffs(who) - 1 : 0);
+      bk = mk;
     }
     const float lp = key_lp(bk);
     const int depth = key_depth(bk), parent = key_parent(bk), rank = key_rank(bk);
@@ -210,20 +223,24 @@ ddtree_build_kernel(const int64_t* __restrict__ tok, const float* __restrict__ l
     const bool sib = rank + 1 < K, child = depth < n;
     __syncwarp();
     if (l == 0) {
+      // every shared-memory read first (the tables share one buffer with the
+      // frontier, so reads after a store would wait for it)
+      const uint64_t last = fr[f - 1];
+      const int64_t token = tk[(depth - 1) * K + rank];
+      const float plp = (sib && parent >= 0) ? nlp[parent] : 0.f;
+      const float lsib = sib ? lb[(depth - 1) * K + rank + 1] : 0.f;
+      const float lch = child ? lb[depth * K] : 0.f;
       const size_t o = (size_t)b * budget + cnt;
-      node_token[o] = tk[(depth - 1) * K + rank];
+      node_token[o] = token;
       node_parent[o] = parent;
       node_depth[o] = depth;
       node_logp[o] = lp;
       nlp[cnt] = lp;
       // the taken slot takes the last candidate; then the next sibling and the first child enter
-      fr[bi] = fr[f - 1];
+      fr[bi] = last;
       int nf = f - 1;
-      if (sib) {
-        const float plp = parent < 0 ? 0.f : nlp[parent];
-        fr[nf++] = cand_key(plp + lb[(depth - 1) * K + rank + 1], depth, parent, rank + 1);
-      }
-      if (child) fr[nf++] = cand_key(lp + lb[depth * K], depth + 1, cnt, 0);
+      if (sib) fr[nf++] = cand_key(plp + lsib, depth, parent, rank + 1);
+      if (child) fr[nf++] = cand_key(lp + lch, depth + 1, cnt, 0);
     }
     f = f - 1 + (sib ? 1 : 0) + (child ? 1 : 0);
     ++cnt;
@@ -232,9 +249,15 @@ ddtree_build_kernel(const int64_t* __restrict__ tok, const float* __restrict__ l
   if (f > 0 && cnt > 0) {
     // the budget ran out: the nearest distinct candidate left behind
     float v = -CUDART_INF_F;
-    for (int j = l; j < f; j += 32) {
-      const float x = key_lp(fr[j]);
-      if (x != prev) v = fmaxf(v, x);
+    for (int j0 = l; j0 < f; j0 += 32 * 8) {
+      uint64_t kk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) kk[u] = j0 + 32 * u < f ? fr[j0 + 32 * u] : 0ull;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float x = key_lp(kk[u]);
+        if (j0 + 32 * u < f && x != prev) v = fmaxf(v, x);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
