@@ -8,7 +8,7 @@ workload at the Llama-3.1-8B shape (B = 64, block 16, ragged contexts of
 512-8192 tokens in 16-token pages, vocabulary 128256), synthetic inputs.
 
 Prints one JSON line. ``--impl reference`` times the CPU oracle instead (the
-reference arm of this build), on a bounded sample of the same workload.
+reference arm), on a bounded sample of the same workload.
 Multi-GPU runs (torchrun) are independent replicas: each rank runs its own
 batch; the barrier and the max over ranks bracket the timed region.
 """
