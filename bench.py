@@ -828,8 +828,8 @@ def report_config(wl, args):
         # drafts only where every earlier gate continued; the gates chain on the device
         # (stage s's active mask is stage s-1's cont) and count the drafted tokens; one
         # sampled verify then checks the S_b * k concatenated candidates, fed the gates'
-        # row LSEs. Attention runs for every sequence at every stage (the kernel has no
-        # per-sequence mask), so the stage cost does not shrink as sequences stop. ----
+        # row LSEs. Stage s's attention computes only the sequences still drafting
+        # (dflash_block_attn_active with the previous gate's cont). ----
         n_q, k, S, n_max = wl.k, wl.n_draft, wl.stages, wl.n_max
         ctx = synth.ctx_lengths(wl, 0)
         cache = synth.paged_cache(wl, headroom=S + n_q, seed=0, layers=1, ctx_len=ctx, device=dev)
@@ -850,7 +850,7 @@ def report_config(wl, args):
                 b_ = blks[s]
                 for _ in range(wl.L):
                     api.block_attn(b_["q"], b_["k_blk"], b_["v_blk"], cache.k_pools[0], cache.v_pools[0], pt, cl,
-                                   out=attn_out[s])
+                                   out=attn_out[s], active=active)
                 api.gate_stage(vb["draft_logits"], vb["cand"], s, k, wl.temperature, wl.gate_g, active=active,
                                row_lse=row_lse, n_verify=n_verify, out=gouts[s])
                 active = gouts[s]["cont"]
@@ -863,11 +863,18 @@ def report_config(wl, args):
         out["looped_steps_per_s"] = 1e6 / us_loop
         out["looped_mean_stages"] = float(n_ver.mean().item()) / k
         out["looped_verified_tokens_per_s"] = float(vout["commit_len"].float().sum().item()) * 1e6 / us_loop
+        masks = [None] + [g_["cont"].clone() for g_ in gouts[:-1]]
         for s in range(S):
             b_ = blks[s]
             us_a = _time_calls(lambda: api.block_attn(b_["q"], b_["k_blk"], b_["v_blk"], cache.k_pools[0],
                                                       cache.v_pools[0], pt, cl, out=attn_out[s]),
                                args.steps, args.warmup)
+            if masks[s] is not None:
+                # the stage as the looped step runs it: only the sequences still drafting
+                out[f"stage{s + 1}_active_sequences"] = int(masks[s].sum().item())
+                out[f"stage{s + 1}_attn_active_us_per_layer"] = _time_calls(
+                    lambda: api.block_attn(b_["q"], b_["k_blk"], b_["v_blk"], cache.k_pools[0], cache.v_pools[0],
+                                           pt, cl, out=attn_out[s], active=masks[s]), args.steps, args.warmup)
             us_g = _time_calls(lambda: api.gate_stage(vb["draft_logits"], vb["cand"], s, k, wl.temperature,
                                                       wl.gate_g, out=gouts[s]), args.steps, args.warmup)
             out[f"stage{s + 1}_attn_us_per_layer"] = us_a

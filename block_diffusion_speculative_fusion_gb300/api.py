@@ -95,6 +95,8 @@ _SIGS = {
     "dflash_block_attn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnDims)]),
     "dflash_block_attn": (ctypes.c_int, [ctypes.POINTER(AttnDims), c_p, c_p, c_p, c_p, c_p, c_p, c_p,
                                          ctypes.c_float, c_p, c_p, ctypes.c_size_t, c_p]),
+    "dflash_block_attn_active": (ctypes.c_int, [ctypes.POINTER(AttnDims), c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p,
+                                                ctypes.c_float, c_p, c_p, ctypes.c_size_t, c_p]),
     "dflash_materialize_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(CtxKvDims)]),
     "dflash_materialize_ctx_kv": (ctypes.c_int, [ctypes.POINTER(CtxKvDims), c_p, c_p, c_p, c_p, c_p,
                                                  c_p, c_p, ctypes.c_float, ctypes.c_float, c_p, c_p,
@@ -494,13 +496,15 @@ def block_attn(q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor, k_pool
                v_pool: torch.Tensor, page_table: torch.Tensor, ctx_len: torch.Tensor,
                max_ctx: Optional[int] = None, scale: Optional[float] = None,
                out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
-               causal: bool = False) -> torch.Tensor:
+               causal: bool = False, active: Optional[torch.Tensor] = None) -> torch.Tensor:
     """GQA attention of the draft block over [paged context ; block]
     (``dflash_block_attn``): unmasked, or with ``causal`` the in-block causal
     variant (query i sees the context and block rows j <= i + n_kv - n_q).
     q [B, n_q, Hq, D]; k_blk, v_blk [B, n_kv, Hkv, D]; pools [num_pages, page,
     Hkv, D]; page_table [B, max_pages] int32; ctx_len [B] int32. ``max_ctx``
-    bounds every ctx_len (defaults to the page table's capacity)."""
+    bounds every ctx_len (defaults to the page table's capacity). With
+    ``active`` [B] uint8 (``dflash_block_attn_active``) only the sequences with
+    active[b] != 0 are computed; the other rows of ``out`` are left as they were."""
     _dev(q, "q")
     B, n_q, Hq, D = q.shape
     n_kv, Hkv = k_blk.shape[1], k_blk.shape[2]
@@ -519,13 +523,17 @@ def block_attn(q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor, k_pool
     if need == 0:
         raise DflashError(ERR_INVALID_ARG, last_error())
     w = ws if ws is not None else workspace(q.device, need, slot=1)
-    rc = lib().dflash_block_attn(
-        ctypes.byref(dims), _dev(q, "q"), _dev(k_blk, "k_blk", None, (B, n_kv, Hkv, D)),
-        _dev(v_blk, "v_blk", None, (B, n_kv, Hkv, D)), _dev(k_pool, "k_pool", None, (num_pages, page, Hkv, D)),
-        _dev(v_pool, "v_pool", None, (num_pages, page, Hkv, D)),
-        _dev(page_table, "page_table", torch.int32, (B, max_pages)), _dev(ctx_len, "ctx_len", torch.int32, (B,)),
-        ctypes.c_float(scale if scale is not None else D ** -0.5), _dev(out, "out", q.dtype, q.shape),
-        w.data_ptr(), w.numel(), _stream(q.device))
+    args = [ctypes.byref(dims), _dev(q, "q"), _dev(k_blk, "k_blk", None, (B, n_kv, Hkv, D)),
+            _dev(v_blk, "v_blk", None, (B, n_kv, Hkv, D)), _dev(k_pool, "k_pool", None, (num_pages, page, Hkv, D)),
+            _dev(v_pool, "v_pool", None, (num_pages, page, Hkv, D)),
+            _dev(page_table, "page_table", torch.int32, (B, max_pages)),
+            _dev(ctx_len, "ctx_len", torch.int32, (B,))]
+    tail = [ctypes.c_float(scale if scale is not None else D ** -0.5), _dev(out, "out", q.dtype, q.shape),
+            w.data_ptr(), w.numel(), _stream(q.device)]
+    if active is None:
+        rc = lib().dflash_block_attn(*args, *tail)
+    else:
+        rc = lib().dflash_block_attn_active(*args, _dev(active, "active", torch.uint8, (B,)), *tail)
     _check(rc)
     return out
 

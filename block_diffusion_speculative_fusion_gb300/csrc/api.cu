@@ -474,11 +474,14 @@ size_t dflash_block_attn_workspace_size(const dflash_attn_dims* d) {
          dflash::attn_ws_bytes(d->B, d->n_q, d->n_kv_blk, d->Hq, d->Hkv, d->D, d->max_ctx, d->page_size, d->dtype);
 }
 
-int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_blk, const void* v_blk,
-                      const void* k_pool, const void* v_pool, const int32_t* page_table,
-                      const int32_t* ctx_len, float scale, void* out, void* workspace, size_t ws_bytes,
-                      dflash_stream_t stream) {
-  CallRange range_("dflash_block_attn");
+}  // extern "C"
+
+namespace {
+
+int block_attn_call(const dflash_attn_dims* d, const void* q, const void* k_blk, const void* v_blk,
+                    const void* k_pool, const void* v_pool, const int32_t* page_table, const int32_t* ctx_len,
+                    const uint8_t* active, float scale, void* out, void* workspace, size_t ws_bytes,
+                    dflash_stream_t stream) {
   int rc = check_attn_dims(d);
   if (rc) return rc;
   if (!q || !k_pool || !v_pool || !page_table || !ctx_len || !out || (d->n_kv_blk > 0 && (!k_blk || !v_blk)))
@@ -490,7 +493,7 @@ int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_bl
   a.page_size = d->page_size; a.max_pages = d->max_pages; a.num_pages = d->num_pages;
   a.max_ctx = d->max_ctx; a.dtype = d->dtype; a.causal = d->causal;
   a.q = q; a.k_blk = k_blk; a.v_blk = v_blk; a.k_pool = k_pool; a.v_pool = v_pool;
-  a.page_table = page_table; a.ctx_len = ctx_len; a.scale = scale; a.out = out;
+  a.page_table = page_table; a.ctx_len = ctx_len; a.active = active; a.scale = scale; a.out = out;
   a.counters = (int32_t*)workspace;
   a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
@@ -499,6 +502,28 @@ int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_bl
   cudaError_t e = dflash::launch_block_attn(a, &launches);
   if (e != cudaSuccess) return cuda_fail(e, "block_attn launch");
   return ok(launches);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dflash_block_attn(const dflash_attn_dims* d, const void* q, const void* k_blk, const void* v_blk,
+                      const void* k_pool, const void* v_pool, const int32_t* page_table,
+                      const int32_t* ctx_len, float scale, void* out, void* workspace, size_t ws_bytes,
+                      dflash_stream_t stream) {
+  CallRange range_("dflash_block_attn");
+  return block_attn_call(d, q, k_blk, v_blk, k_pool, v_pool, page_table, ctx_len, nullptr, scale, out, workspace,
+                         ws_bytes, stream);
+}
+
+int dflash_block_attn_active(const dflash_attn_dims* d, const void* q, const void* k_blk, const void* v_blk,
+                             const void* k_pool, const void* v_pool, const int32_t* page_table,
+                             const int32_t* ctx_len, const uint8_t* active, float scale, void* out,
+                             void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  CallRange range_("dflash_block_attn_active");
+  return block_attn_call(d, q, k_blk, v_blk, k_pool, v_pool, page_table, ctx_len, active, scale, out, workspace,
+                         ws_bytes, stream);
 }
 
 // ------------------------------------------------------------- materialise ---

@@ -35,6 +35,7 @@ struct AttnParams {
   const bf16* v_blk;
   const int32_t* page_table;
   const int32_t* ctx_len;
+  const uint8_t* active;   // [B] or null: sequences with 0 take no tiles
   bf16* out;
   float* part_o;     // [B * Hkv * max_splits][M][128]  (max_splits for the smallest split)
   float2* part_ml;   // [B * Hkv * max_splits][M]  (max in log2 units, sum)
@@ -118,6 +119,7 @@ __device__ __forceinline__ int ctx_tiles(const AttnParams& p, int b) {
 }
 
 __device__ __forceinline__ int group_tiles(const AttnParams& p, int b) {
+  if (p.active && !p.active[b]) return 0;   // an inactive sequence takes no tiles
   return ctx_tiles(p, b) + (p.n_kv > 0 ? 1 : 0);
 }
 
@@ -903,14 +905,16 @@ __global__ void __launch_bounds__(128)
 attn_generic_kernel(const T* __restrict__ q, const T* __restrict__ k_blk, const T* __restrict__ v_blk,
                     const T* __restrict__ k_pool, const T* __restrict__ v_pool,
                     const int32_t* __restrict__ page_table, const int32_t* __restrict__ ctx_len,
-                    T* __restrict__ out, int n_q, int n_kv, int Hq, int Hkv, int D, int page_size,
-                    int max_pages, int num_pages, float scale, int causal, int* __restrict__ err) {
+                    const uint8_t* __restrict__ active, T* __restrict__ out, int n_q, int n_kv, int Hq,
+                    int Hkv, int D, int page_size, int max_pages, int num_pages, float scale, int causal,
+                    int* __restrict__ err) {
   constexpr int KC = 128;   // keys per chunk (one per thread)
   __shared__ float qs[256];
   __shared__ float ps[KC];
   __shared__ int rowidx[KC];
   __shared__ float red[4];
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (active && !active[b]) return;   // an inactive sequence: nothing read or written
   const int g = h / (Hq / Hkv);
   const int tid = threadIdx.x;
   const int C = max(0, ctx_len[b]);
@@ -1037,12 +1041,12 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
     if (a.dtype == 0)
       attn_generic_kernel<float><<<grid, 128, 0, a.stream>>>(
           (const float*)a.q, (const float*)a.k_blk, (const float*)a.v_blk, (const float*)a.k_pool,
-          (const float*)a.v_pool, a.page_table, a.ctx_len, (float*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
+          (const float*)a.v_pool, a.page_table, a.ctx_len, a.active, (float*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
           a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal, a.err);
     else
       attn_generic_kernel<bf16><<<grid, 128, 0, a.stream>>>(
           (const bf16*)a.q, (const bf16*)a.k_blk, (const bf16*)a.v_blk, (const bf16*)a.k_pool,
-          (const bf16*)a.v_pool, a.page_table, a.ctx_len, (bf16*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
+          (const bf16*)a.v_pool, a.page_table, a.ctx_len, a.active, (bf16*)a.out, a.n_q, a.n_kv, a.Hq, a.Hkv,
           a.D, a.page_size, a.max_pages, a.num_pages, a.scale, a.causal, a.err);
     return cudaGetLastError();
   }
@@ -1053,6 +1057,7 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   p.v_blk = (const bf16*)a.v_blk;
   p.page_table = a.page_table;
   p.ctx_len = a.ctx_len;
+  p.active = a.active;
   p.out = (bf16*)a.out;
   p.B = a.B; p.n_q = a.n_q; p.n_kv = a.n_kv; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = a.Hq / a.Hkv;
   p.causal = a.causal;

@@ -185,6 +185,7 @@ struct AttnArgs {
   const void* v_pool;
   const int32_t* page_table;
   const int32_t* ctx_len;
+  const uint8_t* active;   // [B] or null: sequences with 0 are skipped
   float scale;
   void* out;
   int32_t* counters;

@@ -224,6 +224,27 @@ int dflash_block_attn(const dflash_attn_dims* dims,
                       const int32_t* page_table, const int32_t* ctx_len, float scale,
                       void* out, void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
+/*
+ * dflash_block_attn for the sequences whose active[b] != 0 only. The looped
+ * draft of [DLoop] 机制一 stops drafting a sequence once its stage gate fails
+ * (c_s < g): later stages attend only for the sequences still going, and the
+ * gate's cont output (dflash_gate, dflash_gate_stage) is this mask.
+ * active [B] uint8 (device), or NULL: every sequence, exactly as
+ * dflash_block_attn. The rows out[b] of an inactive sequence are not written;
+ * its ctx_len[b] and page-table row are not read. The work of the call shrinks
+ * with the active sequences (they alone are divided among the SMs); the bf16
+ * kernel's partition of the work, and so the rounding of its split merges,
+ * then depends on the mask as well: active rows may differ in the last bits
+ * from dflash_block_attn's, and repeat bit for bit for the same mask.
+ * Workspace: dflash_block_attn_workspace_size(dims).
+ */
+int dflash_block_attn_active(const dflash_attn_dims* dims,
+                             const void* q, const void* k_blk, const void* v_blk,
+                             const void* k_pool, const void* v_pool,
+                             const int32_t* page_table, const int32_t* ctx_len, const uint8_t* active,
+                             float scale, void* out, void* workspace, size_t ws_bytes,
+                             dflash_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* (c) Verify                                                                 */
 /* ------------------------------------------------------------------------- */

@@ -212,3 +212,39 @@ def test_attn_needles_split_boundaries(ctx):
     blk = synth.block_qkv(wl, 0, seed=15)
     synth.plant_needles(wl, blk, cache, seed=15)
     _run(wl, cache, blk, 2e-2)
+
+
+@pytest.mark.parametrize("wl,ctx", [(W.LLAMA8B_B64, [3000, 700, 5200, 1200, 64, 2500]),
+                                    (W.TINY_F32, [40, 77, 20, 64])], ids=["bf16_tensor_core", "f32_generic"])
+def test_active_mask_computes_only_active_sequences(wl, ctx):
+    """dflash_block_attn_active (the DLoop looped draft: later stages attend
+    only for the sequences whose gates continued): the active sequences' rows
+    match the unmasked call (bit for bit on the fp32 path, whose blocks are
+    independent; within 2e-2 on the bf16 kernel, whose static partition of the
+    work then covers the active sequences only, so split merges round
+    differently) and repeat bit for bit, and inactive rows are left as they
+    were."""
+    w, cache, blk = _case(wl, ctx, seed=17)
+    args = [blk["q"].to(DEV), blk["k_blk"].to(DEV), blk["v_blk"].to(DEV), cache.k_pools[0].to(DEV),
+            cache.v_pools[0].to(DEV), cache.page_table.to(DEV), cache.ctx_len.to(DEV)]
+    full = api.block_attn(*args).clone()
+    active = torch.tensor([1, 0, 1, 0, 1, 0][:len(ctx)], dtype=torch.uint8, device=DEV)
+    out = torch.full_like(full, 7.0)
+    api.block_attn(*args, out=out, active=active)
+    torch.cuda.synchronize()
+    on = active.bool()
+    if out.dtype == torch.bfloat16:
+        assert float((out[on].float() - full[on].float()).abs().max()) < 2e-2
+        again = torch.full_like(full, 7.0)
+        api.block_attn(*args, out=again, active=active)
+        assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+    else:
+        assert torch.equal(out[on], full[on])
+    assert bool((out[~on] == 7.0).all())
+    # no sequence active: nothing written; all active: the unmasked call
+    none = torch.full_like(full, 7.0)
+    api.block_attn(*args, out=none, active=torch.zeros_like(active))
+    torch.cuda.synchronize()
+    assert bool((none == 7.0).all())
+    every = api.block_attn(*args, active=torch.ones_like(active))
+    assert torch.equal(every, full)
