@@ -567,16 +567,17 @@ gate_kernel(const T* __restrict__ z, const int64_t* __restrict__ tokens,
 // ===========================================================================
 // Draft-side token choice over the MASK rows (DFlash page, inference steps:
 // each MASK position's logits give a draft token, argmax or one sample per
-// position). One CTA per row (persistent over rows): the row streams through
-// two shared-memory stage buffers in chunks of 256 segments of kSelVecs
-// 16-byte vectors; each thread keeps its segment's record (max * k2, sum of
-// 2^(z k2 - max k2)) and the running (max, lowest index). A sampled row then
-// takes one block scan over the records in token order and one warp walk over
-// the chosen segment (inverse CDF, ascending token order).
+// position). One CTA per row (persistent over rows): the row goes in chunks of
+// 256 segments of kSelVecs 16-byte vectors, each thread loading its own
+// contiguous segment straight from global memory (a warp's lines are used
+// whole over its 8 loads; no staging, no block barrier while streaming); each
+// thread keeps its segment's record (max * k2, sum of 2^(z k2 - max k2)) and
+// the running (max, lowest index). A sampled row then takes one block scan
+// over the records in token order and one warp walk over the chosen segment
+// (inverse CDF, ascending token order).
 // ===========================================================================
 constexpr int kSelVecs = 8;                      // 16-byte vectors per thread and chunk
-constexpr int kSelCtasPerSm = 3;                 // resident CTAs per SM (two 32 KB stage buffers each)
-constexpr int kSelSmem = 2 * kThreads * kSelVecs * 16;
+constexpr int kSelCtasPerSm = 4;                 // resident CTAs per SM
 
 
 template <typename T>
@@ -591,7 +592,6 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
   constexpr int CHUNK = kThreads * SEG;            // tokens per chunk
   constexpr int TPL = SEG / 32;                    // tokens per lane in the segment walk
   const bool need_sum = sampled || row_lse != nullptr;   // argmax alone needs no exponentials
-  extern __shared__ __align__(16) uint4 sel_smem[];
   const int tid = threadIdx.x, wid = tid >> 5, l = tid & 31;
   __shared__ double s_wsum[kThreads / 32];
   __shared__ double s_Z, s_cbefore;
@@ -619,37 +619,23 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
     const T* zr = z + (size_t)row * V;
     float2* rr = rec + (size_t)row * nch * kThreads;
     const bool aligned = (reinterpret_cast<uintptr_t>(zr) & 15u) == 0;
-    // vector j of chunk c lands at stage[j] (coalesced copies)
-    auto issue = [&](int c, uint4* stage) {
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        const int j = k * kThreads + tid;
-        const int e = c * CHUNK + j * N;
-        if (aligned && e + N <= V) cp_async16(&stage[j], zr + e);
-        else stage[j] = load_vec_or_pad<T>(zr, e, V);    // -inf past V
-      }
-      cp_async_commit();
-    };
+    // each thread loads its own contiguous segment of every chunk straight
+    // from global memory (its 8 vectors in a rotated order; the lines a warp
+    // touches are used whole over those loads), no staging and no block barrier
+    const uint4* zv = reinterpret_cast<const uint4*>(zr);
     VI best{-CUDART_INF_F, INT32_MAX};
-    issue(0, sel_smem);
     for (int c = 0; c < nch; ++c) {
-      uint4* stage = sel_smem + (c & 1) * (kThreads * NV);
-      if (c + 1 < nch) {
-        issue(c + 1, sel_smem + ((c + 1) & 1) * (kThreads * NV));
-        cp_async_wait_one();
-      } else {
-        cp_async_wait_all();
-      }
-      __syncthreads();
-      // this thread's contiguous segment, its vectors in a rotated order so that
-      // a quarter warp reads distinct banks
       const int e0 = c * CHUNK + tid * SEG;
       uint4 vv[NV];
       float vmax[NV];
       float tmax = -CUDART_INF_F;
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
-        vv[k] = stage[tid * NV + ((k + tid) & (NV - 1))];
+        const int e = e0 + ((k + tid) & (NV - 1)) * N;
+        vv[k] = (aligned && e + N <= V) ? __ldg(zv + e / N) : load_vec_or_pad<T>(zr, e, V);
+      }
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
         vmax[k] = vec_max<T>(vv[k]);
         tmax = fmaxf(tmax, vmax[k]);
       }
@@ -685,7 +671,6 @@ draft_select_kernel(const T* __restrict__ z, const int64_t* __restrict__ anchor,
         }
         rr[c * kThreads + tid] = make_float2(mt, st);
       }
-      __syncthreads();   // stage c is refilled by chunk c + 2
     }
     // ---- the row's max and its lowest index ----
     const VI rb = block_vi(best);
@@ -953,11 +938,8 @@ static cudaError_t launch_draft_select_t(const DraftSelectArgs& a) {
   const long rows = (long)a.B * a.n_max;
   const bool sampled = a.temperature > 0.f;
   const float k2 = kLog2e / (sampled ? a.temperature : 1.f);
-  static SmemOptIn opt_in;
-  cudaError_t e = opt_in.ensure(draft_select_kernel<T>, kSelSmem);
-  if (e != cudaSuccess) return e;
   const int grid = (int)std::min<long>(rows, (long)kSelCtasPerSm * a.num_sms);
-  draft_select_kernel<T><<<grid, kThreads, kSelSmem, a.stream>>>(
+  draft_select_kernel<T><<<grid, kThreads, 0, a.stream>>>(
       (const T*)a.draft_logits, a.anchor, a.n_draft, a.u_draft, a.B, a.n_max, a.V, nch, k2, sampled ? 1 : 0,
       (float2*)a.scratch, a.cand, a.q_x, a.row_lse, a.flags, a.err);
   return cudaGetLastError();
