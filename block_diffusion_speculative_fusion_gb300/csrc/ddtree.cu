@@ -78,14 +78,39 @@ ddtree_topk_kernel(const T* __restrict__ z, int rows, int V, int K, float k2, in
       s_cnt = 0;
     }
     __syncthreads();
-    // t0: the K-th largest thread max (rank by value, then thread)
-    {
-      int rank = 0;
-      for (int j = 0; j < kThreads; ++j) {
-        const float o = s_max[j];
-        rank += (o > zmax || (o == zmax && j < (int)threadIdx.x)) ? 1 : 0;
+    // t0: the K-th largest thread max in (value desc, thread asc) order. Warp 0
+    // holds the 256 maxima (lane l: threads l, l + 32, ...) and takes the best
+    // one K times; a taken entry becomes (-inf, INT_MAX), behind every other.
+    if (threadIdx.x < 32) {
+      const int l = threadIdx.x;
+      float mv[kThreads / 32];
+      int mj[kThreads / 32];
+#pragma unroll
+      for (int u = 0; u < kThreads / 32; ++u) {
+        mv[u] = s_max[l + 32 * u];
+        mj[u] = l + 32 * u;
       }
-      if (rank == K - 1) s_t0 = zmax;
+      float t = -CUDART_INF_F;
+      for (int r = 0; r < K; ++r) {
+        float bv = -CUDART_INF_F;
+        int bj = INT32_MAX;
+#pragma unroll
+        for (int u = 0; u < kThreads / 32; ++u)
+          if (mv[u] > bv || (mv[u] == bv && mj[u] < bj)) { bv = mv[u]; bj = mj[u]; }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+          if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        }
+        t = bv;
+        if (bj != INT32_MAX && (bj & 31) == l) {
+#pragma unroll
+          for (int u = 0; u < kThreads / 32; ++u)
+            if (mj[u] == bj) { mv[u] = -CUDART_INF_F; mj[u] = INT32_MAX; }
+        }
+      }
+      if (l == 0) s_t0 = t;
     }
     __syncthreads();
     const float t0 = s_t0;
@@ -108,6 +133,26 @@ ddtree_topk_kernel(const T* __restrict__ z, int rows, int V, int K, float k2, in
     for_range<T, 8>(zr, 0, V, col_vec, col_one);
     __syncthreads();
     const int cnt = s_cnt;
+    if (cnt <= kThreads) {
+      // ---- the K best at once: each candidate's rank in (value desc, index asc)
+      // order (indices are distinct), rank r < K written to slot r ----
+      if ((int)threadIdx.x < cnt) {
+        const float v = c_v[threadIdx.x];
+        const int e = c_i[threadIdx.x];
+        int rank = 0;
+        for (int j = 0; j < cnt; ++j) rank += tk_better(c_v[j], c_i[j], v, e) ? 1 : 0;
+        if (rank < K) {
+          tok[(size_t)row * K + rank] = e;
+          logp[(size_t)row * K + rank] = (v * k2 - s_lse2) * 0.6931471805599453f;
+        }
+      }
+      for (int r = cnt + (int)threadIdx.x; r < K; r += kThreads) {   // fewer candidates than K
+        tok[(size_t)row * K + r] = -1;
+        logp[(size_t)row * K + r] = -CUDART_INF_F;
+      }
+      __syncthreads();
+      continue;
+    }
     // ---- the K best: K rounds of a block-wide (value desc, index asc) maximum ----
     for (int r = 0; r < K; ++r) {
       VI best{-CUDART_INF_F, INT32_MAX};
