@@ -460,7 +460,6 @@ static int check_attn_dims(const dflash_attn_dims* d) {
   if ((long)d->max_ctx > (long)d->max_pages * d->page_size)
     return fail(DFLASH_ERR_INVALID_ARG, "max_ctx=%d exceeds max_pages*page_size", d->max_ctx);
   if (d->D > 256) return fail(DFLASH_ERR_UNSUPPORTED, "D=%d > 256", d->D);
-  if ((long)d->B * d->Hkv > kMaxCounters - 2) return fail(DFLASH_ERR_UNSUPPORTED, "B*Hkv too large");
   if (d->n_q > 65535 || d->Hq > 65535 || d->B > 65535) return fail(DFLASH_ERR_UNSUPPORTED, "grid too large");
   if (d->causal != 0 && d->causal != 1) return fail(DFLASH_ERR_INVALID_ARG, "causal=%d is not 0 or 1", d->causal);
   if (d->causal && d->n_kv_blk < d->n_q)
@@ -494,7 +493,6 @@ int block_attn_call(const dflash_attn_dims* d, const void* q, const void* k_blk,
   a.max_ctx = d->max_ctx; a.dtype = d->dtype; a.causal = d->causal;
   a.q = q; a.k_blk = k_blk; a.v_blk = v_blk; a.k_pool = k_pool; a.v_pool = v_pool;
   a.page_table = page_table; a.ctx_len = ctx_len; a.active = active; a.scale = scale; a.out = out;
-  a.counters = (int32_t*)workspace;
   a.err = (int*)workspace + kMaxCounters;
   a.scratch = (char*)workspace + DFLASH_WS_COUNTER_BYTES;
   a.stream = (cudaStream_t)stream;

@@ -9,7 +9,10 @@
 // tcgen05 kernel (below). The n_q * (Hq/Hkv) query rows that share a kv head
 // are packed into the MMA's M dimension (GQA packing), so each K/V byte is read
 // from HBM once per kv head. Context pages arrive by TMA into a ring of 64-row
-// stages; Q, S, P and O live in TMEM; the online softmax runs in fp32.
+// stages; Q, S, P and O live in TMEM; the online softmax runs in fp32. A
+// context split over several CTAs leaves fp32 partials that a small second
+// kernel merges; it is launched as a programmatic dependent of the first, so
+// its launch overlaps the first kernel's tail.
 //
 // Generic path (fp32, or shapes outside the bf16 kernel): one CTA per query
 // row with fp32 CUDA-core arithmetic; used for the tiny fp32 configuration.
@@ -39,7 +42,7 @@ struct AttnParams {
   bf16* out;
   float* part_o;     // [B * Hkv * max_splits][M][128]  (max_splits for the smallest split)
   float2* part_ml;   // [B * Hkv * max_splits][M]  (max in log2 units, sum)
-  int32_t* counters; // [B * Hkv]
+  int32_t* plan_ws;  // [B + 2]: the partition's range size, then cum[0..B] (read by the merge kernel)
   int* err;
   int B, n_q, n_kv, Hq, Hkv, G, M, page_size, max_pages, num_pages, max_splits, max_ctx;
   int causal;        // 1: query i sees block rows j <= i + n_kv - n_q
@@ -108,7 +111,9 @@ constexpr int kBarBytes = (2 * kMaxStages + 33) * 8 + 2 * 32 + (kMaxSeqs + 1) * 
 // work of one CTA, at least 16 tiles, at most what one page-table window
 // holds), and CTA c takes ranges c, c + grid, ... A piece is the part of one
 // range that falls in one (b, g); a (b, g) cut by range borders is computed
-// in pieces whose partial results the piece that finishes last merges.
+// in pieces whose fp32 partial results a second kernel (attn_merge_kernel)
+// merges once the grid has finished.
+
 struct AttnItem {
   int b, g, split, nsplit, t0, C, n_tiles_ctx, n_tiles;   // b < 0: no more pieces
 };
@@ -257,8 +262,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint64_t* mma_done = s_full + 20;
   uint64_t* xbar = s_full + 21;           // [4 quarters][2]: the two softmax warps of a quarter
   uint64_t* l_full = s_full + 29;         // [2]  softmax -> epilogue: row max and sums of the item
-  uint64_t* mg_in = s_full + 31;          // epilogue warps -> ticket taker: split partials published
-  uint64_t* mg_out = s_full + 32;         // ticket taker -> epilogue warps: last_sm holds the ticket
+  // (s_full + 31, + 32: spare)
   AttnItem* ring = reinterpret_cast<AttnItem*>(s_full + 33);  // [2] pieces in flight (b < 0: none left)
   int* cum = reinterpret_cast<int*>(ring + 2);                // [B + 1] tiles per group before sequence b
   int* pt_s = cum + (kMaxSeqs + 1);                           // [2][kPtMax] page rows of two pieces
@@ -267,7 +271,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(ml_s + 2 * 4 * 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sm + 1);
   int* consumed_sm = reinterpret_cast<int*>(tmem_base_sm + 2);
-  volatile int* last_sm = reinterpret_cast<volatile int*>(tmem_base_sm + 4);   // epilogue: merge this item
 
   if (tid == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
@@ -289,13 +292,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     mbar_init(mma_done, 1);
     for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 2);
-    mbar_init(mg_in, W);
-    mbar_init(mg_out, 1);
     *abort_flag = 0;
     *consumed_sm = 0;
     fence_barrier_init();
   }
   if (warp == mma_warp) tmem_alloc(tmem_base_sm, kTmemCols);
+  // the merge kernel that follows may be scheduled once every CTA has got here;
+  // it waits for this grid to complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;");
   // ---- work list: the tiles per group of every sequence, prefix-summed ----
   if (warp == 0) plan_cum_warp(p, cum, lane);
   tc_fence_before();
@@ -303,6 +307,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_sm;
   const AttnPlan plan = make_plan(p, cum);
+  if (blockIdx.x == 0 && warp == 0) {
+    for (int b = lane; b <= p.B; b += 32) p.plan_ws[1 + b] = cum[b];
+    if (lane == 0) p.plan_ws[0] = plan.share;
+  }
   int producer_issued = 0;
 
   if (warp == prod_warp) {
@@ -310,6 +318,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // The next item's page rows are fetched while the current item's last tiles
     // stream, so that item boundaries leave no gap in the K/V stream.
     const int ps = p.page_size;
+    const uint64_t pol_kv = l2_policy_evict_first();   // every page row is read once
     int item_seq = 0, tile_seq = 0;
     bool ok = true;
     // page rows of item `item` into table `tb` (whole warp). Every lane issues
@@ -382,8 +391,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const int row = pt[key0 / ps - lp0] + key0 % ps;
               const int off = jb * HPI * br * 128;
               for (int h = 0; h < 2; ++h) {
-                tma_load_3d(ks + h * (kTileBytes / 2) + off, &kmap, &kv_full[st], h * 64, it.g * HPI, row);
-                tma_load_3d(vs + h * (kTileBytes / 2) + off, &vmap, &kv_full[st], h * 64, it.g * HPI, row);
+                tma_load_3d_hint(ks + h * (kTileBytes / 2) + off, &kmap, &kv_full[st], h * 64, it.g * HPI, row, pol_kv);
+                tma_load_3d_hint(vs + h * (kTileBytes / 2) + off, &vmap, &kv_full[st], h * 64, it.g * HPI, row, pol_kv);
               }
             }
             ++producer_issued;
@@ -733,7 +742,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (lane == 0) mbar_arrive(&q_full[0]);
       return true;
     };
-    int item_seq = 0, n_merge = 0;
+    int item_seq = 0;
     AttnItem it_cur, it_nxt;
     int st_cur = read_item(0, it_cur);
     bool qok = st_cur == 0 ? put_q(it_cur, 0) : false;
@@ -812,72 +821,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[oi]);
-      if (!single) {
-        // Completion ticket of the (sequence, group): the CTA whose split
-        // finishes last merges every split's partial (still in L2) into the
-        // output. Partials are published (fence) before the ticket is taken.
-        // The epilogue warps meet on two mbarriers with bounded waits (not a
-        // bar.sync), so that a warp that gave up a wait strands no other.
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(mg_in);
-        const uint32_t mpar = (uint32_t)(n_merge & 1);
-        ++n_merge;
-        const size_t grp = (size_t)it.b * p.n_groups + it.g;
-        if (quarter == 0) {
-          if (!__all_sync(0xffffffffu, wait_or_abort(mg_in, mpar, abort_flag, p.err, 41, p.wait_ns))) break;
-          if (lane == 0) {
-            const int prev = atomicAdd(&p.counters[grp], 1);
-            const int last = prev == it.nsplit - 1;
-            if (last) p.counters[grp] = 0;   // every split has arrived: ready for the next launch
-            *last_sm = last;
-            mbar_arrive(mg_out);             // release: publishes last_sm
-          }
-        }
-        if (!__all_sync(0xffffffffu, wait_or_abort(mg_out, mpar, abort_flag, p.err, 42, p.wait_ns))) break;
-        if (*last_sm && r < p.Mi) {
-          __threadfence();
-          const float2* ml = p.part_ml + grp * p.max_splits * p.Mi + r;
-          float mx = -CUDART_INF_F;
-          for (int sp = 0; sp < it.nsplit; ++sp) mx = fmaxf(mx, __ldcg(ml + (size_t)sp * p.Mi).x);
-          float L = 0.f;
-          for (int sp = 0; sp < it.nsplit; ++sp) {
-            const float2 v = __ldcg(ml + (size_t)sp * p.Mi);
-            L += v.x == -CUDART_INF_F ? 0.f : v.y * exp2f(v.x - mx);
-          }
-          const float inv_l = L > 0.f ? 1.f / L : 0.f;
-          const int i = r / p.Gi, hh = r - i * p.Gi;
-          bf16* dst = p.out + ((size_t)(it.b * p.n_q + i) * p.Hq + it.g * p.Gi + hh) * attn::kD;
-          for (int c = 0; c < attn::kD; c += 32) {
-            float acc[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
-            for (int sp = 0; sp < it.nsplit; ++sp) {
-              const float2 v = __ldcg(ml + (size_t)sp * p.Mi);
-              const float w = v.x == -CUDART_INF_F ? 0.f : exp2f(v.x - mx) * inv_l;
-              const float4* src =
-                  reinterpret_cast<const float4*>(p.part_o + ((grp * p.max_splits + sp) * p.Mi + r) * attn::kD + c);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 x = __ldcg(src + q);
-                acc[4 * q + 0] += w * x.x;
-                acc[4 * q + 1] += w * x.y;
-                acc[4 * q + 2] += w * x.z;
-                acc[4 * q + 3] += w * x.w;
-              }
-            }
-#pragma unroll
-            for (int q = 0; q < 32; q += 8) {
-              uint4 v;
-              v.x = pack_bf16(acc[q + 0], acc[q + 1]);
-              v.y = pack_bf16(acc[q + 2], acc[q + 3]);
-              v.z = pack_bf16(acc[q + 4], acc[q + 5]);
-              v.w = pack_bf16(acc[q + 6], acc[q + 7]);
-              *reinterpret_cast<uint4*>(dst + c + q) = v;
-            }
-          }
-        }
-      }
       it_cur = it_nxt;
       st_cur = st_nxt;
       ++item_seq;
@@ -894,6 +837,98 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == mma_warp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// Split merge: for every (sequence, kv-head group) whose tiles the partition cut
+// into pieces, out = sum over the pieces s (in split order) of
+// 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s. Thread: one packed row, 16 columns.
+// ===========================================================================
+constexpr int kMergeThreads = 512;
+
+__global__ void __launch_bounds__(kMergeThreads)
+attn_merge_kernel(const AttnParams p) {
+  // launched while the attention grid runs: wait for it to complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int grp = blockIdx.x;
+  const int b = grp / p.n_groups, g = grp - b * p.n_groups;
+  const int* cum = p.plan_ws + 1;
+  const int share = p.plan_ws[0];
+  const int nt = cum[b + 1] - cum[b];
+  if (nt == 0) return;                       // inactive sequence
+  const int base = p.n_groups * cum[b] + g * nt;
+  const int nsplit = (base + nt - 1) / share - base / share + 1;
+  if (nsplit < 2) return;                    // written whole by its one piece
+  const int u = blockIdx.y * kMergeThreads + threadIdx.x;
+  if (u >= p.Mi * 8) return;
+  const int r = u >> 3, c0 = (u & 7) * 16;
+  const float2* ml = p.part_ml + (size_t)grp * p.max_splits * p.Mi + r;
+  const float4* src0 = reinterpret_cast<const float4*>(p.part_o + ((size_t)grp * p.max_splits * p.Mi + r) * attn::kD + c0);
+  const size_t sstride = (size_t)p.Mi * attn::kD / 4;   // float4 per split slot
+  // the first four pieces' statistics and partial sums are loaded together
+  float2 mv[4];
+  float4 x[4][4];
+#pragma unroll
+  for (int sp = 0; sp < 4; ++sp) {
+    if (sp < nsplit) {
+      mv[sp] = __ldg(ml + (size_t)sp * p.Mi);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[sp][q] = __ldg(src0 + sp * sstride + q);
+    }
+  }
+  float mx = -CUDART_INF_F;
+#pragma unroll
+  for (int sp = 0; sp < 4; ++sp)
+    if (sp < nsplit) mx = fmaxf(mx, mv[sp].x);
+  for (int sp = 4; sp < nsplit; ++sp) mx = fmaxf(mx, __ldg(ml + (size_t)sp * p.Mi).x);
+  float L = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < 4; ++sp)
+    if (sp < nsplit) L += mv[sp].x == -CUDART_INF_F ? 0.f : mv[sp].y * exp2f(mv[sp].x - mx);
+  for (int sp = 4; sp < nsplit; ++sp) {
+    const float2 v = __ldg(ml + (size_t)sp * p.Mi);
+    L += v.x == -CUDART_INF_F ? 0.f : v.y * exp2f(v.x - mx);
+  }
+  const float inv_l = L > 0.f ? 1.f / L : 0.f;
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < 4; ++sp) {
+    if (sp < nsplit) {
+      const float w = mv[sp].x == -CUDART_INF_F ? 0.f : exp2f(mv[sp].x - mx) * inv_l;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[4 * q + 0] += w * x[sp][q].x;
+        acc[4 * q + 1] += w * x[sp][q].y;
+        acc[4 * q + 2] += w * x[sp][q].z;
+        acc[4 * q + 3] += w * x[sp][q].w;
+      }
+    }
+  }
+  for (int sp = 4; sp < nsplit; ++sp) {
+    const float2 v = __ldg(ml + (size_t)sp * p.Mi);
+    const float w = v.x == -CUDART_INF_F ? 0.f : exp2f(v.x - mx) * inv_l;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 y = __ldg(src0 + sp * sstride + q);
+      acc[4 * q + 0] += w * y.x;
+      acc[4 * q + 1] += w * y.y;
+      acc[4 * q + 2] += w * y.z;
+      acc[4 * q + 3] += w * y.w;
+    }
+  }
+  const int i = r / p.Gi, hh = r - i * p.Gi;
+  bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.Gi + hh) * attn::kD + c0;
+#pragma unroll
+  for (int q = 0; q < 16; q += 8) {
+    uint4 v;
+    v.x = pack_bf16(acc[q + 0], acc[q + 1]);
+    v.y = pack_bf16(acc[q + 2], acc[q + 3]);
+    v.z = pack_bf16(acc[q + 4], acc[q + 5]);
+    v.w = pack_bf16(acc[q + 6], acc[q + 7]);
+    *reinterpret_cast<uint4*>(dst + q) = v;
   }
 }
 
@@ -1020,17 +1055,35 @@ size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_c
   const int hpi = attn_hpi(n_q, n_kv, Hq, Hkv, page_size);
   const int Mi = hpi * n_q * (Hq / Hkv);
   const size_t ctas = (size_t)B * (Hkv / hpi) * attn_max_splits(max_ctx, attn::kTileK / hpi);
-  return align_up(ctas * Mi * 128 * sizeof(float)) + align_up(ctas * Mi * sizeof(float2));
+  return align_up(ctas * Mi * 128 * sizeof(float)) + align_up(ctas * Mi * sizeof(float2)) +
+         align_up((size_t)(B + 2) * sizeof(int32_t));
 }
 
 template <int kThreadsT, int HPI>
 static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& kbmap,
                                   const CUtensorMap& vbmap, const AttnParams& p,
-                                  int S, size_t smem, cudaStream_t st) {
+                                  int S, size_t smem, cudaStream_t st, int* launches) {
   static SmemOptIn opt_in;
   cudaError_t e = opt_in.ensure(attn_tc_kernel<kThreadsT, HPI>, smem);
   if (e != cudaSuccess) return e;
   attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, kbmap, vbmap, p, S);
+  cudaError_t le = cudaGetLastError();
+  if (le != cudaSuccess || p.max_splits < 2) return le;
+  // the split merge, a programmatic dependent of the attention grid
+  const dim3 mg(p.B * p.n_groups, (p.Mi * 8 + kMergeThreads - 1) / kMergeThreads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = mg;
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  le = cudaLaunchKernelEx(&cfg, attn_merge_kernel, p);
+  if (le != cudaSuccess) return le;
+  *launches = 2;
   return cudaGetLastError();
 }
 
@@ -1078,7 +1131,7 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   char* ws = (char*)a.scratch;
   p.part_o = (float*)ws;
   p.part_ml = (float2*)(ws + align_up(ctas * M * 128 * sizeof(float)));
-  p.counters = a.counters;
+  p.plan_ws = (int32_t*)(ws + align_up(ctas * M * 128 * sizeof(float)) + align_up(ctas * M * sizeof(float2)));
   p.err = a.err;
   // K/V pools and the block rows as [row][head][d]: a box of {64 d, hpi heads,
   // br rows} lands as [row][head][64 d]
@@ -1108,11 +1161,11 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   const bool wide = (M + 31) / 32 > 2;
   cudaError_t e;
   if (wide)
-    e = p.hpi == 2 ? launch_attn_tc<448, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream)
-                   : launch_attn_tc<448, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream);
+    e = p.hpi == 2 ? launch_attn_tc<448, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream, launches)
+                   : launch_attn_tc<448, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream, launches);
   else
-    e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream)
-                   : launch_attn_tc<320, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream);
+    e = p.hpi == 2 ? launch_attn_tc<320, 2>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream, launches)
+                   : launch_attn_tc<320, 1>(kmap, vmap, kbmap, vbmap, p, S, smem, a.stream, launches);
   return e;
 }
 

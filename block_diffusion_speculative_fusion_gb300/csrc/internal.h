@@ -188,7 +188,6 @@ struct AttnArgs {
   const uint8_t* active;   // [B] or null: sequences with 0 are skipped
   float scale;
   void* out;
-  int32_t* counters;
   int* err;
   void* scratch;
   cudaStream_t stream;
