@@ -28,7 +28,7 @@ namespace dflash {
 namespace attn {
 constexpr int kD = 128;
 constexpr int kTileK = 64;                   // keys per tile
-constexpr int kMinSplitTiles = 16;           // smallest key split: 1024 keys
+constexpr int kMinSplitTiles = 8;            // smallest range of the partition, in tiles
 constexpr int kMaxWarps = 8;                 // M <= 128 packed query rows
 }  // namespace attn
 
@@ -40,11 +40,11 @@ struct AttnParams {
   const int32_t* ctx_len;
   const uint8_t* active;   // [B] or null: sequences with 0 take no tiles
   bf16* out;
-  float* part_o;     // [B * Hkv * max_splits][M][128]  (max_splits for the smallest split)
-  float2* part_ml;   // [B * Hkv * max_splits][M]  (max in log2 units, sum)
+  float* part_o;     // [n_slots][Mi][128]: fp32 partial O of the split pieces
+  float2* part_ml;   // [n_slots][Mi]: their row max (log2 units) and sum
   int32_t* plan_ws;  // [B + 2]: the partition's range size, then cum[0..B] (read by the merge kernel)
   int* err;
-  int B, n_q, n_kv, Hq, Hkv, G, M, page_size, max_pages, num_pages, max_splits, max_ctx;
+  int B, n_q, n_kv, Hq, Hkv, G, M, page_size, max_pages, num_pages, n_slots, max_ctx;
   int causal;        // 1: query i sees block rows j <= i + n_kv - n_q
   // work items: hpi kv heads (1 or 2) per item, Gi = hpi * G query heads and
   // Mi = n_q * Gi packed rows per item, n_groups = Hkv / hpi items per split of
@@ -108,11 +108,13 @@ constexpr int kBarBytes = (2 * kMaxStages + 33) * 8 + 2 * 32 + (kMaxSeqs + 1) * 
 // b, kv-head group g) owns nt_b consecutive tiles -- its context tiles, then
 // the block's own rows as one more tile -- in the order b-major, g-minor; the
 // resulting sequence of N tiles is cut into ranges of `share` tiles (the mean
-// work of one CTA, at least 16 tiles, at most what one page-table window
+// work of one CTA, at least 8 tiles, at most what one page-table window
 // holds), and CTA c takes ranges c, c + grid, ... A piece is the part of one
 // range that falls in one (b, g); a (b, g) cut by range borders is computed
 // in pieces whose fp32 partial results a second kernel (attn_merge_kernel)
-// merges once the grid has finished.
+// merges once the grid has finished. Partials sit in two slots per range: 2 v
+// for the piece that starts range v, 2 v + 1 for a piece that starts inside it
+// (only a (b, g)'s first piece can).
 
 struct AttnItem {
   int b, g, split, nsplit, t0, C, n_tiles_ctx, n_tiles;   // b < 0: no more pieces
@@ -776,7 +778,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       const bool single = (it.nsplit == 1);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const size_t cta = ((size_t)it.b * p.n_groups + it.g) * p.max_splits + it.split;
+      // partial slot of a split piece: two per range, one for the piece that
+      // starts the range and one for the piece that starts inside it
+      const int nt_b = cum[it.b + 1] - cum[it.b];
+      const int start = p.n_groups * cum[it.b] + it.g * nt_b + it.t0;
+      const size_t cta = 2 * (size_t)(start / plan.share) + (start % plan.share != 0 ? 1 : 0);
       const uint32_t o_col = 128 + (uint32_t)((ALT == 2 ? 0 : slot) * attn::kD);
       for (int c = 0; c < attn::kD / 32; ++c) {
         uint32_t o[32];
@@ -863,60 +869,74 @@ attn_merge_kernel(const AttnParams p) {
   const int u = blockIdx.y * kMergeThreads + threadIdx.x;
   if (u >= p.Mi * 8) return;
   const int r = u >> 3, c0 = (u & 7) * 16;
-  const float2* ml = p.part_ml + (size_t)grp * p.max_splits * p.Mi + r;
-  const float4* src0 = reinterpret_cast<const float4*>(p.part_o + ((size_t)grp * p.max_splits * p.Mi + r) * attn::kD + c0);
-  const size_t sstride = (size_t)p.Mi * attn::kD / 4;   // float4 per split slot
-  // the first four pieces' statistics and partial sums are loaded together
+  // piece sp of the group sits in range base / share + sp; only the first piece
+  // can start inside its range (slot 2 v + 1), the others start theirs (2 v)
+  const int v0 = base / share, in0 = base % share != 0 ? 1 : 0;
+  auto slot_of = [&](int sp) -> size_t { return 2 * (size_t)(v0 + sp) + (sp == 0 ? in0 : 0); };
+  const float2* ml = p.part_ml + r;
+  const float4* src0 = reinterpret_cast<const float4*>(p.part_o + (size_t)r * attn::kD + c0);
+  const size_t sstride = (size_t)p.Mi * attn::kD / 4;   // float4 per slot
+  const size_t mstride = (size_t)p.Mi;                  // float2 per slot
+  // pieces in groups of four, each group's loads issued together; the first
+  // group's partial sums are loaded with the statistics
   float2 mv[4];
   float4 x[4][4];
 #pragma unroll
-  for (int sp = 0; sp < 4; ++sp) {
-    if (sp < nsplit) {
-      mv[sp] = __ldg(ml + (size_t)sp * p.Mi);
+  for (int j = 0; j < 4; ++j) {
+    if (j < nsplit) {
+      mv[j] = __ldg(ml + slot_of(j) * mstride);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) x[sp][q] = __ldg(src0 + sp * sstride + q);
+      for (int q = 0; q < 4; ++q) x[j][q] = __ldg(src0 + slot_of(j) * sstride + q);
     }
   }
   float mx = -CUDART_INF_F;
 #pragma unroll
-  for (int sp = 0; sp < 4; ++sp)
-    if (sp < nsplit) mx = fmaxf(mx, mv[sp].x);
-  for (int sp = 4; sp < nsplit; ++sp) mx = fmaxf(mx, __ldg(ml + (size_t)sp * p.Mi).x);
+  for (int j = 0; j < 4; ++j)
+    if (j < nsplit) mx = fmaxf(mx, mv[j].x);
+  for (int s0 = 4; s0 < nsplit; s0 += 4) {
+    float2 w4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (s0 + j < nsplit) w4[j] = __ldg(ml + slot_of(s0 + j) * mstride);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (s0 + j < nsplit) mx = fmaxf(mx, w4[j].x);
+  }
   float L = 0.f;
 #pragma unroll
-  for (int sp = 0; sp < 4; ++sp)
-    if (sp < nsplit) L += mv[sp].x == -CUDART_INF_F ? 0.f : mv[sp].y * exp2f(mv[sp].x - mx);
+  for (int j = 0; j < 4; ++j)
+    if (j < nsplit) L += mv[j].x == -CUDART_INF_F ? 0.f : mv[j].y * exp2f(mv[j].x - mx);
   for (int sp = 4; sp < nsplit; ++sp) {
-    const float2 v = __ldg(ml + (size_t)sp * p.Mi);
+    const float2 v = __ldg(ml + slot_of(sp) * mstride);
     L += v.x == -CUDART_INF_F ? 0.f : v.y * exp2f(v.x - mx);
   }
   const float inv_l = L > 0.f ? 1.f / L : 0.f;
   float acc[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += 4) {
+    if (s0 > 0) {
 #pragma unroll
-  for (int sp = 0; sp < 4; ++sp) {
-    if (sp < nsplit) {
-      const float w = mv[sp].x == -CUDART_INF_F ? 0.f : exp2f(mv[sp].x - mx) * inv_l;
+      for (int j = 0; j < 4; ++j) {
+        if (s0 + j < nsplit) {
+          mv[j] = __ldg(ml + slot_of(s0 + j) * mstride);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[4 * q + 0] += w * x[sp][q].x;
-        acc[4 * q + 1] += w * x[sp][q].y;
-        acc[4 * q + 2] += w * x[sp][q].z;
-        acc[4 * q + 3] += w * x[sp][q].w;
+          for (int q = 0; q < 4; ++q) x[j][q] = __ldg(src0 + slot_of(s0 + j) * sstride + q);
+        }
       }
     }
-  }
-  for (int sp = 4; sp < nsplit; ++sp) {
-    const float2 v = __ldg(ml + (size_t)sp * p.Mi);
-    const float w = v.x == -CUDART_INF_F ? 0.f : exp2f(v.x - mx) * inv_l;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 y = __ldg(src0 + sp * sstride + q);
-      acc[4 * q + 0] += w * y.x;
-      acc[4 * q + 1] += w * y.y;
-      acc[4 * q + 2] += w * y.z;
-      acc[4 * q + 3] += w * y.w;
+    for (int j = 0; j < 4; ++j) {
+      if (s0 + j < nsplit) {
+        const float w = mv[j].x == -CUDART_INF_F ? 0.f : exp2f(mv[j].x - mx) * inv_l;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[4 * q + 0] += w * x[j][q].x;
+          acc[4 * q + 1] += w * x[j][q].y;
+          acc[4 * q + 2] += w * x[j][q].z;
+          acc[4 * q + 3] += w * x[j][q].w;
+        }
+      }
     }
   }
   const int i = r / p.Gi, hh = r - i * p.Gi;
@@ -1043,18 +1063,20 @@ static int attn_hpi(int n_q, int n_kv, int Hq, int Hkv, int page_size) {
   return pair ? 2 : 1;
 }
 
-// Pieces of one (sequence, group) at most: its tiles (context and block) over
-// ranges of at least kMinSplitTiles, plus one for a range border inside it.
-static int attn_max_splits(int max_ctx, int TK) {
-  const int tiles = (max_ctx + TK - 1) / TK + 1;
-  return (tiles + attn::kMinSplitTiles - 1) / attn::kMinSplitTiles + 1;
+// Partial slots: two per range of the partition (its first piece and a piece
+// starting inside it). The ranges number at most max(grid, N / window): a
+// range holds at least N / grid tiles unless the page-table window caps it.
+static int attn_slots(int B, int n_groups, int max_ctx, int TK, int page_size) {
+  const long n_max = (long)B * n_groups * ((max_ctx + TK - 1) / TK + 1);
+  const long window = (long)(attn_tc::kPtMax - 1) * page_size / TK;
+  return (int)(2 * std::max<long>(attn_tc::kGrid, (n_max + window - 1) / window));
 }
 
 size_t attn_ws_bytes(int B, int n_q, int n_kv, int Hq, int Hkv, int D, int max_ctx, int page_size, int dtype) {
   if (dtype != 1 || D != 128) return 0;
   const int hpi = attn_hpi(n_q, n_kv, Hq, Hkv, page_size);
   const int Mi = hpi * n_q * (Hq / Hkv);
-  const size_t ctas = (size_t)B * (Hkv / hpi) * attn_max_splits(max_ctx, attn::kTileK / hpi);
+  const size_t ctas = (size_t)attn_slots(B, Hkv / hpi, max_ctx, attn::kTileK / hpi, page_size);
   return align_up(ctas * Mi * 128 * sizeof(float)) + align_up(ctas * Mi * sizeof(float2)) +
          align_up((size_t)(B + 2) * sizeof(int32_t));
 }
@@ -1068,7 +1090,7 @@ static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vm
   if (e != cudaSuccess) return e;
   attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, kbmap, vbmap, p, S);
   cudaError_t le = cudaGetLastError();
-  if (le != cudaSuccess || p.max_splits < 2) return le;
+  if (le != cudaSuccess) return le;
   // the split merge, a programmatic dependent of the attention grid
   const dim3 mg(p.B * p.n_groups, (p.Mi * 8 + kMergeThreads - 1) / kMergeThreads);
   cudaLaunchConfig_t cfg = {};
@@ -1122,12 +1144,12 @@ cudaError_t launch_block_attn(const AttnArgs& a, int* launches) {
   p.n_groups = a.Hkv / p.hpi;
   p.TK = kTileK / p.hpi;
   p.br = p.hpi == 1 ? a.page_size : std::min(a.page_size, 32);
-  p.max_splits = attn_max_splits(a.max_ctx, p.TK);
+  p.n_slots = attn_slots(a.B, p.n_groups, a.max_ctx, p.TK, a.page_size);
   p.max_ctx = a.max_ctx;
   p.scale_log2 = a.scale * kLog2e;
   p.wait_ns = wait_limit_ns();
   const int M = p.Mi;
-  const size_t ctas = (size_t)a.B * p.n_groups * p.max_splits;
+  const size_t ctas = (size_t)p.n_slots;
   char* ws = (char*)a.scratch;
   p.part_o = (float*)ws;
   p.part_ml = (float2*)(ws + align_up(ctas * M * 128 * sizeof(float)));
