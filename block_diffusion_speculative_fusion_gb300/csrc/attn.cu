@@ -849,12 +849,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // ===========================================================================
 // Split merge: for every (sequence, kv-head group) whose tiles the partition cut
 // into pieces, out = sum over the pieces s (in split order) of
-// 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s. Thread: one packed row, 16 columns.
+// 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s. Thread: one packed row, 8 or 16 columns.
 // ===========================================================================
 constexpr int kMergeThreads = 512;
 
+// COLS columns of one packed row per thread; the partial sums of PRE = 64 /
+// COLS pieces are loaded at a time (with the first group, the statistics too).
+template <int COLS>
 __global__ void __launch_bounds__(kMergeThreads)
 attn_merge_kernel(const AttnParams p) {
+  constexpr int PRE = 64 / COLS, V4 = COLS / 4, UPR = attn::kD / COLS;
   // launched while the attention grid runs: wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int grp = blockIdx.x;
@@ -867,8 +871,8 @@ attn_merge_kernel(const AttnParams p) {
   const int nsplit = (base + nt - 1) / share - base / share + 1;
   if (nsplit < 2) return;                    // written whole by its one piece
   const int u = blockIdx.y * kMergeThreads + threadIdx.x;
-  if (u >= p.Mi * 8) return;
-  const int r = u >> 3, c0 = (u & 7) * 16;
+  if (u >= p.Mi * UPR) return;
+  const int r = u / UPR, c0 = (u - r * UPR) * COLS;
   // piece sp of the group sits in range base / share + sp; only the first piece
   // can start inside its range (slot 2 v + 1), the others start theirs (2 v)
   const int v0 = base / share, in0 = base % share != 0 ? 1 : 0;
@@ -877,60 +881,58 @@ attn_merge_kernel(const AttnParams p) {
   const float4* src0 = reinterpret_cast<const float4*>(p.part_o + (size_t)r * attn::kD + c0);
   const size_t sstride = (size_t)p.Mi * attn::kD / 4;   // float4 per slot
   const size_t mstride = (size_t)p.Mi;                  // float2 per slot
-  // pieces in groups of four, each group's loads issued together; the first
-  // group's partial sums are loaded with the statistics
-  float2 mv[4];
-  float4 x[4][4];
+  float2 mv[PRE];
+  float4 x[PRE][V4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < PRE; ++j) {
     if (j < nsplit) {
       mv[j] = __ldg(ml + slot_of(j) * mstride);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) x[j][q] = __ldg(src0 + slot_of(j) * sstride + q);
+      for (int q = 0; q < V4; ++q) x[j][q] = __ldg(src0 + slot_of(j) * sstride + q);
     }
   }
   float mx = -CUDART_INF_F;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < PRE; ++j)
     if (j < nsplit) mx = fmaxf(mx, mv[j].x);
-  for (int s0 = 4; s0 < nsplit; s0 += 4) {
-    float2 w4[4];
+  for (int s0 = PRE; s0 < nsplit; s0 += PRE) {
+    float2 w4[PRE];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < PRE; ++j)
       if (s0 + j < nsplit) w4[j] = __ldg(ml + slot_of(s0 + j) * mstride);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < PRE; ++j)
       if (s0 + j < nsplit) mx = fmaxf(mx, w4[j].x);
   }
   float L = 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < PRE; ++j)
     if (j < nsplit) L += mv[j].x == -CUDART_INF_F ? 0.f : mv[j].y * exp2f(mv[j].x - mx);
-  for (int sp = 4; sp < nsplit; ++sp) {
+  for (int sp = PRE; sp < nsplit; ++sp) {
     const float2 v = __ldg(ml + slot_of(sp) * mstride);
     L += v.x == -CUDART_INF_F ? 0.f : v.y * exp2f(v.x - mx);
   }
   const float inv_l = L > 0.f ? 1.f / L : 0.f;
-  float acc[16];
+  float acc[COLS];
 #pragma unroll
-  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-  for (int s0 = 0; s0 < nsplit; s0 += 4) {
+  for (int q = 0; q < COLS; ++q) acc[q] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += PRE) {
     if (s0 > 0) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < PRE; ++j) {
         if (s0 + j < nsplit) {
           mv[j] = __ldg(ml + slot_of(s0 + j) * mstride);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) x[j][q] = __ldg(src0 + slot_of(s0 + j) * sstride + q);
+          for (int q = 0; q < V4; ++q) x[j][q] = __ldg(src0 + slot_of(s0 + j) * sstride + q);
         }
       }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < PRE; ++j) {
       if (s0 + j < nsplit) {
         const float w = mv[j].x == -CUDART_INF_F ? 0.f : exp2f(mv[j].x - mx) * inv_l;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < V4; ++q) {
           acc[4 * q + 0] += w * x[j][q].x;
           acc[4 * q + 1] += w * x[j][q].y;
           acc[4 * q + 2] += w * x[j][q].z;
@@ -942,7 +944,7 @@ attn_merge_kernel(const AttnParams p) {
   const int i = r / p.Gi, hh = r - i * p.Gi;
   bf16* dst = p.out + ((size_t)(b * p.n_q + i) * p.Hq + g * p.Gi + hh) * attn::kD + c0;
 #pragma unroll
-  for (int q = 0; q < 16; q += 8) {
+  for (int q = 0; q < COLS; q += 8) {
     uint4 v;
     v.x = pack_bf16(acc[q + 0], acc[q + 1]);
     v.y = pack_bf16(acc[q + 2], acc[q + 3]);
@@ -1092,7 +1094,11 @@ static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vm
   cudaError_t le = cudaGetLastError();
   if (le != cudaSuccess) return le;
   // the split merge, a programmatic dependent of the attention grid
-  const dim3 mg(p.B * p.n_groups, (p.Mi * 8 + kMergeThreads - 1) / kMergeThreads);
+  // few (sequence, group)s (small batches, many pieces each): 8 columns per
+  // thread, every piece's loads at once; many: 16 columns, four pieces at once
+  const bool narrow = p.B * p.n_groups < attn_tc::kGrid / 2;
+  const int cols = narrow ? 8 : 16;
+  const dim3 mg(p.B * p.n_groups, (p.Mi * (attn::kD / cols) + kMergeThreads - 1) / kMergeThreads);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = mg;
   cfg.blockDim = dim3(kMergeThreads);
@@ -1103,7 +1109,10 @@ static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vm
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  le = cudaLaunchKernelEx(&cfg, attn_merge_kernel, p);
+  if (narrow)
+    le = cudaLaunchKernelEx(&cfg, attn_merge_kernel<8>, p);
+  else
+    le = cudaLaunchKernelEx(&cfg, attn_merge_kernel<16>, p);
   if (le != cudaSuccess) return le;
   *launches = 2;
   return cudaGetLastError();
