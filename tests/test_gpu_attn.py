@@ -50,8 +50,8 @@ def _run(w, cache, blk, atol, seqs=None, causal=False, repeat=1):
     args = [blk["q"].to(DEV), blk["k_blk"].to(DEV), blk["v_blk"].to(DEV), cache.k_pools[0].to(DEV),
             cache.v_pools[0].to(DEV), cache.page_table.to(DEV), cache.ctx_len.to(DEV)]
     out = api.block_attn(*args, causal=causal).clone()
-    # repeated calls give the same bits: work items go to whichever CTA is free,
-    # and the result must not depend on that assignment
+    # repeated calls give the same bits: the partition of the work depends on
+    # the dims and ctx_len only, and split pieces are merged in a fixed order
     for _ in range(repeat - 1):
         again = api.block_attn(*args, causal=causal)
         assert torch.equal(again.view(torch.int16), out.view(torch.int16))
@@ -212,6 +212,22 @@ def test_attn_needles_split_boundaries(ctx):
     blk = synth.block_qkv(wl, 0, seed=15)
     synth.plant_needles(wl, blk, cache, seed=15)
     _run(wl, cache, blk, 2e-2)
+
+
+@pytest.mark.parametrize("B", [1, 19])
+def test_attn_long_context_split_into_many_pieces(B):
+    """One 8192-key context among short ones: the launch holds few tiles, so
+    the partition's ranges are 8-9 tiles and each kv-head pair of the long
+    context is cut into some 30 pieces. The split-merge kernel combines them
+    with 8 columns per thread and eight pieces' loads at a time when fewer than
+    76 (sequence, kv-head pair)s take part (B = 1), else with 16 columns and
+    four pieces at a time (B = 19: 76 pairs), looping over the rest. Needles
+    on the long context's pages make a lost or misplaced piece visible."""
+    ctx = [8192] + [1 + 7 * i for i in range(B - 1)]
+    w, cache, blk = _case(W.LLAMA8B_B64, ctx, seed=18)
+    synth.plant_needles(w, blk, cache, seed=18)
+    got = _run(w, cache, blk, 2e-2, seqs=sorted({0, B - 1, B // 2}), repeat=2)
+    assert np.abs(got[0]).max() > 0.5
 
 
 @pytest.mark.parametrize("wl,ctx", [(W.LLAMA8B_B64, [3000, 700, 5200, 1200, 64, 2500]),
