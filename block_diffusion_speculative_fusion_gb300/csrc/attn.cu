@@ -301,7 +301,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == mma_warp) tmem_alloc(tmem_base_sm, kTmemCols);
   // the merge kernel that follows may be scheduled once every CTA has got here;
   // it waits for this grid to complete before it reads anything
-  asm volatile("griddepcontrol.launch_dependents;");
+  dependents_may_launch();
   // ---- work list: the tiles per group of every sequence, prefix-summed ----
   if (warp == 0) plan_cum_warp(p, cum, lane);
   tc_fence_before();
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 attn_merge_kernel(const AttnParams p) {
   constexpr int PRE = 64 / COLS, V4 = COLS / 4, UPR = attn::kD / COLS;
   // launched while the attention grid runs: wait for it to complete
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  wait_for_prior_grid();
   const int grp = blockIdx.x;
   const int b = grp / p.n_groups, g = grp - b * p.n_groups;
   const int* cum = p.plan_ws + 1;
@@ -1090,6 +1090,8 @@ static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vm
   static SmemOptIn opt_in;
   cudaError_t e = opt_in.ensure(attn_tc_kernel<kThreadsT, HPI>, smem);
   if (e != cudaSuccess) return e;
+  // a plain launch: as a dependent of the kernel before it, the CTAs reach the
+  // SMs in a different order and the kernel measured 2 % slower
   attn_tc_kernel<kThreadsT, HPI><<<attn_tc::kGrid, kThreadsT, smem, st>>>(kmap, vmap, kbmap, vbmap, p, S);
   cudaError_t le = cudaGetLastError();
   if (le != cudaSuccess) return le;
@@ -1099,20 +1101,10 @@ static cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vm
   const bool narrow = p.B * p.n_groups < attn_tc::kGrid / 2;
   const int cols = narrow ? 8 : 16;
   const dim3 mg(p.B * p.n_groups, (p.Mi * (attn::kD / cols) + kMergeThreads - 1) / kMergeThreads);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = mg;
-  cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
   if (narrow)
-    le = cudaLaunchKernelEx(&cfg, attn_merge_kernel<8>, p);
+    le = launch_dependent(attn_merge_kernel<8>, mg, dim3(kMergeThreads), 0, st, p);
   else
-    le = cudaLaunchKernelEx(&cfg, attn_merge_kernel<16>, p);
+    le = launch_dependent(attn_merge_kernel<16>, mg, dim3(kMergeThreads), 0, st, p);
   if (le != cudaSuccess) return le;
   *launches = 2;
   return cudaGetLastError();

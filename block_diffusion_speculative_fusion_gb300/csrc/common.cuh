@@ -13,6 +13,32 @@ typedef __nv_bfloat16 bf16;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel started with launch_dependent() may
+// be scheduled while the kernel before it in the stream is still running (once
+// every CTA of that kernel has executed dependents_may_launch() or ended); it
+// executes wait_for_prior_grid() before it touches memory that earlier work
+// writes or reads. Both instructions do nothing in a kernel launched plainly.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void wait_for_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void dependents_may_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // 16-byte vectors of logits, unpacked to fp32
 // ---------------------------------------------------------------------------
 template <typename T> struct VecTraits;

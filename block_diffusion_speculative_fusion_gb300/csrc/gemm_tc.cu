@@ -112,6 +112,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
                float* __restrict__ part, const int32_t* __restrict__ meta, int per_idx, int T_max, int N, int MT,
                int KB, int box_l, int box_m, int* err, unsigned long long wait_ns) {
   using namespace tc;
+  // a dependent launch: the rows and the plan come from the kernel before
+  wait_for_prior_grid();
+  dependents_may_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
@@ -318,8 +321,9 @@ cudaError_t launch_gemm_tc(const void* X, const void* W, float* part, const int3
   static SmemOptIn opt_in;
   cudaError_t e = opt_in.ensure(gemm_tc_kernel, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<<<GRID, THREADS, SMEM_BYTES, st>>>(wmap, xmap_l, xmap_m, xmap_s, part, meta, per_idx, T_max, N,
-                                                    N / BM, K / BK, box_l, box_m, err, wait_limit_ns());
+  e = launch_dependent(gemm_tc_kernel, dim3(GRID), dim3(THREADS), SMEM_BYTES, st, wmap, xmap_l, xmap_m, xmap_s, part,
+                       meta, per_idx, T_max, N, N / BM, K / BK, box_l, box_m, err, wait_limit_ns());
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -46,6 +46,7 @@ mat_gather_kernel(const int32_t* __restrict__ commit_len, const int32_t* __restr
                   const __grid_constant__ RopeFreq inv_freq, float2* __restrict__ rope, int half,
                   const int32_t* __restrict__ page_table, int page_size, int max_pages, int num_pages,
                   long long* __restrict__ slots, int* __restrict__ err) {
+  dependents_may_launch();   // the GEMM that follows may be scheduled (it waits for this grid)
   __shared__ int scan[256];
   __shared__ int run_start[257];
   const int tid = threadIdx.x;
@@ -161,6 +162,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(const T* __restrict__ X, const T* __restrict__ W, float* __restrict__ part,
                  const int32_t* __restrict__ meta, int T_max, int N, int K, int k_per_split) {
+  wait_for_prior_grid();   // a dependent launch: the rows come from the kernel before
+  dependents_may_launch();
   __shared__ float As[16][68];
   __shared__ float Bs[16][68];
   const int n0 = blockIdx.x * 64, t0 = blockIdx.y * 64, s = blockIdx.z;
@@ -210,6 +213,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 mat_bias_kernel(const float* __restrict__ part, int splits, const T* __restrict__ b_f, T* __restrict__ h,
                 const int32_t* __restrict__ meta, int T_max, int d, int K1) {
+  wait_for_prior_grid();   // a dependent launch: the partial sums come from the GEMM before
+  dependents_may_launch();
   // grid-stride over the committed rows only; 4 consecutive features per
   // thread (d % 4 == 0: they share one output tile, hence one segment count)
   const int d4 = d / 4;
@@ -300,6 +305,8 @@ __global__ void __launch_bounds__(256, kEpiCtasPerSm)
 mat_epilogue_d128_kernel(const float* __restrict__ part, int splits, const int32_t* __restrict__ meta,
                          const long long* __restrict__ slots, const T* __restrict__ k_norm_w, float rms_eps,
                          const float2* __restrict__ rope, MatPools pools, int T_max, int L, int Hkv, int K2) {
+  wait_for_prior_grid();   // a dependent launch: the partial sums come from the GEMM before
+  dependents_may_launch();
   constexpr int D = 128, half = 64, NH = kEpiHeads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int d0 = 4 * lane;
@@ -400,6 +407,8 @@ mat_epilogue_kernel(const float* __restrict__ part, int splits, const int32_t* _
                     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ page_table,
                     const T* __restrict__ k_norm_w, float rms_eps, const float2* __restrict__ rope, MatPools pools,
                     int T_max, int L, int Hkv, int D, int page_size, int max_pages, int num_pages, int K2) {
+  wait_for_prior_grid();   // a dependent launch: the partial sums come from the GEMM before
+  dependents_may_launch();
   extern __shared__ float esm[];             // [warps][D] staging
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   float* xs = esm + warp * D;
@@ -497,7 +506,9 @@ static cudaError_t run_gemm(const MatPlan& p, bool tc, const void* X, const void
   if (tc) return launch_gemm_tc(X, W, part, meta, p.T_max, N, K, per_idx, err, st);
   const int kps = ((K + S - 1) / S + 15) / 16 * 16;
   dim3 grid((N + 63) / 64, (p.T_max + 63) / 64, S);
-  gemm_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)X, (const T*)W, part, meta, p.T_max, N, K, kps);
+  cudaError_t e = launch_dependent(gemm_simt_kernel<T>, grid, dim3(256), 0, st, (const T*)X, (const T*)W, part, meta,
+                                   p.T_max, N, K, kps);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -535,20 +546,23 @@ static cudaError_t launch_mat_t(const MatArgs& a, int* launches) {
   cudaError_t e = run_gemm<T>(p, p.tc, X, a.W_f, part, meta, p.N1, p.K1, p.S1, 1, a.err, st);
   if (e != cudaSuccess) return e;
   ++n;
-  mat_bias_kernel<T><<<gs, 256, 0, st>>>(part, p.S1, (const T*)a.b_f, h, meta, p.T_max, p.N1, p.K1);
+  e = launch_dependent(mat_bias_kernel<T>, dim3(gs), dim3(256), 0, st, part, p.S1, (const T*)a.b_f, h, meta, p.T_max,
+                       p.N1, p.K1);
+  if (e != cudaSuccess) return e;
   ++n;
   e = run_gemm<T>(p, p.tc, h, a.W_kv, part, meta, p.N2, p.K2, p.S2, 2, a.err, st);
   if (e != cudaSuccess) return e;
   ++n;
   if (a.D == 128) {
-    mat_epilogue_d128_kernel<T><<<kEpiCtasPerSm * 152, 256, 0, st>>>(part, p.S2, meta, slots, (const T*)a.k_norm_w, a.rms_eps,
-                                                   rope, a.pools, p.T_max, a.L, a.Hkv, p.K2);
+    e = launch_dependent(mat_epilogue_d128_kernel<T>, dim3(kEpiCtasPerSm * 152), dim3(256), 0, st, part, p.S2, meta,
+                         slots, (const T*)a.k_norm_w, a.rms_eps, rope, a.pools, p.T_max, a.L, a.Hkv, p.K2);
   } else {
     const size_t esmem = sizeof(float) * 8 * (size_t)a.D;
-    mat_epilogue_kernel<T><<<gs, 256, esmem, st>>>(
-        part, p.S2, meta, row_b, row_j, a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, rope, a.pools,
-        p.T_max, a.L, a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages, p.K2);
+    e = launch_dependent(mat_epilogue_kernel<T>, dim3(gs), dim3(256), esmem, st, part, p.S2, meta, row_b, row_j,
+                         a.start_pos, a.page_table, (const T*)a.k_norm_w, a.rms_eps, rope, a.pools, p.T_max, a.L,
+                         a.Hkv, a.D, a.page_size, a.max_pages, a.num_pages, p.K2);
   }
+  if (e != cudaSuccess) return e;
   ++n;
   *launches = n;
   return cudaGetLastError();

@@ -145,6 +145,7 @@ sample_draw_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const flo
                    float2* __restrict__ parts, float2* __restrict__ segs, int32_t* __restrict__ counters,
                    int64_t* __restrict__ bonus, int64_t* __restrict__ out_tokens, uint8_t* __restrict__ flags_out,
                    float* __restrict__ probs) {
+  wait_for_prior_grid();   // a dependent launch: the jobs come from the statistics kernel
   constexpr int N = VecTraits<T>::N;
   constexpr int NV = kDrawSeg / N;
   const int c = blockIdx.x, b = blockIdx.y;
@@ -370,6 +371,7 @@ sample_stats_kernel(const T* __restrict__ zt, const T* __restrict__ zd, const fl
                     int32_t* __restrict__ counters, SampleJob* __restrict__ jobs,
                     int32_t* __restrict__ accept_len, int32_t* __restrict__ commit_len,
                     int64_t* __restrict__ out_tokens, float* __restrict__ probs, int* __restrict__ err) {
+  dependents_may_launch();   // the draw may be scheduled (it waits for this grid)
   const int R = n_max + 1;
   const int RR = R + n_max;              // target rows then draft rows of a sequence
   // with the draft rows' log-sum-exps supplied, only the target rows stream
@@ -913,9 +915,10 @@ static cudaError_t launch_sample_t(const VerifyArgs& a, int num_sms) {
   static SmemOptIn opt_in;
   e = opt_in.ensure(sample_draw_kernel<T>, kDrawSmem);
   if (e != cudaSuccess) return e;
-  sample_draw_kernel<T><<<dim3(nch2, a.B), kThreads, kDrawSmem, a.stream>>>(
-      (const T*)a.target_logits, (const T*)a.draft_logits, a.u_final, a.n_max, a.V, nch2, k2, jobs, dparts, dsegs,
-      a.counters, a.bonus, a.out_tokens, a.flags, a.probs);
+  e = launch_dependent(sample_draw_kernel<T>, dim3(nch2, a.B), dim3(kThreads), kDrawSmem, a.stream,
+                       (const T*)a.target_logits, (const T*)a.draft_logits, a.u_final, a.n_max, a.V, nch2, k2, jobs,
+                       dparts, dsegs, a.counters, a.bonus, a.out_tokens, a.flags, a.probs);
+  if (e != cudaSuccess) return e;
   (void)R;
   return cudaGetLastError();
 }
