@@ -296,16 +296,37 @@ def cuda_kernel_times(torch, fn, reps):
             torch.cuda.synchronize()
     except Exception as exc:   # noqa: BLE001 - reported, not fatal
         return {"_error": f"{type(exc).__name__}: {exc}"[:300]}
-    out = {}
     evs = [e for e in prof.events() if str(getattr(e, "device_type", "")).endswith("CUDA")]
     if not evs:
         return {"_error": f"no device events among {len(prof.events())} profiler events"}
-    evs.sort(key=lambda e: e.time_range.start)
-    for e in evs:
-        dur = e.time_range.end - e.time_range.start
-        name = e.name.split("(")[0].split("<")[0].strip().split(" ")[-1].split("::")[-1]
-        out.setdefault(name, []).append(float(dur))
+    return kernel_durations([(e.name, e.time_range.start, e.time_range.end) for e in evs])
+
+
+def kernel_durations(events):
+    """{kernel name: [durations]} from (name, start, end) device events. A
+    programmatic dependent may start before the kernel it waits for has
+    finished; its time is counted from that kernel's end."""
+    out, last_end = {}, {}
+    for raw, start, end in sorted(events, key=lambda x: x[1]):
+        name = raw.split("(")[0].split("<")[0].strip().split(" ")[-1].split("::")[-1]
+        for pred in PDL_PREDECESSORS.get(name, ()):
+            if pred in last_end and last_end[pred] <= end:
+                start = max(start, last_end[pred])
+        out.setdefault(name, []).append(float(end - start))
+        last_end[name] = end
     return out
+
+
+# Kernels launched as programmatic dependents, with the kernels they wait for.
+PDL_PREDECESSORS = {
+    "attn_merge_kernel": ("attn_tc_kernel",),
+    "gemm_tc_kernel": ("mat_gather_kernel", "mat_bias_kernel"),
+    "gemm_simt_kernel": ("mat_gather_kernel", "mat_bias_kernel"),
+    "mat_bias_kernel": ("gemm_tc_kernel", "gemm_simt_kernel"),
+    "mat_epilogue_d128_kernel": ("gemm_tc_kernel", "gemm_simt_kernel"),
+    "mat_epilogue_kernel": ("gemm_tc_kernel", "gemm_simt_kernel"),
+    "sample_draw_kernel": ("sample_stats_kernel",),
+}
 
 
 def step_rooflines(torch, st, wl, hbm, tf, reps=4):

@@ -69,3 +69,16 @@ def test_committed_profile_carries_the_keys_bench_reads():
 @pytest.mark.parametrize("steps,ms,world,expect", [(500, 820.0, 1, 500 / 0.82), (500, 820.0, 4, 4 * 500 / 0.82)])
 def test_replica_throughput_counts_all_ranks(steps, ms, world, expect):
     assert abs(bench.replica_throughput(steps, ms, world) - expect) < 1e-9
+
+
+def test_kernel_durations_count_dependents_from_their_predecessor():
+    # a programmatic dependent that started while its predecessor ran is
+    # charged from the predecessor's end; other kernels keep their own span
+    ev = [("void dflash::mat_gather_kernel(int)", 0.0, 10.0),
+          ("dflash::gemm_tc_kernel(CUtensorMap_st)", 5.0, 50.0),
+          ("void dflash::mat_bias_kernel<__nv_bfloat16>(float*)", 40.0, 60.0),
+          ("void dflash::greedy_kernel<__nv_bfloat16>(int)", 45.0, 70.0),
+          ("void dflash::sample_draw_kernel<float>(int)", 65.0, 80.0)]
+    d = bench.kernel_durations(ev)
+    assert d == {"mat_gather_kernel": [10.0], "gemm_tc_kernel": [40.0], "mat_bias_kernel": [10.0],
+                 "greedy_kernel": [25.0], "sample_draw_kernel": [15.0]}
