@@ -225,3 +225,61 @@ def test_debug_library_builds_and_exports_every_symbol(L):
     finally:
         api.select_library(debug=False)
     assert api.LIB_PATH.endswith("libdflash.so")
+
+
+def _attn_partition_slots(ctx, n_groups, TK, page_size, max_ctx, floor=8, grid=152, pt_max=512):
+    """The split pieces of the attention kernel's static partition and the
+    partial slot each one writes (two per range: 2v for the piece starting
+    range v, 2v + 1 for a piece starting inside it), restated on the host."""
+    nt = [(min(max(c, 0), max_ctx) + TK - 1) // TK + 1 for c in ctx]
+    cum = [0]
+    for x in nt:
+        cum.append(cum[-1] + x)
+    N = n_groups * cum[-1]
+    window = (pt_max - 1) * page_size // TK
+    share = min(window, max(floor, -(-N // grid)))
+    slots = []
+    for b, ntb in enumerate(nt):
+        for g in range(n_groups):
+            base = n_groups * cum[b] + g * ntb
+            nsplit = (base + ntb - 1) // share - base // share + 1
+            if nsplit < 2:
+                continue
+            for sp in range(nsplit):
+                start = base if sp == 0 else (base // share + sp) * share
+                slots.append(2 * (start // share) + (1 if start % share else 0))
+    return slots
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_attention_workspace_holds_every_split_partial(L, seed):
+    # random batches, including the adversarial one (a single long context among
+    # empty ones, the smallest ranges): the pieces' slots are distinct and the
+    # workspace the library sizes from the dims alone holds all of them
+    import random
+    rng = random.Random(seed)
+    for _ in range(40):
+        B = rng.choice([1, 2, 7, 19, 64, 200, 1024])
+        n_q = rng.choice([4, 7, 10, 16])
+        Hkv = rng.choice([1, 2, 3, 4, 8])
+        Hq = Hkv * rng.choice([1, 2, 4])
+        page = rng.choice([8, 16, 32, 64])
+        max_ctx = rng.choice([0, 1, 100, 2048, 8192, 40000])
+        n_kv = n_q
+        ctx = [rng.randint(0, max_ctx) for _ in range(B)]
+        if rng.random() < 0.3:
+            ctx = [max_ctx] + [0] * (B - 1)
+        G = Hq // Hkv
+        hpi = 2 if (Hkv % 2 == 0 and 2 * n_q * G <= 128 and page >= 16 and n_kv <= 32) else 1
+        Mi, n_groups, TK = hpi * n_q * G, Hkv // hpi, 64 // hpi
+        slots = _attn_partition_slots(ctx, n_groups, TK, page, max_ctx)
+        assert len(slots) == len(set(slots))
+        max_pages = max(1, -(-max_ctx // page))
+        d = api.AttnDims(B, n_q, n_kv, Hq, Hkv, 128, page, max_pages, B * max_pages, max_ctx, api.BF16, 0)
+        ws = L.dflash_block_attn_workspace_size(ctypes.byref(d))
+        assert ws > api.WS_COUNTER_BYTES, api.last_error()
+        # fp32 O rows and (max, sum) pairs per slot, plus the plan words and at
+        # most three 256-byte alignment pads
+        per_slot = Mi * 128 * 4 + Mi * 8
+        n_slots_min = (ws - api.WS_COUNTER_BYTES - (B + 2) * 4 - 3 * 256) // per_slot
+        assert not slots or max(slots) < n_slots_min, (B, n_q, Hq, Hkv, page, max_ctx, max(slots), n_slots_min)
