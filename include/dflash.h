@@ -24,6 +24,11 @@
  *     must use different workspaces.
  *   - Every call is asynchronous on the given stream and performs no host
  *     synchronisation. Outputs are valid once the stream reaches that point.
+ *     A call's first kernel is an ordinary launch, so it starts after all
+ *     earlier work in the stream; a call's later kernels (the attention split
+ *     merge, the materialisation's GEMMs, bias and epilogue, the sampled
+ *     draw) are programmatic dependent launches that may become resident
+ *     while the kernel before them runs but read nothing until it completes.
  *   - Return value: DFLASH_OK, or an error code with a message available from
  *     dflash_last_error() (thread-local). Argument errors are detected on the
  *     host before anything is launched; DFLASH_ERR_CUDA reports a launch error.
